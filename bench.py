@@ -1,0 +1,467 @@
+#!/usr/bin/env python3
+"""Benchmark of the conv2d input gradient (implicit GEMM) on GB300.
+
+Metric: dgrad TFLOP/s (useful FLOPs 2*N*Co*OH*OW*Ci*kH*kW) and the fraction of
+the kernel's roofline, on the ResNet 3x3 workload (N=32, Ci=Co=64, 56x56,
+stride 1, pad 1, bf16 in, float32 out) unless --config names another.
+
+One step = one pass of the whole path over one batch: the weight pre-pack
+kernel, then the dgrad kernel.  Inputs are resident in HBM; every step uses
+the next of several buffer sets whose total exceeds 3x the L2 cache, so each
+step starts cold.  The timed region replays a CUDA graph of those steps (with
+an event pair around every dgrad launch for the per-launch kernel time) and is
+bracketed by a barrier and synchronisation on both sides.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle (the
+only reference there is) on a bounded sample of the same workload instead.
+Multi-GPU (torchrun): every rank runs the full workload on its own GPU
+(weak scaling, no collective on the data path); value = all ranks' FLOPs / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dgrad TFLOP/s and % of dense tensor-core roofline per config (1 GB300)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ("conv2d_backward_implicit_gb300/csrc/dgrad_tc.cu",
+                  "conv2d_backward_implicit_gb300/csrc/dgrad_internal.h",
+                  "conv2d_backward_implicit_gb300/csrc/plan.cu")
+
+
+# ------------------------------------------------------------------ helpers
+def useful_flops(wl) -> float:
+    return 2.0 * wl.N * wl.Co * wl.OH * wl.OW * wl.Ci * wl.kH * wl.kW
+
+
+def algorithmic_bytes(wl) -> int:
+    """grad_out + weight + grad_in, each moved once (no materialised im2col)."""
+    esize = 4 if wl.dtype == "f32" else 2
+    go = wl.N * wl.Co * wl.OH * wl.OW * esize
+    w = wl.Co * wl.Ci * wl.kH * wl.kW * esize
+    gi = wl.N * wl.Ci * wl.H * wl.W * 4
+    return go + w + gi
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_fingerprint() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config_key: str):
+    """dram bytes per launch from a committed ncu summary, if it is for this kernel source."""
+    path = os.path.join(ROOT, "profiles", f"dgrad_tc_{config_key}.traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_fingerprint") != kernel_fingerprint():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def reduce_max(value: float, dist_on: bool, device=None) -> float:
+    """Max of a scalar over ranks (identity when not distributed)."""
+    if not dist_on:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(flops_per_rank: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank's useful FLOPs over the slowest rank's time."""
+    return flops_per_rank * steps * world / (max_ms * 1e-3) / 1e12
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=timestamp," + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        rows = []
+        t0, t1 = self.window or (0, float("inf"))
+        for ts, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 1 + len(self.FIELDS):
+                continue
+            rows.append((ts, parts))
+        inside = [r for ts, r in rows if t0 - 0.06 <= ts <= t1 + 0.06]
+        use = inside if inside else rows[-5:]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in use if num(r[1]) is not None]
+        mx = [num(r[2]) for r in use if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# ------------------------------------------------------------------ CPU oracle legs
+def oracle_sample(wl, planes_per_step: int, steps: int, warmup: int):
+    """Time the oracle on `steps` samples of one image x `planes_per_step` input channels."""
+    import numpy as np
+    import oracle
+    from conv2d_backward_implicit_gb300 import workloads
+    one = wl.with_batch(1)
+    g, w = workloads.make_inputs(one, seed=0)
+    g = g.double().numpy()
+    w = w.double().numpy()
+    cs = max(1, min(planes_per_step, wl.Ci))
+    ws = [np.ascontiguousarray(w[:, (k * cs) % wl.Ci:(k * cs) % wl.Ci + cs])
+          for k in range(max(1, wl.Ci // cs))]
+    ws = [x for x in ws if x.shape[1] == cs] or [np.ascontiguousarray(w[:, :cs])]
+    threads = 0
+    for i in range(warmup):
+        oracle.dgrad(g, ws[i % len(ws)], wl.H, wl.W, wl.stride, wl.padding_h, wl.padding_w)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        _, threads = oracle.dgrad(g, ws[i % len(ws)], wl.H, wl.W, wl.stride, wl.padding_h,
+                                  wl.padding_w, return_threads=True)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * wl.Co * wl.OH * wl.OW * cs * wl.kH * wl.kW * steps
+    return flops, dt, threads, cs
+
+
+def cpu_baseline(wl, budget_s: float = 12.0):
+    """The oracle as it stands on the host cores: whole images, repeated for ~budget_s."""
+    flops1, dt1, threads, _ = oracle_sample(wl, wl.Ci, 1, 0)
+    reps = max(1, min(int(budget_s / max(dt1, 1e-3)), 200))
+    flops, dt, threads, _ = oracle_sample(wl, wl.Ci, reps, 0)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{reps} x one image (all {wl.Ci} input channels) of the {wl.name} "
+                      f"workload, {dt:.1f} s of CPU time"}
+
+
+def run_reference(args, wl, key):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    # Size each step so the whole run stays within about two minutes.
+    probe_flops, probe_dt, _, _ = oracle_sample(wl, 16, 1, 0)
+    per_plane = probe_dt / 16.0
+    total_budget = 90.0
+    planes = int(total_budget / max(1, args.steps + args.warmup) / max(per_plane, 1e-6))
+    planes = max(1, min(planes, wl.Ci))
+    flops, dt, threads, cs = oracle_sample(wl, planes, args.steps, args.warmup)
+    value = flops / dt / 1e12
+    sample = (f"each step: one image x {cs} of {wl.Ci} input channels of the {wl.name} workload "
+              f"(double-precision direct loop)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, same recipe as the GPU arm)",
+        "config": workload_config(wl, key, l2_note="CPU oracle"),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl, key, l2_note):
+    return {"workload": f"{wl.name}: N={wl.N} Ci={wl.Ci} Co={wl.Co} H=W={wl.H} "
+                        f"k={wl.kH}x{wl.kW} s={wl.stride} p={wl.padding_h},{wl.padding_w} "
+                        f"{wl.dtype} in, f32 out",
+            "key": key, "N": wl.N, "Ci": wl.Ci, "Co": wl.Co, "H": wl.H, "W": wl.W,
+            "kernel": [wl.kH, wl.kW], "stride": wl.stride,
+            "padding": [wl.padding_h, wl.padding_w], "out": [wl.OH, wl.OW],
+            "input_dtype": wl.dtype, "l2": l2_note}
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, wl, key):
+    import torch
+    import torch.distributed as dist
+
+    import conv2d_backward_implicit_gb300 as dg
+    from conv2d_backward_implicit_gb300 import workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist_on = world > 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if dist_on:
+        dist.init_process_group("nccl", device_id=dev)
+    dg.library()
+
+    g_cpu, w_cpu = workloads.make_inputs(wl, seed=0)
+    p = dg.params_from_shapes(g_cpu.shape, w_cpu.shape, wl.H, wl.W, wl.stride, wl.padding_h,
+                              wl.padding_w)
+    code = dg.DTYPE_CODE[wl.dtype]
+    kernel = dg.conv2d_grad_input_select_kernel(p, code)
+    ws = dg.conv2d_grad_input_workspace_size(p, code)
+    alg = algorithmic_bytes(wl)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 * 2**20)
+    n_sets = max(2, math.ceil(3 * l2 / alg))
+    sets = []
+    for _ in range(n_sets):
+        sets.append({"g": g_cpu.to(dev), "w": w_cpu.to(dev),
+                     "out": torch.empty(wl.grad_in_shape, device=dev, dtype=torch.float32),
+                     "packed": torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)})
+    stream = torch.cuda.Stream(dev)
+
+    def step(i, st, ev=None):
+        s = sets[i % n_sets]
+        if kernel == dg.DGRAD_KERNEL_TC:
+            dg.conv2d_grad_input_pack_weight(s["w"], s["packed"], ws, p, code, st)
+            if ev is not None:
+                ev[0].record(st)
+            dg.conv2d_grad_input_prepacked(s["g"], s["packed"], s["out"], p, code, st)
+        else:
+            if ev is not None:
+                ev[0].record(st)
+            dg.conv2d_grad_input_prepacked(s["g"], s["w"], s["out"], p, code, st)
+        if ev is not None:
+            ev[1].record(st)
+
+    launches_per_step = 2 if kernel == dg.DGRAD_KERNEL_TC else 1
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i, stream)
+    stream.synchronize()
+    rc = dg.conv2d_grad_input_check_errors(stream)
+    if rc != 0:
+        raise RuntimeError(f"warm-up failed: {dg.conv2d_grad_input_status_string(rc)}")
+
+    # One graph = one step per buffer set, an external event pair around each dgrad launch.
+    graph = torch.cuda.CUDAGraph()
+    try:
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n_sets)]
+        per_launch_events = True
+    except TypeError:
+        evs = [None] * n_sets
+        per_launch_events = False
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(n_sets):
+            step(i, stream, evs[i])
+    for _ in range(3):
+        graph.replay()
+    stream.synchronize()
+
+    K = args.steps
+    reps, rest = divmod(K, n_sets)
+    gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local] \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else str(local)
+    uuid = getattr(props, "uuid", None)
+    if uuid is not None:
+        gpu_id = "GPU-" + str(uuid) if not str(uuid).startswith("GPU-") else str(uuid)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist_on:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        for i in range(rest):
+            step(i, stream)
+        t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    if dist_on:
+        dist.barrier()
+    sampler.mark(wall0, wall1)
+    time.sleep(0.15)
+    sampler.stop()
+    rc = dg.conv2d_grad_input_check_errors(stream)
+    if rc != 0:
+        raise RuntimeError(f"timed region failed: {dg.conv2d_grad_input_status_string(rc)}")
+    local_ms = t_start.elapsed_time(t_end)
+    max_ms = reduce_max(local_ms, dist_on, dev)
+    flops = useful_flops(wl)
+    value = aggregate_throughput(flops, K, world, max_ms)
+
+    # Per-launch dgrad kernel time: the event pairs of the last graph replay (or,
+    # without graph-capturable events, eager launches queued behind a sleep kernel).
+    if per_launch_events and reps > 0:
+        kernel_ms = [a.elapsed_time(b) for a, b in evs]
+    else:
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(n_sets)]
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(50_000_000)
+            for i in range(n_sets):
+                step(i, stream, pairs[i])
+        stream.synchronize()
+        kernel_ms = [a.elapsed_time(b) for a, b in pairs]
+    k_ms = statistics.mean(kernel_ms)
+
+    # End to end through the public one-call API with pinned host buffers.
+    g_host = g_cpu.pin_memory()
+    w_host = w_cpu.pin_memory()
+    out_host = torch.empty(wl.grad_in_shape, dtype=torch.float32).pin_memory()
+    gd, wd = sets[0]["g"], sets[0]["w"]
+    od = sets[0]["out"]
+    Ke = max(3, min(K, 200))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for it in range(Ke + 3):
+            if it == 3:
+                e0.record(stream)
+            gd.copy_(g_host, non_blocking=True)
+            wd.copy_(w_host, non_blocking=True)
+            dg.conv2d_grad_input(gd, wd, od, p, code, stream)
+            out_host.copy_(od, non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    rc = dg.conv2d_grad_input_check_errors(stream)
+    if rc != 0:
+        raise RuntimeError(f"e2e failed: {dg.conv2d_grad_input_status_string(rc)}")
+    e2e_ms = reduce_max(e0.elapsed_time(e1), dist_on, dev)
+    e2e_value = aggregate_throughput(flops, Ke, world, e2e_ms)
+
+    peaks, peak_src = load_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    # fp32 inputs run on TF32 tensor cores: nominal TF32 rate is half the bf16 rate.
+    tc_peak = bf16_peak / 2 if wl.dtype == "f32" else bf16_peak
+    achieved_gbs = alg / (k_ms * 1e-3) / 1e9
+    achieved_tflops = flops / (k_ms * 1e-3) / 1e12
+    traffic = recorded_traffic(key)
+    out = None
+    if rank == 0:
+        clocks = sampler.summary()
+        out = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": max_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": {"bf16": "bf16", "f16": "f16", "f32": "tf32"}[wl.dtype] + " in, f32 accumulate/out",
+            "data": "synthetic (seeded torch.Generator, recipe of the workload)",
+            "config": workload_config(
+                wl, key, l2_note=f"rotating {n_sets} buffer sets of {alg / 1e6:.1f} MB "
+                                 f"({n_sets * alg / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)"),
+            "kernel": {1: "tcgen05", 2: "cuda-core"}.get(kernel, str(kernel)),
+            "gpu_launches": K * launches_per_step,
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": achieved_gbs / hbm_peak,
+                         "traffic": traffic, "kernel_ms": k_ms,
+                         "algorithmic_bytes": alg, "peak_source": peak_src,
+                         "per_launch_events": "graph" if per_launch_events else "eager"},
+            "tensor_roofline": {"achieved": achieved_tflops, "peak": tc_peak, "unit": "TFLOP/s",
+                                "frac": achieved_tflops / tc_peak, "peak_source": peak_src},
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": g_cpu.numel() * g_cpu.element_size()
+                    + w_cpu.numel() * w_cpu.element_size(),
+                    "d2h_bytes_per_step": out_host.numel() * 4, "steps": Ke},
+            "clocks": clocks,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(wl)
+        print(json.dumps(out), flush=True)
+    if dist_on:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="resnet",
+                    choices=["tiny", "resnet", "strided", "pointwise", "stem"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    from conv2d_backward_implicit_gb300 import workloads
+    wl = workloads.BY_KEY[args.config]
+    if args.impl == "reference":
+        args.steps = 10 if args.steps is None else args.steps
+        args.warmup = 1 if args.warmup is None else args.warmup
+        return run_reference(args, wl, args.config)
+    args.steps = 60000 if args.steps is None else args.steps
+    args.warmup = 100 if args.warmup is None else args.warmup
+    if args.warmup < 3:
+        args.warmup = 3
+    return run_gpu(args, wl, args.config)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

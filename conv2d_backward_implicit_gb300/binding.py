@@ -1,0 +1,169 @@
+"""ctypes binding for the C ABI in include/conv2d_grad_input.h (argument marshalling only).
+
+Every function here has the name of the C entry point it calls, accepts torch
+tensors (or raw integer addresses) for the buffers, and raises
+:class:`DgradError` when the C call returns a non-zero status.  No part of the
+computation runs in Python, and there is no fallback: if the library has not
+been built, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build_ext
+
+DGRAD_F32, DGRAD_BF16, DGRAD_F16 = 0, 1, 2
+DGRAD_KERNEL_AUTO, DGRAD_KERNEL_TC, DGRAD_KERNEL_SIMT = 0, 1, 2
+DGRAD_DEBUG_SKIP_ARRIVE = 1
+STATUS = {
+    0: "DGRAD_OK", 1: "DGRAD_ERR_INVALID_ARG", 2: "DGRAD_ERR_SHAPE", 3: "DGRAD_ERR_ALIGNMENT",
+    4: "DGRAD_ERR_UNSUPPORTED", 5: "DGRAD_ERR_CUDA", 6: "DGRAD_ERR_TIMEOUT",
+    7: "DGRAD_ERR_WORKSPACE",
+}
+DTYPE_CODE = {"f32": DGRAD_F32, "bf16": DGRAD_BF16, "f16": DGRAD_F16}
+
+PARAM_FIELDS = ("batch", "in_channels", "in_h", "in_w", "out_channels", "kernel_h", "kernel_w",
+                "stride", "padding_h", "out_h", "out_w", "padding_w")
+
+
+class Params(ctypes.Structure):
+    """conv2d_grad_input_params: twelve uint32 fields in the header's order."""
+    _fields_ = [(name, ctypes.c_uint32) for name in PARAM_FIELDS]
+
+    def as_dict(self):
+        return {k: int(getattr(self, k)) for k in PARAM_FIELDS}
+
+
+class DgradError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+def params_from_shapes(grad_out_shape, weight_shape, in_h: int, in_w: int, stride: int,
+                       padding_h: int, padding_w: int) -> Params:
+    """Fill Params from tensor shapes: grad_out [N,Co,OH,OW], weight [Co,Ci,kH,kW]."""
+    N, Co, OH, OW = (int(v) for v in grad_out_shape)
+    Co2, Ci, kH, kW = (int(v) for v in weight_shape)
+    if Co != Co2:
+        raise ValueError("grad_out and weight disagree on out_channels")
+    return Params(N, Ci, in_h, in_w, Co, kH, kW, stride, padding_h, OH, OW, padding_w)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return build_ext.LIB_PATH
+
+
+def library() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"CUDA library {path} is missing: build it with __graft_entry__.build() "
+                    "(or python -m conv2d_backward_implicit_gb300.build_ext); there is no fallback")
+            lib = ctypes.CDLL(path)
+            P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            PP = ctypes.POINTER(Params)
+            lib.conv2d_grad_input.argtypes = [P, P, P, PP, I, P]
+            lib.conv2d_grad_input.restype = I
+            lib.conv2d_grad_input_workspace_size.argtypes = [PP, I]
+            lib.conv2d_grad_input_workspace_size.restype = S
+            lib.conv2d_grad_input_pack_weight.argtypes = [P, P, S, PP, I, P]
+            lib.conv2d_grad_input_pack_weight.restype = I
+            lib.conv2d_grad_input_prepacked.argtypes = [P, P, P, PP, I, P]
+            lib.conv2d_grad_input_prepacked.restype = I
+            lib.conv2d_grad_input_check_errors.argtypes = [P]
+            lib.conv2d_grad_input_check_errors.restype = I
+            lib.conv2d_grad_input_status_string.argtypes = [I]
+            lib.conv2d_grad_input_status_string.restype = ctypes.c_char_p
+            lib.conv2d_grad_input_select_kernel.argtypes = [PP, I]
+            lib.conv2d_grad_input_select_kernel.restype = I
+            lib.conv2d_grad_input_set_kernel.argtypes = [I]
+            lib.conv2d_grad_input_set_kernel.restype = I
+            lib.conv2d_grad_input_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+            lib.conv2d_grad_input_set_wait_limit_ns.restype = ctypes.c_uint64
+            lib.conv2d_grad_input_set_debug.argtypes = [I]
+            lib.conv2d_grad_input_set_debug.restype = I
+            _lib = lib
+    return _lib
+
+
+def _addr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str) -> int:
+    if rc != 0:
+        raise DgradError(rc, where)
+    return rc
+
+
+def conv2d_grad_input(grad_out, weight, grad_in, params: Params, dtype: int, stream=None) -> None:
+    rc = library().conv2d_grad_input(_addr(grad_out), _addr(weight), _addr(grad_in),
+                                     ctypes.byref(params), int(dtype), _stream(stream))
+    _check(rc, "conv2d_grad_input")
+
+
+def conv2d_grad_input_workspace_size(params: Params, dtype: int) -> int:
+    return int(library().conv2d_grad_input_workspace_size(ctypes.byref(params), int(dtype)))
+
+
+def conv2d_grad_input_pack_weight(weight, packed, packed_bytes: int, params: Params, dtype: int,
+                                  stream=None) -> None:
+    rc = library().conv2d_grad_input_pack_weight(_addr(weight), _addr(packed), int(packed_bytes),
+                                                 ctypes.byref(params), int(dtype), _stream(stream))
+    _check(rc, "conv2d_grad_input_pack_weight")
+
+
+def conv2d_grad_input_prepacked(grad_out, packed, grad_in, params: Params, dtype: int,
+                                stream=None) -> None:
+    rc = library().conv2d_grad_input_prepacked(_addr(grad_out), _addr(packed), _addr(grad_in),
+                                               ctypes.byref(params), int(dtype), _stream(stream))
+    _check(rc, "conv2d_grad_input_prepacked")
+
+
+def conv2d_grad_input_check_errors(stream=None) -> int:
+    """Returns the status (0, DGRAD_ERR_TIMEOUT = 6 or DGRAD_ERR_CUDA = 5) without raising."""
+    return int(library().conv2d_grad_input_check_errors(_stream(stream)))
+
+
+def conv2d_grad_input_status_string(status: int) -> str:
+    return library().conv2d_grad_input_status_string(int(status)).decode()
+
+
+def conv2d_grad_input_select_kernel(params: Params, dtype: int) -> int:
+    """DGRAD_KERNEL_TC (1) or DGRAD_KERNEL_SIMT (2), or a negative status."""
+    return int(library().conv2d_grad_input_select_kernel(ctypes.byref(params), int(dtype)))
+
+
+def conv2d_grad_input_set_kernel(kernel: int) -> int:
+    return int(library().conv2d_grad_input_set_kernel(int(kernel)))
+
+
+def conv2d_grad_input_set_wait_limit_ns(ns: int) -> int:
+    return int(library().conv2d_grad_input_set_wait_limit_ns(int(ns)))
+
+
+def conv2d_grad_input_set_debug(flags: int) -> int:
+    return int(library().conv2d_grad_input_set_debug(int(flags)))

@@ -1,0 +1,154 @@
+// api.cu -- the extern "C" entry points declared in include/conv2d_grad_input.h.
+//
+// Argument checks happen on the host before anything is enqueued; nothing
+// here aborts, throws across the ABI or leaves a CUDA error pending.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "conv2d_grad_input.h"
+#include "dgrad_internal.h"
+
+namespace {
+
+std::atomic<int> g_kernel_choice{DGRAD_KERNEL_AUTO};
+std::atomic<int> g_debug_flags{0};
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
+
+int cuda_status(int err) {
+    if (err == (int)cudaSuccess) return DGRAD_OK;
+    (void)cudaGetLastError();  // do not leave a (non-sticky) error for the caller
+    return DGRAD_ERR_CUDA;
+}
+
+bool aligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+int plan_for(const conv2d_grad_input_params *p, int dtype, dgrad::Plan *plan) {
+    int rc = dgrad::make_plan(p, dtype, g_kernel_choice.load(), plan);
+    if (rc != DGRAD_OK) return rc;
+    plan->tc.debug_flags = g_debug_flags.load();
+    plan->tc.wait_limit_ns = g_wait_limit_ns.load();
+    return DGRAD_OK;
+}
+
+int run_main(const dgrad::Plan &plan, const void *grad_out, const void *packed_or_weight,
+             float *grad_in, cudaStream_t stream) {
+    if (plan.kernel == DGRAD_KERNEL_SIMT)
+        return cuda_status(dgrad::launch_simt(plan, grad_out, packed_or_weight, grad_in, stream));
+    return cuda_status(dgrad::launch_tc(plan, grad_out, packed_or_weight, grad_in, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int conv2d_grad_input(const void *grad_out, const void *weight, float *grad_in,
+                      const conv2d_grad_input_params *p, int dtype, struct CUstream_st *stream) {
+    if (!grad_out || !weight || !grad_in || !p) return DGRAD_ERR_INVALID_ARG;
+    dgrad::Plan plan;
+    int rc = plan_for(p, dtype, &plan);
+    if (rc != DGRAD_OK) return rc;
+    if (!aligned(grad_out, plan.esize) || !aligned(weight, plan.esize) || !aligned(grad_in, 4))
+        return DGRAD_ERR_ALIGNMENT;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (plan.kernel == DGRAD_KERNEL_SIMT) return run_main(plan, grad_out, weight, grad_in, st);
+
+    void *ws = nullptr;
+    if (plan.workspace > 0) {
+        cudaError_t e = cudaMallocAsync(&ws, plan.workspace, st);
+        if (e != cudaSuccess) return cuda_status((int)e);
+        int le = dgrad::launch_pack(plan, weight, ws, st);
+        if (le != (int)cudaSuccess) {
+            (void)cudaFreeAsync(ws, st);
+            return cuda_status(le);
+        }
+    }
+    rc = run_main(plan, grad_out, ws, grad_in, st);
+    if (ws) {
+        cudaError_t e = cudaFreeAsync(ws, st);
+        if (rc == DGRAD_OK && e != cudaSuccess) rc = cuda_status((int)e);
+    }
+    return rc;
+}
+
+size_t conv2d_grad_input_workspace_size(const conv2d_grad_input_params *p, int dtype) {
+    if (!p) return 0;
+    dgrad::Plan plan;
+    if (plan_for(p, dtype, &plan) != DGRAD_OK) return 0;
+    return plan.kernel == DGRAD_KERNEL_TC ? plan.workspace : 0;
+}
+
+int conv2d_grad_input_pack_weight(const void *weight, void *packed, size_t packed_bytes,
+                                  const conv2d_grad_input_params *p, int dtype,
+                                  struct CUstream_st *stream) {
+    if (!weight || !p) return DGRAD_ERR_INVALID_ARG;
+    dgrad::Plan plan;
+    int rc = plan_for(p, dtype, &plan);
+    if (rc != DGRAD_OK) return rc;
+    if (plan.kernel != DGRAD_KERNEL_TC || plan.workspace == 0) return DGRAD_OK;  // nothing to pack
+    if (!packed) return DGRAD_ERR_INVALID_ARG;
+    if (packed_bytes < plan.workspace) return DGRAD_ERR_WORKSPACE;
+    if (!aligned(weight, plan.esize) || !aligned(packed, 16)) return DGRAD_ERR_ALIGNMENT;
+    return cuda_status(dgrad::launch_pack(plan, weight, packed, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int conv2d_grad_input_prepacked(const void *grad_out, const void *packed, float *grad_in,
+                                const conv2d_grad_input_params *p, int dtype,
+                                struct CUstream_st *stream) {
+    if (!grad_out || !grad_in || !p) return DGRAD_ERR_INVALID_ARG;
+    dgrad::Plan plan;
+    int rc = plan_for(p, dtype, &plan);
+    if (rc != DGRAD_OK) return rc;
+    if (!packed && (plan.kernel == DGRAD_KERNEL_SIMT || plan.workspace > 0))
+        return DGRAD_ERR_INVALID_ARG;
+    const uintptr_t pa = plan.kernel == DGRAD_KERNEL_TC ? 16 : (uintptr_t)plan.esize;
+    if (!aligned(grad_out, plan.esize) || !aligned(grad_in, 4) || (packed && !aligned(packed, pa)))
+        return DGRAD_ERR_ALIGNMENT;
+    return run_main(plan, grad_out, packed, grad_in, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int conv2d_grad_input_check_errors(struct CUstream_st *stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_status((int)e);
+    unsigned int flag = 0;
+    int le = dgrad::tc_read_and_clear_error(&flag);
+    if (le != (int)cudaSuccess) return cuda_status(le);
+    return flag ? DGRAD_ERR_TIMEOUT : DGRAD_OK;
+}
+
+const char *conv2d_grad_input_status_string(int status) {
+    switch (status) {
+    case DGRAD_OK: return "ok";
+    case DGRAD_ERR_INVALID_ARG: return "invalid argument";
+    case DGRAD_ERR_SHAPE: return "invalid or inconsistent shape";
+    case DGRAD_ERR_ALIGNMENT: return "misaligned pointer";
+    case DGRAD_ERR_UNSUPPORTED: return "unsupported size or kernel choice";
+    case DGRAD_ERR_CUDA: return "CUDA runtime error";
+    case DGRAD_ERR_TIMEOUT: return "device wait timed out";
+    case DGRAD_ERR_WORKSPACE: return "packed-weight buffer too small";
+    default: return "unknown status";
+    }
+}
+
+int conv2d_grad_input_select_kernel(const conv2d_grad_input_params *p, int dtype) {
+    if (!p) return -DGRAD_ERR_INVALID_ARG;
+    dgrad::Plan plan;
+    int rc = plan_for(p, dtype, &plan);
+    return rc == DGRAD_OK ? plan.kernel : -rc;
+}
+
+int conv2d_grad_input_set_kernel(int kernel) {
+    if (kernel != DGRAD_KERNEL_AUTO && kernel != DGRAD_KERNEL_TC && kernel != DGRAD_KERNEL_SIMT)
+        return -DGRAD_ERR_INVALID_ARG;
+    return g_kernel_choice.exchange(kernel);
+}
+
+uint64_t conv2d_grad_input_set_wait_limit_ns(uint64_t ns) {
+    return g_wait_limit_ns.exchange(ns ? ns : kDefaultWaitNs);
+}
+
+int conv2d_grad_input_set_debug(int flags) { return g_debug_flags.exchange(flags); }
+
+}  // extern "C"

@@ -1,0 +1,114 @@
+// dgrad_internal.h -- plan and kernel-parameter structures shared by the host
+// planner (plan.cu / api.cu) and the kernels (pack.cu, dgrad_tc.cu,
+// dgrad_simt.cu).  Not part of the public ABI.
+//
+// The sub-pixel phase split.  For stride s, grad_in pixel (ih, iw) belongs to
+// phase (rh, rw) = (ih mod s, iw mod s) and sits at (a, b) = (ih div s, iw div
+// s) of that phase's grid.  Following the divisibility test of the page's
+// strided staging branch (conv2d_grad_input_gemm_coop.wgsl), tap kh reaches
+// ih iff ih + ph - kh = s*oh.  Writing th = (rh + ph) mod s and qh = (rh + ph)
+// div s, the taps of the phase are kh = s*j + th for j < Jh = ceil((kH - th) /
+// s), and they read oh = a + qh - j.  So every phase is a dense stride-1
+// correlation over the grad_out grid with its own (Jh x Jw) sub-kernel: no
+// structural-zero products are ever issued.  Stride 1 is the single phase
+// th = ph mod 1 = 0, qh = ph, Jh = kH.
+//
+// The frame.  Each phase's output positions are laid out in a linear space
+// Lambda of pitch X = Wr + Jw - 1 and R = Hr + Jh - 1 rows per image; output
+// (n, a, b) sits at Lambda = (n*R + a)*X + b.  The grad_out value that tap
+// (j, i) needs for that output sits at Lambda + (Jh-1-j)*X + (Jw-1-i), where
+// frame element (rho, kappa) of image n holds grad_out[n, rho-(Jh-1)+qh,
+// kappa-(Jw-1)+qw] (zero outside the grad_out grid).  A tile of 128
+// consecutive outputs therefore needs one contiguous window of
+// 128 + (Jh-1)*X + Jw-1 frame elements, and each tap is the same window seen
+// from a different start: the tap loop runs backwards over the frame, which is
+// the kernel flip of the forward-style correlation.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace dgrad {
+
+constexpr int kMaxPhases = 16;  // stride <= 4
+constexpr int kTileM = 128;     // outputs per tile (tcgen05 M)
+constexpr int kEpiWarps = 4;    // warps 0..3: TMEM -> global epilogue
+constexpr int kMmaWarp = 4;     // warp 4: TMEM alloc + MMA issue
+constexpr int kBWarp = 5;       // warp 5: packed-weight bulk copies
+constexpr int kAWarp0 = 6;      // warps 6..: grad_out gather
+constexpr int kAWarps = 4;
+constexpr int kThreads = 32 * (kAWarp0 + kAWarps);
+constexpr int kSmemLimit = 232448;  // 227 KB dynamic shared memory per block
+constexpr int kBarrierBytes = 1024;
+
+struct PhaseDesc {
+    int rh, rw;         // residues of (ih, iw) modulo the stride
+    int Hr, Wr;         // grad_in pixels of this phase per image (rows, columns)
+    int Jh, Jw;         // taps per axis (0: no tap reaches this phase)
+    int th, tw;         // kh = s*j + th, kw = s*i + tw
+    int qh, qw;         // oh = a + qh - j, ow = b + qw - i
+    int X, R;           // frame pitch and frame rows per image
+    int m_tiles;        // 128-output tiles of this phase
+    int hb;             // frame elements one tile needs
+    int64_t tile_begin; // first global tile of this phase (m-tiles x n-tiles)
+    int64_t pack_off;   // byte offset of this phase's packed weights
+};
+
+struct TcParams {
+    const void *grad_out;
+    const void *packed;
+    float *grad_in;
+    int N, Ci, H, W, Co, OH, OW, stride;
+    int n_phases;
+    int n_ntiles, n_tile;   // tiles over Ci and columns per tile (MMA N)
+    int kc, n_cchunks;      // grad_out channels per stage, stages per tile
+    int hbp;                // frame elements per A stage (multiple of 8)
+    int a_stage_bytes, b_stage_bytes;
+    int b_unit_bytes;       // one tap x one channel chunk of packed weights
+    int na, nb;             // ring depths; nb == 0: all packed weights resident
+    int64_t packed_bytes;
+    int64_t total_tiles;
+    uint32_t idesc;         // tcgen05 instruction descriptor
+    uint32_t tmem_cols;
+    int smem_bytes;
+    int debug_flags;
+    uint64_t wait_limit_ns;
+    PhaseDesc ph[kMaxPhases];
+};
+
+struct PackParams {
+    int Ci, Co, kH, kW, stride;
+    int n_tile, n_ntiles, kc, n_cchunks, elems16;  // elems16: elements per 16 bytes
+    int n_phases;
+    int64_t total_elems;
+    int64_t elem_begin[kMaxPhases + 1];
+    int th[kMaxPhases], tw[kMaxPhases], Jh[kMaxPhases], Jw[kMaxPhases];
+};
+
+struct SimtParams {
+    int N, Ci, H, W, Co, kH, kW, stride, ph, pw, OH, OW;
+};
+
+// A complete host-side plan for one (params, dtype) pair.
+struct Plan {
+    int dtype;
+    int esize;
+    int kernel;          // DGRAD_KERNEL_TC or DGRAD_KERNEL_SIMT
+    TcParams tc;         // valid when kernel == TC
+    PackParams pack;     // valid when kernel == TC
+    SimtParams simt;
+    size_t workspace;    // packed-weight bytes (TC), 0 otherwise
+};
+
+// plan.cu: validation + planning.  Returns a dgrad_status.
+int make_plan(const void *params, int dtype, int forced_kernel, Plan *out);
+
+// Launchers (return cudaError_t as int).
+int launch_pack(const Plan &plan, const void *weight, void *packed, void *stream);
+int launch_tc(const Plan &plan, const void *grad_out, const void *packed, float *grad_in,
+              void *stream);
+int launch_simt(const Plan &plan, const void *grad_out, const void *weight, float *grad_in,
+                void *stream);
+int tc_read_and_clear_error(unsigned int *out);  // cudaError_t
+
+}  // namespace dgrad

@@ -1,0 +1,87 @@
+// pack.cu -- the weight pre-pack kernel.
+//
+// The page's shader (conv2d_grad_input_gemm_coop.wgsl, weight staging of the
+// A tiles) re-gathers A[ci, k] = weight[co, ci, kh, kw] with K ordered
+// (co, kh, kw) for every output tile and every batch item.  Here that gather
+// runs once per call and writes the exact shared-memory image the
+// tensor-core kernel consumes, so the kernel moves it with plain bulk copies:
+//
+//   for each phase (rh, rw) with taps kh = s*j + th, kw = s*i + tw,
+//     for each Ci tile nt, grad_out channel chunk cc, tap j, tap i:
+//       [kc/E sixteen-byte chunks][n_tile rows = ci][E elements = co]
+//
+// i.e. K-major [Ci, K] core matrices of 8 rows x 16 bytes (no swizzle), with
+// zeros for ci >= Ci and co >= Co.  E = 16 / element size.  For float32 input
+// the values are rounded to TF32 (nearest, ties away from zero), the operand
+// precision of kind::tf32.
+#include <cuda_runtime.h>
+
+#include "conv2d_grad_input.h"
+#include "dgrad_internal.h"
+
+namespace dgrad {
+namespace {
+
+__device__ __forceinline__ uint32_t to_tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) pack_weight_kernel(const T *__restrict__ w,
+                                                          T *__restrict__ out,
+                                                          const __grid_constant__ PackParams k) {
+    const int64_t stride_all = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < k.total_elems;
+         idx += stride_all) {
+        int ph = 0;
+        while (ph + 1 < k.n_phases && idx >= k.elem_begin[ph + 1]) ++ph;
+        int64_t r = idx - k.elem_begin[ph];
+        const int E = k.elems16;
+        const int chunks = k.kc / E;
+        const int e = (int)(r % E); r /= E;
+        const int row = (int)(r % k.n_tile); r /= k.n_tile;
+        const int kcg = (int)(r % chunks); r /= chunks;
+        const int i = (int)(r % k.Jw[ph]); r /= k.Jw[ph];
+        const int j = (int)(r % k.Jh[ph]); r /= k.Jh[ph];
+        const int cc = (int)(r % k.n_cchunks); r /= k.n_cchunks;
+        const int nt = (int)r;
+        const int co = cc * k.kc + kcg * E + e;
+        const int ci = nt * k.n_tile + row;
+        const int kh = k.stride * j + k.th[ph];
+        const int kw = k.stride * i + k.tw[ph];
+        T v;
+        if (co < k.Co && ci < k.Ci) {
+            v = w[(((int64_t)co * k.Ci + ci) * k.kH + kh) * k.kW + kw];
+        } else {
+            v = T(0);
+        }
+        if constexpr (sizeof(T) == 4) {
+            out[idx] = __uint_as_float(to_tf32_rna(v));
+        } else {
+            out[idx] = v;
+        }
+    }
+}
+
+}  // namespace
+
+int launch_pack(const Plan &plan, const void *weight, void *packed, void *stream) {
+    const PackParams &k = plan.pack;
+    if (k.total_elems == 0) return (int)cudaSuccess;
+    const int threads = 256;
+    int64_t blocks = (k.total_elems + threads - 1) / threads;
+    if (blocks > 4096) blocks = 4096;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (plan.esize == 4) {
+        pack_weight_kernel<float><<<(int)blocks, threads, 0, st>>>(
+            static_cast<const float *>(weight), static_cast<float *>(packed), k);
+    } else {
+        pack_weight_kernel<unsigned short><<<(int)blocks, threads, 0, st>>>(
+            static_cast<const unsigned short *>(weight), static_cast<unsigned short *>(packed), k);
+    }
+    return (int)cudaGetLastError();
+}
+
+}  // namespace dgrad

@@ -1,0 +1,114 @@
+"""The C-ABI library on the host: it loads, exports every declared symbol, and
+rejects bad arguments before any device work (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import conv2d_backward_implicit_gb300 as dg
+from conv2d_backward_implicit_gb300 import build_ext, workloads
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "conv2d_grad_input.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if build_ext.is_stale():
+        build_ext.build()
+    return dg.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(conv2d_grad_input\w*)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for must in ("conv2d_grad_input", "conv2d_grad_input_workspace_size",
+                 "conv2d_grad_input_pack_weight", "conv2d_grad_input_prepacked",
+                 "conv2d_grad_input_check_errors", "conv2d_grad_input_status_string"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def params(wl):
+    return dg.Params(wl.N, wl.Ci, wl.H, wl.W, wl.Co, wl.kH, wl.kW, wl.stride, wl.padding_h,
+                     wl.OH, wl.OW, wl.padding_w)
+
+
+def test_workloads_select_tensor_cores(lib):
+    for wl in workloads.ALL:
+        assert dg.conv2d_grad_input_select_kernel(params(wl), dg.DTYPE_CODE[wl.dtype]) == \
+            dg.DGRAD_KERNEL_TC, wl.name
+
+
+def test_workspace_sizes_closed_form(lib):
+    # Packed weights hold each (tap, co, ci) product once, Ci padded to a multiple of 16:
+    # 9 taps x 64 x 64 bf16; 9 taps (over 4 phases) x 256 x 128 bf16; 1024 x 256 fp16;
+    # 49 taps (9+12+12+16 over 4 phases) x 64 x 16 fp32; 9 x 16 x 16 fp32.
+    want = {"resnet": 9 * 64 * 64 * 2, "strided": 9 * 256 * 128 * 2, "pointwise": 1024 * 256 * 2,
+            "stem": 49 * 64 * 16 * 4, "tiny": 9 * 16 * 16 * 4}
+    for key, nbytes in want.items():
+        wl = workloads.BY_KEY[key]
+        assert dg.conv2d_grad_input_workspace_size(params(wl), dg.DTYPE_CODE[wl.dtype]) == nbytes
+
+
+def test_shape_validation(lib):
+    wl = workloads.RESNET
+    p = params(wl)
+    code = dg.DGRAD_BF16
+    for field, value, status in [("out_h", 55, 2), ("out_w", 57, 2), ("batch", 0, 2),
+                                 ("stride", 0, 2), ("kernel_h", 0, 2), ("in_channels", 0, 2),
+                                 ("kernel_w", 60, 2), ("padding_h", 2, 2)]:
+        q = dg.Params(*[getattr(p, f) for f in dg.PARAM_FIELDS])
+        setattr(q, field, value)
+        assert dg.conv2d_grad_input_select_kernel(q, code) == -status, field
+        assert dg.conv2d_grad_input_workspace_size(q, code) == 0
+    assert dg.conv2d_grad_input_select_kernel(p, 9) == -1
+    huge = dg.Params(*[getattr(p, f) for f in dg.PARAM_FIELDS])
+    huge.batch = 1 << 30
+    assert dg.conv2d_grad_input_select_kernel(huge, code) == -4
+
+
+def test_null_and_bad_arguments_fail_on_the_host(lib):
+    p = params(workloads.TINY)
+    assert lib.conv2d_grad_input(None, None, None, ctypes.byref(p), 0, None) == 1
+    bad = params(workloads.TINY)
+    bad.out_w = 3
+    # Valid-looking (never dereferenced) addresses: validation rejects before any CUDA call.
+    assert lib.conv2d_grad_input(16, 16, 16, ctypes.byref(bad), 0, None) == 2
+    assert lib.conv2d_grad_input(16, 16, 16, ctypes.byref(p), 7, None) == 1
+    assert lib.conv2d_grad_input(18, 16, 16, ctypes.byref(p), 0, None) == 3
+    assert lib.conv2d_grad_input_prepacked(16, None, 16, ctypes.byref(p), 0, None) == 1
+    assert lib.conv2d_grad_input_pack_weight(16, 16, 8, ctypes.byref(p), 0, None) == 7
+
+
+def test_status_strings_and_settings(lib):
+    assert dg.conv2d_grad_input_status_string(0) == "ok"
+    assert dg.conv2d_grad_input_status_string(6) == "device wait timed out"
+    assert dg.conv2d_grad_input_status_string(99) == "unknown status"
+    prev = dg.conv2d_grad_input_set_kernel(dg.DGRAD_KERNEL_SIMT)
+    assert prev == dg.DGRAD_KERNEL_AUTO
+    assert dg.conv2d_grad_input_select_kernel(params(workloads.RESNET), 1) == dg.DGRAD_KERNEL_SIMT
+    assert dg.conv2d_grad_input_workspace_size(params(workloads.RESNET), 1) == 0
+    assert dg.conv2d_grad_input_set_kernel(dg.DGRAD_KERNEL_AUTO) == dg.DGRAD_KERNEL_SIMT
+    assert dg.conv2d_grad_input_set_kernel(5) < 0
+    old = dg.conv2d_grad_input_set_wait_limit_ns(1000)
+    assert dg.conv2d_grad_input_set_wait_limit_ns(0) == 1000
+    assert old == 2_000_000_000
+    assert dg.conv2d_grad_input_set_debug(0) == 0
+
+
+def test_stride_above_four_uses_cuda_cores(lib):
+    p = dg.Params(1, 4, 20, 20, 4, 3, 3, 5, 1, 4, 4, 1)
+    assert dg.conv2d_grad_input_select_kernel(p, 0) == dg.DGRAD_KERNEL_SIMT
