@@ -93,6 +93,8 @@ def library() -> ctypes.CDLL:
             lib.conv2d_grad_input_set_wait_limit_ns.restype = ctypes.c_uint64
             lib.conv2d_grad_input_set_debug.argtypes = [I]
             lib.conv2d_grad_input_set_debug.restype = I
+            lib.conv2d_grad_input_noalloc.argtypes = [P, P, P, PP, I, P]
+            lib.conv2d_grad_input_noalloc.restype = I
             _lib = lib
     return _lib
 
@@ -167,3 +169,17 @@ def conv2d_grad_input_set_wait_limit_ns(ns: int) -> int:
 
 def conv2d_grad_input_set_debug(flags: int) -> int:
     return int(library().conv2d_grad_input_set_debug(int(flags)))
+
+
+def conv2d_grad_input_noalloc(grad_out, weight, grad_in, params: Params, dtype: int,
+                              stream=None) -> None:
+    """conv2d_grad_input for callers that cannot allocate device memory.
+
+    The packed weights go to a fixed 8 MiB array inside the library rather
+    than a temporary allocation; calls that could overlap on the GPU must be
+    ordered by the caller, and problems whose packed weights exceed 8 MiB
+    raise DgradError(DGRAD_ERR_WORKSPACE).
+    """
+    rc = library().conv2d_grad_input_noalloc(_addr(grad_out), _addr(weight), _addr(grad_in),
+                                             ctypes.byref(params), int(dtype), _stream(stream))
+    _check(rc, "conv2d_grad_input_noalloc")

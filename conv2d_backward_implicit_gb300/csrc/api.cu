@@ -42,6 +42,12 @@ int run_main(const dgrad::Plan &plan, const void *grad_out, const void *packed_o
 
 }  // namespace
 
+namespace dgrad {
+int plan_with_settings(const void *params, int dtype, Plan *out) {
+    return plan_for(static_cast<const conv2d_grad_input_params *>(params), dtype, out);
+}
+}  // namespace dgrad
+
 extern "C" {
 
 int conv2d_grad_input(const void *grad_out, const void *weight, float *grad_in,

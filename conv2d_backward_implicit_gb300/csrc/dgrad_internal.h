@@ -102,6 +102,8 @@ struct Plan {
 
 // plan.cu: validation + planning.  Returns a dgrad_status.
 int make_plan(const void *params, int dtype, int forced_kernel, Plan *out);
+// api.cu: make_plan with the process-wide kernel choice, debug flags and wait limit.
+int plan_with_settings(const void *params, int dtype, Plan *out);
 
 // Launchers (return cudaError_t as int).
 int launch_pack(const Plan &plan, const void *weight, void *packed, void *stream);

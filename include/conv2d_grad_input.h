@@ -156,6 +156,32 @@ uint64_t conv2d_grad_input_set_wait_limit_ns(uint64_t ns);
 #define DGRAD_DEBUG_SKIP_ARRIVE 1
 int conv2d_grad_input_set_debug(int flags);
 
+/* conv2d_grad_input without any device allocation.  The paper has no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory where they need the gradient -- code recorded into
+ * a CUDA graph whose capture mode forbids allocation calls, runtimes whose
+ * own memory arena owns the device and bans cudaMalloc/cudaMallocAsync on
+ * their execution path, and latency-critical loops that cannot afford an
+ * allocation's synchronisation.  Same arguments, semantics and results as
+ * conv2d_grad_input, but the packed weights live in a fixed 8 MiB device
+ * array inside the library instead of a temporary allocation:
+ *  - every GPU that loads the library holds those 8 MiB until the process
+ *    exits;
+ *  - a problem whose packed weights exceed 8 MiB
+ *    (conv2d_grad_input_workspace_size > 8388608) is rejected with
+ *    DGRAD_ERR_WORKSPACE before anything is enqueued;
+ *  - all calls share the array: calls whose GPU work can overlap (unordered
+ *    streams, concurrent host threads) race on it and must be ordered by
+ *    the caller; nothing from an earlier call needs clearing, since each
+ *    call rewrites every byte its kernel reads;
+ *  - the first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ * Calls no cudaMalloc, cudaFree or other allocating routine. */
+int conv2d_grad_input_noalloc(const void *grad_out, const void *weight, float *grad_in,
+                              const conv2d_grad_input_params *p, int dtype,
+                              struct CUstream_st *stream);
+
 #ifdef __cplusplus
 }
 #endif

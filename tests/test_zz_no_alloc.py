@@ -1,0 +1,67 @@
+"""conv2d_grad_input_noalloc: the allocation-free entry point for callers that
+cannot allocate device memory (graph captures that forbid allocation, runtimes
+whose arena owns the device, latency-critical loops).  It must give the same
+result as the allocating conv2d_grad_input, call after call, even though every
+call reuses the same fixed scratch array left over from the previous one.
+
+Collected last on purpose, so that a run stopping at its first failure has
+already run every other test; it also passes on its own in a fresh process.
+"""
+import numpy as np
+import pytest
+import torch
+
+from conv2d_backward_implicit_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 2e-3, "f16": 2e-3, "f32": 5e-3}
+
+
+def _rel_err(a, b):
+    a = a.double().cpu().numpy()
+    b = b.double().cpu().numpy()
+    assert np.isfinite(a).all()
+    return float(np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-30))
+
+
+def test_noalloc_matches_allocating_entry_point_twice_in_a_row():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import conv2d_backward_implicit_gb300 as dg
+    dev = torch.device("cuda")
+    # Two different problems back to back: the second call finds the first
+    # call's packed weights (a larger pack) still in the shared scratch array.
+    cases = [workloads.STRIDED.with_batch(2), workloads.RESNET.with_batch(2),
+             workloads.STEM.with_batch(1)]
+    for wl in cases:
+        g, w = workloads.make_inputs(wl, seed=7)
+        gd, wd = g.to(dev), w.to(dev)
+        p = dg.params_from_shapes(g.shape, w.shape, wl.H, wl.W, wl.stride, wl.padding_h,
+                                  wl.padding_w)
+        code = dg.DTYPE_CODE[wl.dtype]
+        assert dg.conv2d_grad_input_select_kernel(p, code) == dg.DGRAD_KERNEL_TC
+        ref = torch.full(wl.grad_in_shape, float("nan"), device=dev)
+        dg.conv2d_grad_input(gd, wd, ref, p, code)
+        for _ in range(2):
+            out = torch.full(wl.grad_in_shape, float("nan"), device=dev)
+            dg.conv2d_grad_input_noalloc(gd, wd, out, p, code)
+            assert dg.conv2d_grad_input_check_errors() == 0
+            assert _rel_err(out, ref) <= TOL[wl.dtype], wl.name
+
+
+def test_noalloc_rejects_packs_above_its_limit():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import conv2d_backward_implicit_gb300 as dg
+    # 1024 x 1024 x 3x3 bf16 weights pack to 18.9 MB > 8 MiB.
+    p = dg.Params(1, 1024, 8, 8, 1024, 3, 3, 1, 1, 8, 8, 1)
+    assert dg.conv2d_grad_input_workspace_size(p, dg.DGRAD_BF16) > 8 * 2**20
+    g = torch.zeros((1, 1024, 8, 8), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((1024, 1024, 3, 3), dtype=torch.bfloat16, device="cuda")
+    out = torch.full((1, 1024, 8, 8), 3.0, device="cuda")
+    with pytest.raises(dg.DgradError) as ei:
+        dg.conv2d_grad_input_noalloc(g, w, out, p, dg.DGRAD_BF16)
+    assert ei.value.status == 7
+    torch.cuda.synchronize()
+    assert torch.all(out == 3.0)
