@@ -18,12 +18,19 @@
 // (n, a, b) sits at Lambda = (n*R + a)*X + b.  The grad_out value that tap
 // (j, i) needs for that output sits at Lambda + (Jh-1-j)*X + (Jw-1-i), where
 // frame element (rho, kappa) of image n holds grad_out[n, rho-(Jh-1)+qh,
-// kappa-(Jw-1)+qw] (zero outside the grad_out grid).  A tile of 128
+// kappa-(Jw-1)+qw] (zero outside the grad_out grid).  A tile of kTileP = 256
 // consecutive outputs therefore needs one contiguous window of
-// 128 + (Jh-1)*X + Jw-1 frame elements, and each tap is the same window seen
+// 256 + (Jh-1)*X + Jw-1 frame elements, and each tap is the same window seen
 // from a different start: the tap loop runs backwards over the frame, which is
 // the kernel flip of the forward-style correlation.
+//
+// The GEMM per tile is D[ci, position] += W[ci, co] * G[co, position] for
+// each tap: input channels on the tcgen05 M side (64 or 128 rows), the 256
+// positions on the N side (the tensor cores run at full rate only when N is
+// wide), grad_out channels (128 bytes at a time) on K.
 #pragma once
+
+#include <cuda.h>
 
 #include <cstddef>
 #include <cstdint>
@@ -31,15 +38,18 @@
 namespace dgrad {
 
 constexpr int kMaxPhases = 16;  // stride <= 4
-constexpr int kTileM = 128;     // outputs per tile (tcgen05 M)
+constexpr int kTileP = 256;     // output positions per tile (tcgen05 N); 128 for very wide frames
 constexpr int kEpiWarps = 4;    // warps 0..3: TMEM -> global epilogue
 constexpr int kMmaWarp = 4;     // warp 4: TMEM alloc + MMA issue
-constexpr int kBWarp = 5;       // warp 5: packed-weight bulk copies
-constexpr int kAWarp0 = 6;      // warps 6..: grad_out gather
-constexpr int kAWarps = 4;
-constexpr int kThreads = 32 * (kAWarp0 + kAWarps);
+constexpr int kWWarp = 5;       // warp 5: packed-weight bulk copies
+constexpr int kGWarp0 = 6;      // warps 6..: grad_out gather
+constexpr int kGWarps = 8;
+constexpr int kThreads = 32 * (kGWarp0 + kGWarps);
 constexpr int kSmemLimit = 232448;  // 227 KB dynamic shared memory per block
 constexpr int kBarrierBytes = 1024;
+constexpr int kEpiChunk = 32;                 // positions per step of the staged epilogue
+constexpr int kEpiRowFloats = kEpiChunk + 1;  // padded staging row (conflict-free)
+constexpr int kTmaBoxCi = 16;                 // channels per TMA store box
 
 struct PhaseDesc {
     int rh, rw;         // residues of (ih, iw) modulo the stride
@@ -48,24 +58,31 @@ struct PhaseDesc {
     int th, tw;         // kh = s*j + th, kw = s*i + tw
     int qh, qw;         // oh = a + qh - j, ow = b + qw - i
     int X, R;           // frame pitch and frame rows per image
-    int m_tiles;        // 128-output tiles of this phase
+    int p_tiles;        // position tiles of this phase
     int hb;             // frame elements one tile needs
-    int64_t tile_begin; // first global tile of this phase (m-tiles x n-tiles)
+    int64_t tile_begin; // first global tile of this phase (p-tiles x m-tiles)
     int64_t pack_off;   // byte offset of this phase's packed weights
 };
 
 struct TcParams {
+    CUtensorMap out_map;    // grad_in as [N][Ci][H][W] float32 (TMA store epilogue only)
     const void *grad_out;
     const void *packed;
     float *grad_in;
     int N, Ci, H, W, Co, OH, OW, stride;
     int n_phases;
-    int n_ntiles, n_tile;   // tiles over Ci and columns per tile (MMA N)
-    int kc, n_cchunks;      // grad_out channels per stage, stages per tile
-    int hbp;                // frame elements per A stage (multiple of 8)
-    int a_stage_bytes, b_stage_bytes;
-    int b_unit_bytes;       // one tap x one channel chunk of packed weights
-    int na, nb;             // ring depths; nb == 0: all packed weights resident
+    int m_tile, n_mtiles;   // input channels per tile (MMA M: 64 or 128) and tiles over Ci
+    int tile_p;             // accumulator columns per tile (MMA N)
+    int rows_per_tile;      // > 0: tiles are whole frame rows (stride 1), this many per tile
+    int epi_tma;            // 1: epilogue stores through TMA (set at launch)
+    int epi_stage_bytes;    // shared-memory staging of the epilogue
+    int kc, n_cchunks;      // grad_out channels per stage (128 bytes), stages per tile
+    int hbp;                // frame elements per G stage (multiple of 8)
+    int g_stage_bytes;      // grad_out frame window stage
+    int w_unit_bytes;       // one tap x one channel chunk of packed weights
+    int w_stage_bytes;      // one streamed weight stage (taps_per_w taps)
+    int taps_per_w;         // taps per streamed weight stage
+    int ng, nw;             // ring depths; nw == 0: all packed weights resident
     int64_t packed_bytes;
     int64_t total_tiles;
     uint32_t idesc;         // tcgen05 instruction descriptor
@@ -78,7 +95,7 @@ struct TcParams {
 
 struct PackParams {
     int Ci, Co, kH, kW, stride;
-    int n_tile, n_ntiles, kc, n_cchunks, elems16;  // elems16: elements per 16 bytes
+    int m_tile, n_mtiles, kc, n_cchunks, elems16;  // elems16: elements per 16 bytes
     int n_phases;
     int64_t total_elems;
     int64_t elem_begin[kMaxPhases + 1];

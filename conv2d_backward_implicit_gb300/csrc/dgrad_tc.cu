@@ -27,6 +27,8 @@
 // expiry the CTA raises an abort flag in shared memory, sets bit 0 of the
 // device error word, drains copies and MMAs it has in flight, releases TMEM
 // and returns; no wait is unbounded and nothing traps.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -41,7 +43,7 @@ __device__ unsigned int g_dgrad_error_word = 0;
 namespace {
 
 struct Shared {
-    uint64_t full_a[4], empty_a[4], full_b[4], empty_b[4];
+    uint64_t full_g[4], empty_g[4], full_w[4], empty_w[4];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t w_full, mma_done;
     uint32_t tmem_base;
@@ -115,6 +117,16 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ uint32_t ldg_u16(const unsigned short *p) {
     unsigned short v;
     asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
@@ -178,33 +190,92 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
     }
 }
 
-// 32 lanes x 16 consecutive float32 columns of TMEM, waited for before return.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// 32 lanes x 16 consecutive 32-bit columns of TMEM into registers.  The load
+// is asynchronous: the registers are valid only after tmem_wait_ld(r).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
           "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Shared-memory matrix descriptor (tcgen05 format): K-major, no swizzle.
-// Core matrices are 8 rows x 16 bytes stored contiguously; `lbo` is the byte
-// step between core matrices adjacent in K, `sbo` the step between core
-// matrices adjacent in M/N.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr >> 4) & 0x3FFFu);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;  // descriptor version
-    return d;                // base offset 0, relative LBO, layout SWIZZLE_NONE
+// Waits for this thread's outstanding TMEM loads; naming the destination
+// registers as in-out operands keeps their uses after the wait.
+__device__ __forceinline__ void tmem_wait_ld4(uint32_t (&r)[4][16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0][0]), "+r"(r[0][1]), "+r"(r[0][2]), "+r"(r[0][3]), "+r"(r[0][4]), "+r"(r[0][5]), "+r"(r[0][6]), "+r"(r[0][7]), "+r"(r[0][8]), "+r"(r[0][9]), "+r"(r[0][10]), "+r"(r[0][11]), "+r"(r[0][12]), "+r"(r[0][13]), "+r"(r[0][14]), "+r"(r[0][15]), "+r"(r[1][0]), "+r"(r[1][1]), "+r"(r[1][2]), "+r"(r[1][3]), "+r"(r[1][4]), "+r"(r[1][5]), "+r"(r[1][6]), "+r"(r[1][7]), "+r"(r[1][8]), "+r"(r[1][9]), "+r"(r[1][10]), "+r"(r[1][11]), "+r"(r[1][12]), "+r"(r[1][13]), "+r"(r[1][14]), "+r"(r[1][15]), "+r"(r[2][0]), "+r"(r[2][1]), "+r"(r[2][2]), "+r"(r[2][3]), "+r"(r[2][4]), "+r"(r[2][5]), "+r"(r[2][6]), "+r"(r[2][7]), "+r"(r[2][8]), "+r"(r[2][9]), "+r"(r[2][10]), "+r"(r[2][11]), "+r"(r[2][12]), "+r"(r[2][13]), "+r"(r[2][14]), "+r"(r[2][15]), "+r"(r[3][0]), "+r"(r[3][1]), "+r"(r[3][2]), "+r"(r[3][3]), "+r"(r[3][4]), "+r"(r[3][5]), "+r"(r[3][6]), "+r"(r[3][7]), "+r"(r[3][8]), "+r"(r[3][9]), "+r"(r[3][10]), "+r"(r[3][11]), "+r"(r[3][12]), "+r"(r[3][13]), "+r"(r[3][14]), "+r"(r[3][15])
+                 :
+                 : "memory");
+}
+
+// TMA tensor store of a [16 ch][1 row][W] float32 box from shared memory
+// (bulk-group completion), and the waits on this thread's bulk groups.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t smem_src, int x,
+                                             int y, int z, int w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_src)
+        : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// 32 lanes x 8 / 4 consecutive 32-bit TMEM columns, asynchronous like tmem_ld16.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+}
+
+// Waits for this thread's outstanding TMEM loads into r (in-out operands keep
+// every use of r after the wait).
+__device__ __forceinline__ void tmem_wait_ld16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format) for a K-major operand in
+// the 128-byte swizzle layout: rows of 128 bytes, groups of 8 rows (1024 B)
+// one after another, and within a group the 16-byte chunk c of row r stored
+// at chunk position c ^ r.  The swizzle is applied to absolute shared-memory
+// address bits (chunk bits 4-6 XOR row bits 7-9), so with the data written
+// the same way and the ring 1024-byte aligned, `addr` may start at any
+// 128-byte row -- a tap's shifted view of the frame window -- and at any
+// 32-byte K step inside a row, with the base-offset field left at 0.
+// (Setting that field to the row phase instead gives wrong results on
+// sm_103a: checked against the oracle.)
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+    uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;             // leading byte offset: unused for swizzled K-major
+    d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset: next group of 8 rows
+    d |= (uint64_t)1 << 46;             // descriptor version
+    d |= (uint64_t)2 << 61;             // SWIZZLE_128B, base offset 0
+    return d;
 }
 
 // ----------------------------------------------------------- bounded waits
@@ -253,7 +324,7 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, const 
 
 // ------------------------------------------------------------ tile decode
 struct Tile {
-    int phase, mt, nt;
+    int phase, pt, mt;  // phase, 256-position tile, input-channel tile
 };
 
 __device__ __forceinline__ Tile decode_tile(const TcParams &p, int64_t t) {
@@ -262,21 +333,42 @@ __device__ __forceinline__ Tile decode_tile(const TcParams &p, int64_t t) {
     const int64_t local = t - p.ph[ph].tile_begin;
     Tile r;
     r.phase = ph;
-    r.mt = (int)(local / p.n_ntiles);
-    r.nt = (int)(local - (int64_t)r.mt * p.n_ntiles);
+    r.pt = (int)(local / p.n_mtiles);
+    r.mt = (int)(local - (int64_t)r.pt * p.n_mtiles);
     return r;
+}
+
+// First frame position of a position tile, and how many positions it owns:
+// whole frame rows (stride 1) or tile_p consecutive positions.
+__device__ __forceinline__ int tile_start(const TcParams &p, const PhaseDesc &d, int pt) {
+    if (p.rows_per_tile > 0) {
+        const int tpi = (d.Hr + p.rows_per_tile - 1) / p.rows_per_tile;  // tiles per image
+        const int n = pt / tpi, g = pt - n * tpi;
+        return (n * d.R + g * p.rows_per_tile) * d.X;
+    }
+    return pt * p.tile_p;
+}
+
+__device__ __forceinline__ int tile_own(const TcParams &p, const PhaseDesc &d) {
+    return p.rows_per_tile > 0 ? p.rows_per_tile * d.X : p.tile_p;
+}
+
+// Byte offset, inside the packed weights, of (phase, ci tile, channel chunk).
+__device__ __forceinline__ int64_t w_block_off(const TcParams &p, const PhaseDesc &d, int mt,
+                                               int cc) {
+    return d.pack_off + ((int64_t)mt * p.n_cchunks + cc) * (d.Jh * d.Jw) * p.w_unit_bytes;
 }
 
 // ------------------------------------------------------------------ roles
 // Warp 5, lane 0: packed weights into shared memory with bulk copies.
-__device__ void role_weights(const TcParams &p, Shared &sh, uint32_t b_base) {
+__device__ void role_weights(const TcParams &p, Shared &sh, uint32_t w_base) {
     const uint8_t *src = static_cast<const uint8_t *>(p.packed);
-    if (p.nb == 0) {
+    if (p.nw == 0) {
         const uint32_t bar = smem_u32(&sh.w_full);
         mbar_arrive_expect_tx(bar, (uint32_t)p.packed_bytes);
         for (int64_t off = 0; off < p.packed_bytes; off += 32768) {
             const int64_t left = p.packed_bytes - off;
-            bulk_g2s(b_base + (uint32_t)off, src + off, (uint32_t)(left < 32768 ? left : 32768), bar);
+            bulk_g2s(w_base + (uint32_t)off, src + off, (uint32_t)(left < 32768 ? left : 32768), bar);
         }
         wait_drain(bar, 0, p, sh);  // never leave a copy in flight
         return;
@@ -290,46 +382,47 @@ __device__ void role_weights(const TcParams &p, Shared &sh, uint32_t b_base) {
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
         const int taps = d.Jh * d.Jw;
-        const uint32_t bytes = (uint32_t)(taps * p.b_unit_bytes);
-        for (int cc = 0; cc < p.n_cchunks; ++cc) {
-            if (!wait_bar(smem_u32(&sh.empty_b[stage]), phase ^ 1u, p, sh)) {
-                aborted = true;
-                break;
-            }
-            const uint8_t *s =
-                src + d.pack_off + ((int64_t)ti.nt * p.n_cchunks + cc) * taps * p.b_unit_bytes;
-            const uint32_t full = smem_u32(&sh.full_b[stage]);
-            mbar_arrive_expect_tx(full, bytes);
-            bulk_g2s(b_base + (uint32_t)stage * p.b_stage_bytes, s, bytes, full);
-            ++issued;
-            if (++stage == p.nb) {
-                stage = 0;
-                phase ^= 1u;
+        for (int cc = 0; cc < p.n_cchunks && !aborted; ++cc) {
+            const uint8_t *blk = src + w_block_off(p, d, ti.mt, cc);
+            for (int t0 = 0; t0 < taps; t0 += p.taps_per_w) {
+                if (!wait_bar(smem_u32(&sh.empty_w[stage]), phase ^ 1u, p, sh)) {
+                    aborted = true;
+                    break;
+                }
+                const int ng = taps - t0 < p.taps_per_w ? taps - t0 : p.taps_per_w;
+                const uint32_t bytes = (uint32_t)(ng * p.w_unit_bytes);
+                const uint32_t full = smem_u32(&sh.full_w[stage]);
+                mbar_arrive_expect_tx(full, bytes);
+                bulk_g2s(w_base + (uint32_t)stage * p.w_stage_bytes,
+                         blk + (int64_t)t0 * p.w_unit_bytes, bytes, full);
+                ++issued;
+                if (++stage == p.nw) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
         }
     }
     if (aborted) {
         // Let every copy that may still be landing finish before the CTA exits.
-        const int64_t k_end = issued < p.nb ? issued : p.nb;
+        const int64_t k_end = issued < p.nw ? issued : p.nw;
         for (int64_t k = 0; k < k_end; ++k) {
             const int64_t q = issued - 1 - k;
-            wait_drain(smem_u32(&sh.full_b[q % p.nb]), (uint32_t)((q / p.nb) & 1), p, sh);
+            wait_drain(smem_u32(&sh.full_w[q % p.nw]), (uint32_t)((q / p.nw) & 1), p, sh);
         }
     }
 }
 
-// Warp 4, lane 0: tcgen05.mma issue.
+// Warp 4, lane 0: tcgen05.mma issue.  D[ci, pos] (TMEM, 256 columns per
+// buffer) += W_tap[ci, co] (A: packed weights) x G[co, pos + shift(tap)]
+// (B: the frame window seen from the tap's start row).
 template <bool TF32>
-__device__ void role_mma(const TcParams &p, Shared &sh, uint32_t a_base, uint32_t b_base,
+__device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_t w_base,
                          uint32_t tmem) {
-    constexpr int E = TF32 ? 4 : 8;  // elements per 16 bytes
-    const int ksteps = p.kc / (2 * E);  // MMA K-steps (32 bytes each) per tap and stage
-    int as = 0, bs = 0, acc = 0;
-    uint32_t aph = 0, bph = 0, accph = 0;
+    int gs = 0, ws = 0, acc = 0;
+    uint32_t gph = 0, wph = 0, accph = 0;
     bool aborted = false;
-    if (p.nb == 0 && !wait_bar(smem_u32(&sh.w_full), 0, p, sh)) aborted = true;
-    const uint32_t a_lbo = (uint32_t)p.hbp * 16u;
-    const uint32_t b_lbo = (uint32_t)p.n_tile * 16u;
+    if (p.nw == 0 && !wait_bar(smem_u32(&sh.w_full), 0, p, sh)) aborted = true;
     for (int64_t t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
         const Tile ti = decode_tile(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
@@ -339,51 +432,56 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t a_base, uint32_
             break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(acc * p.n_tile);
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * p.tile_p);
         const int taps = d.Jh * d.Jw;
         uint32_t accumulate = 0;
         for (int cc = 0; cc < p.n_cchunks; ++cc) {
-            if (!wait_bar(smem_u32(&sh.full_a[as]), aph, p, sh)) {
+            if (!wait_bar(smem_u32(&sh.full_g[gs]), gph, p, sh)) {
                 aborted = true;
                 break;
             }
-            uint32_t b_stage;
-            if (p.nb == 0) {
-                b_stage = b_base + (uint32_t)(d.pack_off + ((int64_t)ti.nt * p.n_cchunks + cc) *
-                                                               taps * p.b_unit_bytes);
-            } else {
-                if (!wait_bar(smem_u32(&sh.full_b[bs]), bph, p, sh)) {
-                    aborted = true;
-                    break;
-                }
-                b_stage = b_base + (uint32_t)bs * p.b_stage_bytes;
-            }
             tc_fence_after();
-            const uint32_t a_stage = a_base + (uint32_t)as * p.a_stage_bytes;
-            for (int j = 0; j < d.Jh; ++j) {
-                for (int i = 0; i < d.Jw; ++i) {
-                    const uint32_t a_tap =
-                        a_stage + (uint32_t)(((d.Jh - 1 - j) * d.X + (d.Jw - 1 - i)) * 16);
-                    const uint32_t b_tap = b_stage + (uint32_t)((j * d.Jw + i) * p.b_unit_bytes);
-                    for (int k = 0; k < ksteps; ++k) {
-                        const uint64_t ad = smem_desc(a_tap + 2u * k * a_lbo, a_lbo, 128);
-                        const uint64_t bd = smem_desc(b_tap + 2u * k * b_lbo, b_lbo, 128);
+            const uint32_t g_stage = g_base + (uint32_t)gs * p.g_stage_bytes;
+            const uint32_t w_res = w_base + (uint32_t)w_block_off(p, d, ti.mt, cc);
+            for (int t0 = 0; t0 < taps && !aborted; t0 += p.taps_per_w) {
+                const int t1 = taps - t0 < p.taps_per_w ? taps : t0 + p.taps_per_w;
+                uint32_t w_grp;
+                if (p.nw == 0) {
+                    w_grp = w_res + (uint32_t)(t0 * p.w_unit_bytes);
+                } else {
+                    if (!wait_bar(smem_u32(&sh.full_w[ws]), wph, p, sh)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    w_grp = w_base + (uint32_t)ws * p.w_stage_bytes;
+                }
+                for (int tap = t0; tap < t1; ++tap) {
+                    const int j = tap / d.Jw, i = tap - j * d.Jw;
+                    const uint32_t g_tap =
+                        g_stage + (uint32_t)(((d.Jh - 1 - j) * d.X + (d.Jw - 1 - i)) * 128);
+                    const uint32_t w_tap = w_grp + (uint32_t)((tap - t0) * p.w_unit_bytes);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {  // four 32-byte K steps per 128-byte row
+                        const uint64_t ad = sw128_desc(w_tap + 32u * k);
+                        const uint64_t bd = sw128_desc(g_tap + 32u * k);
                         tc_mma<TF32>(d_tmem, ad, bd, p.idesc, accumulate);
                         accumulate = 1;
                     }
                 }
-            }
-            tc_commit(smem_u32(&sh.empty_a[as]));
-            if (++as == p.na) {
-                as = 0;
-                aph ^= 1u;
-            }
-            if (p.nb != 0) {
-                tc_commit(smem_u32(&sh.empty_b[bs]));
-                if (++bs == p.nb) {
-                    bs = 0;
-                    bph ^= 1u;
+                if (p.nw != 0) {
+                    tc_commit(smem_u32(&sh.empty_w[ws]));
+                    if (++ws == p.nw) {
+                        ws = 0;
+                        wph ^= 1u;
+                    }
                 }
+            }
+            if (aborted) break;
+            tc_commit(smem_u32(&sh.empty_g[gs]));
+            if (++gs == p.ng) {
+                gs = 0;
+                gph ^= 1u;
             }
         }
         if (aborted) break;
@@ -398,9 +496,10 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t a_base, uint32_
     wait_drain(smem_u32(&sh.mma_done), 0, p, sh);
 }
 
-// Warps 6..9: grad_out frame windows into K-major core matrices.
-template <int ESIZE, int CHUNKS>
-__device__ void role_gather(const TcParams &p, Shared &sh, uint32_t a_base, int gw, int lane) {
+// Gather warps: grad_out frame windows into 128-byte swizzled K-major rows
+// (one row per frame element, 128 bytes of grad_out channels).
+template <int ESIZE>
+__device__ void role_gather(const TcParams &p, Shared &sh, uint32_t g_base, int gw, int lane) {
     const int64_t plane = (int64_t)p.OH * p.OW;
     int stage = 0;
     uint32_t phase = 0;
@@ -409,14 +508,14 @@ __device__ void role_gather(const TcParams &p, Shared &sh, uint32_t a_base, int 
         const Tile ti = decode_tile(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
-        const int L0 = ti.mt * kTileM;
+        const int L0 = tile_start(p, d, ti.pt);
         const int img = d.R * d.X;
         for (int cc = 0; cc < p.n_cchunks; ++cc) {
-            if (!wait_bar_warp(smem_u32(&sh.empty_a[stage]), phase ^ 1u, p, sh, lane)) return;
-            const uint32_t s_base = a_base + (uint32_t)stage * p.a_stage_bytes;
+            if (!wait_bar_warp(smem_u32(&sh.empty_g[stage]), phase ^ 1u, p, sh, lane)) return;
+            const uint32_t s_base = g_base + (uint32_t)stage * p.g_stage_bytes;
             const int co0 = cc * p.kc;
             const int cleft = p.Co - co0;
-            for (int h = gw * 32 + lane; h < p.hbp; h += kAWarps * 32) {
+            for (int h = gw * 32 + lane; h < p.hbp; h += kGWarps * 32) {
                 const int lam = L0 + h;
                 const int n = lam / img;
                 const int rem = lam - n * img;
@@ -428,6 +527,7 @@ __device__ void role_gather(const TcParams &p, Shared &sh, uint32_t a_base, int 
                 const int cvalid = ok ? (cleft < p.kc ? cleft : p.kc) : 0;
                 const int64_t off =
                     ok ? ((int64_t)n * p.Co + co0) * plane + (int64_t)u * p.OW + v : 0;
+                constexpr int CHUNKS = 8;
                 uint32_t q[CHUNKS][4];
                 if constexpr (ESIZE == 2) {
                     const unsigned short *g = static_cast<const unsigned short *>(p.grad_out) + off;
@@ -452,9 +552,10 @@ __device__ void role_gather(const TcParams &p, Shared &sh, uint32_t a_base, int 
                         }
                     }
                 }
+                const uint32_t row = s_base + (uint32_t)h * 128u;
 #pragma unroll
                 for (int kc = 0; kc < CHUNKS; ++kc)
-                    st_shared_v4(s_base + (uint32_t)(kc * p.hbp + h) * 16u, q[kc][0], q[kc][1],
+                    st_shared_v4(row + (uint32_t)((kc ^ (h & 7)) << 4), q[kc][0], q[kc][1],
                                  q[kc][2], q[kc][3]);
             }
             fence_proxy_async();
@@ -463,9 +564,9 @@ __device__ void role_gather(const TcParams &p, Shared &sh, uint32_t a_base, int 
                 if (withhold)
                     withhold = false;  // failure injection: this stage is never signalled
                 else
-                    mbar_arrive(smem_u32(&sh.full_a[stage]));
+                    mbar_arrive(smem_u32(&sh.full_g[stage]));
             }
-            if (++stage == p.na) {
+            if (++stage == p.ng) {
                 stage = 0;
                 phase ^= 1u;
             }
@@ -473,45 +574,169 @@ __device__ void role_gather(const TcParams &p, Shared &sh, uint32_t a_base, int 
     }
 }
 
-// Warps 0..3: TMEM accumulator -> float32 NCHW grad_in.
-__device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t tmem, int q, int lane) {
+// A position of the tile walked along the frame: (image, frame row, column).
+struct FramePos {
+    int n, a, b;
+};
+
+__device__ __forceinline__ FramePos frame_pos(const PhaseDesc &d, int lam) {
+    const int img = d.R * d.X;
+    FramePos f;
+    f.n = lam / img;
+    const int rem = lam - f.n * img;
+    f.a = rem / d.X;
+    f.b = rem - f.a * d.X;
+    return f;
+}
+
+__device__ __forceinline__ void frame_advance(const PhaseDesc &d, FramePos &f, int step) {
+    f.b += step;
+    while (f.b >= d.X) {
+        f.b -= d.X;
+        if (++f.a == d.R) {
+            f.a = 0;
+            ++f.n;
+        }
+    }
+}
+
+// grad_in offset of channel 0 at a frame position, or -1 for frame padding
+// and positions past the last image.
+__device__ __forceinline__ int64_t out_offset(const TcParams &p, const PhaseDesc &d,
+                                              const FramePos &f) {
+    if (f.n >= p.N || f.a >= d.Hr || f.b >= d.Wr) return -1;
+    return ((int64_t)f.n * p.Ci * p.H + (p.stride * f.a + d.rh)) * p.W + (p.stride * f.b + d.rw);
+}
+
+// Warps 0..3: TMEM accumulator -> float32 NCHW grad_in.  Warp q drains its
+// TMEM lane quadrant: rows (input channels) 32q..32q+31 for a 128-row tile, or
+// 16q..16q+15 (lanes 0..15 of the quadrant) for a 64-row tile.
+//
+// Staged epilogue (any shape): a step takes 32 columns (positions); the TMEM
+// loads of two steps are in flight per wait; the values are turned around
+// through a padded staging block in shared memory (row pitch 33 floats:
+// conflict-free both ways) so that each store instruction writes 32
+// consecutive positions of one channel.
+template <int ROWS>
+__device__ void epilogue_staged(const TcParams &p, const PhaseDesc &d, const Tile &ti,
+                                uint32_t taddr, uint32_t st_base, int q, int lane) {
     const int64_t HW = (int64_t)p.H * p.W;
+    const int ci_base = ti.mt * p.m_tile + q * ROWS;
+    int ci_here = p.Ci - ci_base;  // channels of this warp that exist
+    ci_here = ci_here < 0 ? 0 : (ci_here > ROWS ? ROWS : ci_here);
+    const int L0 = tile_start(p, d, ti.pt), own = tile_own(p, d);
+    FramePos f = frame_pos(d, L0 + lane);
+    const uint32_t st_row = st_base + 4u * kEpiRowFloats * lane;  // row written by this lane
+    const uint32_t st_col = st_base + 4u * lane;                  // column read by this lane
+    for (int g0 = 0; g0 < p.tile_p; g0 += 2 * kEpiChunk) {
+        uint32_t v[4][16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tmem_ld16(taddr + (uint32_t)(g0 + 16 * k), v[k]);
+        tmem_wait_ld4(v);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            if (lane < ROWS) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    st_shared_f32(st_row + 4u * e, v[2 * h + e / 16][e % 16]);
+            }
+            __syncwarp();
+            float val[ROWS];
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r) val[r] = ld_shared_f32(st_col + 4u * kEpiRowFloats * r);
+            __syncwarp();
+            const int col = g0 + h * kEpiChunk + lane;
+            const int64_t o = col < own ? out_offset(p, d, f) : -1;
+            if (o >= 0) {
+                float *out = p.grad_in + o + (int64_t)ci_base * HW;
+#pragma unroll
+                for (int r = 0; r < ROWS; ++r)
+                    if (r < ci_here) out[(int64_t)r * HW] = val[r];
+            }
+            frame_advance(d, f, kEpiChunk);
+        }
+    }
+}
+
+// TMA-store epilogue (stride 1, tiles of whole frame rows, W a multiple of 4
+// up to 64, grad_in 16-byte aligned): for each output row of the tile and
+// each 16-lane group, the warp copies the row's W accumulator columns into a
+// dense [16 channels][W] box in shared memory and one lane stores the box with
+// a TMA tensor store, so grad_in is written in whole, aligned rows.
+__device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &ti,
+                             uint32_t taddr, uint32_t box, int q, int lane) {
+    const int groups = p.m_tile == 64 ? 1 : 2;
+    const int tpi = (d.Hr + p.rows_per_tile - 1) / p.rows_per_tile;
+    const int n = ti.pt / tpi, a0 = (ti.pt - n * tpi) * p.rows_per_tile;
+    const int W = p.W;
+    for (int gi = 0; gi < groups; ++gi) {
+        const int ci0 = ti.mt * p.m_tile + q * 16 * groups + 16 * gi;
+        if (ci0 >= p.Ci) break;
+        // Rows of this 16-lane group: lanes 16*gi .. 16*gi+15 of the quadrant.
+        const bool mine = (lane >> 4) == gi;
+        const uint32_t row_addr = box + 4u * (uint32_t)(W * (lane & 15));
+        for (int r = 0; r < p.rows_per_tile && a0 + r < d.Hr; ++r) {
+            const uint32_t cbase = taddr + (uint32_t)(r * d.X);
+            // The previous box of this warp must have been read by the TMA unit.
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            for (int c = 0; c < W; c += 16) {
+                uint32_t v[16] = {};
+                if (W - c >= 16) {
+                    tmem_ld16(cbase + (uint32_t)c, v);
+                } else if (W - c >= 8) {
+                    tmem_ld8(cbase + (uint32_t)c, v);
+                    if (W - c > 8) tmem_ld4(cbase + (uint32_t)c + 8u, v + 8);
+                } else {
+                    tmem_ld4(cbase + (uint32_t)c, v);
+                }
+                tmem_wait_ld16(v);
+                if (mine) {
+                    const int m = W - c < 16 ? W - c : 16;
+                    for (int e = 0; e < m; e += 4)
+                        st_shared_v4(row_addr + 4u * (c + e), v[e], v[e + 1], v[e + 2], v[e + 3]);
+                }
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) tma_store_4d(&p.out_map, box, 0, a0 + r, ci0, n);
+        }
+    }
+}
+
+__device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uint32_t tmem,
+                              int q, int lane) {
+    const int64_t HW = (int64_t)p.H * p.W;
+    const int rows = p.m_tile == 64 ? 16 : 32;  // channels this warp owns
+    const uint32_t st_base = stage + (uint32_t)(p.epi_stage_bytes / kEpiWarps) * q;
     int acc = 0;
     uint32_t accph = 0;
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
         const Tile ti = decode_tile(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
-        const int lam = ti.mt * kTileM + q * 32 + lane;
-        const int img = d.R * d.X;
-        const int n = lam / img;
-        const int rem = lam - n * img;
-        const int a = rem / d.X;
-        const int b = rem - a * d.X;
-        const bool valid = n < p.N && a < d.Hr && b < d.Wr;
-        const int ci0 = ti.nt * p.n_tile;
-        const int ci_lim = p.Ci - ci0 < p.n_tile ? p.Ci - ci0 : p.n_tile;
-        const int64_t out_off =
-            valid ? (((int64_t)n * p.Ci + ci0) * p.H + (p.stride * a + d.rh)) * p.W +
-                        (p.stride * b + d.rw)
-                  : 0;
-        float *out = p.grad_in + out_off;
         if (d.Jh == 0) {  // no tap reaches this phase: grad_in is zero there
-            if (valid)
-                for (int c = 0; c < ci_lim; ++c) out[c * HW] = 0.f;
+            const int ci_base = ti.mt * p.m_tile + q * rows;
+            int ci_here = p.Ci - ci_base;
+            ci_here = ci_here < 0 ? 0 : (ci_here > rows ? rows : ci_here);
+            const int L0 = tile_start(p, d, ti.pt), own = tile_own(p, d);
+            FramePos f = frame_pos(d, L0 + lane);
+            for (int c0 = 0; c0 < own; c0 += kEpiChunk) {
+                const int64_t o = c0 + lane < own ? out_offset(p, d, f) : -1;
+                if (o >= 0)
+                    for (int r = 0; r < ci_here; ++r) p.grad_in[o + (int64_t)(ci_base + r) * HW] = 0.f;
+                frame_advance(d, f, kEpiChunk);
+            }
             continue;
         }
-        if (!wait_bar_warp(smem_u32(&sh.acc_full[acc]), accph, p, sh, lane)) return;
+        if (!wait_bar_warp(smem_u32(&sh.acc_full[acc]), accph, p, sh, lane)) break;
         tc_fence_after();
-        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.n_tile);
-        for (int c0 = 0; c0 < p.n_tile; c0 += 16) {
-            float v[16];
-            tmem_ld16(taddr + (uint32_t)c0, v);
-            if (valid) {
-#pragma unroll
-                for (int jj = 0; jj < 16; ++jj)
-                    if (c0 + jj < ci_lim) out[(int64_t)(c0 + jj) * HW] = v[jj];
-            }
-        }
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.tile_p);
+        if (p.epi_tma)
+            epilogue_tma(p, d, ti, taddr, st_base, q, lane);
+        else if (rows == 16)
+            epilogue_staged<16>(p, d, ti, taddr, st_base, q, lane);
+        else
+            epilogue_staged<32>(p, d, ti, taddr, st_base, q, lane);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.acc_empty[acc]));
@@ -520,24 +745,29 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t tmem, int 
             accph ^= 1u;
         }
     }
+    // Every TMA store of this warp must be complete before the CTA exits.
+    if (p.epi_tma && lane == 0) bulk_wait_all();
+    __syncwarp();
 }
 
-template <int ESIZE, int CHUNKS>
+template <int ESIZE>
 __global__ void __launch_bounds__(kThreads, 1) dgrad_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     Shared &sh = *reinterpret_cast<Shared *>(smem);
-    const uint32_t a_base = smem_u32(smem + kBarrierBytes);
-    const uint32_t b_base = a_base + (uint32_t)(p.na * p.a_stage_bytes);
+    // Rings start on a 1024-byte boundary: the swizzle pattern is tied to it.
+    const uint32_t epi_stage = smem_u32(smem) + kBarrierBytes;
+    const uint32_t g_base = (epi_stage + (uint32_t)p.epi_stage_bytes + 1023u) & ~1023u;
+    const uint32_t w_base = g_base + (uint32_t)(p.ng * p.g_stage_bytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < p.na; ++s) {
-            mbar_init(smem_u32(&sh.full_a[s]), kAWarps);
-            mbar_init(smem_u32(&sh.empty_a[s]), 1);
+        for (int s = 0; s < p.ng; ++s) {
+            mbar_init(smem_u32(&sh.full_g[s]), kGWarps);
+            mbar_init(smem_u32(&sh.empty_g[s]), 1);
         }
-        for (int s = 0; s < p.nb; ++s) {
-            mbar_init(smem_u32(&sh.full_b[s]), 1);
-            mbar_init(smem_u32(&sh.empty_b[s]), 1);
+        for (int s = 0; s < p.nw; ++s) {
+            mbar_init(smem_u32(&sh.full_w[s]), 1);
+            mbar_init(smem_u32(&sh.empty_w[s]), 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&sh.acc_full[s]), 1);
@@ -557,16 +787,16 @@ __global__ void __launch_bounds__(kThreads, 1) dgrad_tc_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
 
-    if (warp == kBWarp) {
-        if (lane == 0) role_weights(p, sh, b_base);
+    if (warp == kWWarp) {
+        if (lane == 0) role_weights(p, sh, w_base);
         __syncwarp();
     } else if (warp == kMmaWarp) {
-        if (lane == 0) role_mma<ESIZE == 4>(p, sh, a_base, b_base, tmem);
+        if (lane == 0) role_mma<ESIZE == 4>(p, sh, g_base, w_base, tmem);
         __syncwarp();
-    } else if (warp >= kAWarp0) {
-        role_gather<ESIZE, CHUNKS>(p, sh, a_base, warp - kAWarp0, lane);
+    } else if (warp >= kGWarp0) {
+        role_gather<ESIZE>(p, sh, g_base, warp - kGWarp0, lane);
     } else {
-        role_epilogue(p, sh, tmem, warp, lane);
+        role_epilogue(p, sh, epi_stage, tmem, warp, lane);
     }
     tc_fence_before();
     __syncthreads();
@@ -579,10 +809,10 @@ __global__ void __launch_bounds__(kThreads, 1) dgrad_tc_kernel(const __grid_cons
 // Dynamic shared memory is raised once per device and variant to the full
 // limit, so no attribute call happens on later launches (e.g. during stream
 // capture).
-template <int ESIZE, int CHUNKS>
+template <int ESIZE>
 int launch_variant(const TcParams &p, int grid, cudaStream_t st, int dev) {
     static std::atomic<uint64_t> configured{0};  // bit per device
-    auto kern = dgrad_tc_kernel<ESIZE, CHUNKS>;
+    auto kern = dgrad_tc_kernel<ESIZE>;
     const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
     if (!bit || !(configured.load() & bit)) {
         cudaError_t e =
@@ -600,6 +830,40 @@ int sm_count(int dev) {
     return n;
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            ptr = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }();
+    return fn;
+}
+
+// grad_in as a 4-D float32 tensor [N][Ci][H][W] with a [1][16][1][W] store box.
+bool encode_out_map(TcParams &p) {
+    if (p.rows_per_tile <= 0 || p.stride != 1 || p.W % 4 != 0 || p.W > 64) return false;
+    if ((reinterpret_cast<uintptr_t>(p.grad_in) & 15u) != 0) return false;
+    if (p.epi_stage_bytes < kEpiWarps * kTmaBoxCi * p.W * 4) return false;
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)p.Ci,
+                                (cuuint64_t)p.N};
+    const cuuint64_t strides[3] = {(cuuint64_t)p.W * 4, (cuuint64_t)p.H * p.W * 4,
+                                   (cuuint64_t)p.Ci * p.H * p.W * 4};
+    const cuuint32_t box[4] = {(cuuint32_t)p.W, 1u, (cuuint32_t)kTmaBoxCi, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    CUresult r = fn(&p.out_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.grad_in, dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 int launch_tc(const Plan &plan, const void *grad_out, const void *packed, float *grad_in,
@@ -608,6 +872,7 @@ int launch_tc(const Plan &plan, const void *grad_out, const void *packed, float 
     p.grad_out = grad_out;
     p.packed = packed;
     p.grad_in = grad_in;
+    p.epi_tma = encode_out_map(p) ? 1 : 0;
     int dev = 0;
     cudaError_t de = cudaGetDevice(&dev);
     if (de != cudaSuccess) return (int)de;
@@ -619,15 +884,8 @@ int launch_tc(const Plan &plan, const void *grad_out, const void *packed, float 
     const int grid = (int)(p.total_tiles < sms ? p.total_tiles : sms);
     if (grid <= 0) return (int)cudaSuccess;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int chunks = p.kc / (16 / plan.esize);
-    if (plan.esize == 2) {
-        if (chunks == 8) return launch_variant<2, 8>(p, grid, st, dev);
-        if (chunks == 4) return launch_variant<2, 4>(p, grid, st, dev);
-        return launch_variant<2, 2>(p, grid, st, dev);
-    }
-    if (chunks == 8) return launch_variant<4, 8>(p, grid, st, dev);
-    if (chunks == 4) return launch_variant<4, 4>(p, grid, st, dev);
-    return launch_variant<4, 2>(p, grid, st, dev);
+    if (plan.esize == 2) return launch_variant<2>(p, grid, st, dev);
+    return launch_variant<4>(p, grid, st, dev);
 }
 
 int tc_read_and_clear_error(unsigned int *out) {

@@ -7,13 +7,14 @@
 // tensor-core kernel consumes, so the kernel moves it with plain bulk copies:
 //
 //   for each phase (rh, rw) with taps kh = s*j + th, kw = s*i + tw,
-//     for each Ci tile nt, grad_out channel chunk cc, tap j, tap i:
-//       [kc/E sixteen-byte chunks][n_tile rows = ci][E elements = co]
+//     for each Ci tile mt, grad_out channel chunk cc, tap j, tap i:
+//       m_tile rows (ci) of 128 bytes (kc consecutive co), 128-byte swizzled
 //
-// i.e. K-major [Ci, K] core matrices of 8 rows x 16 bytes (no swizzle), with
-// zeros for ci >= Ci and co >= Co.  E = 16 / element size.  For float32 input
-// the values are rounded to TF32 (nearest, ties away from zero), the operand
-// precision of kind::tf32.
+// i.e. K-major [Ci, K] operand tiles in the 128-byte swizzle layout of the
+// tcgen05 shared-memory descriptors: within each group of 8 rows, the 16-byte
+// chunk c of row r is stored at chunk position c ^ (r mod 8).  Rows ci >= Ci
+// and channels co >= Co are zero.  For float32 input the values are rounded
+// to TF32 (nearest, ties away from zero), the operand precision of kind::tf32.
 #include <cuda_runtime.h>
 
 #include "conv2d_grad_input.h"
@@ -38,17 +39,18 @@ __global__ void __launch_bounds__(256) pack_weight_kernel(const T *__restrict__ 
         int ph = 0;
         while (ph + 1 < k.n_phases && idx >= k.elem_begin[ph + 1]) ++ph;
         int64_t r = idx - k.elem_begin[ph];
-        const int E = k.elems16;
-        const int chunks = k.kc / E;
-        const int e = (int)(r % E); r /= E;
-        const int row = (int)(r % k.n_tile); r /= k.n_tile;
-        const int kcg = (int)(r % chunks); r /= chunks;
+        const int E = k.elems16;                 // elements per 16-byte chunk
+        const int row_elems = k.kc;              // elements per 128-byte row
+        const int pos = (int)(r % row_elems);    // physical element slot within the row
+        r /= row_elems;
+        const int row = (int)(r % k.m_tile); r /= k.m_tile;
         const int i = (int)(r % k.Jw[ph]); r /= k.Jw[ph];
         const int j = (int)(r % k.Jh[ph]); r /= k.Jh[ph];
         const int cc = (int)(r % k.n_cchunks); r /= k.n_cchunks;
-        const int nt = (int)r;
-        const int co = cc * k.kc + kcg * E + e;
-        const int ci = nt * k.n_tile + row;
+        const int mt = (int)r;
+        const int chunk = (pos / E) ^ (row & 7);  // logical chunk stored at this slot
+        const int co = cc * k.kc + chunk * E + pos % E;
+        const int ci = mt * k.m_tile + row;
         const int kh = k.stride * j + k.th[ph];
         const int kw = k.stride * i + k.tw[ph];
         T v;

@@ -32,105 +32,146 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
     t.N = (int)N; t.Ci = (int)Ci; t.H = (int)H; t.W = (int)W; t.Co = (int)Co;
     t.OH = (int)p.out_h; t.OW = (int)p.out_w; t.stride = s;
 
-    t.n_ntiles = (int)cdiv(Ci, 256);
-    t.n_tile = (int)round_up(cdiv(Ci, t.n_ntiles), 16);
+    // Input channels on the MMA M side: one 64-row tile, or 128-row tiles.
+    t.m_tile = Ci <= 64 ? 64 : 128;
+    t.n_mtiles = (int)cdiv(Ci, t.m_tile);
 
-    // Phases.
-    int max_hb = 0, max_taps = 0, np = 0;
-    for (int rh = 0; rh < s; ++rh) {
-        for (int rw = 0; rw < s; ++rw) {
-            PhaseDesc d;
-            std::memset(&d, 0, sizeof(d));
-            d.rh = rh; d.rw = rw;
-            d.Hr = rh < H ? (int)cdiv(H - rh, s) : 0;
-            d.Wr = rw < W ? (int)cdiv(W - rw, s) : 0;
-            if (d.Hr == 0 || d.Wr == 0) continue;  // no grad_in pixel in this phase
-            d.th = (int)((rh + p.padding_h) % s);
-            d.qh = (int)((rh + p.padding_h) / s);
-            d.tw = (int)((rw + p.padding_w) % s);
-            d.qw = (int)((rw + p.padding_w) / s);
-            d.Jh = d.th < kH ? (int)cdiv(kH - d.th, s) : 0;
-            d.Jw = d.tw < kW ? (int)cdiv(kW - d.tw, s) : 0;
-            if (d.Jh == 0 || d.Jw == 0) {
-                d.Jh = d.Jw = 0;          // zero-filled phase
-                d.X = d.Wr;
-                d.R = d.Hr;
-                d.hb = 0;
-            } else {
-                d.X = d.Wr + d.Jw - 1;
-                d.R = d.Hr + d.Jh - 1;
-                d.hb = kTileM + (d.Jh - 1) * d.X + (d.Jw - 1);
-            }
-            const int64_t positions = N * d.R * d.X;
-            if (positions + 4096 > INT32_MAX) return false;  // 32-bit frame arithmetic
-            d.m_tiles = (int)cdiv(positions, kTileM);
-            max_hb = std::max(max_hb, d.hb);
-            max_taps = std::max(max_taps, d.Jh * d.Jw);
-            t.ph[np++] = d;
-        }
-    }
-    t.n_phases = np;
-    if (np == 0) return false;
-
-    const int budget = kSmemLimit - kBarrierBytes;
-    // Grad_out channels per stage: 2, 4 or 8 sixteen-byte chunks (K = 32, 64, 128 bytes).
-    int chunks_pref = Co > 4 * E ? 8 : (Co > 2 * E ? 4 : 2);
+    // Output positions per tile: 256 (full-rate N); 128 when a 256-wide
+    // tile's frame window would not leave room for two stages.
     bool ok = false;
-    for (int chunks = chunks_pref; chunks >= 2 && !ok; chunks /= 2) {
-        t.kc = chunks * E;
+    int np = 0;
+    for (int cap = kTileP; cap >= 128 && !ok; cap /= 2) {
+        // Stride 1: tiles of whole frame rows (k rows of X positions, the
+        // accumulator rounded up to 16 columns), so each tile owns complete
+        // output rows.  Otherwise tiles are `cap` consecutive frame positions.
+        int tile_p = cap, rows_per_tile = 0;
+        if (s == 1) {
+            const int64_t X1 = W + kW - 1;
+            int64_t k = cap / X1;
+            while (k > 0 && round_up(k * X1, 16) > cap) --k;
+            if (k > 0) {
+                rows_per_tile = (int)std::min<int64_t>(k, H);
+                tile_p = (int)round_up(rows_per_tile * X1, 16);
+            }
+        }
+        t.rows_per_tile = rows_per_tile;
+        // Phases.
+        int max_hb = 0, max_taps = 0;
+        np = 0;
+        for (int rh = 0; rh < s; ++rh) {
+            for (int rw = 0; rw < s; ++rw) {
+                PhaseDesc d;
+                std::memset(&d, 0, sizeof(d));
+                d.rh = rh; d.rw = rw;
+                d.Hr = rh < H ? (int)cdiv(H - rh, s) : 0;
+                d.Wr = rw < W ? (int)cdiv(W - rw, s) : 0;
+                if (d.Hr == 0 || d.Wr == 0) continue;  // no grad_in pixel in this phase
+                d.th = (int)((rh + p.padding_h) % s);
+                d.qh = (int)((rh + p.padding_h) / s);
+                d.tw = (int)((rw + p.padding_w) % s);
+                d.qw = (int)((rw + p.padding_w) / s);
+                d.Jh = d.th < kH ? (int)cdiv(kH - d.th, s) : 0;
+                d.Jw = d.tw < kW ? (int)cdiv(kW - d.tw, s) : 0;
+                if (d.Jh == 0 || d.Jw == 0) {
+                    d.Jh = d.Jw = 0;          // zero-filled phase
+                    d.X = d.Wr;
+                    d.R = d.Hr;
+                    d.hb = 0;
+                } else {
+                    d.X = d.Wr + d.Jw - 1;
+                    d.R = d.Hr + d.Jh - 1;
+                    d.hb = tile_p + (d.Jh - 1) * d.X + (d.Jw - 1);
+                }
+                const int64_t positions = N * d.R * d.X;
+                if (positions + 8192 > INT32_MAX) return false;  // 32-bit frame arithmetic
+                d.p_tiles = rows_per_tile > 0 ? (int)(N * cdiv(d.Hr, rows_per_tile))
+                                              : (int)cdiv(positions, tile_p);
+                max_hb = std::max(max_hb, d.hb);
+                max_taps = std::max(max_taps, d.Jh * d.Jw);
+                t.ph[np++] = d;
+            }
+        }
+        t.n_phases = np;
+        if (np == 0) return false;
+        t.tile_p = tile_p;
+
+        // Shared memory: barriers, 1 KB to align the rings to 1024 B, then the
+        // grad_out (G) ring and the weight (W) ring.
+        // Epilogue staging: padded 33-float rows per channel of a warp, or (TMA
+        // store epilogue, stride 1 with W a multiple of 4 up to 64) one box of
+        // 16 channels x W floats per warp.
+        int epi = kEpiWarps * (t.m_tile / 4) * kEpiRowFloats * 4;
+        if (rows_per_tile > 0 && W % 4 == 0 && W <= 64)
+            epi = std::max(epi, (int)(kEpiWarps * kTmaBoxCi * W * 4));
+        epi = (int)round_up(epi, kEpiWarps * 128);  // each warp's area 128-byte aligned
+        t.epi_stage_bytes = epi;
+        const int budget = kSmemLimit - kBarrierBytes - 1024 - epi;
+        // Each stage carries 128 bytes of grad_out channels per frame element or
+        // weight row (64 bf16/fp16 or 32 fp32 channels): one 128-byte swizzle row.
+        t.kc = 128 / esize;
         t.n_cchunks = (int)cdiv(Co, t.kc);
         t.hbp = (int)round_up(std::max(max_hb, 8), 8);
-        const int64_t a_stage = (int64_t)chunks * t.hbp * 16;
-        const int64_t b_unit = (int64_t)chunks * t.n_tile * 16;  // one tap, one channel chunk
+        const int64_t g_stage = (int64_t)t.hbp * 128;
+        const int64_t w_unit = (int64_t)t.m_tile * 128;  // one tap, one channel chunk
         int64_t packed = 0;
         for (int i = 0; i < np; ++i) {
             PhaseDesc &d = t.ph[i];
             d.pack_off = packed;
-            packed += (int64_t)t.n_ntiles * t.n_cchunks * d.Jh * d.Jw * b_unit;
+            packed += (int64_t)t.n_mtiles * t.n_cchunks * d.Jh * d.Jw * w_unit;
         }
-        if (a_stage > budget) continue;
-        t.a_stage_bytes = (int)a_stage;
-        t.b_unit_bytes = (int)b_unit;
+        if (2 * g_stage > budget) continue;
+        t.g_stage_bytes = (int)g_stage;
+        t.w_unit_bytes = (int)w_unit;
         t.packed_bytes = packed;
-        // Resident weights when they fit beside three A stages.
-        if (packed + 3 * a_stage <= budget && packed <= (int64_t)160 * 1024) {
-            t.nb = 0;
-            t.b_stage_bytes = (int)(max_taps * b_unit);
-            t.na = (int)std::min<int64_t>(4, (budget - packed) / a_stage);
-            ok = t.na >= 2;
-            if (ok) t.smem_bytes = kBarrierBytes + (int)(packed + t.na * a_stage);
-            continue;
+        const int fixed = kBarrierBytes + 1024 + epi;
+        if (packed + 3 * g_stage <= budget) {
+            // Resident weights: loaded once per CTA, beside at least three G stages.
+            t.nw = 0;
+            t.taps_per_w = std::max(max_taps, 1);
+            t.w_stage_bytes = (int)(t.taps_per_w * w_unit);
+            t.ng = (int)std::min<int64_t>(4, (budget - packed) / g_stage);
+            ok = true;
+            t.smem_bytes = fixed + (int)(packed + t.ng * g_stage);
+        } else {
+            // Streamed weights: each W stage holds a group of up to taps_per_w
+            // consecutive taps of one channel chunk; four stages when they fit.
+            const int64_t room = budget - 2 * g_stage;
+            int64_t tpw = std::min<int64_t>(std::max(max_taps, 1), room / (4 * w_unit));
+            if (tpw < 1) tpw = std::min<int64_t>(std::max(max_taps, 1), room / (2 * w_unit));
+            if (tpw >= 1) {
+                t.taps_per_w = (int)tpw;
+                const int64_t w_stage = tpw * w_unit;
+                t.w_stage_bytes = (int)w_stage;
+                t.nw = (int)std::min<int64_t>(4, room / w_stage);
+                t.ng = (int)std::min<int64_t>(4, (budget - t.nw * w_stage) / g_stage);
+                ok = t.ng >= 2 && t.nw >= 2;
+                t.smem_bytes = fixed + (int)(t.nw * w_stage + t.ng * g_stage);
+            }
         }
-        const int64_t b_stage = std::max<int64_t>(1, max_taps) * b_unit;
-        if (2 * b_stage + 2 * a_stage > budget) continue;
-        t.b_stage_bytes = (int)b_stage;
-        t.nb = (int)std::min<int64_t>(4, (budget - 2 * a_stage) / b_stage);
-        t.na = (int)std::min<int64_t>(4, (budget - t.nb * b_stage) / a_stage);
-        ok = t.na >= 2 && t.nb >= 2;
-        if (ok) t.smem_bytes = kBarrierBytes + (int)(t.nb * b_stage + t.na * a_stage);
     }
     if (!ok) return false;
 
     int64_t tiles = 0;
     for (int i = 0; i < np; ++i) {
         t.ph[i].tile_begin = tiles;
-        tiles += (int64_t)t.ph[i].m_tiles * t.n_ntiles;
+        tiles += (int64_t)t.ph[i].p_tiles * t.n_mtiles;
     }
     t.total_tiles = tiles;
 
-    // tcgen05 instruction descriptor: D f32, A/B K-major, M = 128, N = n_tile.
-    uint32_t fmt = dtype == DGRAD_F32 ? 2u : (dtype == DGRAD_BF16 ? 1u : 0u);
-    t.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(t.n_tile >> 3) << 17) |
-              ((uint32_t)(kTileM >> 4) << 24);
-    uint32_t cols = 32;
-    while (cols < (uint32_t)(2 * t.n_tile)) cols *= 2;
+    // tcgen05 instruction descriptor: D f32, A (weights) and B (grad_out
+    // window) K-major, M = m_tile, N = tile_p.
+    const uint32_t fmt = dtype == DGRAD_F32 ? 2u : (dtype == DGRAD_BF16 ? 1u : 0u);
+    t.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(t.tile_p >> 3) << 17) |
+              ((uint32_t)(t.m_tile >> 4) << 24);
+    uint32_t cols = 32;  // double-buffered accumulator, allocated in a power of two
+    while (cols < (uint32_t)(2 * t.tile_p)) cols *= 2;
     t.tmem_cols = cols;
 
     // Pack parameters mirror the layout above.
     PackParams &k = plan->pack;
     std::memset(&k, 0, sizeof(k));
     k.Ci = (int)Ci; k.Co = (int)Co; k.kH = (int)kH; k.kW = (int)kW; k.stride = s;
-    k.n_tile = t.n_tile; k.n_ntiles = t.n_ntiles; k.kc = t.kc; k.n_cchunks = t.n_cchunks;
+    k.m_tile = t.m_tile; k.n_mtiles = t.n_mtiles; k.kc = t.kc; k.n_cchunks = t.n_cchunks;
     k.elems16 = E;
     k.n_phases = np;
     for (int i = 0; i < np; ++i) {

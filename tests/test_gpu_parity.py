@@ -243,6 +243,23 @@ def test_guard_bands_untouched(dg):
         assert err <= TOL["bf16"]
 
 
+def test_grad_in_only_4_byte_aligned(dg):
+    # grad_in needs only element (4-byte) alignment; the kernel must not use
+    # wider stores when the buffer is not 8-byte aligned.
+    wl = workloads.RESNET.with_batch(1)
+    g, w = workloads.make_inputs(wl, seed=4)
+    dev = torch.device("cuda")
+    n = int(np.prod(wl.grad_in_shape))
+    buf = torch.full((n + 1,), 5.0, device=dev, dtype=torch.float32)
+    out = buf[1:].view(wl.grad_in_shape)
+    assert out.data_ptr() % 8 == 4
+    p = dg.params_from_shapes(g.shape, w.shape, wl.H, wl.W, wl.stride, wl.padding_h, wl.padding_w)
+    dg.conv2d_grad_input(g.to(dev), w.to(dev), out, p, dg.DGRAD_BF16)
+    assert dg.conv2d_grad_input_check_errors() == 0
+    assert buf[0].item() == 5.0
+    assert rel_err(out.cpu().numpy(), oracle_full(wl, g, w)) <= TOL["bf16"]
+
+
 def test_deterministic_and_nondefault_stream(dg):
     wl = workloads.RESNET.with_batch(3)
     g, w = workloads.make_inputs(wl, seed=1)
