@@ -198,7 +198,7 @@ def oracle_sample(wl, planes_per_step: int, steps: int, warmup: int):
 def cpu_baseline(wl, budget_s: float = 12.0):
     """The oracle as it stands on the host cores: whole images, repeated for ~budget_s."""
     flops1, dt1, threads, _ = oracle_sample(wl, wl.Ci, 1, 0)
-    reps = max(1, min(int(budget_s / max(dt1, 1e-3)), 200))
+    reps = max(1, min(int(budget_s / max(dt1, 1e-3)), 2000))
     flops, dt, threads, _ = oracle_sample(wl, wl.Ci, reps, 0)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{reps} x one image (all {wl.Ci} input channels) of the {wl.name} "
