@@ -66,16 +66,24 @@ struct PhaseDesc {
 
 struct TcParams {
     CUtensorMap out_map;    // grad_in as [N][Ci][H][W] float32 (TMA store epilogue only)
+    CUtensorMap in_map;     // grad_out as [N][Co][OH][OW] (TMA gather only)
     const void *grad_out;
     const void *packed;
     float *grad_in;
     int N, Ci, H, W, Co, OH, OW, stride;
+    int esize;              // bytes per grad_out / weight element
     int n_phases;
     int m_tile, n_mtiles;   // input channels per tile (MMA M: 64 or 128) and tiles over Ci
     int tile_p;             // accumulator columns per tile (MMA N)
     int rows_per_tile;      // > 0: tiles are whole frame rows (stride 1), this many per tile
     int epi_tma;            // 1: epilogue stores through TMA (set at launch)
     int epi_stage_bytes;    // shared-memory staging of the epilogue
+    // TMA gather (stride 1, whole-row tiles, resident weights): grad_out rows
+    // arrive as [raw_cs channels][raw_br rows][raw_bw columns] slices starting
+    // at column raw_x0, through a ring of raw_nr slots, and are transposed in
+    // shared memory into the frame window.
+    int gather_tma;         // 1: use it (set at launch)
+    int raw_nr, raw_cs, raw_br, raw_bw, raw_x0, raw_slice_bytes;
     int kc, n_cchunks;      // grad_out channels per stage (128 bytes), stages per tile
     int hbp;                // frame elements per G stage (multiple of 8)
     int g_stage_bytes;      // grad_out frame window stage

@@ -43,7 +43,7 @@ __device__ unsigned int g_dgrad_error_word = 0;
 namespace {
 
 struct Shared {
-    uint64_t full_g[4], empty_g[4], full_w[4], empty_w[4];
+    uint64_t full_g[4], empty_g[4], full_w[4], empty_w[4], full_raw[2], empty_raw[2];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t w_full, mma_done;
     uint32_t tmem_base;
@@ -108,6 +108,38 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
             "r"(dst),
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+
+// TMA tensor load of one box into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            int z, int w, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_shared_tf32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+    return r;
+}
+
+__device__ __forceinline__ void prefetch_line_l2(const void *ptr) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -360,8 +392,97 @@ __device__ __forceinline__ int64_t w_block_off(const TcParams &p, const PhaseDes
 }
 
 // ------------------------------------------------------------------ roles
+// L2 prefetch of the grad_out rows every tile of this CTA will gather: per
+// image the tile's window touches, per grad_out channel, one contiguous run of
+// whole rows, fetched with a bulk prefetch (16-byte aligned, clamped to the
+// tensor).  The gather warps' scalar loads then hit L2 instead of waiting on
+// DRAM one miss at a time.
+__device__ void prefetch_windows(const TcParams &p, int64_t first_tile) {
+    const int esize = p.esize;
+    const uint64_t base = reinterpret_cast<uint64_t>(p.grad_out);
+    const uint64_t total = (uint64_t)p.N * p.Co * p.OH * p.OW * esize;
+    const uint64_t plane = (uint64_t)p.OH * p.OW * esize, row = (uint64_t)p.OW * esize;
+    for (int64_t t = first_tile; t < p.total_tiles; t += gridDim.x) {
+        const Tile ti = decode_tile(p, t);
+        if (ti.mt != 0) continue;  // the window is the same for every channel tile
+        const PhaseDesc &d = p.ph[ti.phase];
+        if (d.Jh == 0) continue;
+        const int img = d.R * d.X;
+        const int L0 = tile_start(p, d, ti.pt), L1 = L0 + p.hbp - 1;
+        for (int n = L0 / img; n <= L1 / img && n < p.N; ++n) {
+            const int a = L0 > n * img ? L0 - n * img : 0;
+            const int b = L1 < (n + 1) * img - 1 ? L1 - n * img : img - 1;
+            int u0 = a / d.X - (d.Jh - 1) + d.qh, u1 = b / d.X - (d.Jh - 1) + d.qh;
+            u0 = u0 < 0 ? 0 : u0;
+            u1 = u1 >= p.OH ? p.OH - 1 : u1;
+            if (u0 > u1) continue;
+            for (int co = 0; co < p.Co; ++co) {
+                uint64_t lo = base + ((uint64_t)n * p.Co + co) * plane + (uint64_t)u0 * row;
+                uint64_t hi = lo + (uint64_t)(u1 - u0 + 1) * row;
+                lo = (lo + 15) & ~15ull;
+                hi = hi & ~15ull;
+                if (hi > base + total) hi = (base + total) & ~15ull;
+                if (hi > lo) prefetch_l2(reinterpret_cast<const void *>(lo), (uint32_t)(hi - lo));
+            }
+        }
+    }
+}
+
+// First grad_out row of a whole-row tile's window, and its image.
+__device__ __forceinline__ void row_tile_origin(const TcParams &p, const PhaseDesc &d, int pt,
+                                                int &n, int &u_first) {
+    const int tpi = (d.Hr + p.rows_per_tile - 1) / p.rows_per_tile;
+    n = pt / tpi;
+    u_first = (pt - n * tpi) * p.rows_per_tile - (d.Jh - 1) + d.qh;
+}
+
+// TMA gather producer (warp 5, lane 0, after the resident weights): for every
+// tile and channel chunk of this CTA, the raw grad_out slices of the tile's
+// window -- raw_cs channels x raw_br rows x raw_bw columns from column raw_x0
+// -- into the raw ring.  Rows and columns outside grad_out are zero-filled by
+// the TMA unit.
+__device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base) {
+    const uint32_t box_bytes = (uint32_t)(p.raw_cs * p.raw_br * p.raw_bw * p.esize);
+    const int slices = p.kc / p.raw_cs;
+    int slot = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    bool aborted = false;
+    for (int64_t t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
+        const Tile ti = decode_tile(p, t);
+        const PhaseDesc &d = p.ph[ti.phase];
+        if (d.Jh == 0) continue;
+        int n, u_first;
+        row_tile_origin(p, d, ti.pt, n, u_first);
+        for (int cc = 0; cc < p.n_cchunks && !aborted; ++cc) {
+            for (int sl = 0; sl < slices; ++sl) {
+                if (!wait_bar(smem_u32(&sh.empty_raw[slot]), phase ^ 1u, p, sh)) {
+                    aborted = true;
+                    break;
+                }
+                const uint32_t full = smem_u32(&sh.full_raw[slot]);
+                mbar_arrive_expect_tx(full, box_bytes);
+                tma_load_4d(raw_base + (uint32_t)slot * p.raw_slice_bytes, &p.in_map, p.raw_x0,
+                            u_first, cc * p.kc + sl * p.raw_cs, n, full);
+                ++issued;
+                if (++slot == p.raw_nr) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    }
+    if (aborted) {
+        const int64_t k_end = issued < p.raw_nr ? issued : p.raw_nr;
+        for (int64_t k = 0; k < k_end; ++k) {
+            const int64_t q = issued - 1 - k;
+            wait_drain(smem_u32(&sh.full_raw[q % p.raw_nr]), (uint32_t)((q / p.raw_nr) & 1), p, sh);
+        }
+    }
+}
+
 // Warp 5, lane 0: packed weights into shared memory with bulk copies.
-__device__ void role_weights(const TcParams &p, Shared &sh, uint32_t w_base) {
+__device__ void role_weights(const TcParams &p, Shared &sh, uint32_t w_base, uint32_t raw_base) {
     const uint8_t *src = static_cast<const uint8_t *>(p.packed);
     if (p.nw == 0) {
         const uint32_t bar = smem_u32(&sh.w_full);
@@ -370,9 +491,15 @@ __device__ void role_weights(const TcParams &p, Shared &sh, uint32_t w_base) {
             const int64_t left = p.packed_bytes - off;
             bulk_g2s(w_base + (uint32_t)off, src + off, (uint32_t)(left < 32768 ? left : 32768), bar);
         }
+        if (p.gather_tma) {
+            raw_producer(p, sh, raw_base);
+        } else {
+            prefetch_windows(p, blockIdx.x);
+        }
         wait_drain(bar, 0, p, sh);  // never leave a copy in flight
         return;
     }
+    prefetch_windows(p, blockIdx.x);
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
@@ -494,6 +621,102 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
     // No MMA may still be running when TMEM is released.
     tc_commit(smem_u32(&sh.mma_done));
     wait_drain(smem_u32(&sh.mma_done), 0, p, sh);
+}
+
+// Gather warps, TMA variant: the frame window of each stage is assembled
+// from raw slices (raw_cs channels of whole grad_out rows) by a transpose in
+// shared memory: frame element h, channel c comes from slice row h / X,
+// column (h mod X) + vmin - raw_x0.  Each slice fills two 16-byte chunks of
+// every 128-byte window row.
+template <int ESIZE>
+__device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
+                                uint32_t raw_base, int gw, int lane) {
+    constexpr int E = 16 / ESIZE;  // elements per 16-byte chunk
+    const int slices = p.kc / p.raw_cs;
+    int stage = 0, rs = 0;
+    uint32_t phase = 0, rph = 0;
+    bool withhold = (p.debug_flags & DGRAD_DEBUG_SKIP_ARRIVE) && gw == 0;
+    const uint32_t row_bytes = (uint32_t)(p.raw_bw * ESIZE);
+    const uint32_t ch_bytes = row_bytes * (uint32_t)p.raw_br;
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        const Tile ti = decode_tile(p, t);
+        const PhaseDesc &d = p.ph[ti.phase];
+        if (d.Jh == 0) continue;
+        const int xoff = -(d.Jw - 1) + d.qw - p.raw_x0;  // raw column of frame column 0
+        // The next tile's window rows (all channels) into L2, spread over the
+        // gather threads: its TMA slices then come from L2, not DRAM.
+        if (t + gridDim.x < p.total_tiles) {
+            const Tile tn = decode_tile(p, t + gridDim.x);
+            const PhaseDesc &dn = p.ph[tn.phase];
+            if (dn.Jh > 0 && tn.mt == 0) {
+                int n2, u2;
+                row_tile_origin(p, dn, tn.pt, n2, u2);
+                const char *base = static_cast<const char *>(p.grad_out);
+                const int64_t rowb = (int64_t)p.OW * p.esize;
+                const int segs = p.Co * p.raw_br;
+                for (int k = gw * 32 + lane; k < 2 * segs; k += kGWarps * 32) {
+                    const int seg = k >> 1, ch = seg / p.raw_br, u = u2 + seg - ch * p.raw_br;
+                    if (u < 0 || u >= p.OH) continue;
+                    const int64_t off = (((int64_t)n2 * p.Co + ch) * p.OH + u) * rowb +
+                                        ((k & 1) ? rowb - 1 : 0);
+                    prefetch_line_l2(base + off);
+                }
+            }
+        }
+        for (int cc = 0; cc < p.n_cchunks; ++cc) {
+            if (!wait_bar_warp(smem_u32(&sh.empty_g[stage]), phase ^ 1u, p, sh, lane)) return;
+            const uint32_t s_base = g_base + (uint32_t)stage * p.g_stage_bytes;
+            for (int sl = 0; sl < slices; ++sl) {
+                if (!wait_bar_warp(smem_u32(&sh.full_raw[rs]), rph, p, sh, lane)) return;
+                const uint32_t raw = raw_base + (uint32_t)rs * p.raw_slice_bytes;
+                for (int h = gw * 32 + lane; h < p.hbp; h += kGWarps * 32) {
+                    const int rho = h / d.X;
+                    const int x = h - rho * d.X + xoff;
+                    const uint32_t src = raw + (uint32_t)rho * row_bytes + (uint32_t)x * ESIZE;
+                    uint32_t q[2][4];
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        if constexpr (ESIZE == 2) {
+#pragma unroll
+                            for (int e = 0; e < 8; e += 2) {
+                                const uint32_t c = (uint32_t)(j * 8 + e);
+                                q[j][e / 2] = ld_shared_u16(src + c * ch_bytes) |
+                                              (ld_shared_u16(src + (c + 1) * ch_bytes) << 16);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                q[j][e] = ld_shared_tf32(src + (uint32_t)(j * 4 + e) * ch_bytes);
+                        }
+                    }
+                    const uint32_t row = s_base + (uint32_t)h * 128u;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        st_shared_v4(row + (uint32_t)(((2 * sl + j) ^ (h & 7)) << 4), q[j][0],
+                                     q[j][1], q[j][2], q[j][3]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&sh.empty_raw[rs]));
+                if (++rs == p.raw_nr) {
+                    rs = 0;
+                    rph ^= 1u;
+                }
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+                if (withhold)
+                    withhold = false;  // failure injection: this stage is never signalled
+                else
+                    mbar_arrive(smem_u32(&sh.full_g[stage]));
+            }
+            if (++stage == p.ng) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    (void)E;
 }
 
 // Gather warps: grad_out frame windows into 128-byte swizzled K-major rows
@@ -756,7 +979,9 @@ __global__ void __launch_bounds__(kThreads, 1) dgrad_tc_kernel(const __grid_cons
     Shared &sh = *reinterpret_cast<Shared *>(smem);
     // Rings start on a 1024-byte boundary: the swizzle pattern is tied to it.
     const uint32_t epi_stage = smem_u32(smem) + kBarrierBytes;
-    const uint32_t g_base = (epi_stage + (uint32_t)p.epi_stage_bytes + 1023u) & ~1023u;
+    const uint32_t raw_base = (epi_stage + (uint32_t)p.epi_stage_bytes + 1023u) & ~1023u;
+    const uint32_t g_base =
+        (raw_base + (uint32_t)(p.raw_nr * p.raw_slice_bytes) + 1023u) & ~1023u;
     const uint32_t w_base = g_base + (uint32_t)(p.ng * p.g_stage_bytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -772,6 +997,8 @@ __global__ void __launch_bounds__(kThreads, 1) dgrad_tc_kernel(const __grid_cons
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&sh.acc_full[s]), 1);
             mbar_init(smem_u32(&sh.acc_empty[s]), kEpiWarps);
+            mbar_init(smem_u32(&sh.full_raw[s]), 1);
+            mbar_init(smem_u32(&sh.empty_raw[s]), kGWarps);
         }
         mbar_init(smem_u32(&sh.w_full), 1);
         mbar_init(smem_u32(&sh.mma_done), 1);
@@ -788,13 +1015,16 @@ __global__ void __launch_bounds__(kThreads, 1) dgrad_tc_kernel(const __grid_cons
     const uint32_t tmem = sh.tmem_base;
 
     if (warp == kWWarp) {
-        if (lane == 0) role_weights(p, sh, w_base);
+        if (lane == 0) role_weights(p, sh, w_base, raw_base);
         __syncwarp();
     } else if (warp == kMmaWarp) {
         if (lane == 0) role_mma<ESIZE == 4>(p, sh, g_base, w_base, tmem);
         __syncwarp();
     } else if (warp >= kGWarp0) {
-        role_gather<ESIZE>(p, sh, g_base, warp - kGWarp0, lane);
+        if (p.gather_tma)
+            gather_from_raw<ESIZE>(p, sh, g_base, raw_base, warp - kGWarp0, lane);
+        else
+            role_gather<ESIZE>(p, sh, g_base, warp - kGWarp0, lane);
     } else {
         role_epilogue(p, sh, epi_stage, tmem, warp, lane);
     }
@@ -845,6 +1075,30 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// grad_out as a 4-D tensor [N][Co][OH][OW] with a [1][raw_cs][raw_br][raw_bw]
+// load box, for the TMA gather (whole-row tiles with resident weights only).
+bool encode_in_map(TcParams &p) {
+    if (p.raw_nr <= 0 || p.rows_per_tile <= 0 || p.nw != 0) return false;
+    if ((reinterpret_cast<uintptr_t>(p.grad_out) & 15u) != 0) return false;
+    if (((int64_t)p.OW * p.esize) % 16 != 0) return false;
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    const int64_t e = p.esize;
+    const cuuint64_t dims[4] = {(cuuint64_t)p.OW, (cuuint64_t)p.OH, (cuuint64_t)p.Co,
+                                (cuuint64_t)p.N};
+    const cuuint64_t strides[3] = {(cuuint64_t)(p.OW * e), (cuuint64_t)(p.OH * p.OW * e),
+                                   (cuuint64_t)((int64_t)p.Co * p.OH * p.OW * e)};
+    const cuuint32_t box[4] = {(cuuint32_t)p.raw_bw, (cuuint32_t)p.raw_br, (cuuint32_t)p.raw_cs,
+                               1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    const CUtensorMapDataType dt =
+        e == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    CUresult r = fn(&p.in_map, dt, 4, const_cast<void *>(p.grad_out), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // grad_in as a 4-D float32 tensor [N][Ci][H][W] with a [1][16][1][W] store box.
 bool encode_out_map(TcParams &p) {
     if (p.rows_per_tile <= 0 || p.stride != 1 || p.W % 4 != 0 || p.W > 64) return false;
@@ -873,6 +1127,7 @@ int launch_tc(const Plan &plan, const void *grad_out, const void *packed, float 
     p.packed = packed;
     p.grad_in = grad_in;
     p.epi_tma = encode_out_map(p) ? 1 : 0;
+    p.gather_tma = encode_in_map(p) ? 1 : 0;
     int dev = 0;
     cudaError_t de = cudaGetDevice(&dev);
     if (de != cudaSuccess) return (int)de;

@@ -31,6 +31,7 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
 
     t.N = (int)N; t.Ci = (int)Ci; t.H = (int)H; t.W = (int)W; t.Co = (int)Co;
     t.OH = (int)p.out_h; t.OW = (int)p.out_w; t.stride = s;
+    t.esize = esize;
 
     // Input channels on the MMA M side: one 64-row tile, or 128-row tiles.
     t.m_tile = Ci <= 64 ? 64 : 128;
@@ -105,7 +106,28 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
             epi = std::max(epi, (int)(kEpiWarps * kTmaBoxCi * W * 4));
         epi = (int)round_up(epi, kEpiWarps * 128);  // each warp's area 128-byte aligned
         t.epi_stage_bytes = epi;
-        const int budget = kSmemLimit - kBarrierBytes - 1024 - epi;
+        // Raw grad_out slices for the TMA gather (reserved when it can apply).
+        int raw = 0;
+        t.raw_nr = 0;
+        if (rows_per_tile > 0 && (p.out_w * (int64_t)esize) % 16 == 0) {
+            const int A = 16 / esize;                      // elements per 16 bytes
+            const int64_t vmin = -(int64_t)(kW - 1) + p.padding_w;
+            const int64_t vmax = W - 1 + p.padding_w;
+            const int64_t x0 = vmin >= 0 ? vmin / A * A : -((-vmin + A - 1) / A) * A;
+            t.raw_x0 = (int)x0;
+            t.raw_bw = (int)round_up(vmax - x0 + 1, A);
+            const int64_t X1 = W + kW - 1;
+            t.raw_cs = 32 / esize;                         // two 16-byte chunks per slice
+            // rows of one window: kTileP-sized tiles never exceed this
+            const int64_t hbp1 = round_up(tile_p + (kH - 1) * X1 + (kW - 1), 8);
+            t.raw_br = (int)((hbp1 - 1) / X1 + 1);
+            t.raw_slice_bytes = (int)round_up((int64_t)t.raw_cs * t.raw_br * t.raw_bw * esize, 128);
+            if (t.raw_bw <= 256 && t.raw_br <= 256) {
+                t.raw_nr = 2;
+                raw = t.raw_nr * t.raw_slice_bytes;
+            }
+        }
+        const int budget = kSmemLimit - kBarrierBytes - 2048 - epi - raw;
         // Each stage carries 128 bytes of grad_out channels per frame element or
         // weight row (64 bf16/fp16 or 32 fp32 channels): one 128-byte swizzle row.
         t.kc = 128 / esize;
@@ -123,9 +145,10 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
         t.g_stage_bytes = (int)g_stage;
         t.w_unit_bytes = (int)w_unit;
         t.packed_bytes = packed;
-        const int fixed = kBarrierBytes + 1024 + epi;
-        if (packed + 3 * g_stage <= budget) {
-            // Resident weights: loaded once per CTA, beside at least three G stages.
+        const int fixed = kBarrierBytes + 2048 + epi + raw;
+        if (packed + (raw ? 2 : 3) * g_stage <= budget) {
+            // Resident weights: loaded once per CTA, beside at least three G
+            // stages (two when the TMA gather's raw ring also needs room).
             t.nw = 0;
             t.taps_per_w = std::max(max_taps, 1);
             t.w_stage_bytes = (int)(t.taps_per_w * w_unit);
