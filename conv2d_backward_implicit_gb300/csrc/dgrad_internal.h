@@ -49,7 +49,7 @@ constexpr int kSmemLimit = 232448;  // 227 KB dynamic shared memory per block
 constexpr int kBarrierBytes = 1024;
 constexpr int kEpiChunk = 32;                 // positions per step of the staged epilogue
 constexpr int kEpiRowFloats = kEpiChunk + 1;  // padded staging row (conflict-free)
-constexpr int kTmaBoxCi = 16;                 // channels per TMA store box
+constexpr int kTmaBoxCi = 8;                  // channels per TMA store box (two per warp)
 
 struct PhaseDesc {
     int rh, rw;         // residues of (ih, iw) modulo the stride

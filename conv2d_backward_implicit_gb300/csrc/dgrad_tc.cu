@@ -43,7 +43,7 @@ __device__ unsigned int g_dgrad_error_word = 0;
 namespace {
 
 struct Shared {
-    uint64_t full_g[4], empty_g[4], full_w[4], empty_w[4], full_raw[2], empty_raw[2];
+    uint64_t full_g[4], empty_g[4], full_w[4], empty_w[4], full_raw[4], empty_raw[4];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t w_full, mma_done;
     uint32_t tmem_base;
@@ -91,6 +91,17 @@ __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// Programmatic dependent launch: wait until the preceding kernel of the
+// stream has completed and its writes are visible; let the next kernel of the
+// stream start its own prologue.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void fence_barrier_init() {
@@ -256,8 +267,9 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t sm
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-__device__ __forceinline__ void bulk_wait_read_all() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// At most one of this thread's bulk groups may still be reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all_but_one() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
 __device__ __forceinline__ void bulk_wait_all() {
@@ -277,6 +289,14 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t *r) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(taddr)
+                 : "memory");
+}
+
+// Waits for this thread's outstanding TMEM loads into r[0..63].
+__device__ __forceinline__ void tmem_wait_ld64(uint32_t (&r)[64]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]), "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63])
+                 :
                  : "memory");
 }
 
@@ -672,21 +692,25 @@ __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
                 for (int h = gw * 32 + lane; h < p.hbp; h += kGWarps * 32) {
                     const int rho = h / d.X;
                     const int x = h - rho * d.X + xoff;
-                    const uint32_t src = raw + (uint32_t)rho * row_bytes + (uint32_t)x * ESIZE;
-                    uint32_t q[2][4];
+                    const bool inside = x >= 0 && x < p.raw_bw;  // else a zero column of the frame
+                    const uint32_t src =
+                        raw + (uint32_t)rho * row_bytes + (uint32_t)(inside ? x : 0) * ESIZE;
+                    uint32_t q[2][4] = {};
+                    if (inside) {
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        if constexpr (ESIZE == 2) {
+                        for (int j = 0; j < 2; ++j) {
+                            if constexpr (ESIZE == 2) {
 #pragma unroll
-                            for (int e = 0; e < 8; e += 2) {
-                                const uint32_t c = (uint32_t)(j * 8 + e);
-                                q[j][e / 2] = ld_shared_u16(src + c * ch_bytes) |
-                                              (ld_shared_u16(src + (c + 1) * ch_bytes) << 16);
+                                for (int e = 0; e < 8; e += 2) {
+                                    const uint32_t c = (uint32_t)(j * 8 + e);
+                                    q[j][e / 2] = ld_shared_u16(src + c * ch_bytes) |
+                                                  (ld_shared_u16(src + (c + 1) * ch_bytes) << 16);
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    q[j][e] = ld_shared_tf32(src + (uint32_t)(j * 4 + e) * ch_bytes);
                             }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                q[j][e] = ld_shared_tf32(src + (uint32_t)(j * 4 + e) * ch_bytes);
                         }
                     }
                     const uint32_t row = s_base + (uint32_t)h * 128u;
@@ -883,46 +907,61 @@ __device__ void epilogue_staged(const TcParams &p, const PhaseDesc &d, const Til
 
 // TMA-store epilogue (stride 1, tiles of whole frame rows, W a multiple of 4
 // up to 64, grad_in 16-byte aligned): for each output row of the tile and
-// each 16-lane group, the warp copies the row's W accumulator columns into a
-// dense [16 channels][W] box in shared memory and one lane stores the box with
-// a TMA tensor store, so grad_in is written in whole, aligned rows.
+// each 16-lane group, the warp loads the row's W accumulator columns, copies
+// them into dense [8 channels][W] boxes in shared memory and one lane stores
+// each box with a TMA tensor store, so grad_in is written in whole, aligned
+// rows.  The warp's two boxes alternate: staging one overlaps the TMA unit's
+// read of the other.
 __device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &ti,
-                             uint32_t taddr, uint32_t box, int q, int lane) {
+                             uint32_t taddr, uint32_t boxes, int q, int lane) {
     const int groups = p.m_tile == 64 ? 1 : 2;
     const int tpi = (d.Hr + p.rows_per_tile - 1) / p.rows_per_tile;
     const int n = ti.pt / tpi, a0 = (ti.pt - n * tpi) * p.rows_per_tile;
     const int W = p.W;
+    const uint32_t box_bytes = (uint32_t)(kTmaBoxCi * W * 4);
     for (int gi = 0; gi < groups; ++gi) {
         const int ci0 = ti.mt * p.m_tile + q * 16 * groups + 16 * gi;
         if (ci0 >= p.Ci) break;
-        // Rows of this 16-lane group: lanes 16*gi .. 16*gi+15 of the quadrant.
-        const bool mine = (lane >> 4) == gi;
-        const uint32_t row_addr = box + 4u * (uint32_t)(W * (lane & 15));
+        // Rows of this 16-lane group: lanes 16*gi .. 16*gi+15 of the quadrant;
+        // lanes 8h .. 8h+7 of the group fill box h.
+        const int lg = lane - 16 * gi;
+        const bool mine = lg >= 0 && lg < 16;
+        const int half_of_lane = (lg >> 3) & 1;
+        const uint32_t row_addr =
+            boxes + (uint32_t)half_of_lane * box_bytes + 4u * (uint32_t)(W * (lg & 7));
         for (int r = 0; r < p.rows_per_tile && a0 + r < d.Hr; ++r) {
             const uint32_t cbase = taddr + (uint32_t)(r * d.X);
-            // The previous box of this warp must have been read by the TMA unit.
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
-            for (int c = 0; c < W; c += 16) {
-                uint32_t v[16] = {};
+            uint32_t v[64];
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) {
+                if (c >= W) break;
+                uint32_t *vc = v + c;
                 if (W - c >= 16) {
-                    tmem_ld16(cbase + (uint32_t)c, v);
+                    tmem_ld16(cbase + (uint32_t)c, *reinterpret_cast<uint32_t(*)[16]>(vc));
                 } else if (W - c >= 8) {
-                    tmem_ld8(cbase + (uint32_t)c, v);
-                    if (W - c > 8) tmem_ld4(cbase + (uint32_t)c + 8u, v + 8);
+                    tmem_ld8(cbase + (uint32_t)c, vc);
+                    if (W - c > 8) tmem_ld4(cbase + (uint32_t)c + 8u, vc + 8);
                 } else {
-                    tmem_ld4(cbase + (uint32_t)c, v);
-                }
-                tmem_wait_ld16(v);
-                if (mine) {
-                    const int m = W - c < 16 ? W - c : 16;
-                    for (int e = 0; e < m; e += 4)
-                        st_shared_v4(row_addr + 4u * (c + e), v[e], v[e + 1], v[e + 2], v[e + 3]);
+                    tmem_ld4(cbase + (uint32_t)c, vc);
                 }
             }
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) tma_store_4d(&p.out_map, box, 0, a0 + r, ci0, n);
+            tmem_wait_ld64(v);
+            for (int h = 0; h < 2; ++h) {
+                // The store that last read box h must be done reading.
+                if (lane == 0) bulk_wait_read_all_but_one();
+                __syncwarp();
+                if (mine && half_of_lane == h) {
+#pragma unroll
+                    for (int e = 0; e < 64; e += 4)
+                        if (e < W)
+                            st_shared_v4(row_addr + 4u * e, v[e], v[e + 1], v[e + 2], v[e + 3]);
+                }
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0 && ci0 + 8 * h < p.Ci)
+                    tma_store_4d(&p.out_map, boxes + (uint32_t)h * box_bytes, 0, a0 + r,
+                                 ci0 + 8 * h, n);
+            }
         }
     }
 }
@@ -997,6 +1036,8 @@ __global__ void __launch_bounds__(kThreads, 1) dgrad_tc_kernel(const __grid_cons
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&sh.acc_full[s]), 1);
             mbar_init(smem_u32(&sh.acc_empty[s]), kEpiWarps);
+        }
+        for (int s = 0; s < p.raw_nr; ++s) {
             mbar_init(smem_u32(&sh.full_raw[s]), 1);
             mbar_init(smem_u32(&sh.empty_raw[s]), kGWarps);
         }
@@ -1013,6 +1054,10 @@ __global__ void __launch_bounds__(kThreads, 1) dgrad_tc_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
+    // Everything above touched only this CTA's shared memory and TMEM, so it
+    // may overlap the previous kernel; global memory is used only from here.
+    if (threadIdx.x == 0) grid_launch_dependents();
+    grid_dependency_wait();
 
     if (warp == kWWarp) {
         if (lane == 0) role_weights(p, sh, w_base, raw_base);
@@ -1050,7 +1095,20 @@ int launch_variant(const TcParams &p, int grid, cudaStream_t st, int dev) {
         if (e != cudaSuccess) return (int)e;
         configured.fetch_or(bit);
     }
-    kern<<<grid, kThreads, p.smem_bytes, st>>>(p);
+    // Launched with programmatic stream serialization: the prologue of this
+    // kernel may overlap the tail of the previous one (see grid_dependency_wait).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)p.smem_bytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
 }
 
@@ -1103,7 +1161,7 @@ bool encode_in_map(TcParams &p) {
 bool encode_out_map(TcParams &p) {
     if (p.rows_per_tile <= 0 || p.stride != 1 || p.W % 4 != 0 || p.W > 64) return false;
     if ((reinterpret_cast<uintptr_t>(p.grad_in) & 15u) != 0) return false;
-    if (p.epi_stage_bytes < kEpiWarps * kTmaBoxCi * p.W * 4) return false;
+    if (p.epi_stage_bytes < kEpiWarps * 2 * kTmaBoxCi * p.W * 4) return false;
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)p.Ci,

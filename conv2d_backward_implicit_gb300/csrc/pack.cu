@@ -33,6 +33,11 @@ template <typename T>
 __global__ void __launch_bounds__(256) pack_weight_kernel(const T *__restrict__ w,
                                                           T *__restrict__ out,
                                                           const __grid_constant__ PackParams k) {
+    // Launched with programmatic stream serialization: let the next kernel
+    // start its prologue, and wait for the previous kernel (which may still
+    // read `out` or produce `w`) before touching global memory.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t stride_all = (int64_t)gridDim.x * blockDim.x;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < k.total_elems;
          idx += stride_all) {
@@ -76,13 +81,25 @@ int launch_pack(const Plan &plan, const void *weight, void *packed, void *stream
     int64_t blocks = (k.total_elems + threads - 1) / threads;
     if (blocks > 4096) blocks = 4096;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(threads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
     if (plan.esize == 4) {
-        pack_weight_kernel<float><<<(int)blocks, threads, 0, st>>>(
-            static_cast<const float *>(weight), static_cast<float *>(packed), k);
+        e = cudaLaunchKernelEx(&cfg, pack_weight_kernel<float>, static_cast<const float *>(weight),
+                               static_cast<float *>(packed), k);
     } else {
-        pack_weight_kernel<unsigned short><<<(int)blocks, threads, 0, st>>>(
-            static_cast<const unsigned short *>(weight), static_cast<unsigned short *>(packed), k);
+        e = cudaLaunchKernelEx(&cfg, pack_weight_kernel<unsigned short>,
+                               static_cast<const unsigned short *>(weight),
+                               static_cast<unsigned short *>(packed), k);
     }
+    if (e != cudaSuccess) return (int)e;
     return (int)cudaGetLastError();
 }
 

@@ -99,11 +99,11 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
         // Shared memory: barriers, 1 KB to align the rings to 1024 B, then the
         // grad_out (G) ring and the weight (W) ring.
         // Epilogue staging: padded 33-float rows per channel of a warp, or (TMA
-        // store epilogue, stride 1 with W a multiple of 4 up to 64) one box of
-        // 16 channels x W floats per warp.
+        // store epilogue, stride 1 with W a multiple of 4 up to 64) two boxes
+        // of 8 channels x W floats per warp.
         int epi = kEpiWarps * (t.m_tile / 4) * kEpiRowFloats * 4;
         if (rows_per_tile > 0 && W % 4 == 0 && W <= 64)
-            epi = std::max(epi, (int)(kEpiWarps * kTmaBoxCi * W * 4));
+            epi = std::max(epi, (int)(kEpiWarps * 2 * kTmaBoxCi * W * 4));
         epi = (int)round_up(epi, kEpiWarps * 128);  // each warp's area 128-byte aligned
         t.epi_stage_bytes = epi;
         // Raw grad_out slices for the TMA gather (reserved when it can apply).
@@ -113,9 +113,12 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
             const int A = 16 / esize;                      // elements per 16 bytes
             const int64_t vmin = -(int64_t)(kW - 1) + p.padding_w;
             const int64_t vmax = W - 1 + p.padding_w;
-            const int64_t x0 = vmin >= 0 ? vmin / A * A : -((-vmin + A - 1) / A) * A;
+            // Only columns inside grad_out carry data: the box spans them (from
+            // an aligned start), the transpose writes zero elsewhere.
+            const int64_t lo = std::max<int64_t>(vmin, 0), hi = std::min<int64_t>(vmax, p.out_w - 1);
+            const int64_t x0 = lo / A * A;
             t.raw_x0 = (int)x0;
-            t.raw_bw = (int)round_up(vmax - x0 + 1, A);
+            t.raw_bw = (int)round_up(std::max<int64_t>(hi - x0 + 1, 1), A);
             const int64_t X1 = W + kW - 1;
             t.raw_cs = 32 / esize;                         // two 16-byte chunks per slice
             // rows of one window: kTileP-sized tiles never exceed this
@@ -123,7 +126,7 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
             t.raw_br = (int)((hbp1 - 1) / X1 + 1);
             t.raw_slice_bytes = (int)round_up((int64_t)t.raw_cs * t.raw_br * t.raw_bw * esize, 128);
             if (t.raw_bw <= 256 && t.raw_br <= 256) {
-                t.raw_nr = 2;
+                t.raw_nr = 3;
                 raw = t.raw_nr * t.raw_slice_bytes;
             }
         }
