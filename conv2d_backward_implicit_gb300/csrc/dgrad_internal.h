@@ -39,17 +39,17 @@ namespace dgrad {
 
 constexpr int kMaxPhases = 16;  // stride <= 4
 constexpr int kTileP = 256;     // output positions per tile (tcgen05 N); 128 for very wide frames
-constexpr int kEpiWarps = 4;    // warps 0..3: TMEM -> global epilogue
-constexpr int kMmaWarp = 4;     // warp 4: TMEM alloc + MMA issue
-constexpr int kWWarp = 5;       // warp 5: packed-weight bulk copies
-constexpr int kGWarp0 = 6;      // warps 6..: grad_out gather
-constexpr int kGWarps = 8;
+constexpr int kEpiWarps = 8;    // warps 0..7: TMEM -> global epilogue (two per lane quadrant)
+constexpr int kMmaWarp = 8;     // warp 8: TMEM alloc + MMA issue
+constexpr int kWWarp = 9;       // warp 9: packed-weight bulk copies / raw grad_out TMA loads
+constexpr int kGWarp0 = 10;     // warps 10..: grad_out gather
+constexpr int kGWarps = 6;
 constexpr int kThreads = 32 * (kGWarp0 + kGWarps);
 constexpr int kSmemLimit = 232448;  // 227 KB dynamic shared memory per block
 constexpr int kBarrierBytes = 1024;
 constexpr int kEpiChunk = 32;                 // positions per step of the staged epilogue
 constexpr int kEpiRowFloats = kEpiChunk + 1;  // padded staging row (conflict-free)
-constexpr int kTmaBoxCi = 8;                  // channels per TMA store box (two per warp)
+constexpr int kTmaBoxCi = 8;                  // channels per TMA store box (one box per warp)
 
 struct PhaseDesc {
     int rh, rw;         // residues of (ih, iw) modulo the stride

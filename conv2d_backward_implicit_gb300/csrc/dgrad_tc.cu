@@ -267,9 +267,9 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t sm
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-// At most one of this thread's bulk groups may still be reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_all_but_one() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+// None of this thread's bulk groups may still be reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void bulk_wait_all() {
@@ -289,6 +289,14 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t *r) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(taddr)
+                 : "memory");
+}
+
+// Waits for this thread's outstanding TMEM loads into r[0..1][0..15].
+__device__ __forceinline__ void tmem_wait_ld16x2(uint32_t (&r)[2][16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0][0]), "+r"(r[0][1]), "+r"(r[0][2]), "+r"(r[0][3]), "+r"(r[0][4]), "+r"(r[0][5]), "+r"(r[0][6]), "+r"(r[0][7]), "+r"(r[0][8]), "+r"(r[0][9]), "+r"(r[0][10]), "+r"(r[0][11]), "+r"(r[0][12]), "+r"(r[0][13]), "+r"(r[0][14]), "+r"(r[0][15]), "+r"(r[1][0]), "+r"(r[1][1]), "+r"(r[1][2]), "+r"(r[1][3]), "+r"(r[1][4]), "+r"(r[1][5]), "+r"(r[1][6]), "+r"(r[1][7]), "+r"(r[1][8]), "+r"(r[1][9]), "+r"(r[1][10]), "+r"(r[1][11]), "+r"(r[1][12]), "+r"(r[1][13]), "+r"(r[1][14]), "+r"(r[1][15])
+                 :
                  : "memory");
 }
 
@@ -855,81 +863,74 @@ __device__ __forceinline__ int64_t out_offset(const TcParams &p, const PhaseDesc
     return ((int64_t)f.n * p.Ci * p.H + (p.stride * f.a + d.rh)) * p.W + (p.stride * f.b + d.rw);
 }
 
-// Warps 0..3: TMEM accumulator -> float32 NCHW grad_in.  Warp q drains its
-// TMEM lane quadrant: rows (input channels) 32q..32q+31 for a 128-row tile, or
-// 16q..16q+15 (lanes 0..15 of the quadrant) for a 64-row tile.
+// Warps 0..7: TMEM accumulator -> float32 NCHW grad_in.  Warps q and q + 4
+// share TMEM lane quadrant q: rows (input channels) 32q..32q+31 for a 128-row
+// tile, or 16q..16q+15 (lanes 0..15 of the quadrant) for a 64-row tile; they
+// split the tile's columns (positions) between them ("part" 0 and 1).
 //
-// Staged epilogue (any shape): a step takes 32 columns (positions); the TMEM
-// loads of two steps are in flight per wait; the values are turned around
-// through a padded staging block in shared memory (row pitch 33 floats:
-// conflict-free both ways) so that each store instruction writes 32
-// consecutive positions of one channel.
+// Staged epilogue (any shape): a step takes 32 columns (positions); the values
+// are turned around through a padded staging block in shared memory (row
+// pitch 33 floats: conflict-free both ways) so that each store instruction
+// writes 32 consecutive positions of one channel.  Part p takes the 32-column
+// chunks whose index has parity p.
 template <int ROWS>
 __device__ void epilogue_staged(const TcParams &p, const PhaseDesc &d, const Tile &ti,
-                                uint32_t taddr, uint32_t st_base, int q, int lane) {
+                                uint32_t taddr, uint32_t st_base, int q, int part, int lane) {
     const int64_t HW = (int64_t)p.H * p.W;
     const int ci_base = ti.mt * p.m_tile + q * ROWS;
     int ci_here = p.Ci - ci_base;  // channels of this warp that exist
     ci_here = ci_here < 0 ? 0 : (ci_here > ROWS ? ROWS : ci_here);
     const int L0 = tile_start(p, d, ti.pt), own = tile_own(p, d);
-    FramePos f = frame_pos(d, L0 + lane);
+    FramePos f = frame_pos(d, L0 + part * kEpiChunk + lane);
     const uint32_t st_row = st_base + 4u * kEpiRowFloats * lane;  // row written by this lane
     const uint32_t st_col = st_base + 4u * lane;                  // column read by this lane
-    for (int g0 = 0; g0 < p.tile_p; g0 += 2 * kEpiChunk) {
-        uint32_t v[4][16];
+    for (int c0 = part * kEpiChunk; c0 < p.tile_p; c0 += 2 * kEpiChunk) {
+        uint32_t v[2][16];
+        tmem_ld16(taddr + (uint32_t)c0, v[0]);
+        tmem_ld16(taddr + (uint32_t)(c0 + 16), v[1]);
+        tmem_wait_ld16x2(v);
+        if (lane < ROWS) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) tmem_ld16(taddr + (uint32_t)(g0 + 16 * k), v[k]);
-        tmem_wait_ld4(v);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            if (lane < ROWS) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    st_shared_f32(st_row + 4u * e, v[2 * h + e / 16][e % 16]);
-            }
-            __syncwarp();
-            float val[ROWS];
-#pragma unroll
-            for (int r = 0; r < ROWS; ++r) val[r] = ld_shared_f32(st_col + 4u * kEpiRowFloats * r);
-            __syncwarp();
-            const int col = g0 + h * kEpiChunk + lane;
-            const int64_t o = col < own ? out_offset(p, d, f) : -1;
-            if (o >= 0) {
-                float *out = p.grad_in + o + (int64_t)ci_base * HW;
-#pragma unroll
-                for (int r = 0; r < ROWS; ++r)
-                    if (r < ci_here) out[(int64_t)r * HW] = val[r];
-            }
-            frame_advance(d, f, kEpiChunk);
+            for (int e = 0; e < 32; ++e) st_shared_f32(st_row + 4u * e, v[e / 16][e % 16]);
         }
+        __syncwarp();
+        float val[ROWS];
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) val[r] = ld_shared_f32(st_col + 4u * kEpiRowFloats * r);
+        __syncwarp();
+        const int64_t o = c0 + lane < own ? out_offset(p, d, f) : -1;
+        if (o >= 0) {
+            float *out = p.grad_in + o + (int64_t)ci_base * HW;
+#pragma unroll
+            for (int r = 0; r < ROWS; ++r)
+                if (r < ci_here) out[(int64_t)r * HW] = val[r];
+        }
+        frame_advance(d, f, 2 * kEpiChunk);
     }
 }
 
 // TMA-store epilogue (stride 1, tiles of whole frame rows, W a multiple of 4
-// up to 64, grad_in 16-byte aligned): for each output row of the tile and
-// each 16-lane group, the warp loads the row's W accumulator columns, copies
-// them into dense [8 channels][W] boxes in shared memory and one lane stores
-// each box with a TMA tensor store, so grad_in is written in whole, aligned
-// rows.  The warp's two boxes alternate: staging one overlaps the TMA unit's
-// read of the other.
+// up to 64, grad_in 16-byte aligned): for each output row of the tile (part p
+// takes the rows of parity p) and each group of 8 channels, the warp loads the
+// row's W accumulator columns, copies them into a dense [8 channels][W] box in
+// shared memory and one lane stores the box with a TMA tensor store, so
+// grad_in is written in whole, aligned rows.
 __device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &ti,
-                             uint32_t taddr, uint32_t boxes, int q, int lane) {
+                             uint32_t taddr, uint32_t box, int q, int part, int lane) {
     const int groups = p.m_tile == 64 ? 1 : 2;
     const int tpi = (d.Hr + p.rows_per_tile - 1) / p.rows_per_tile;
     const int n = ti.pt / tpi, a0 = (ti.pt - n * tpi) * p.rows_per_tile;
     const int W = p.W;
-    const uint32_t box_bytes = (uint32_t)(kTmaBoxCi * W * 4);
     for (int gi = 0; gi < groups; ++gi) {
         const int ci0 = ti.mt * p.m_tile + q * 16 * groups + 16 * gi;
         if (ci0 >= p.Ci) break;
         // Rows of this 16-lane group: lanes 16*gi .. 16*gi+15 of the quadrant;
-        // lanes 8h .. 8h+7 of the group fill box h.
+        // lanes 8h .. 8h+7 of the group hold the channels of box pass h.
         const int lg = lane - 16 * gi;
         const bool mine = lg >= 0 && lg < 16;
         const int half_of_lane = (lg >> 3) & 1;
-        const uint32_t row_addr =
-            boxes + (uint32_t)half_of_lane * box_bytes + 4u * (uint32_t)(W * (lg & 7));
-        for (int r = 0; r < p.rows_per_tile && a0 + r < d.Hr; ++r) {
+        const uint32_t row_addr = box + 4u * (uint32_t)(W * (lg & 7));
+        for (int r = part; r < p.rows_per_tile && a0 + r < d.Hr; r += 2) {
             const uint32_t cbase = taddr + (uint32_t)(r * d.X);
             uint32_t v[64];
 #pragma unroll
@@ -947,8 +948,9 @@ __device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &
             }
             tmem_wait_ld64(v);
             for (int h = 0; h < 2; ++h) {
-                // The store that last read box h must be done reading.
-                if (lane == 0) bulk_wait_read_all_but_one();
+                if (ci0 + 8 * h >= p.Ci) break;
+                // The previous store from this box must be done reading it.
+                if (lane == 0) bulk_wait_read_all();
                 __syncwarp();
                 if (mine && half_of_lane == h) {
 #pragma unroll
@@ -958,19 +960,18 @@ __device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &
                 }
                 fence_proxy_async();
                 __syncwarp();
-                if (lane == 0 && ci0 + 8 * h < p.Ci)
-                    tma_store_4d(&p.out_map, boxes + (uint32_t)h * box_bytes, 0, a0 + r,
-                                 ci0 + 8 * h, n);
+                if (lane == 0) tma_store_4d(&p.out_map, box, 0, a0 + r, ci0 + 8 * h, n);
             }
         }
     }
 }
 
 __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uint32_t tmem,
-                              int q, int lane) {
+                              int warp, int lane) {
     const int64_t HW = (int64_t)p.H * p.W;
-    const int rows = p.m_tile == 64 ? 16 : 32;  // channels this warp owns
-    const uint32_t st_base = stage + (uint32_t)(p.epi_stage_bytes / kEpiWarps) * q;
+    const int q = warp & 3, part = warp >> 2;
+    const int rows = p.m_tile == 64 ? 16 : 32;  // channels this warp's quadrant owns
+    const uint32_t st_base = stage + (uint32_t)(p.epi_stage_bytes / kEpiWarps) * warp;
     int acc = 0;
     uint32_t accph = 0;
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
@@ -981,12 +982,12 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
             int ci_here = p.Ci - ci_base;
             ci_here = ci_here < 0 ? 0 : (ci_here > rows ? rows : ci_here);
             const int L0 = tile_start(p, d, ti.pt), own = tile_own(p, d);
-            FramePos f = frame_pos(d, L0 + lane);
-            for (int c0 = 0; c0 < own; c0 += kEpiChunk) {
+            FramePos f = frame_pos(d, L0 + part * kEpiChunk + lane);
+            for (int c0 = part * kEpiChunk; c0 < own; c0 += 2 * kEpiChunk) {
                 const int64_t o = c0 + lane < own ? out_offset(p, d, f) : -1;
                 if (o >= 0)
                     for (int r = 0; r < ci_here; ++r) p.grad_in[o + (int64_t)(ci_base + r) * HW] = 0.f;
-                frame_advance(d, f, kEpiChunk);
+                frame_advance(d, f, 2 * kEpiChunk);
             }
             continue;
         }
@@ -994,11 +995,11 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.tile_p);
         if (p.epi_tma)
-            epilogue_tma(p, d, ti, taddr, st_base, q, lane);
+            epilogue_tma(p, d, ti, taddr, st_base, q, part, lane);
         else if (rows == 16)
-            epilogue_staged<16>(p, d, ti, taddr, st_base, q, lane);
+            epilogue_staged<16>(p, d, ti, taddr, st_base, q, part, lane);
         else
-            epilogue_staged<32>(p, d, ti, taddr, st_base, q, lane);
+            epilogue_staged<32>(p, d, ti, taddr, st_base, q, part, lane);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.acc_empty[acc]));
@@ -1161,7 +1162,7 @@ bool encode_in_map(TcParams &p) {
 bool encode_out_map(TcParams &p) {
     if (p.rows_per_tile <= 0 || p.stride != 1 || p.W % 4 != 0 || p.W > 64) return false;
     if ((reinterpret_cast<uintptr_t>(p.grad_in) & 15u) != 0) return false;
-    if (p.epi_stage_bytes < kEpiWarps * 2 * kTmaBoxCi * p.W * 4) return false;
+    if (p.epi_stage_bytes < kEpiWarps * kTmaBoxCi * p.W * 4) return false;
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)p.Ci,

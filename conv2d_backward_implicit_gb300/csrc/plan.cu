@@ -99,11 +99,11 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
         // Shared memory: barriers, 1 KB to align the rings to 1024 B, then the
         // grad_out (G) ring and the weight (W) ring.
         // Epilogue staging: padded 33-float rows per channel of a warp, or (TMA
-        // store epilogue, stride 1 with W a multiple of 4 up to 64) two boxes
-        // of 8 channels x W floats per warp.
+        // store epilogue, stride 1 with W a multiple of 4 up to 64) one box of
+        // 8 channels x W floats per warp.
         int epi = kEpiWarps * (t.m_tile / 4) * kEpiRowFloats * 4;
         if (rows_per_tile > 0 && W % 4 == 0 && W <= 64)
-            epi = std::max(epi, (int)(kEpiWarps * 2 * kTmaBoxCi * W * 4));
+            epi = std::max(epi, (int)(kEpiWarps * kTmaBoxCi * W * 4));
         epi = (int)round_up(epi, kEpiWarps * 128);  // each warp's area 128-byte aligned
         t.epi_stage_bytes = epi;
         // Raw grad_out slices for the TMA gather (reserved when it can apply).
