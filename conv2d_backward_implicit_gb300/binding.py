@@ -15,7 +15,7 @@ import threading
 from . import build_ext
 
 DGRAD_F32, DGRAD_BF16, DGRAD_F16 = 0, 1, 2
-DGRAD_KERNEL_AUTO, DGRAD_KERNEL_TC, DGRAD_KERNEL_SIMT = 0, 1, 2
+DGRAD_KERNEL_AUTO, DGRAD_KERNEL_TC, DGRAD_KERNEL_SIMT, DGRAD_KERNEL_TC_POSM = 0, 1, 2, 3
 DGRAD_DEBUG_SKIP_ARRIVE = 1
 STATUS = {
     0: "DGRAD_OK", 1: "DGRAD_ERR_INVALID_ARG", 2: "DGRAD_ERR_SHAPE", 3: "DGRAD_ERR_ALIGNMENT",
@@ -155,7 +155,7 @@ def conv2d_grad_input_status_string(status: int) -> str:
 
 
 def conv2d_grad_input_select_kernel(params: Params, dtype: int) -> int:
-    """DGRAD_KERNEL_TC (1) or DGRAD_KERNEL_SIMT (2), or a negative status."""
+    """DGRAD_KERNEL_TC (1), DGRAD_KERNEL_SIMT (2) or DGRAD_KERNEL_TC_POSM (3), or a negative status."""
     return int(library().conv2d_grad_input_select_kernel(ctypes.byref(params), int(dtype)))
 
 

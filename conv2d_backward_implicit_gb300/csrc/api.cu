@@ -28,8 +28,8 @@ bool aligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>
 int plan_for(const conv2d_grad_input_params *p, int dtype, dgrad::Plan *plan) {
     int rc = dgrad::make_plan(p, dtype, g_kernel_choice.load(), plan);
     if (rc != DGRAD_OK) return rc;
-    plan->tc.debug_flags = g_debug_flags.load();
-    plan->tc.wait_limit_ns = g_wait_limit_ns.load();
+    plan->tc.debug_flags = plan->tc_alt.debug_flags = g_debug_flags.load();
+    plan->tc.wait_limit_ns = plan->tc_alt.wait_limit_ns = g_wait_limit_ns.load();
     return DGRAD_OK;
 }
 
@@ -142,11 +142,13 @@ int conv2d_grad_input_select_kernel(const conv2d_grad_input_params *p, int dtype
     if (!p) return -DGRAD_ERR_INVALID_ARG;
     dgrad::Plan plan;
     int rc = plan_for(p, dtype, &plan);
-    return rc == DGRAD_OK ? plan.kernel : -rc;
+    if (rc != DGRAD_OK) return -rc;
+    return plan.kernel == DGRAD_KERNEL_TC && plan.tc.pos_m ? DGRAD_KERNEL_TC_POSM : plan.kernel;
 }
 
 int conv2d_grad_input_set_kernel(int kernel) {
-    if (kernel != DGRAD_KERNEL_AUTO && kernel != DGRAD_KERNEL_TC && kernel != DGRAD_KERNEL_SIMT)
+    if (kernel != DGRAD_KERNEL_AUTO && kernel != DGRAD_KERNEL_TC && kernel != DGRAD_KERNEL_SIMT &&
+        kernel != DGRAD_KERNEL_TC_POSM)
         return -DGRAD_ERR_INVALID_ARG;
     return g_kernel_choice.exchange(kernel);
 }

@@ -50,6 +50,21 @@ constexpr int kBarrierBytes = 1024;
 constexpr int kEpiChunk = 32;                 // positions per step of the staged epilogue
 constexpr int kEpiRowFloats = kEpiChunk + 1;  // padded staging row (conflict-free)
 constexpr int kTmaBoxCi = 8;                  // channels per TMA store box (one box per warp)
+constexpr int kPmPitch = 64;  // positions-on-M mode: frame positions per grad_out row
+constexpr int kPmLeft = 8;    // zero columns before grad_out column 0 in each frame row
+constexpr int kPmMaxKw = 3;   // column taps stacked on N (kW x 64 columns)
+constexpr int kPmEpiWarps = 16;  // positions-on-M roles: warps 0..15 epilogue (4 per quadrant),
+constexpr int kPmMmaWarp = 16;   // 16 MMA, 17 raw loads + weights, 18..21 gather
+constexpr int kPmWWarp = 17;
+constexpr int kPmGWarp0 = 18;
+constexpr int kPmGWarps = 4;
+constexpr int kPmThreads = 32 * (kPmGWarp0 + kPmGWarps);
+constexpr int kPmGroups = 6;  // ldmatrix.x4 groups per gather warp and raw slice (at most)
+// Boundary-exchange buffer of the positions-on-M epilogue: 8 warp pairs x 2
+// slots x 3 (tap, lane) values x 16 floats: block 1 of lane 31, block 2 of
+// lanes 30 and 31.
+constexpr int kPmXSlotBytes = 3 * 16 * 4;
+constexpr int kPmXBytes = 8 * 2 * kPmXSlotBytes;
 
 struct PhaseDesc {
     int rh, rw;         // residues of (ih, iw) modulo the stride
@@ -98,6 +113,13 @@ struct TcParams {
     int smem_bytes;
     int debug_flags;
     uint64_t wait_limit_ns;
+    // Positions-on-M mode (stride 1, Ci <= 64, Co <= 64, kW <= 3, 16-bit,
+    // W <= 56): the MMA takes 128 frame positions on M and the kW column taps
+    // of one kernel row stacked on N (kW x 64 columns); the frame pitch is 64
+    // with kPmLeft zero columns in front of each grad_out row.  See dgrad_tc.cu.
+    int pos_m;
+    int pad_w;              // padding_w: start of the row-tap views in the window
+    int pm_rows;            // window rows holding grad_out data (raw_br >= pm_rows)
     PhaseDesc ph[kMaxPhases];
 };
 
@@ -120,6 +142,8 @@ struct Plan {
     int esize;
     int kernel;          // DGRAD_KERNEL_TC or DGRAD_KERNEL_SIMT
     TcParams tc;         // valid when kernel == TC
+    TcParams tc_alt;     // general-mode plan when tc is positions-on-M (same packed weights),
+                         // used when grad_out is not 16-byte aligned for the TMA gather
     PackParams pack;     // valid when kernel == TC
     SimtParams simt;
     size_t workspace;    // packed-weight bytes (TC), 0 otherwise

@@ -45,6 +45,7 @@ namespace {
 struct Shared {
     uint64_t full_g[4], empty_g[4], full_w[4], empty_w[4], full_raw[4], empty_raw[4];
     uint64_t acc_full[2], acc_empty[2];
+    uint64_t x_full[16], x_empty[16];  // positions-on-M epilogue boundary exchange
     uint64_t w_full, mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -131,6 +132,30 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// TMA tensor prefetch of one box into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *map, int x, int y, int z, int w) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
+// Four 8x8 16-bit matrices, transposed on the way into registers (rows of
+// 16 bytes at the addresses lanes 8m..8m+7 give for matrix m).
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+// Four 8x8 16-bit matrices from registers into rows of 16 bytes.
+__device__ __forceinline__ void stmatrix_x4(uint32_t addr, const uint32_t (&r)[4]) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
     unsigned short v;
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
@@ -143,10 +168,6 @@ __device__ __forceinline__ uint32_t ld_shared_tf32(uint32_t addr) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
     return r;
-}
-
-__device__ __forceinline__ void prefetch_line_l2(const void *ptr) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
 }
 
 __device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes) {
@@ -162,6 +183,15 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 __device__ __forceinline__ void st_shared_f32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ float4 ld_shared_f32x4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
@@ -289,6 +319,14 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t *r) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(taddr)
+                 : "memory");
+}
+
+// Waits for this thread's outstanding TMEM loads into r[0..2][0..15].
+__device__ __forceinline__ void tmem_wait_ld3(uint32_t (&r)[3][16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0][0]), "+r"(r[0][1]), "+r"(r[0][2]), "+r"(r[0][3]), "+r"(r[0][4]), "+r"(r[0][5]), "+r"(r[0][6]), "+r"(r[0][7]), "+r"(r[0][8]), "+r"(r[0][9]), "+r"(r[0][10]), "+r"(r[0][11]), "+r"(r[0][12]), "+r"(r[0][13]), "+r"(r[0][14]), "+r"(r[0][15]), "+r"(r[1][0]), "+r"(r[1][1]), "+r"(r[1][2]), "+r"(r[1][3]), "+r"(r[1][4]), "+r"(r[1][5]), "+r"(r[1][6]), "+r"(r[1][7]), "+r"(r[1][8]), "+r"(r[1][9]), "+r"(r[1][10]), "+r"(r[1][11]), "+r"(r[1][12]), "+r"(r[1][13]), "+r"(r[1][14]), "+r"(r[1][15]), "+r"(r[2][0]), "+r"(r[2][1]), "+r"(r[2][2]), "+r"(r[2][3]), "+r"(r[2][4]), "+r"(r[2][5]), "+r"(r[2][6]), "+r"(r[2][7]), "+r"(r[2][8]), "+r"(r[2][9]), "+r"(r[2][10]), "+r"(r[2][11]), "+r"(r[2][12]), "+r"(r[2][13]), "+r"(r[2][14]), "+r"(r[2][15])
+                 :
                  : "memory");
 }
 
@@ -464,18 +502,50 @@ __device__ __forceinline__ void row_tile_origin(const TcParams &p, const PhaseDe
     u_first = (pt - n * tpi) * p.rows_per_tile - (d.Jh - 1) + d.qh;
 }
 
-// TMA gather producer (warp 5, lane 0, after the resident weights): for every
-// tile and channel chunk of this CTA, the raw grad_out slices of the tile's
-// window -- raw_cs channels x raw_br rows x raw_bw columns from column raw_x0
-// -- into the raw ring.  Rows and columns outside grad_out are zero-filled by
-// the TMA unit.
-__device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base) {
+// Bulk copies of the resident packed weights, completing on w_full.
+__device__ void issue_weights(const TcParams &p, Shared &sh, uint32_t w_base) {
+    const uint8_t *src = static_cast<const uint8_t *>(p.packed);
+    const uint32_t bar = smem_u32(&sh.w_full);
+    mbar_arrive_expect_tx(bar, (uint32_t)p.packed_bytes);
+    for (int64_t off = 0; off < p.packed_bytes; off += 32768) {
+        const int64_t left = p.packed_bytes - off;
+        bulk_g2s(w_base + (uint32_t)off, src + off, (uint32_t)(left < 32768 ? left : 32768), bar);
+    }
+}
+
+// L2 prefetch of every raw slice of tile t (if it exists): the ring's TMA
+// loads of that tile then hit L2.
+constexpr int kRawLookahead = 2;  // general mode: tiles of this CTA prefetched ahead
+__device__ void prefetch_raw_tile(const TcParams &p, int64_t t) {
+    if (t >= p.total_tiles) return;
+    const Tile ti = decode_tile(p, t);
+    const PhaseDesc &d = p.ph[ti.phase];
+    if (d.Jh == 0 || ti.mt != 0) return;  // channel tiles share the window
+    int n, u_first;
+    row_tile_origin(p, d, ti.pt, n, u_first);
+    const int slices = p.kc / p.raw_cs;
+    for (int cc = 0; cc < p.n_cchunks; ++cc)
+        for (int sl = 0; sl < slices; ++sl)
+            tma_prefetch_4d(&p.in_map, p.raw_x0, u_first, cc * p.kc + sl * p.raw_cs, n);
+}
+
+// TMA gather producer (warp 9, lane 0): for every tile and channel chunk of
+// this CTA, the raw grad_out slices of the tile's window -- raw_cs channels x
+// raw_br rows x raw_bw columns from column raw_x0 -- into the raw ring.  Rows
+// and columns outside grad_out are zero-filled by the TMA unit.  The first
+// tile's slices go out before the resident weights (the weights come from L2,
+// grad_out from DRAM).  General mode (a ring shorter than a tile): then the
+// L2 prefetch of the next kRawLookahead tiles, and each later tile prefetches
+// the one kRawLookahead tiles after it.  Positions-on-M mode (the ring holds a
+// whole tile): once all slices of a tile are queued, the next tile's slices
+// are prefetched (earlier, they would compete with the first tile's loads).
+__device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, uint32_t w_base) {
     const uint32_t box_bytes = (uint32_t)(p.raw_cs * p.raw_br * p.raw_bw * p.esize);
     const int slices = p.kc / p.raw_cs;
     int slot = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
-    bool aborted = false;
+    bool aborted = false, rest_issued = false;
     for (int64_t t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
         const Tile ti = decode_tile(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
@@ -484,6 +554,15 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base) {
         row_tile_origin(p, d, ti.pt, n, u_first);
         for (int cc = 0; cc < p.n_cchunks && !aborted; ++cc) {
             for (int sl = 0; sl < slices; ++sl) {
+                if (!rest_issued && issued == p.raw_nr) {
+                    issue_weights(p, sh, w_base);
+                    if (!p.pos_m)
+                        for (int k = 1; k <= kRawLookahead; ++k)
+                            prefetch_raw_tile(p, t + (int64_t)k * gridDim.x);
+                    rest_issued = true;
+                } else if (!p.pos_m && rest_issued && cc == 0 && sl == 0) {
+                    prefetch_raw_tile(p, t + (int64_t)kRawLookahead * gridDim.x);
+                }
                 if (!wait_bar(smem_u32(&sh.empty_raw[slot]), phase ^ 1u, p, sh)) {
                     aborted = true;
                     break;
@@ -499,7 +578,11 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base) {
                 }
             }
         }
+        // Positions-on-M mode (the ring holds a whole tile): all of this
+        // tile's slices are queued, the next tile's go to L2.
+        if (p.pos_m && !aborted) prefetch_raw_tile(p, t + gridDim.x);
     }
+    if (!rest_issued) issue_weights(p, sh, w_base);  // fewer slices than ring slots
     if (aborted) {
         const int64_t k_end = issued < p.raw_nr ? issued : p.raw_nr;
         for (int64_t k = 0; k < k_end; ++k) {
@@ -513,18 +596,13 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base) {
 __device__ void role_weights(const TcParams &p, Shared &sh, uint32_t w_base, uint32_t raw_base) {
     const uint8_t *src = static_cast<const uint8_t *>(p.packed);
     if (p.nw == 0) {
-        const uint32_t bar = smem_u32(&sh.w_full);
-        mbar_arrive_expect_tx(bar, (uint32_t)p.packed_bytes);
-        for (int64_t off = 0; off < p.packed_bytes; off += 32768) {
-            const int64_t left = p.packed_bytes - off;
-            bulk_g2s(w_base + (uint32_t)off, src + off, (uint32_t)(left < 32768 ? left : 32768), bar);
-        }
         if (p.gather_tma) {
-            raw_producer(p, sh, raw_base);
+            raw_producer(p, sh, raw_base, w_base);
         } else {
+            issue_weights(p, sh, w_base);
             prefetch_windows(p, blockIdx.x);
         }
-        wait_drain(bar, 0, p, sh);  // never leave a copy in flight
+        wait_drain(smem_u32(&sh.w_full), 0, p, sh);  // never leave a copy in flight
         return;
     }
     prefetch_windows(p, blockIdx.x);
@@ -671,26 +749,6 @@ __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
         const int xoff = -(d.Jw - 1) + d.qw - p.raw_x0;  // raw column of frame column 0
-        // The next tile's window rows (all channels) into L2, spread over the
-        // gather threads: its TMA slices then come from L2, not DRAM.
-        if (t + gridDim.x < p.total_tiles) {
-            const Tile tn = decode_tile(p, t + gridDim.x);
-            const PhaseDesc &dn = p.ph[tn.phase];
-            if (dn.Jh > 0 && tn.mt == 0) {
-                int n2, u2;
-                row_tile_origin(p, dn, tn.pt, n2, u2);
-                const char *base = static_cast<const char *>(p.grad_out);
-                const int64_t rowb = (int64_t)p.OW * p.esize;
-                const int segs = p.Co * p.raw_br;
-                for (int k = gw * 32 + lane; k < 2 * segs; k += kGWarps * 32) {
-                    const int seg = k >> 1, ch = seg / p.raw_br, u = u2 + seg - ch * p.raw_br;
-                    if (u < 0 || u >= p.OH) continue;
-                    const int64_t off = (((int64_t)n2 * p.Co + ch) * p.OH + u) * rowb +
-                                        ((k & 1) ? rowb - 1 : 0);
-                    prefetch_line_l2(base + off);
-                }
-            }
-        }
         for (int cc = 0; cc < p.n_cchunks; ++cc) {
             if (!wait_bar_warp(smem_u32(&sh.empty_g[stage]), phase ^ 1u, p, sh, lane)) return;
             const uint32_t s_base = g_base + (uint32_t)stage * p.g_stage_bytes;
@@ -1013,8 +1071,277 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
     __syncwarp();
 }
 
-template <int ESIZE>
-__global__ void __launch_bounds__(kThreads, 1) dgrad_tc_kernel(const __grid_constant__ TcParams p) {
+// ------------------------------------------------- positions-on-M mode
+// (plan_pm in plan.cu).  A tile is 4 output rows of one image; its window in
+// a G stage is hbp rows of 128 bytes (64 grad_out channels), row h = 64u + b
+// holding grad_out[n, :, ih0 + ph - (kH-1) + u, b - kPmLeft].
+
+// MMA warp, lane 0: two M = 128 halves per tile, each into its own
+// accumulator buffer (kW x 64 columns): for kernel row kh, A = window rows
+// from 64 (kH-1-kh) + pw + 128 half, B = the kW packed taps (kh, 0..kW-1).
+__device__ void role_mma_pm(const TcParams &p, Shared &sh, uint32_t g_base, uint32_t w_base,
+                            uint32_t tmem) {
+    const PhaseDesc &d = p.ph[0];
+    const uint32_t acc_cols = (uint32_t)(d.Jw * 64);
+    const uint32_t w_row = (uint32_t)(d.Jw * p.w_unit_bytes);  // one kernel row of taps
+    int gs = 0, acc = 0;
+    uint32_t gph = 0, accph = 0;
+    bool aborted = !wait_bar(smem_u32(&sh.w_full), 0, p, sh);
+    for (int64_t t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
+        if (!wait_bar(smem_u32(&sh.full_g[gs]), gph, p, sh)) break;
+        tc_fence_after();
+        const uint32_t g_stage = g_base + (uint32_t)gs * p.g_stage_bytes;
+        for (int half = 0; half < 2; ++half) {
+            if (!wait_bar(smem_u32(&sh.acc_empty[acc]), accph ^ 1u, p, sh)) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + (uint32_t)acc * acc_cols;
+            uint32_t accumulate = 0;
+            for (int kh = 0; kh < d.Jh; ++kh) {
+                const uint32_t a_row =
+                    (uint32_t)(kPmPitch * (d.Jh - 1 - kh) + p.pad_w + 128 * half);
+                const uint32_t a0 = g_stage + a_row * 128u, b0 = w_base + (uint32_t)kh * w_row;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    tc_mma<false>(d_tmem, sw128_desc(a0 + 32u * k), sw128_desc(b0 + 32u * k),
+                                  p.idesc, accumulate);
+                    accumulate = 1;
+                }
+            }
+            tc_commit(smem_u32(&sh.acc_full[acc]));
+            if (++acc == 2) {
+                acc = 0;
+                accph ^= 1u;
+            }
+        }
+        if (aborted) break;
+        tc_commit(smem_u32(&sh.empty_g[gs]));
+        if (++gs == p.ng) {
+            gs = 0;
+            gph ^= 1u;
+        }
+    }
+    tc_commit(smem_u32(&sh.mma_done));
+    wait_drain(smem_u32(&sh.mma_done), 0, p, sh);
+}
+
+// Gather warps: the frame columns b < kPmLeft of every window row are zero in
+// every tile, so they are cleared once per G stage; each raw slice (16
+// channels x raw_br rows x 56 columns) then lands in the window by 8x8 block
+// transposes: ldmatrix.trans reads 8 channels x 8 columns, stmatrix writes 8
+// window rows x 16 bytes (the slice's two 16-byte channel chunks, swizzled).
+__device__ void gather_pm(const TcParams &p, Shared &sh, uint32_t g_base, uint32_t raw_base,
+                          int gw, int lane) {
+    const int slices = p.kc / p.raw_cs;
+    const uint32_t row_bytes = (uint32_t)(p.raw_bw * 2);
+    const uint32_t ch_bytes = row_bytes * (uint32_t)p.raw_br;
+    const int nb_col = p.raw_bw / 8;                   // 8-column blocks per grad_out row
+    const int blocks = 2 * p.pm_rows * nb_col;         // per slice: 2 channel groups
+    const int groups = (blocks + 3) / 4;               // ldmatrix.x4 per slice
+    const int zrows = (p.hbp + kPmPitch - 1) / kPmPitch * kPmLeft;
+    for (int s = 0; s < p.ng; ++s) {
+        const uint32_t sb = g_base + (uint32_t)s * p.g_stage_bytes;
+        for (int k = gw * 32 + lane; k < zrows * 8; k += kPmGWarps * 32) {
+            const int zr = k >> 3, h = (zr / kPmLeft) * kPmPitch + zr % kPmLeft;
+            if (h < p.hbp) st_shared_v4(sb + (uint32_t)h * 128u + (uint32_t)(k & 7) * 16u, 0u, 0u, 0u, 0u);
+        }
+    }
+    int stage = 0, rs = 0;
+    uint32_t phase = 0, rph = 0;
+    bool withhold = (p.debug_flags & DGRAD_DEBUG_SKIP_ARRIVE) && gw == 0;
+    // This lane's rows of the warp's (at most kPmGroups) ldmatrix.x4 groups,
+    // the same for every slice: source offset in a raw slot, destination
+    // window row and channel group.
+    uint32_t src_off[kPmGroups], dst_row[kPmGroups];
+    int cgk[kPmGroups];
+    int ng_mine = 0;
+    {
+        const int m = lane >> 3, kr = lane & 7;
+#pragma unroll
+        for (int j = 0; j < kPmGroups; ++j) {
+            const int gi = gw + j * kPmGWarps;
+            if (gi < groups) ng_mine = j + 1;
+            int b = gi * 4 + m;
+            b = b < blocks ? b : blocks - 1;  // a ragged last group repeats a block
+            const int pb = b % nb_col, rest = b / nb_col;
+            const int u = rest % p.pm_rows, cg = rest / p.pm_rows;
+            const int h = kPmPitch * u + kPmLeft + 8 * pb + kr;
+            src_off[j] = (uint32_t)(8 * cg + kr) * ch_bytes + (uint32_t)u * row_bytes + (uint32_t)pb * 16u;
+            dst_row[j] = (uint32_t)h * 128u;
+            cgk[j] = cg ^ (h & 7);  // XOR with the slice's chunk pair gives the swizzled chunk
+        }
+    }
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        if (!wait_bar_warp(smem_u32(&sh.empty_g[stage]), phase ^ 1u, p, sh, lane)) return;
+        const uint32_t s_base = g_base + (uint32_t)stage * p.g_stage_bytes;
+        for (int sl = 0; sl < slices; ++sl) {
+            if (!wait_bar_warp(smem_u32(&sh.full_raw[rs]), rph, p, sh, lane)) return;
+            const uint32_t raw = raw_base + (uint32_t)rs * p.raw_slice_bytes;
+            uint32_t r[kPmGroups][4];
+#pragma unroll
+            for (int j = 0; j < kPmGroups; ++j)
+                if (j < ng_mine) ldmatrix_x4_trans(raw + src_off[j], r[j]);
+#pragma unroll
+            for (int j = 0; j < kPmGroups; ++j)
+                if (j < ng_mine)
+                    stmatrix_x4(s_base + dst_row[j] + (uint32_t)(((2 * sl) ^ cgk[j]) << 4), r[j]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sh.empty_raw[rs]));
+            if (++rs == p.raw_nr) {
+                rs = 0;
+                rph ^= 1u;
+            }
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+            if (withhold)
+                withhold = false;  // failure injection: this stage is never signalled
+            else
+                mbar_arrive(smem_u32(&sh.full_g[stage]));
+        }
+        if (++stage == p.ng) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+}
+
+// Entry of the exchange slot holding block kw (1 or 2) of even-quadrant lane
+// l (32 - kw <= l <= 31): 0 for (1, 31), 1 and 2 for (2, 30) and (2, 31).
+__device__ __forceinline__ int x_entry(int kw, int l) { return kw * (kw - 1) / 2 + l - (32 - kw); }
+
+// Warps 0..15 in two groups of 8: group g = w / 8 drains half g of every
+// tile (accumulator buffer g), so one group's stores overlap the other's TMEM
+// reads and shuffles.  Warp w reads TMEM lane quadrant q = w mod 4 (positions
+// 32q..32q+31 of the half: output row 2g + q / 2, columns 32 (q mod 2) + lane
+// - kPmLeft) for the 16-channel chunks {2 part, 2 part + 1}, part = (w / 4)
+// mod 2.  out(lane l) = sum over kw of block kw at lane l - kw: a shuffle
+// within the warp, except for the first kw lanes of an odd quadrant, whose
+// values come from the last lanes of the even quadrant below through a small
+// shared buffer (the "pair" of warps q-1, q with the same group and part; one
+// slot per chunk, each with a full / empty mbarrier).  Even quadrants' first
+// lanes are frame padding (b < 8), so no value crosses a 64-position frame
+// row.  Each store instruction writes 32 consecutive grad_in floats of one
+// channel.
+__device__ void epilogue_pm(const TcParams &p, Shared &sh, uint32_t xbase, uint32_t tmem,
+                            int warp, int lane) {
+    const PhaseDesc &d = p.ph[0];
+    const int half = warp >> 3, q = warp & 3, part = (warp >> 2) & 1, odd = q & 1;
+    const int pair = half * 4 + part * 2 + (q >> 1);
+    const int Jw = d.Jw, nchunks = (p.Ci + 15) / 16;
+    const int my_chunks = nchunks - 2 * part < 0 ? 0 : (nchunks - 2 * part > 2 ? 2 : nchunks - 2 * part);
+    const uint32_t taddr =
+        tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * Jw * 64);  // accumulator `half`
+    const uint32_t acc_full = smem_u32(&sh.acc_full[half]), acc_empty = smem_u32(&sh.acc_empty[half]);
+    const int tpi = (p.H + p.rows_per_tile - 1) / p.rows_per_tile;
+    const int64_t HW = (int64_t)p.H * p.W;
+    const int iw = 32 * odd + lane - kPmLeft;
+    uint32_t accph = 0;
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x, accph ^= 1u) {
+        const int n = (int)(t / tpi), ih0 = (int)(t - (int64_t)n * tpi) * p.rows_per_tile;
+        const int ih = ih0 + 2 * half + (q >> 1);
+        const bool valid = ih < p.H && iw >= 0 && iw < p.W;
+        if (!wait_bar_warp(acc_full, accph, p, sh, lane)) return;
+        tc_fence_after();
+        if (my_chunks == 0) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+        }
+        for (int lc = 0; lc < my_chunks; ++lc) {
+            const int ci0 = (2 * part + lc) * 16;
+            uint32_t v[kPmMaxKw][16] = {};
+#pragma unroll
+            for (int kw = 0; kw < kPmMaxKw; ++kw)
+                if (kw < Jw) tmem_ld16(taddr + (uint32_t)(kw * 64 + ci0), v[kw]);
+            tmem_wait_ld3(v);
+            if (lc == my_chunks - 1) {
+                // The accumulator is in registers: the MMA may reuse it.
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+            }
+            const uint32_t xslot = xbase + (uint32_t)((pair * 2 + lc) * kPmXSlotBytes);
+            const uint32_t xf = smem_u32(&sh.x_full[pair * 2 + lc]);
+            const uint32_t xe = smem_u32(&sh.x_empty[pair * 2 + lc]);
+            if (!odd && Jw > 1) {
+                // Publish lanes 32-kw.. of block kw for the odd quadrant.
+                if (!wait_bar_warp(xe, accph ^ 1u, p, sh, lane)) return;
+#pragma unroll
+                for (int kw = 1; kw < kPmMaxKw; ++kw) {
+                    if (kw < Jw && lane >= 32 - kw) {
+                        const uint32_t a = xslot + (uint32_t)(x_entry(kw, lane) * 64);
+#pragma unroll
+                        for (int k = 0; k < 16; k += 4)
+                            st_shared_v4(a + 4u * k, v[kw][k], v[kw][k + 1], v[kw][k + 2], v[kw][k + 3]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xf);
+            }
+            // Sum of block kw at lane l - kw; an odd quadrant's first kw lanes
+            // take that term from the exchange buffer instead.
+            float out[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) out[k] = __uint_as_float(v[0][k]);
+#pragma unroll
+            for (int kw = 1; kw < kPmMaxKw; ++kw) {
+                if (kw < Jw) {
+                    const bool mine = !(odd && lane < kw);
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const float sv = __shfl_up_sync(0xffffffffu, __uint_as_float(v[kw][k]), kw);
+                        out[k] += mine ? sv : 0.f;
+                    }
+                }
+            }
+            if (odd && Jw > 1) {
+                if (!wait_bar_warp(xf, accph, p, sh, lane)) return;
+                if (lane < Jw - 1) {
+                    for (int kw = lane + 1; kw < Jw; ++kw) {
+                        const uint32_t a = xslot + (uint32_t)(x_entry(kw, lane + 32 - kw) * 64);
+#pragma unroll
+                        for (int k = 0; k < 16; k += 4) {
+                            const float4 x = ld_shared_f32x4(a + 4u * k);
+                            out[k] += x.x;
+                            out[k + 1] += x.y;
+                            out[k + 2] += x.z;
+                            out[k + 3] += x.w;
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xe);
+            }
+            if (valid) {
+                float *o = p.grad_in + ((int64_t)n * p.Ci + ci0) * HW + (int64_t)ih * p.W + iw;
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    if (ci0 + k < p.Ci) o[(int64_t)k * HW] = out[k];
+            }
+        }
+    }
+}
+
+// Warp roles of the two kernel variants.
+template <bool PM>
+struct Roles {
+    static constexpr int epi_warps = kEpiWarps, mma_warp = kMmaWarp, w_warp = kWWarp;
+    static constexpr int g_warp0 = kGWarp0, g_warps = kGWarps, threads = kThreads;
+};
+template <>
+struct Roles<true> {
+    static constexpr int epi_warps = kPmEpiWarps, mma_warp = kPmMmaWarp, w_warp = kPmWWarp;
+    static constexpr int g_warp0 = kPmGWarp0, g_warps = kPmGWarps, threads = kPmThreads;
+};
+
+// PM: the positions-on-M roles and warp layout.
+template <int ESIZE, bool PM>
+__global__ void __launch_bounds__(Roles<PM>::threads, 1)
+    dgrad_tc_kernel(const __grid_constant__ TcParams p) {
+    using R = Roles<PM>;
     extern __shared__ __align__(1024) uint8_t smem[];
     Shared &sh = *reinterpret_cast<Shared *>(smem);
     // Rings start on a 1024-byte boundary: the swizzle pattern is tied to it.
@@ -1027,7 +1354,7 @@ __global__ void __launch_bounds__(kThreads, 1) dgrad_tc_kernel(const __grid_cons
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.ng; ++s) {
-            mbar_init(smem_u32(&sh.full_g[s]), kGWarps);
+            mbar_init(smem_u32(&sh.full_g[s]), R::g_warps);
             mbar_init(smem_u32(&sh.empty_g[s]), 1);
         }
         for (int s = 0; s < p.nw; ++s) {
@@ -1036,18 +1363,22 @@ __global__ void __launch_bounds__(kThreads, 1) dgrad_tc_kernel(const __grid_cons
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&sh.acc_full[s]), 1);
-            mbar_init(smem_u32(&sh.acc_empty[s]), kEpiWarps);
+            mbar_init(smem_u32(&sh.acc_empty[s]), PM ? R::epi_warps / 2 : R::epi_warps);
+        }
+        for (int s = 0; s < 16; ++s) {
+            mbar_init(smem_u32(&sh.x_full[s]), 1);
+            mbar_init(smem_u32(&sh.x_empty[s]), 1);
         }
         for (int s = 0; s < p.raw_nr; ++s) {
             mbar_init(smem_u32(&sh.full_raw[s]), 1);
-            mbar_init(smem_u32(&sh.empty_raw[s]), kGWarps);
+            mbar_init(smem_u32(&sh.empty_raw[s]), R::g_warps);
         }
         mbar_init(smem_u32(&sh.w_full), 1);
         mbar_init(smem_u32(&sh.mma_done), 1);
         sh.abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == kMmaWarp) {
+    if (warp == R::mma_warp) {
         tmem_alloc(smem_u32(&sh.tmem_base), p.tmem_cols);
         tmem_relinquish();
     }
@@ -1055,28 +1386,41 @@ __global__ void __launch_bounds__(kThreads, 1) dgrad_tc_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
-    // Everything above touched only this CTA's shared memory and TMEM, so it
-    // may overlap the previous kernel; global memory is used only from here.
+    if (warp == R::w_warp && lane == 0 && p.gather_tma)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.in_map)) : "memory");
+    // Everything above touched only this CTA's shared memory, TMEM and its own
+    // parameters, so it may overlap the previous kernel; global memory is used
+    // only from here.
     if (threadIdx.x == 0) grid_launch_dependents();
     grid_dependency_wait();
 
-    if (warp == kWWarp) {
+    if (warp == R::w_warp) {
         if (lane == 0) role_weights(p, sh, w_base, raw_base);
         __syncwarp();
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) role_mma<ESIZE == 4>(p, sh, g_base, w_base, tmem);
+    } else if (warp == R::mma_warp) {
+        if (lane == 0) {
+            if constexpr (PM)
+                role_mma_pm(p, sh, g_base, w_base, tmem);
+            else
+                role_mma<ESIZE == 4>(p, sh, g_base, w_base, tmem);
+        }
         __syncwarp();
-    } else if (warp >= kGWarp0) {
-        if (p.gather_tma)
-            gather_from_raw<ESIZE>(p, sh, g_base, raw_base, warp - kGWarp0, lane);
+    } else if (warp >= R::g_warp0) {
+        if constexpr (PM)
+            gather_pm(p, sh, g_base, raw_base, warp - R::g_warp0, lane);
+        else if (p.gather_tma)
+            gather_from_raw<ESIZE>(p, sh, g_base, raw_base, warp - R::g_warp0, lane);
         else
-            role_gather<ESIZE>(p, sh, g_base, warp - kGWarp0, lane);
+            role_gather<ESIZE>(p, sh, g_base, warp - R::g_warp0, lane);
     } else {
-        role_epilogue(p, sh, epi_stage, tmem, warp, lane);
+        if constexpr (PM)
+            epilogue_pm(p, sh, epi_stage, tmem, warp, lane);
+        else
+            role_epilogue(p, sh, epi_stage, tmem, warp, lane);
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == R::mma_warp) {
         tc_fence_after();
         tmem_dealloc(tmem, p.tmem_cols);
     }
@@ -1085,10 +1429,10 @@ __global__ void __launch_bounds__(kThreads, 1) dgrad_tc_kernel(const __grid_cons
 // Dynamic shared memory is raised once per device and variant to the full
 // limit, so no attribute call happens on later launches (e.g. during stream
 // capture).
-template <int ESIZE>
+template <int ESIZE, bool PM>
 int launch_variant(const TcParams &p, int grid, cudaStream_t st, int dev) {
     static std::atomic<uint64_t> configured{0};  // bit per device
-    auto kern = dgrad_tc_kernel<ESIZE>;
+    auto kern = dgrad_tc_kernel<ESIZE, PM>;
     const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
     if (!bit || !(configured.load() & bit)) {
         cudaError_t e =
@@ -1100,7 +1444,7 @@ int launch_variant(const TcParams &p, int grid, cudaStream_t st, int dev) {
     // kernel may overlap the tail of the previous one (see grid_dependency_wait).
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Roles<PM>::threads);
     cfg.dynamicSmemBytes = (size_t)p.smem_bytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -1185,8 +1529,18 @@ int launch_tc(const Plan &plan, const void *grad_out, const void *packed, float 
     p.grad_out = grad_out;
     p.packed = packed;
     p.grad_in = grad_in;
-    p.epi_tma = encode_out_map(p) ? 1 : 0;
+    p.epi_tma = 0;
     p.gather_tma = encode_in_map(p) ? 1 : 0;
+    if (p.pos_m && !p.gather_tma) {
+        // The positions-on-M mode needs the TMA gather (grad_out 16-byte
+        // aligned); the general plan shares its packed weights.
+        p = plan.tc_alt;
+        p.grad_out = grad_out;
+        p.packed = packed;
+        p.grad_in = grad_in;
+        p.gather_tma = encode_in_map(p) ? 1 : 0;
+    }
+    if (!p.pos_m) p.epi_tma = encode_out_map(p) ? 1 : 0;
     int dev = 0;
     cudaError_t de = cudaGetDevice(&dev);
     if (de != cudaSuccess) return (int)de;
@@ -1198,8 +1552,10 @@ int launch_tc(const Plan &plan, const void *grad_out, const void *packed, float 
     const int grid = (int)(p.total_tiles < sms ? p.total_tiles : sms);
     if (grid <= 0) return (int)cudaSuccess;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (plan.esize == 2) return launch_variant<2>(p, grid, st, dev);
-    return launch_variant<4>(p, grid, st, dev);
+    if (plan.esize == 2)
+        return p.pos_m ? launch_variant<2, true>(p, grid, st, dev)
+                       : launch_variant<2, false>(p, grid, st, dev);
+    return launch_variant<4, false>(p, grid, st, dev);
 }
 
 int tc_read_and_clear_error(unsigned int *out) {

@@ -211,6 +211,76 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
     return true;
 }
 
+// Positions-on-M plan (stride 1, 16-bit, Ci <= 64, Co <= 64, kW <= 3,
+// W <= 56, OW <= 56 with 16-byte grad_out rows), derived from the general
+// plan `g` whose packed weights it shares: [kh][kw][ci 0..63][co 0..63],
+// 128-byte swizzled rows.
+//
+// Frame: kPmPitch = 64 positions per grad_out row, kPmLeft = 8 zero columns
+// first, so window row h = 64u + b of a tile whose first output row is ih0
+// holds grad_out[oh = ih0 + ph - (kH-1) + u, ow = b - 8] (zero outside the
+// grid).  A tile is 4 output rows = 256 positions, processed as two halves of
+// 128 on the MMA M side.  For kernel row kh the MMA reads the window from row
+// 64 (kH-1-kh) + pw + 128 half, with the kW taps' weights stacked on N, so
+// column block kw of lane l holds the tap (kh, kw) sum for output column
+// c = (l mod 64) + kw; the epilogue adds block kw of lane l - kw.  Output
+// (ih0 + r, iw) is lane 64 r + iw + 8.
+bool plan_pm(const conv2d_grad_input_params &p, int esize, const TcParams &g, TcParams *out) {
+    if (p.stride != 1 || esize != 2) return false;
+    const int64_t H = p.in_h, W = p.in_w, kH = p.kernel_h, kW = p.kernel_w;
+    const int64_t Ci = p.in_channels, Co = p.out_channels;
+    if (Ci > 64 || Co > 64 || kW > kPmMaxKw || W > kPmPitch - kPmLeft) return false;
+    if (p.out_w > (uint32_t)(kPmPitch - kPmLeft) || (p.out_w * (int64_t)esize) % 16 != 0) return false;
+    if (p.padding_w > (uint32_t)kPmLeft) return false;
+    if (g.m_tile != 64 || g.n_mtiles != 1 || g.n_cchunks != 1 || g.n_phases != 1) return false;
+    TcParams t = g;
+    t.pos_m = 1;
+    t.pad_w = (int)p.padding_w;
+    t.rows_per_tile = 4;
+    t.tile_p = 4 * kPmPitch;
+    const int64_t view_end = kPmPitch * (kH - 1) + p.padding_w + t.tile_p;  // rows the MMA reads
+    t.pm_rows = (int)cdiv(view_end - kPmLeft, kPmPitch);
+    t.hbp = (int)round_up(std::max<int64_t>(view_end, (int64_t)kPmPitch * t.pm_rows), 8);
+    // 8x8 transpose blocks of one 16-channel slice, four per gather ldmatrix.x4.
+    if (2 * t.pm_rows * ((kPmPitch - kPmLeft) / 8) > 4 * kPmGWarps * kPmGroups) return false;
+    t.g_stage_bytes = t.hbp * 128;
+    PhaseDesc &d = t.ph[0];
+    std::memset(&d, 0, sizeof(d));
+    d.Hr = (int)H; d.Wr = (int)W;
+    d.Jh = (int)kH; d.Jw = (int)kW;
+    d.qh = (int)p.padding_h; d.qw = (int)p.padding_w;
+    d.X = kPmPitch; d.R = (int)(H + kH - 1);
+    d.p_tiles = (int)((int64_t)p.batch * cdiv(H, t.rows_per_tile));
+    d.hb = t.hbp;
+    t.n_phases = 1;
+    t.total_tiles = d.p_tiles;
+    // Raw slices: 16 channels x raw_br rows x 56 columns from column 0; an
+    // odd row count keeps the transposing ldmatrix reads free of bank
+    // conflicts (channel pitch an odd number of 16-byte units).
+    t.raw_cs = 16;
+    t.raw_bw = kPmPitch - kPmLeft;
+    t.raw_x0 = 0;
+    t.raw_br = t.pm_rows | 1;
+    t.raw_slice_bytes = (int)round_up((int64_t)t.raw_cs * t.raw_br * t.raw_bw * esize, 128);
+    t.epi_stage_bytes = kPmXBytes;
+    t.ng = 2;
+    t.nw = 0;
+    const int64_t fixed = kBarrierBytes + 2048 + t.epi_stage_bytes + t.packed_bytes + 2 * (int64_t)t.g_stage_bytes;
+    const int64_t room = kSmemLimit - fixed;
+    if (room < 2 * (int64_t)t.raw_slice_bytes) return false;
+    t.raw_nr = (int)std::min<int64_t>(4, room / t.raw_slice_bytes);
+    t.smem_bytes = (int)(fixed + (int64_t)t.raw_nr * t.raw_slice_bytes);
+    // M = 128 positions, N = kW x 64 (taps of one kernel row), A and B K-major.
+    const uint32_t fmt = (g.idesc >> 7) & 7u;  // operand format of the general plan
+    const int n = (int)kW * 64;
+    t.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    uint32_t cols = 32;
+    while (cols < (uint32_t)(2 * n)) cols *= 2;  // two accumulator buffers
+    t.tmem_cols = cols;
+    *out = t;
+    return true;
+}
+
 }  // namespace
 
 int make_plan(const void *params_v, int dtype, int forced_kernel, Plan *plan) {
@@ -253,9 +323,14 @@ int make_plan(const void *params_v, int dtype, int forced_kernel, Plan *plan) {
     }
     if (plan_tc(p, plan->esize, dtype, plan)) {
         plan->kernel = DGRAD_KERNEL_TC;
+        plan->tc_alt = plan->tc;
+        TcParams pm;
+        if (forced_kernel == DGRAD_KERNEL_TC_POSM && plan_pm(p, plan->esize, plan->tc, &pm))
+            plan->tc = pm;
         return DGRAD_OK;
     }
-    if (forced_kernel == DGRAD_KERNEL_TC) return DGRAD_ERR_UNSUPPORTED;
+    if (forced_kernel == DGRAD_KERNEL_TC || forced_kernel == DGRAD_KERNEL_TC_POSM)
+        return DGRAD_ERR_UNSUPPORTED;
     plan->kernel = DGRAD_KERNEL_SIMT;
     plan->workspace = 0;
     return DGRAD_OK;

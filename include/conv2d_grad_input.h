@@ -90,7 +90,14 @@ typedef enum dgrad_status {
 typedef enum dgrad_kernel {
     DGRAD_KERNEL_AUTO = 0, /* tensor-core kernel where it applies, else the CUDA-core kernel */
     DGRAD_KERNEL_TC = 1,   /* tcgen05 implicit GEMM (weights pre-packed) */
-    DGRAD_KERNEL_SIMT = 2  /* direct CUDA-core kernel, one thread per grad_in element */
+    DGRAD_KERNEL_SIMT = 2, /* direct CUDA-core kernel, one thread per grad_in element */
+    /* tcgen05 implicit GEMM with the output positions on the MMA M side and
+     * the kW taps of a kernel row side by side on N, for stride 1, bf16 or
+     * fp16, in_channels and out_channels <= 64, kernel_w <= 3, in_w and
+     * out_w <= 56 with 16-byte grad_out rows; other shapes run as
+     * DGRAD_KERNEL_TC.  Same packed weights as DGRAD_KERNEL_TC.  Opt-in:
+     * its epilogue writes grad_in with plain stores from the epilogue warps. */
+    DGRAD_KERNEL_TC_POSM = 3
 } dgrad_kernel;
 
 /* The whole operation: packs the weights into a stream-ordered temporary
@@ -133,8 +140,9 @@ int conv2d_grad_input_check_errors(struct CUstream_st *stream);
 /* A static, human-readable name for a dgrad_status value. */
 const char *conv2d_grad_input_status_string(int status);
 
-/* Which kernel a call with these arguments runs: DGRAD_KERNEL_TC or
- * DGRAD_KERNEL_SIMT, or a negative dgrad_status for invalid arguments. */
+/* Which kernel a call with these arguments runs: DGRAD_KERNEL_TC,
+ * DGRAD_KERNEL_TC_POSM or DGRAD_KERNEL_SIMT, or a negative dgrad_status for
+ * invalid arguments. */
 int conv2d_grad_input_select_kernel(const conv2d_grad_input_params *p, int dtype);
 
 /* Process-wide kernel choice (DGRAD_KERNEL_AUTO by default).  Forcing

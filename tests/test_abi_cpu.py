@@ -111,6 +111,22 @@ def test_status_strings_and_settings(lib):
     assert dg.conv2d_grad_input_set_debug(0) == 0
 
 
+def test_positions_on_m_selection(lib):
+    prev = dg.conv2d_grad_input_set_kernel(dg.DGRAD_KERNEL_TC_POSM)
+    try:
+        assert dg.conv2d_grad_input_select_kernel(params(workloads.RESNET), 1) == dg.DGRAD_KERNEL_TC_POSM
+        assert dg.conv2d_grad_input_select_kernel(params(workloads.RESNET), 2) == dg.DGRAD_KERNEL_TC_POSM
+        # fp32, Ci > 64 and stride 2 stay with the general tensor-core mode
+        assert dg.conv2d_grad_input_select_kernel(params(workloads.RESNET), 0) == dg.DGRAD_KERNEL_TC
+        assert dg.conv2d_grad_input_select_kernel(params(workloads.STRIDED), 1) == dg.DGRAD_KERNEL_TC
+        assert dg.conv2d_grad_input_select_kernel(params(workloads.POINTWISE), 2) == dg.DGRAD_KERNEL_TC
+        # same packed weights as the general mode
+        assert dg.conv2d_grad_input_workspace_size(params(workloads.RESNET), 1) == 9 * 64 * 64 * 2
+    finally:
+        dg.conv2d_grad_input_set_kernel(prev)
+    assert dg.conv2d_grad_input_select_kernel(params(workloads.RESNET), 1) == dg.DGRAD_KERNEL_TC
+
+
 def test_stride_above_four_uses_cuda_cores(lib):
     p = dg.Params(1, 4, 20, 20, 4, 3, 3, 5, 1, 4, 4, 1)
     assert dg.conv2d_grad_input_select_kernel(p, 0) == dg.DGRAD_KERNEL_SIMT
