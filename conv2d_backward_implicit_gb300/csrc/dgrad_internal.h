@@ -50,6 +50,7 @@ constexpr int kBarrierBytes = 1024;
 constexpr int kEpiChunk = 32;                 // positions per step of the staged epilogue
 constexpr int kEpiRowFloats = kEpiChunk + 1;  // padded staging row (conflict-free)
 constexpr int kTmaBoxCi = 8;                  // channels per TMA store box (one box per warp)
+constexpr int kMaxEarly = 4;                  // raw slices parked in G stage 1 at the start
 constexpr int kPmPitch = 64;  // positions-on-M mode: frame positions per grad_out row
 constexpr int kPmLeft = 8;    // zero columns before grad_out column 0 in each frame row
 constexpr int kPmMaxKw = 3;   // column taps stacked on N (kW x 64 columns)
@@ -60,6 +61,7 @@ constexpr int kPmGWarp0 = 18;
 constexpr int kPmGWarps = 4;
 constexpr int kPmThreads = 32 * (kPmGWarp0 + kPmGWarps);
 constexpr int kPmGroups = 6;  // ldmatrix.x4 groups per gather warp and raw slice (at most)
+constexpr int kF64Groups = 4; // the same with the general mode's kGWarps gather warps
 // Boundary-exchange buffer of the positions-on-M epilogue: 8 warp pairs x 2
 // slots x 3 (tap, lane) values x 16 floats: block 1 of lane 31, block 2 of
 // lanes 30 and 31.
@@ -99,6 +101,9 @@ struct TcParams {
     // shared memory into the frame window.
     int gather_tma;         // 1: use it (set at launch)
     int raw_nr, raw_cs, raw_br, raw_bw, raw_x0, raw_slice_bytes;
+    // The first raw_early slices (at most kMaxEarly) land in G stage 1, idle
+    // until the second tile, so more of the first tile's grad_out is in flight.
+    int raw_early;
     int kc, n_cchunks;      // grad_out channels per stage (128 bytes), stages per tile
     int hbp;                // frame elements per G stage (multiple of 8)
     int g_stage_bytes;      // grad_out frame window stage
@@ -118,6 +123,12 @@ struct TcParams {
     // of one kernel row stacked on N (kW x 64 columns); the frame pitch is 64
     // with kPmLeft zero columns in front of each grad_out row.  See dgrad_tc.cu.
     int pos_m;
+    // 64-wide frame in the general mode (stride 1, 16-bit, W <= 56): the
+    // window layout of positions-on-M mode (kPmLeft zero columns, then the
+    // grad_out row), filled by the same ldmatrix transpose; tap (j, i)
+    // reads it from row (Jh-1-j) * 64 + (Jw-1-i) + view0.
+    int frame64;
+    int view0;
     int pad_w;              // padding_w: start of the row-tap views in the window
     int pm_rows;            // window rows holding grad_out data (raw_br >= pm_rows)
     PhaseDesc ph[kMaxPhases];
@@ -142,8 +153,8 @@ struct Plan {
     int esize;
     int kernel;          // DGRAD_KERNEL_TC or DGRAD_KERNEL_SIMT
     TcParams tc;         // valid when kernel == TC
-    TcParams tc_alt;     // general-mode plan when tc is positions-on-M (same packed weights),
-                         // used when grad_out is not 16-byte aligned for the TMA gather
+    TcParams tc_alt;     // general-mode plan with the Wr + Jw - 1 frame (same packed weights),
+                         // used when tc needs TMA (gather or store) that the pointers rule out
     PackParams pack;     // valid when kernel == TC
     SimtParams simt;
     size_t workspace;    // packed-weight bytes (TC), 0 otherwise

@@ -46,6 +46,8 @@ struct Shared {
     uint64_t full_g[4], empty_g[4], full_w[4], empty_w[4], full_raw[4], empty_raw[4];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t x_full[16], x_empty[16];  // positions-on-M epilogue boundary exchange
+    uint64_t full_early[kMaxEarly];    // raw slices parked in G stage 1
+    uint64_t early_free;               // every gather warp is done with them
     uint64_t w_full, mma_done;
     uint32_t tmem_base;
     int abort_flag;
@@ -533,19 +535,23 @@ __device__ void prefetch_raw_tile(const TcParams &p, int64_t t) {
 // this CTA, the raw grad_out slices of the tile's window -- raw_cs channels x
 // raw_br rows x raw_bw columns from column raw_x0 -- into the raw ring.  Rows
 // and columns outside grad_out are zero-filled by the TMA unit.  The first
-// tile's slices go out before the resident weights (the weights come from L2,
-// grad_out from DRAM).  General mode (a ring shorter than a tile): then the
-// L2 prefetch of the next kRawLookahead tiles, and each later tile prefetches
-// the one kRawLookahead tiles after it.  Positions-on-M mode (the ring holds a
-// whole tile): once all slices of a tile are queued, the next tile's slices
-// are prefetched (earlier, they would compete with the first tile's loads).
-__device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, uint32_t w_base) {
+// tile's slices go out first, then the resident weights, then slices into the
+// remaining free slots.  Once those are all queued and the first tile's last
+// slice has landed (earlier, prefetches would compete with it for DRAM), the
+// L2 prefetch starts: general mode (a ring shorter than a tile) the next
+// kRawLookahead tiles, then each later tile the one kRawLookahead after it;
+// positions-on-M mode (the ring holds a whole tile) the tile after the ring's,
+// then at each tile's end the next one.
+__device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, uint32_t w_base,
+                             uint32_t early_base) {
     const uint32_t box_bytes = (uint32_t)(p.raw_cs * p.raw_br * p.raw_bw * p.esize);
     const int slices = p.kc / p.raw_cs;
+    const int64_t per_tile = (int64_t)slices * p.n_cchunks;
+    const int64_t fill = p.raw_early + p.raw_nr;  // slices that need no free slot
     int slot = 0;
     uint32_t phase = 0;
-    int64_t issued = 0;
-    bool aborted = false, rest_issued = false;
+    int64_t issued = 0;  // slices, parked ones included
+    bool aborted = false, weights_issued = false, prefetching = false;
     for (int64_t t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
         const Tile ti = decode_tile(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
@@ -554,14 +560,39 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
         row_tile_origin(p, d, ti.pt, n, u_first);
         for (int cc = 0; cc < p.n_cchunks && !aborted; ++cc) {
             for (int sl = 0; sl < slices; ++sl) {
-                if (!rest_issued && issued == p.raw_nr) {
+                // The weights right after the first tile's slices.
+                if (!weights_issued && issued == (per_tile < fill ? per_tile : fill)) {
                     issue_weights(p, sh, w_base);
-                    if (!p.pos_m)
-                        for (int k = 1; k <= kRawLookahead; ++k)
-                            prefetch_raw_tile(p, t + (int64_t)k * gridDim.x);
-                    rest_issued = true;
-                } else if (!p.pos_m && rest_issued && cc == 0 && sl == 0) {
+                    weights_issued = true;
+                }
+                // Once every free slot is filled and the first tile's last
+                // slice has landed, later tiles go to L2 ahead of the ring.
+                if (weights_issued && !prefetching && issued == fill) {
+                    const int64_t last = (per_tile < fill ? per_tile : fill) - 1;
+                    const int64_t j = last - p.raw_early;
+                    const bool ok = last < p.raw_early
+                                        ? wait_bar(smem_u32(&sh.full_early[last]), 0, p, sh)
+                                        : wait_bar(smem_u32(&sh.full_raw[j % p.raw_nr]),
+                                                   (uint32_t)((j / p.raw_nr) & 1), p, sh);
+                    if (!ok) {
+                        aborted = true;
+                        break;
+                    }
+                    // From the tile this slice belongs to: kRawLookahead tiles
+                    // beyond it (general) or itself (positions-on-M).
+                    prefetching = true;
+                    for (int k = 0; k <= (p.pos_m ? 0 : kRawLookahead); ++k)
+                        prefetch_raw_tile(p, t + (int64_t)k * gridDim.x);
+                } else if (!p.pos_m && prefetching && cc == 0 && sl == 0) {
                     prefetch_raw_tile(p, t + (int64_t)kRawLookahead * gridDim.x);
+                }
+                if (issued < p.raw_early) {  // parked in G stage 1: no slot to wait for
+                    const uint32_t full = smem_u32(&sh.full_early[issued]);
+                    mbar_arrive_expect_tx(full, box_bytes);
+                    tma_load_4d(early_base + (uint32_t)issued * p.raw_slice_bytes, &p.in_map,
+                                p.raw_x0, u_first, cc * p.kc + sl * p.raw_cs, n, full);
+                    ++issued;
+                    continue;
                 }
                 if (!wait_bar(smem_u32(&sh.empty_raw[slot]), phase ^ 1u, p, sh)) {
                     aborted = true;
@@ -580,24 +611,28 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
         }
         // Positions-on-M mode (the ring holds a whole tile): all of this
         // tile's slices are queued, the next tile's go to L2.
-        if (p.pos_m && !aborted) prefetch_raw_tile(p, t + gridDim.x);
+        if (p.pos_m && prefetching && !aborted) prefetch_raw_tile(p, t + gridDim.x);
     }
-    if (!rest_issued) issue_weights(p, sh, w_base);  // fewer slices than ring slots
+    if (!weights_issued) issue_weights(p, sh, w_base);  // fewer slices than free slots
     if (aborted) {
-        const int64_t k_end = issued < p.raw_nr ? issued : p.raw_nr;
+        const int64_t parked = issued < p.raw_early ? issued : p.raw_early;
+        for (int64_t k = 0; k < parked; ++k) wait_drain(smem_u32(&sh.full_early[k]), 0, p, sh);
+        const int64_t ring = issued - parked;
+        const int64_t k_end = ring < p.raw_nr ? ring : p.raw_nr;
         for (int64_t k = 0; k < k_end; ++k) {
-            const int64_t q = issued - 1 - k;
+            const int64_t q = ring - 1 - k;
             wait_drain(smem_u32(&sh.full_raw[q % p.raw_nr]), (uint32_t)((q / p.raw_nr) & 1), p, sh);
         }
     }
 }
 
 // Warp 5, lane 0: packed weights into shared memory with bulk copies.
-__device__ void role_weights(const TcParams &p, Shared &sh, uint32_t w_base, uint32_t raw_base) {
+__device__ void role_weights(const TcParams &p, Shared &sh, uint32_t w_base, uint32_t raw_base,
+                             uint32_t early_base) {
     const uint8_t *src = static_cast<const uint8_t *>(p.packed);
     if (p.nw == 0) {
         if (p.gather_tma) {
-            raw_producer(p, sh, raw_base, w_base);
+            raw_producer(p, sh, raw_base, w_base, early_base);
         } else {
             issue_weights(p, sh, w_base);
             prefetch_windows(p, blockIdx.x);
@@ -692,7 +727,7 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
                 for (int tap = t0; tap < t1; ++tap) {
                     const int j = tap / d.Jw, i = tap - j * d.Jw;
                     const uint32_t g_tap =
-                        g_stage + (uint32_t)(((d.Jh - 1 - j) * d.X + (d.Jw - 1 - i)) * 128);
+                        g_stage + (uint32_t)(((d.Jh - 1 - j) * d.X + (d.Jw - 1 - i) + p.view0) * 128);
                     const uint32_t w_tap = w_grp + (uint32_t)((tap - t0) * p.w_unit_bytes);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {  // four 32-byte K steps per 128-byte row
@@ -729,6 +764,53 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
     wait_drain(smem_u32(&sh.mma_done), 0, p, sh);
 }
 
+// Consumer side of the raw slices (gather warps): the first raw_early come
+// from G stage 1, the rest through the ring.  After its last parked slice a
+// warp arrives on early_free; a warp waits for it before it first writes
+// G stage 1.
+struct RawCursor {
+    int64_t k = 0;  // slices consumed
+    int rs = 0;
+    uint32_t rph = 0;
+};
+
+__device__ __forceinline__ bool raw_acquire(const TcParams &p, Shared &sh, const RawCursor &c,
+                                            uint32_t raw_base, uint32_t early_base, int lane,
+                                            uint32_t &addr) {
+    if (c.k < p.raw_early) {
+        if (!wait_bar_warp(smem_u32(&sh.full_early[c.k]), 0, p, sh, lane)) return false;
+        addr = early_base + (uint32_t)c.k * p.raw_slice_bytes;
+    } else {
+        if (!wait_bar_warp(smem_u32(&sh.full_raw[c.rs]), c.rph, p, sh, lane)) return false;
+        addr = raw_base + (uint32_t)c.rs * p.raw_slice_bytes;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void raw_release(const TcParams &p, Shared &sh, RawCursor &c,
+                                            int lane) {
+    __syncwarp();
+    if (c.k < p.raw_early) {
+        if (c.k == p.raw_early - 1 && lane == 0) mbar_arrive(smem_u32(&sh.early_free));
+    } else {
+        if (lane == 0) mbar_arrive(smem_u32(&sh.empty_raw[c.rs]));
+        if (++c.rs == p.raw_nr) {
+            c.rs = 0;
+            c.rph ^= 1u;
+        }
+    }
+    ++c.k;
+}
+
+// Before a warp first writes G stage `stage`: stage 1 may still hold parked
+// raw slices that other gather warps read.
+__device__ __forceinline__ bool stage_writable(const TcParams &p, Shared &sh, int stage,
+                                               bool &early_done, int lane) {
+    if (stage != 1 || early_done || p.raw_early == 0) return true;
+    early_done = true;
+    return wait_bar_warp(smem_u32(&sh.early_free), 0, p, sh, lane);
+}
+
 // Gather warps, TMA variant: the frame window of each stage is assembled
 // from raw slices (raw_cs channels of whole grad_out rows) by a transpose in
 // shared memory: frame element h, channel c comes from slice row h / X,
@@ -736,11 +818,13 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
 // every 128-byte window row.
 template <int ESIZE>
 __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
-                                uint32_t raw_base, int gw, int lane) {
+                                uint32_t raw_base, uint32_t early_base, int gw, int lane) {
     constexpr int E = 16 / ESIZE;  // elements per 16-byte chunk
     const int slices = p.kc / p.raw_cs;
-    int stage = 0, rs = 0;
-    uint32_t phase = 0, rph = 0;
+    int stage = 0;
+    uint32_t phase = 0;
+    RawCursor rc;
+    bool early_done = false;
     bool withhold = (p.debug_flags & DGRAD_DEBUG_SKIP_ARRIVE) && gw == 0;
     const uint32_t row_bytes = (uint32_t)(p.raw_bw * ESIZE);
     const uint32_t ch_bytes = row_bytes * (uint32_t)p.raw_br;
@@ -751,10 +835,11 @@ __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
         const int xoff = -(d.Jw - 1) + d.qw - p.raw_x0;  // raw column of frame column 0
         for (int cc = 0; cc < p.n_cchunks; ++cc) {
             if (!wait_bar_warp(smem_u32(&sh.empty_g[stage]), phase ^ 1u, p, sh, lane)) return;
+            if (!stage_writable(p, sh, stage, early_done, lane)) return;
             const uint32_t s_base = g_base + (uint32_t)stage * p.g_stage_bytes;
             for (int sl = 0; sl < slices; ++sl) {
-                if (!wait_bar_warp(smem_u32(&sh.full_raw[rs]), rph, p, sh, lane)) return;
-                const uint32_t raw = raw_base + (uint32_t)rs * p.raw_slice_bytes;
+                uint32_t raw;
+                if (!raw_acquire(p, sh, rc, raw_base, early_base, lane, raw)) return;
                 for (int h = gw * 32 + lane; h < p.hbp; h += kGWarps * 32) {
                     const int rho = h / d.X;
                     const int x = h - rho * d.X + xoff;
@@ -785,12 +870,7 @@ __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
                         st_shared_v4(row + (uint32_t)(((2 * sl + j) ^ (h & 7)) << 4), q[j][0],
                                      q[j][1], q[j][2], q[j][3]);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&sh.empty_raw[rs]));
-                if (++rs == p.raw_nr) {
-                    rs = 0;
-                    rph ^= 1u;
-                }
+                raw_release(p, sh, rc, lane);
             }
             fence_proxy_async();
             __syncwarp();
@@ -1127,13 +1207,16 @@ __device__ void role_mma_pm(const TcParams &p, Shared &sh, uint32_t g_base, uint
     wait_drain(smem_u32(&sh.mma_done), 0, p, sh);
 }
 
-// Gather warps: the frame columns b < kPmLeft of every window row are zero in
-// every tile, so they are cleared once per G stage; each raw slice (16
+// Gather warps of the 64-wide frame (positions-on-M mode and the general
+// mode's frame64 plans): the frame columns b < kPmLeft of every window row are
+// zero in every tile, so they are cleared once per G stage (before its first
+// use); each raw slice (16
 // channels x raw_br rows x 56 columns) then lands in the window by 8x8 block
 // transposes: ldmatrix.trans reads 8 channels x 8 columns, stmatrix writes 8
 // window rows x 16 bytes (the slice's two 16-byte channel chunks, swizzled).
+template <int GW, int NG>  // gather warps, ldmatrix.x4 groups per warp and slice
 __device__ void gather_pm(const TcParams &p, Shared &sh, uint32_t g_base, uint32_t raw_base,
-                          int gw, int lane) {
+                          uint32_t early_base, int gw, int lane) {
     const int slices = p.kc / p.raw_cs;
     const uint32_t row_bytes = (uint32_t)(p.raw_bw * 2);
     const uint32_t ch_bytes = row_bytes * (uint32_t)p.raw_br;
@@ -1141,27 +1224,22 @@ __device__ void gather_pm(const TcParams &p, Shared &sh, uint32_t g_base, uint32
     const int blocks = 2 * p.pm_rows * nb_col;         // per slice: 2 channel groups
     const int groups = (blocks + 3) / 4;               // ldmatrix.x4 per slice
     const int zrows = (p.hbp + kPmPitch - 1) / kPmPitch * kPmLeft;
-    for (int s = 0; s < p.ng; ++s) {
-        const uint32_t sb = g_base + (uint32_t)s * p.g_stage_bytes;
-        for (int k = gw * 32 + lane; k < zrows * 8; k += kPmGWarps * 32) {
-            const int zr = k >> 3, h = (zr / kPmLeft) * kPmPitch + zr % kPmLeft;
-            if (h < p.hbp) st_shared_v4(sb + (uint32_t)h * 128u + (uint32_t)(k & 7) * 16u, 0u, 0u, 0u, 0u);
-        }
-    }
-    int stage = 0, rs = 0;
-    uint32_t phase = 0, rph = 0;
+    int stage = 0;
+    uint32_t phase = 0, zeroed = 0;  // bit s: this warp has cleared its share of stage s
+    RawCursor rc;
+    bool early_done = false;
     bool withhold = (p.debug_flags & DGRAD_DEBUG_SKIP_ARRIVE) && gw == 0;
-    // This lane's rows of the warp's (at most kPmGroups) ldmatrix.x4 groups,
+    // This lane's rows of the warp's (at most NG) ldmatrix.x4 groups,
     // the same for every slice: source offset in a raw slot, destination
     // window row and channel group.
-    uint32_t src_off[kPmGroups], dst_row[kPmGroups];
-    int cgk[kPmGroups];
+    uint32_t src_off[NG], dst_row[NG];
+    int cgk[NG];
     int ng_mine = 0;
     {
         const int m = lane >> 3, kr = lane & 7;
 #pragma unroll
-        for (int j = 0; j < kPmGroups; ++j) {
-            const int gi = gw + j * kPmGWarps;
+        for (int j = 0; j < NG; ++j) {
+            const int gi = gw + j * GW;
             if (gi < groups) ng_mine = j + 1;
             int b = gi * 4 + m;
             b = b < blocks ? b : blocks - 1;  // a ragged last group repeats a block
@@ -1173,26 +1251,31 @@ __device__ void gather_pm(const TcParams &p, Shared &sh, uint32_t g_base, uint32
             cgk[j] = cg ^ (h & 7);  // XOR with the slice's chunk pair gives the swizzled chunk
         }
     }
-    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x)
+    for (int cc = 0; cc < p.n_cchunks; ++cc) {
         if (!wait_bar_warp(smem_u32(&sh.empty_g[stage]), phase ^ 1u, p, sh, lane)) return;
+        if (!stage_writable(p, sh, stage, early_done, lane)) return;
         const uint32_t s_base = g_base + (uint32_t)stage * p.g_stage_bytes;
+        if (!(zeroed >> stage & 1u)) {  // frame columns b < kPmLeft: zero in every tile
+            zeroed |= 1u << stage;
+            for (int k = gw * 32 + lane; k < zrows * 8; k += GW * 32) {
+                const int zr = k >> 3, h = (zr / kPmLeft) * kPmPitch + zr % kPmLeft;
+                if (h < p.hbp)
+                    st_shared_v4(s_base + (uint32_t)h * 128u + (uint32_t)(k & 7) * 16u, 0u, 0u, 0u, 0u);
+            }
+        }
         for (int sl = 0; sl < slices; ++sl) {
-            if (!wait_bar_warp(smem_u32(&sh.full_raw[rs]), rph, p, sh, lane)) return;
-            const uint32_t raw = raw_base + (uint32_t)rs * p.raw_slice_bytes;
-            uint32_t r[kPmGroups][4];
+            uint32_t raw;
+            if (!raw_acquire(p, sh, rc, raw_base, early_base, lane, raw)) return;
+            uint32_t r[NG][4];
 #pragma unroll
-            for (int j = 0; j < kPmGroups; ++j)
+            for (int j = 0; j < NG; ++j)
                 if (j < ng_mine) ldmatrix_x4_trans(raw + src_off[j], r[j]);
 #pragma unroll
-            for (int j = 0; j < kPmGroups; ++j)
+            for (int j = 0; j < NG; ++j)
                 if (j < ng_mine)
                     stmatrix_x4(s_base + dst_row[j] + (uint32_t)(((2 * sl) ^ cgk[j]) << 4), r[j]);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&sh.empty_raw[rs]));
-            if (++rs == p.raw_nr) {
-                rs = 0;
-                rph ^= 1u;
-            }
+            raw_release(p, sh, rc, lane);
         }
         fence_proxy_async();
         __syncwarp();
@@ -1350,6 +1433,7 @@ __global__ void __launch_bounds__(Roles<PM>::threads, 1)
     const uint32_t g_base =
         (raw_base + (uint32_t)(p.raw_nr * p.raw_slice_bytes) + 1023u) & ~1023u;
     const uint32_t w_base = g_base + (uint32_t)(p.ng * p.g_stage_bytes);
+    const uint32_t early_base = g_base + (uint32_t)p.g_stage_bytes;  // G stage 1
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -1373,6 +1457,8 @@ __global__ void __launch_bounds__(Roles<PM>::threads, 1)
             mbar_init(smem_u32(&sh.full_raw[s]), 1);
             mbar_init(smem_u32(&sh.empty_raw[s]), R::g_warps);
         }
+        for (int s = 0; s < kMaxEarly; ++s) mbar_init(smem_u32(&sh.full_early[s]), 1);
+        mbar_init(smem_u32(&sh.early_free), R::g_warps);
         mbar_init(smem_u32(&sh.w_full), 1);
         mbar_init(smem_u32(&sh.mma_done), 1);
         sh.abort_flag = 0;
@@ -1395,7 +1481,7 @@ __global__ void __launch_bounds__(Roles<PM>::threads, 1)
     grid_dependency_wait();
 
     if (warp == R::w_warp) {
-        if (lane == 0) role_weights(p, sh, w_base, raw_base);
+        if (lane == 0) role_weights(p, sh, w_base, raw_base, early_base);
         __syncwarp();
     } else if (warp == R::mma_warp) {
         if (lane == 0) {
@@ -1407,9 +1493,11 @@ __global__ void __launch_bounds__(Roles<PM>::threads, 1)
         __syncwarp();
     } else if (warp >= R::g_warp0) {
         if constexpr (PM)
-            gather_pm(p, sh, g_base, raw_base, warp - R::g_warp0, lane);
+            gather_pm<kPmGWarps, kPmGroups>(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
+        else if (ESIZE == 2 && p.frame64)
+            gather_pm<kGWarps, kF64Groups>(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
         else if (p.gather_tma)
-            gather_from_raw<ESIZE>(p, sh, g_base, raw_base, warp - R::g_warp0, lane);
+            gather_from_raw<ESIZE>(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
         else
             role_gather<ESIZE>(p, sh, g_base, warp - R::g_warp0, lane);
     } else {
@@ -1531,16 +1619,20 @@ int launch_tc(const Plan &plan, const void *grad_out, const void *packed, float 
     p.grad_in = grad_in;
     p.epi_tma = 0;
     p.gather_tma = encode_in_map(p) ? 1 : 0;
-    if (p.pos_m && !p.gather_tma) {
+    if (!p.pos_m) p.epi_tma = encode_out_map(p) ? 1 : 0;
+    if ((p.pos_m && !p.gather_tma) || (p.frame64 && !(p.gather_tma && p.epi_tma))) {
         // The positions-on-M mode needs the TMA gather (grad_out 16-byte
-        // aligned); the general plan shares its packed weights.
+        // aligned), the 64-wide frame also the TMA store epilogue (grad_in
+        // 16-byte aligned); the general plan on the Wr + Jw - 1 frame shares
+        // their packed weights.
         p = plan.tc_alt;
         p.grad_out = grad_out;
         p.packed = packed;
         p.grad_in = grad_in;
         p.gather_tma = encode_in_map(p) ? 1 : 0;
+        p.epi_tma = encode_out_map(p) ? 1 : 0;
     }
-    if (!p.pos_m) p.epi_tma = encode_out_map(p) ? 1 : 0;
+    if (!p.gather_tma) p.raw_early = 0;
     int dev = 0;
     cudaError_t de = cudaGetDevice(&dev);
     if (de != cudaSuccess) return (int)de;

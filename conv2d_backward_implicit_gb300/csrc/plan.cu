@@ -176,6 +176,9 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
         }
     }
     if (!ok) return false;
+    t.raw_early = (t.raw_nr > 0 && t.ng >= 2 && t.nw == 0)
+                      ? (int)std::min<int64_t>(kMaxEarly, t.g_stage_bytes / t.raw_slice_bytes)
+                      : 0;
 
     int64_t tiles = 0;
     for (int i = 0; i < np; ++i) {
@@ -269,6 +272,7 @@ bool plan_pm(const conv2d_grad_input_params &p, int esize, const TcParams &g, Tc
     const int64_t room = kSmemLimit - fixed;
     if (room < 2 * (int64_t)t.raw_slice_bytes) return false;
     t.raw_nr = (int)std::min<int64_t>(4, room / t.raw_slice_bytes);
+    t.raw_early = (int)std::min<int64_t>(kMaxEarly, t.g_stage_bytes / t.raw_slice_bytes);
     t.smem_bytes = (int)(fixed + (int64_t)t.raw_nr * t.raw_slice_bytes);
     // M = 128 positions, N = kW x 64 (taps of one kernel row), A and B K-major.
     const uint32_t fmt = (g.idesc >> 7) & 7u;  // operand format of the general plan
@@ -277,6 +281,56 @@ bool plan_pm(const conv2d_grad_input_params &p, int esize, const TcParams &g, Tc
     uint32_t cols = 32;
     while (cols < (uint32_t)(2 * n)) cols *= 2;  // two accumulator buffers
     t.tmem_cols = cols;
+    *out = t;
+    return true;
+}
+
+// General mode on the 64-wide frame (stride 1, 16-bit, W <= 56, OW <= 56
+// with 16-byte grad_out rows), derived from the general plan `g` (same packed
+// weights, same tiles of output rows).  Window row h = 64u + b holds
+// grad_out[oh = ih0 + ph - (kH-1) + u, ow = b - kPmLeft]; output position
+// 64 r + iw reads tap (kh, kw) at row 64 (r + kH-1-kh) + iw + pw - kw + 8,
+// i.e. the tap's view starts at (kH-1-kh) * 64 + (kW-1-kw) + view0 with
+// view0 = pw + 8 - (kW-1).  Needs the TMA gather and the TMA store epilogue.
+bool plan_frame64(const conv2d_grad_input_params &p, int esize, const TcParams &g, TcParams *out) {
+    if (p.stride != 1 || esize != 2 || g.n_phases != 1 || g.rows_per_tile <= 0 || g.nw != 0)
+        return false;
+    const int64_t H = p.in_h, W = p.in_w, kH = p.kernel_h, kW = p.kernel_w;
+    if (W > kPmPitch - kPmLeft || p.out_w > (uint32_t)(kPmPitch - kPmLeft)) return false;
+    if ((p.out_w * (int64_t)esize) % 16 != 0 || W % 4 != 0) return false;
+    if (kW - 1 > (int64_t)p.padding_w + kPmLeft || p.padding_w > (uint32_t)kPmLeft) return false;
+    TcParams t = g;
+    t.frame64 = 1;
+    t.view0 = (int)(p.padding_w + kPmLeft - (kW - 1));
+    t.rows_per_tile = 4;
+    t.tile_p = 4 * kPmPitch;
+    const int64_t view_end = kPmPitch * (kH - 1) + p.padding_w + kPmLeft + t.tile_p;
+    t.pm_rows = (int)(t.rows_per_tile + kH - 1);
+    t.hbp = (int)round_up(std::max<int64_t>(view_end, (int64_t)kPmPitch * t.pm_rows), 8);
+    if (2 * t.pm_rows * ((kPmPitch - kPmLeft) / 8) > 4 * kGWarps * kF64Groups) return false;
+    t.g_stage_bytes = t.hbp * 128;
+    PhaseDesc &d = t.ph[0];
+    d.X = kPmPitch;
+    d.R = (int)(H + kH - 1);
+    d.p_tiles = (int)((int64_t)p.batch * cdiv(H, t.rows_per_tile));
+    d.hb = t.hbp;
+    d.tile_begin = 0;
+    t.total_tiles = (int64_t)d.p_tiles * t.n_mtiles;
+    t.raw_cs = 16;
+    t.raw_bw = kPmPitch - kPmLeft;
+    t.raw_x0 = 0;
+    t.raw_br = t.pm_rows | 1;
+    t.raw_slice_bytes = (int)round_up((int64_t)t.raw_cs * t.raw_br * t.raw_bw * esize, 128);
+    t.epi_stage_bytes = (int)round_up(kEpiWarps * kTmaBoxCi * W * 4, kEpiWarps * 128);  // TMA boxes only
+    t.ng = 2;
+    const int64_t fixed = kBarrierBytes + 2048 + t.epi_stage_bytes + t.packed_bytes + 2 * (int64_t)t.g_stage_bytes;
+    const int64_t room = kSmemLimit - fixed;
+    if (room < 2 * (int64_t)t.raw_slice_bytes) return false;
+    t.raw_nr = (int)std::min<int64_t>(3, room / t.raw_slice_bytes);
+    t.raw_early = (int)std::min<int64_t>(kMaxEarly, t.g_stage_bytes / t.raw_slice_bytes);
+    t.smem_bytes = (int)(fixed + (int64_t)t.raw_nr * t.raw_slice_bytes);
+    t.idesc = (g.idesc & ~(0x3Fu << 17)) | ((uint32_t)(t.tile_p >> 3) << 17);  // N = 256
+    t.tmem_cols = 2 * t.tile_p;
     *out = t;
     return true;
 }
@@ -324,9 +378,11 @@ int make_plan(const void *params_v, int dtype, int forced_kernel, Plan *plan) {
     if (plan_tc(p, plan->esize, dtype, plan)) {
         plan->kernel = DGRAD_KERNEL_TC;
         plan->tc_alt = plan->tc;
-        TcParams pm;
-        if (forced_kernel == DGRAD_KERNEL_TC_POSM && plan_pm(p, plan->esize, plan->tc, &pm))
-            plan->tc = pm;
+        TcParams v;
+        if (forced_kernel == DGRAD_KERNEL_TC_POSM && plan_pm(p, plan->esize, plan->tc_alt, &v))
+            plan->tc = v;
+        else if (plan_frame64(p, plan->esize, plan->tc_alt, &v))
+            plan->tc = v;
         return DGRAD_OK;
     }
     if (forced_kernel == DGRAD_KERNEL_TC || forced_kernel == DGRAD_KERNEL_TC_POSM)
