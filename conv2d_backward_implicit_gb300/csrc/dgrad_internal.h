@@ -47,6 +47,13 @@ constexpr int kGWarps = 6;
 constexpr int kThreads = 32 * (kGWarp0 + kGWarps);
 constexpr int kSmemLimit = 232448;  // 227 KB dynamic shared memory per block
 constexpr int kBarrierBytes = 1024;
+// Shared memory of a plan: 1 KB to align the base, the barrier block, then the
+// epilogue staging and the raw ring each rounded up to 1 KB, the G stages and
+// the weights (multiples of 1 KB): the rings start on 1 KB boundaries, which
+// the 128-byte swizzle pattern is tied to.
+constexpr int64_t smem_layout_bytes(int64_t epi, int64_t raw, int64_t g_and_w) {
+    return 1024 + kBarrierBytes + (epi + 1023) / 1024 * 1024 + (raw + 1023) / 1024 * 1024 + g_and_w;
+}
 constexpr int kEpiChunk = 32;                 // positions per step of the staged epilogue
 constexpr int kEpiRowFloats = kEpiChunk + 1;  // padded staging row (conflict-free)
 constexpr int kTmaBoxCi = 8;                  // channels per TMA store box (one box per warp)
@@ -95,6 +102,7 @@ struct TcParams {
     int rows_per_tile;      // > 0: tiles are whole frame rows (stride 1), this many per tile
     int epi_tma;            // 1: epilogue stores through TMA (set at launch)
     int epi_stage_bytes;    // shared-memory staging of the epilogue
+    int epi_boxes;          // TMA store boxes per epilogue warp (1, or 2: double-buffered)
     // TMA gather (stride 1, whole-row tiles, resident weights): grad_out rows
     // arrive as [raw_cs channels][raw_br rows][raw_bw columns] slices starting
     // at column raw_x0, through a ring of raw_nr slots, and are transposed in

@@ -304,6 +304,11 @@ __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// All but the latest bulk group of this thread are done reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
@@ -552,6 +557,10 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
     uint32_t phase = 0;
     int64_t issued = 0;  // slices, parked ones included
     bool aborted = false, weights_issued = false, prefetching = false;
+    // This thread reaches here before the grid dependency wait (the setup
+    // below is cold code, run while the previous kernel finishes) and waits
+    // right before its first global-memory access.
+    bool waited = false;
     for (int64_t t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
         const Tile ti = decode_tile(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
@@ -586,6 +595,10 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
                 } else if (!p.pos_m && prefetching && cc == 0 && sl == 0) {
                     prefetch_raw_tile(p, t + (int64_t)kRawLookahead * gridDim.x);
                 }
+                if (!waited) {
+                    grid_dependency_wait();
+                    waited = true;
+                }
                 if (issued < p.raw_early) {  // parked in G stage 1: no slot to wait for
                     const uint32_t full = smem_u32(&sh.full_early[issued]);
                     mbar_arrive_expect_tx(full, box_bytes);
@@ -613,6 +626,7 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
         // tile's slices are queued, the next tile's go to L2.
         if (p.pos_m && prefetching && !aborted) prefetch_raw_tile(p, t + gridDim.x);
     }
+    if (!waited) grid_dependency_wait();
     if (!weights_issued) issue_weights(p, sh, w_base);  // fewer slices than free slots
     if (aborted) {
         const int64_t parked = issued < p.raw_early ? issued : p.raw_early;
@@ -1054,7 +1068,7 @@ __device__ void epilogue_staged(const TcParams &p, const PhaseDesc &d, const Til
 // shared memory and one lane stores the box with a TMA tensor store, so
 // grad_in is written in whole, aligned rows.
 __device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &ti,
-                             uint32_t taddr, uint32_t box, int q, int part, int lane) {
+                             uint32_t taddr, uint32_t box, int q, int part, int lane, int &bsel) {
     const int groups = p.m_tile == 64 ? 1 : 2;
     const int tpi = (d.Hr + p.rows_per_tile - 1) / p.rows_per_tile;
     const int n = ti.pt / tpi, a0 = (ti.pt - n * tpi) * p.rows_per_tile;
@@ -1067,7 +1081,7 @@ __device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &
         const int lg = lane - 16 * gi;
         const bool mine = lg >= 0 && lg < 16;
         const int half_of_lane = (lg >> 3) & 1;
-        const uint32_t row_addr = box + 4u * (uint32_t)(W * (lg & 7));
+        const uint32_t row_off = 4u * (uint32_t)(W * (lg & 7));
         for (int r = part; r < p.rows_per_tile && a0 + r < d.Hr; r += 2) {
             const uint32_t cbase = taddr + (uint32_t)(r * d.X);
             uint32_t v[64];
@@ -1087,18 +1101,26 @@ __device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &
             tmem_wait_ld64(v);
             for (int h = 0; h < 2; ++h) {
                 if (ci0 + 8 * h >= p.Ci) break;
-                // The previous store from this box must be done reading it.
-                if (lane == 0) bulk_wait_read_all();
+                // The store that last used this box must be done reading it
+                // (with two boxes, the one before the latest).
+                if (lane == 0) {
+                    if (p.epi_boxes == 2)
+                        bulk_wait_read_1();
+                    else
+                        bulk_wait_read_all();
+                }
                 __syncwarp();
+                const uint32_t bx = box + (uint32_t)(bsel * kTmaBoxCi * W * 4);
                 if (mine && half_of_lane == h) {
 #pragma unroll
                     for (int e = 0; e < 64; e += 4)
                         if (e < W)
-                            st_shared_v4(row_addr + 4u * e, v[e], v[e + 1], v[e + 2], v[e + 3]);
+                            st_shared_v4(bx + row_off + 4u * e, v[e], v[e + 1], v[e + 2], v[e + 3]);
                 }
                 fence_proxy_async();
                 __syncwarp();
-                if (lane == 0) tma_store_4d(&p.out_map, box, 0, a0 + r, ci0 + 8 * h, n);
+                if (lane == 0) tma_store_4d(&p.out_map, bx, 0, a0 + r, ci0 + 8 * h, n);
+                if (p.epi_boxes == 2) bsel ^= 1;
             }
         }
     }
@@ -1110,6 +1132,7 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
     const int q = warp & 3, part = warp >> 2;
     const int rows = p.m_tile == 64 ? 16 : 32;  // channels this warp's quadrant owns
     const uint32_t st_base = stage + (uint32_t)(p.epi_stage_bytes / kEpiWarps) * warp;
+    int bsel = 0;  // TMA store box in use (double-buffered epilogue)
     int acc = 0;
     uint32_t accph = 0;
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
@@ -1133,7 +1156,7 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.tile_p);
         if (p.epi_tma)
-            epilogue_tma(p, d, ti, taddr, st_base, q, part, lane);
+            epilogue_tma(p, d, ti, taddr, st_base, q, part, lane, bsel);
         else if (rows == 16)
             epilogue_staged<16>(p, d, ti, taddr, st_base, q, part, lane);
         else
@@ -1426,12 +1449,15 @@ __global__ void __launch_bounds__(Roles<PM>::threads, 1)
     dgrad_tc_kernel(const __grid_constant__ TcParams p) {
     using R = Roles<PM>;
     extern __shared__ __align__(1024) uint8_t smem[];
-    Shared &sh = *reinterpret_cast<Shared *>(smem);
-    // Rings start on a 1024-byte boundary: the swizzle pattern is tied to it.
-    const uint32_t epi_stage = smem_u32(smem) + kBarrierBytes;
-    const uint32_t raw_base = (epi_stage + (uint32_t)p.epi_stage_bytes + 1023u) & ~1023u;
+    // Layout (smem_layout_bytes): the base rounded up to 1 KB, the barrier
+    // block, then epilogue staging, raw ring, G stages and weights, each ring
+    // on a 1 KB boundary (the 128-byte swizzle pattern is tied to it).
+    const uint32_t base = (smem_u32(smem) + 1023u) & ~1023u;
+    Shared &sh = *reinterpret_cast<Shared *>(smem + (base - smem_u32(smem)));
+    const uint32_t epi_stage = base + kBarrierBytes;
+    const uint32_t raw_base = epi_stage + (((uint32_t)p.epi_stage_bytes + 1023u) & ~1023u);
     const uint32_t g_base =
-        (raw_base + (uint32_t)(p.raw_nr * p.raw_slice_bytes) + 1023u) & ~1023u;
+        raw_base + (((uint32_t)(p.raw_nr * p.raw_slice_bytes) + 1023u) & ~1023u);
     const uint32_t w_base = g_base + (uint32_t)(p.ng * p.g_stage_bytes);
     const uint32_t early_base = g_base + (uint32_t)p.g_stage_bytes;  // G stage 1
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1478,7 +1504,11 @@ __global__ void __launch_bounds__(Roles<PM>::threads, 1)
     // parameters, so it may overlap the previous kernel; global memory is used
     // only from here.
     if (threadIdx.x == 0) grid_launch_dependents();
-    grid_dependency_wait();
+    // The TMA producer (lane 0 of its warp) waits inside raw_producer, right
+    // before its first global-memory access; the other lanes of that warp
+    // never touch global memory.  Every other thread waits here.
+    const bool lazy_wait = warp == R::w_warp && p.nw == 0 && p.gather_tma;
+    if (!lazy_wait) grid_dependency_wait();
 
     if (warp == R::w_warp) {
         if (lane == 0) role_weights(p, sh, w_base, raw_base, early_base);
@@ -1594,7 +1624,7 @@ bool encode_in_map(TcParams &p) {
 bool encode_out_map(TcParams &p) {
     if (p.rows_per_tile <= 0 || p.stride != 1 || p.W % 4 != 0 || p.W > 64) return false;
     if ((reinterpret_cast<uintptr_t>(p.grad_in) & 15u) != 0) return false;
-    if (p.epi_stage_bytes < kEpiWarps * kTmaBoxCi * p.W * 4) return false;
+    if (p.epi_stage_bytes < kEpiWarps * p.epi_boxes * kTmaBoxCi * p.W * 4) return false;
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)p.Ci,

@@ -106,6 +106,7 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
             epi = std::max(epi, (int)(kEpiWarps * kTmaBoxCi * W * 4));
         epi = (int)round_up(epi, kEpiWarps * 128);  // each warp's area 128-byte aligned
         t.epi_stage_bytes = epi;
+        t.epi_boxes = 1;
         // Raw grad_out slices for the TMA gather (reserved when it can apply).
         int raw = 0;
         t.raw_nr = 0;
@@ -130,7 +131,7 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
                 raw = t.raw_nr * t.raw_slice_bytes;
             }
         }
-        const int budget = kSmemLimit - kBarrierBytes - 2048 - epi - raw;
+        const int budget = (int)(kSmemLimit - smem_layout_bytes(epi, raw, 0));
         // Each stage carries 128 bytes of grad_out channels per frame element or
         // weight row (64 bf16/fp16 or 32 fp32 channels): one 128-byte swizzle row.
         t.kc = 128 / esize;
@@ -148,7 +149,7 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
         t.g_stage_bytes = (int)g_stage;
         t.w_unit_bytes = (int)w_unit;
         t.packed_bytes = packed;
-        const int fixed = kBarrierBytes + 2048 + epi + raw;
+        const int fixed = (int)smem_layout_bytes(epi, raw, 0);
         if (packed + (raw ? 2 : 3) * g_stage <= budget) {
             // Resident weights: loaded once per CTA, beside at least three G
             // stages (two when the TMA gather's raw ring also needs room).
@@ -266,14 +267,16 @@ bool plan_pm(const conv2d_grad_input_params &p, int esize, const TcParams &g, Tc
     t.raw_br = t.pm_rows | 1;
     t.raw_slice_bytes = (int)round_up((int64_t)t.raw_cs * t.raw_br * t.raw_bw * esize, 128);
     t.epi_stage_bytes = kPmXBytes;
+    t.epi_boxes = 0;
     t.ng = 2;
     t.nw = 0;
-    const int64_t fixed = kBarrierBytes + 2048 + t.epi_stage_bytes + t.packed_bytes + 2 * (int64_t)t.g_stage_bytes;
-    const int64_t room = kSmemLimit - fixed;
-    if (room < 2 * (int64_t)t.raw_slice_bytes) return false;
-    t.raw_nr = (int)std::min<int64_t>(4, room / t.raw_slice_bytes);
+    const int64_t gw = t.packed_bytes + 2 * (int64_t)t.g_stage_bytes;
+    t.raw_nr = 0;
+    for (int r = 4; r >= 2 && !t.raw_nr; --r)
+        if (smem_layout_bytes(t.epi_stage_bytes, (int64_t)r * t.raw_slice_bytes, gw) <= kSmemLimit) t.raw_nr = r;
+    if (!t.raw_nr) return false;
     t.raw_early = (int)std::min<int64_t>(kMaxEarly, t.g_stage_bytes / t.raw_slice_bytes);
-    t.smem_bytes = (int)(fixed + (int64_t)t.raw_nr * t.raw_slice_bytes);
+    t.smem_bytes = (int)smem_layout_bytes(t.epi_stage_bytes, (int64_t)t.raw_nr * t.raw_slice_bytes, gw);
     // M = 128 positions, N = kW x 64 (taps of one kernel row), A and B K-major.
     const uint32_t fmt = (g.idesc >> 7) & 7u;  // operand format of the general plan
     const int n = (int)kW * 64;
@@ -321,14 +324,25 @@ bool plan_frame64(const conv2d_grad_input_params &p, int esize, const TcParams &
     t.raw_x0 = 0;
     t.raw_br = t.pm_rows | 1;
     t.raw_slice_bytes = (int)round_up((int64_t)t.raw_cs * t.raw_br * t.raw_bw * esize, 128);
-    t.epi_stage_bytes = (int)round_up(kEpiWarps * kTmaBoxCi * W * 4, kEpiWarps * 128);  // TMA boxes only
+    // TMA store boxes only (8 channels x W floats per warp), two per warp when
+    // that still leaves two raw slots, else one.
+    const int64_t box = kTmaBoxCi * W * 4;
     t.ng = 2;
-    const int64_t fixed = kBarrierBytes + 2048 + t.epi_stage_bytes + t.packed_bytes + 2 * (int64_t)t.g_stage_bytes;
-    const int64_t room = kSmemLimit - fixed;
-    if (room < 2 * (int64_t)t.raw_slice_bytes) return false;
-    t.raw_nr = (int)std::min<int64_t>(3, room / t.raw_slice_bytes);
+    const int64_t gw = t.packed_bytes + 2 * (int64_t)t.g_stage_bytes;
+    t.raw_nr = 0;
+    for (int boxes = 2; boxes >= 1 && !t.raw_nr; --boxes) {
+        const int64_t epi = round_up(kEpiWarps * boxes * box, kEpiWarps * 128);
+        for (int r = 3; r >= 2 && !t.raw_nr; --r) {
+            if (smem_layout_bytes(epi, (int64_t)r * t.raw_slice_bytes, gw) <= kSmemLimit) {
+                t.raw_nr = r;
+                t.epi_boxes = boxes;
+                t.epi_stage_bytes = (int)epi;
+            }
+        }
+    }
+    if (!t.raw_nr) return false;
     t.raw_early = (int)std::min<int64_t>(kMaxEarly, t.g_stage_bytes / t.raw_slice_bytes);
-    t.smem_bytes = (int)(fixed + (int64_t)t.raw_nr * t.raw_slice_bytes);
+    t.smem_bytes = (int)smem_layout_bytes(t.epi_stage_bytes, (int64_t)t.raw_nr * t.raw_slice_bytes, gw);
     t.idesc = (g.idesc & ~(0x3Fu << 17)) | ((uint32_t)(t.tile_p >> 3) << 17);  // N = 256
     t.tmem_cols = 2 * t.tile_p;
     *out = t;
