@@ -103,6 +103,7 @@ struct TcParams {
     int epi_tma;            // 1: epilogue stores through TMA (set at launch)
     int epi_stage_bytes;    // shared-memory staging of the epilogue
     int epi_boxes;          // TMA store boxes per epilogue warp (1, or 2: double-buffered)
+    int epi_box_ci;         // channels per TMA store box: 8, or 16 (64-row tiles, 16x256b reads)
     // TMA gather (stride 1, whole-row tiles, resident weights): grad_out rows
     // arrive as [raw_cs channels][raw_br rows][raw_bw columns] slices starting
     // at column raw_x0, through a ring of raw_nr slots, and are transposed in

@@ -329,6 +329,39 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t *r) {
                  : "memory");
 }
 
+// 16 lanes x 64 columns (eight 16x256b blocks): thread t gets, for block b,
+// r[4b], r[4b+1] = lane t/4, columns 8b + 2(t%4) + {0, 1} and r[4b+2],
+// r[4b+3] = lane t/4 + 8, the same columns.  Asynchronous like tmem_ld16.
+__device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+        "%29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                   "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]),
+                   "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),
+                   "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),
+                   "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, uint32_t a, uint32_t b) {
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
 // Waits for this thread's outstanding TMEM loads into r[0..2][0..15].
 __device__ __forceinline__ void tmem_wait_ld3(uint32_t (&r)[3][16]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;"
@@ -510,6 +543,7 @@ __device__ __forceinline__ void row_tile_origin(const TcParams &p, const PhaseDe
 }
 
 // Bulk copies of the resident packed weights, completing on w_full.
+// Bulk copies of the resident packed weights, completing on w_full.
 __device__ void issue_weights(const TcParams &p, Shared &sh, uint32_t w_base) {
     const uint8_t *src = static_cast<const uint8_t *>(p.packed);
     const uint32_t bar = smem_u32(&sh.w_full);
@@ -569,8 +603,14 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
         row_tile_origin(p, d, ti.pt, n, u_first);
         for (int cc = 0; cc < p.n_cchunks && !aborted; ++cc) {
             for (int sl = 0; sl < slices; ++sl) {
-                // The weights right after the first tile's slices.
-                if (!weights_issued && issued == (per_tile < fill ? per_tile : fill)) {
+                // The weights first: every CTA reads the same packed weights,
+                // so they mostly come from L2 while the first slices' DRAM reads
+                // are in flight.
+                if (!weights_issued) {
+                    if (!waited) {
+                        grid_dependency_wait();
+                        waited = true;
+                    }
                     issue_weights(p, sh, w_base);
                     weights_issued = true;
                 }
@@ -738,17 +778,24 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
                     tc_fence_after();
                     w_grp = w_base + (uint32_t)ws * p.w_stage_bytes;
                 }
+                // Descriptors are linear in the address (start field = addr >> 4,
+                // far from overflowing inside shared memory): a tap's view or a
+                // 32-byte K step is an add to a base descriptor.
+                const uint64_t wd0 = sw128_desc(w_grp);
+                const uint64_t gd0 = sw128_desc(g_stage + (uint32_t)(p.view0 * 128));
+                const uint32_t w_step = (uint32_t)(p.w_unit_bytes >> 4);
+                int j = t0 / d.Jw, i = t0 - j * d.Jw;
                 for (int tap = t0; tap < t1; ++tap) {
-                    const int j = tap / d.Jw, i = tap - j * d.Jw;
-                    const uint32_t g_tap =
-                        g_stage + (uint32_t)(((d.Jh - 1 - j) * d.X + (d.Jw - 1 - i) + p.view0) * 128);
-                    const uint32_t w_tap = w_grp + (uint32_t)((tap - t0) * p.w_unit_bytes);
+                    const uint64_t bd = gd0 + (uint64_t)(((d.Jh - 1 - j) * d.X + (d.Jw - 1 - i)) * 8);
+                    const uint64_t ad = wd0 + (uint64_t)((tap - t0) * w_step);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {  // four 32-byte K steps per 128-byte row
-                        const uint64_t ad = sw128_desc(w_tap + 32u * k);
-                        const uint64_t bd = sw128_desc(g_tap + 32u * k);
-                        tc_mma<TF32>(d_tmem, ad, bd, p.idesc, accumulate);
+                        tc_mma<TF32>(d_tmem, ad + 2u * k, bd + 2u * k, p.idesc, accumulate);
                         accumulate = 1;
+                    }
+                    if (++i == d.Jw) {
+                        i = 0;
+                        ++j;
                     }
                 }
                 if (p.nw != 0) {
@@ -1073,6 +1120,33 @@ __device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &
     const int tpi = (d.Hr + p.rows_per_tile - 1) / p.rows_per_tile;
     const int n = ti.pt / tpi, a0 = (ti.pt - n * tpi) * p.rows_per_tile;
     const int W = p.W;
+    if (p.epi_box_ci == 16) {
+        // 64-row tile: the quadrant's 16 channels (TMEM lanes 0..15 of it) in
+        // one [16][W] box per output row; thread t holds channels t/4 and
+        // t/4 + 8 at two adjacent columns of each 8-column block.
+        const int ci0 = ti.mt * p.m_tile + q * 16;
+        if (ci0 >= p.Ci) return;
+        const int ch = lane >> 2, c2 = 2 * (lane & 3);
+        const uint32_t off_a = 4u * (uint32_t)(ch * W + c2), off_b = off_a + 4u * (uint32_t)(8 * W);
+        for (int r = part; r < p.rows_per_tile && a0 + r < d.Hr; r += 2) {
+            uint32_t v[32];
+            tmem_ld_16x256b_x8(taddr + (uint32_t)(r * d.X), v);
+            tmem_wait_ld32(v);
+            if (lane == 0) bulk_wait_read_all();  // the previous store has read the box
+            __syncwarp();
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                if (8 * b + c2 < W) {  // W is a multiple of 4: both columns or neither
+                    st_shared_v2(box + off_a + 32u * b, v[4 * b], v[4 * b + 1]);
+                    st_shared_v2(box + off_b + 32u * b, v[4 * b + 2], v[4 * b + 3]);
+                }
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) tma_store_4d(&p.out_map, box, 0, a0 + r, ci0, n);
+        }
+        return;
+    }
     for (int gi = 0; gi < groups; ++gi) {
         const int ci0 = ti.mt * p.m_tile + q * 16 * groups + 16 * gi;
         if (ci0 >= p.Ci) break;
@@ -1110,7 +1184,7 @@ __device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &
                         bulk_wait_read_all();
                 }
                 __syncwarp();
-                const uint32_t bx = box + (uint32_t)(bsel * kTmaBoxCi * W * 4);
+                const uint32_t bx = box + (uint32_t)(bsel * p.epi_box_ci * W * 4);
                 if (mine && half_of_lane == h) {
 #pragma unroll
                     for (int e = 0; e < 64; e += 4)
@@ -1620,18 +1694,18 @@ bool encode_in_map(TcParams &p) {
     return r == CUDA_SUCCESS;
 }
 
-// grad_in as a 4-D float32 tensor [N][Ci][H][W] with a [1][16][1][W] store box.
+// grad_in as a 4-D float32 tensor [N][Ci][H][W] with a [1][epi_box_ci][1][W] store box.
 bool encode_out_map(TcParams &p) {
     if (p.rows_per_tile <= 0 || p.stride != 1 || p.W % 4 != 0 || p.W > 64) return false;
     if ((reinterpret_cast<uintptr_t>(p.grad_in) & 15u) != 0) return false;
-    if (p.epi_stage_bytes < kEpiWarps * p.epi_boxes * kTmaBoxCi * p.W * 4) return false;
+    if (p.epi_stage_bytes < kEpiWarps * p.epi_boxes * p.epi_box_ci * p.W * 4) return false;
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)p.Ci,
                                 (cuuint64_t)p.N};
     const cuuint64_t strides[3] = {(cuuint64_t)p.W * 4, (cuuint64_t)p.H * p.W * 4,
                                    (cuuint64_t)p.Ci * p.H * p.W * 4};
-    const cuuint32_t box[4] = {(cuuint32_t)p.W, 1u, (cuuint32_t)kTmaBoxCi, 1u};
+    const cuuint32_t box[4] = {(cuuint32_t)p.W, 1u, (cuuint32_t)p.epi_box_ci, 1u};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     CUresult r = fn(&p.out_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.grad_in, dims, strides, box,
                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,

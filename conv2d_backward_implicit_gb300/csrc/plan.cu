@@ -107,6 +107,7 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
         epi = (int)round_up(epi, kEpiWarps * 128);  // each warp's area 128-byte aligned
         t.epi_stage_bytes = epi;
         t.epi_boxes = 1;
+        t.epi_box_ci = kTmaBoxCi;
         // Raw grad_out slices for the TMA gather (reserved when it can apply).
         int raw = 0;
         t.raw_nr = 0;
@@ -324,13 +325,16 @@ bool plan_frame64(const conv2d_grad_input_params &p, int esize, const TcParams &
     t.raw_x0 = 0;
     t.raw_br = t.pm_rows | 1;
     t.raw_slice_bytes = (int)round_up((int64_t)t.raw_cs * t.raw_br * t.raw_bw * esize, 128);
-    // TMA store boxes only (8 channels x W floats per warp), two per warp when
-    // that still leaves two raw slots, else one.
-    const int64_t box = kTmaBoxCi * W * 4;
+    // TMA store boxes only: 64-row tiles read a quadrant's 16 channels with
+    // the 16x256b TMEM shape (all 32 threads busy) into one 16-channel box
+    // per warp; 128-row tiles use 8-channel boxes, two per warp when that
+    // still leaves two raw slots, else one.
+    t.epi_box_ci = t.m_tile == 64 ? 16 : kTmaBoxCi;
+    const int64_t box = (int64_t)t.epi_box_ci * W * 4;
     t.ng = 2;
     const int64_t gw = t.packed_bytes + 2 * (int64_t)t.g_stage_bytes;
     t.raw_nr = 0;
-    for (int boxes = 2; boxes >= 1 && !t.raw_nr; --boxes) {
+    for (int boxes = t.epi_box_ci == 16 ? 1 : 2; boxes >= 1 && !t.raw_nr; --boxes) {
         const int64_t epi = round_up(kEpiWarps * boxes * box, kEpiWarps * 128);
         for (int r = 3; r >= 2 && !t.raw_nr; --r) {
             if (smem_layout_bytes(epi, (int64_t)r * t.raw_slice_bytes, gw) <= kSmemLimit) {
@@ -344,6 +348,7 @@ bool plan_frame64(const conv2d_grad_input_params &p, int esize, const TcParams &
     t.raw_early = (int)std::min<int64_t>(kMaxEarly, t.g_stage_bytes / t.raw_slice_bytes);
     t.smem_bytes = (int)smem_layout_bytes(t.epi_stage_bytes, (int64_t)t.raw_nr * t.raw_slice_bytes, gw);
     t.idesc = (g.idesc & ~(0x3Fu << 17)) | ((uint32_t)(t.tile_p >> 3) << 17);  // N = 256
+
     t.tmem_cols = 2 * t.tile_p;
     *out = t;
     return true;
