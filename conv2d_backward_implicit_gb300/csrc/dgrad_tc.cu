@@ -172,10 +172,6 @@ __device__ __forceinline__ uint32_t ld_shared_tf32(uint32_t addr) {
     return r;
 }
 
-__device__ __forceinline__ void prefetch_l2(const void *ptr, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -498,42 +494,6 @@ __device__ __forceinline__ int64_t w_block_off(const TcParams &p, const PhaseDes
 }
 
 // ------------------------------------------------------------------ roles
-// L2 prefetch of the grad_out rows every tile of this CTA will gather: per
-// image the tile's window touches, per grad_out channel, one contiguous run of
-// whole rows, fetched with a bulk prefetch (16-byte aligned, clamped to the
-// tensor).  The gather warps' scalar loads then hit L2 instead of waiting on
-// DRAM one miss at a time.
-__device__ void prefetch_windows(const TcParams &p, int64_t first_tile) {
-    const int esize = p.esize;
-    const uint64_t base = reinterpret_cast<uint64_t>(p.grad_out);
-    const uint64_t total = (uint64_t)p.N * p.Co * p.OH * p.OW * esize;
-    const uint64_t plane = (uint64_t)p.OH * p.OW * esize, row = (uint64_t)p.OW * esize;
-    for (int64_t t = first_tile; t < p.total_tiles; t += gridDim.x) {
-        const Tile ti = decode_tile(p, t);
-        if (ti.mt != 0) continue;  // the window is the same for every channel tile
-        const PhaseDesc &d = p.ph[ti.phase];
-        if (d.Jh == 0) continue;
-        const int img = d.R * d.X;
-        const int L0 = tile_start(p, d, ti.pt), L1 = L0 + p.hbp - 1;
-        for (int n = L0 / img; n <= L1 / img && n < p.N; ++n) {
-            const int a = L0 > n * img ? L0 - n * img : 0;
-            const int b = L1 < (n + 1) * img - 1 ? L1 - n * img : img - 1;
-            int u0 = a / d.X - (d.Jh - 1) + d.qh, u1 = b / d.X - (d.Jh - 1) + d.qh;
-            u0 = u0 < 0 ? 0 : u0;
-            u1 = u1 >= p.OH ? p.OH - 1 : u1;
-            if (u0 > u1) continue;
-            for (int co = 0; co < p.Co; ++co) {
-                uint64_t lo = base + ((uint64_t)n * p.Co + co) * plane + (uint64_t)u0 * row;
-                uint64_t hi = lo + (uint64_t)(u1 - u0 + 1) * row;
-                lo = (lo + 15) & ~15ull;
-                hi = hi & ~15ull;
-                if (hi > base + total) hi = (base + total) & ~15ull;
-                if (hi > lo) prefetch_l2(reinterpret_cast<const void *>(lo), (uint32_t)(hi - lo));
-            }
-        }
-    }
-}
-
 // First grad_out row of a whole-row tile's window, and its image.
 __device__ __forceinline__ void row_tile_origin(const TcParams &p, const PhaseDesc &d, int pt,
                                                 int &n, int &u_first) {
@@ -689,12 +649,10 @@ __device__ void role_weights(const TcParams &p, Shared &sh, uint32_t w_base, uin
             raw_producer(p, sh, raw_base, w_base, early_base);
         } else {
             issue_weights(p, sh, w_base);
-            prefetch_windows(p, blockIdx.x);
         }
         wait_drain(smem_u32(&sh.w_full), 0, p, sh);  // never leave a copy in flight
         return;
     }
-    prefetch_windows(p, blockIdx.x);
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
