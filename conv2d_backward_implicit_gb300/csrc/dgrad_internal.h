@@ -58,6 +58,10 @@ constexpr int kEpiChunk = 32;                 // positions per step of the stage
 constexpr int kEpiRowFloats = kEpiChunk + 1;  // padded staging row (conflict-free)
 constexpr int kTmaBoxCi = 8;                  // channels per TMA store box (one box per warp)
 constexpr int kMaxEarly = 4;                  // raw slices parked in G stage 1 at the start
+constexpr int kRawNone = 0, kRawTiled = 1, kRawRows = 2, kRawPlanes = 3;  // TcParams::raw_mode
+constexpr int kRawPlaneMaxBytes = 16384;      // largest whole-plane raw slice
+constexpr int kMaxRaw = 8;                    // raw-slice ring slots
+constexpr int kMaxW = 8;                      // streamed weight stages
 constexpr int kPmPitch = 64;  // positions-on-M mode: frame positions per grad_out row
 constexpr int kPmLeft = 8;    // zero columns before grad_out column 0 in each frame row
 constexpr int kPmMaxKw = 3;   // column taps stacked on N (kW x 64 columns)
@@ -99,17 +103,27 @@ struct TcParams {
     int n_phases;
     int m_tile, n_mtiles;   // input channels per tile (MMA M: 64 or 128) and tiles over Ci
     int tile_p;             // accumulator columns per tile (MMA N)
-    int rows_per_tile;      // > 0: tiles are whole frame rows (stride 1), this many per tile
+    int rows_per_tile;      // > 0: tiles are whole frame rows of one phase, this many per tile
     int epi_tma;            // 1: epilogue stores through TMA (set at launch)
     int epi_stage_bytes;    // shared-memory staging of the epilogue
     int epi_boxes;          // TMA store boxes per epilogue warp (1, or 2: double-buffered)
     int epi_box_ci;         // channels per TMA store box: 8, or 16 (64-row tiles, 16x256b reads)
-    // TMA gather (stride 1, whole-row tiles, resident weights): grad_out rows
-    // arrive as [raw_cs channels][raw_br rows][raw_bw columns] slices starting
-    // at column raw_x0, through a ring of raw_nr slots, and are transposed in
-    // shared memory into the frame window.
+    // Raw-slice gather (whole-row tiles): grad_out rows arrive as [raw_cs
+    // channels][raw_br rows][raw_bw columns] slices starting at column raw_x0,
+    // through a ring of raw_nr slots, and are transposed in shared memory into
+    // the frame window.
     int gather_tma;         // 1: use it (set at launch)
     int raw_nr, raw_cs, raw_br, raw_bw, raw_x0, raw_slice_bytes;
+    // How raw slices are loaded (kRaw*): a 4-D TMA tensor map whose rows are
+    // raw_rowg grad_out rows (a multiple of 16 bytes), one 1-D bulk copy per
+    // channel of a row range (channel planes a multiple of 16 bytes), or one
+    // 1-D bulk copy of whole planes of raw_cs consecutive channels (tiles that
+    // cover whole images).  With raw_rowg > 1 a slice starts on a row that is
+    // a multiple of raw_rowg.
+    int raw_mode, raw_rowg;
+    // 1: tiles are ordered (position tile, phase, channel tile), so the phases
+    // of the same output rows run side by side (all phases have p_tiles).
+    int interleave;
     // The first raw_early slices (at most kMaxEarly) land in G stage 1, idle
     // until the second tile, so more of the first tile's grad_out is in flight.
     int raw_early;

@@ -42,8 +42,11 @@ __device__ unsigned int g_dgrad_error_word = 0;
 
 namespace {
 
+constexpr int kVarGeneral = 0, kVarFrame64 = 1, kVarPosM = 2;  // kernel variants
+
 struct Shared {
-    uint64_t full_g[4], empty_g[4], full_w[4], empty_w[4], full_raw[4], empty_raw[4];
+    uint64_t full_g[4], empty_g[4], full_w[kMaxW], empty_w[kMaxW], full_raw[kMaxRaw],
+        empty_raw[kMaxRaw];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t x_full[16], x_empty[16];  // positions-on-M epilogue boundary exchange
     uint64_t full_early[kMaxEarly];    // raw slices parked in G stage 1
@@ -83,6 +86,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking probe of a phase (no suspend window, unlike try_wait).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -461,7 +477,18 @@ struct Tile {
     int phase, pt, mt;  // phase, 256-position tile, input-channel tile
 };
 
+// V: the kernel variant; only the general mode has interleaved phases.
+template <int V = kVarGeneral>
 __device__ __forceinline__ Tile decode_tile(const TcParams &p, int64_t t) {
+    if (V == kVarGeneral && p.interleave) {  // (position tile, phase, channel tile), phases side by side
+        const int per = p.n_phases * p.n_mtiles;
+        Tile r;
+        r.pt = (int)(t / per);
+        const int rem = (int)(t - (int64_t)r.pt * per);
+        r.phase = rem / p.n_mtiles;
+        r.mt = rem - r.phase * p.n_mtiles;
+        return r;
+    }
     int ph = 0;
     while (ph + 1 < p.n_phases && t >= p.ph[ph + 1].tile_begin) ++ph;
     const int64_t local = t - p.ph[ph].tile_begin;
@@ -483,8 +510,14 @@ __device__ __forceinline__ int tile_start(const TcParams &p, const PhaseDesc &d,
     return pt * p.tile_p;
 }
 
-__device__ __forceinline__ int tile_own(const TcParams &p, const PhaseDesc &d) {
-    return p.rows_per_tile > 0 ? p.rows_per_tile * d.X : p.tile_p;
+// The last row tile of an image owns only the rows left in it: positions past
+// them continue into the next image's frame, which that image's own tiles
+// write.
+__device__ __forceinline__ int tile_own(const TcParams &p, const PhaseDesc &d, int pt) {
+    if (p.rows_per_tile <= 0) return p.tile_p;
+    const int tpi = (d.Hr + p.rows_per_tile - 1) / p.rows_per_tile;
+    const int left = d.Hr - (pt % tpi) * p.rows_per_tile;
+    return (left < p.rows_per_tile ? left : p.rows_per_tile) * d.X;
 }
 
 // Byte offset, inside the packed weights, of (phase, ci tile, channel chunk).
@@ -502,7 +535,103 @@ __device__ __forceinline__ void row_tile_origin(const TcParams &p, const PhaseDe
     u_first = (pt - n * tpi) * p.rows_per_tile - (d.Jh - 1) + d.qh;
 }
 
-// Bulk copies of the resident packed weights, completing on w_full.
+// First grad_out row held by a raw slice whose window starts at row
+// u_first: the window's own first row (tiled mode), that row rounded down to
+// a multiple of raw_rowg (the copy must start 16-byte aligned), or row 0
+// (planes mode: whole planes).
+__device__ __forceinline__ int raw_row_origin(const TcParams &p, int u_first) {
+    if (p.raw_mode == kRawPlanes) return 0;
+    const int g = p.raw_rowg;
+    if (g > 1) return u_first >= 0 ? u_first / g * g : -((-u_first + g - 1) / g) * g;
+    return u_first;
+}
+
+// 1-D bulk prefetch of [src, src + bytes) into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// The grad_out rows [r0, r1) of a rows-mode raw slice that lie inside the
+// grid (r1 <= r0: none).
+__device__ __forceinline__ void raw_rows_inside(const TcParams &p, int u_lo, int &r0, int &r1) {
+    r0 = u_lo < 0 ? 0 : u_lo;
+    r1 = u_lo + p.raw_br < p.OH ? u_lo + p.raw_br : p.OH;
+}
+
+// grad_out channels of the raw slice that starts at channel c0 (0 when c0 is
+// past the last channel: slices come in whole channel chunks).
+__device__ __forceinline__ int raw_slice_channels(const TcParams &p, int c0) {
+    const int left = p.Co - c0;
+    return left <= 0 ? 0 : (left < p.raw_cs ? left : p.raw_cs);
+}
+
+// Loads one raw slice -- raw_cs channels from c0 of image n, the window that
+// starts at grad_out row u_first -- into shared memory at dst, completing on
+// bar.  Tiled mode: one TMA box (rows and channels outside grad_out
+// zero-filled).  Rows / planes modes: 1-D bulk copies of the rows inside the
+// grid and the channels below Co; the gather never reads the rest.
+__device__ __noinline__ void issue_raw_slice_bulk(const TcParams &p, uint32_t dst, int u_first,
+                                                  int c0, int n, uint32_t bar);
+
+__device__ __forceinline__ void issue_raw_slice(const TcParams &p, uint32_t dst, int u_first, int c0,
+                                                int n, uint32_t bar) {
+    if (p.raw_mode == kRawTiled) {  // box rows of raw_rowg grad_out rows
+        mbar_arrive_expect_tx(bar, (uint32_t)(p.raw_cs * p.raw_br * p.raw_bw * p.esize));
+        tma_load_4d(dst, &p.in_map, p.raw_x0, raw_row_origin(p, u_first) / p.raw_rowg, c0, n, bar);
+        return;
+    }
+    issue_raw_slice_bulk(p, dst, u_first, c0, n, bar);
+}
+
+// The 1-D bulk-copy modes of issue_raw_slice.
+__device__ __noinline__ void issue_raw_slice_bulk(const TcParams &p, uint32_t dst, int u_first,
+                                                  int c0, int n, uint32_t bar) {
+    const int64_t plane = (int64_t)p.OH * p.OW * p.esize;
+    const uint8_t *img = static_cast<const uint8_t *>(p.grad_out) + (int64_t)n * p.Co * plane;
+    const int chans = raw_slice_channels(p, c0);
+    if (p.raw_mode == kRawPlanes) {
+        const uint32_t bytes = (uint32_t)(chans * plane);
+        mbar_arrive_expect_tx(bar, bytes);
+        if (bytes) bulk_g2s(dst, img + (int64_t)c0 * plane, bytes, bar);
+        return;
+    }
+    const int u_lo = raw_row_origin(p, u_first);
+    int r0, r1;
+    raw_rows_inside(p, u_lo, r0, r1);
+    const uint32_t row_bytes = (uint32_t)(p.OW * p.esize);
+    const uint32_t bytes = r1 > r0 ? (uint32_t)(r1 - r0) * row_bytes : 0u;
+    mbar_arrive_expect_tx(bar, bytes * (uint32_t)chans);
+    if (bytes == 0 || chans == 0) return;
+    const uint32_t ch_bytes = row_bytes * (uint32_t)p.raw_br;
+    const uint8_t *src = img + (int64_t)c0 * plane + (int64_t)r0 * row_bytes;
+    const uint32_t d0 = dst + (uint32_t)(r0 - u_lo) * row_bytes;
+    for (int c = 0; c < chans; ++c)
+        bulk_g2s(d0 + (uint32_t)c * ch_bytes, src + (int64_t)c * plane, bytes, bar);
+}
+
+// L2 prefetch of one raw slice (same footprint as issue_raw_slice).
+__device__ __noinline__ void prefetch_raw_slice(const TcParams &p, int u_first, int c0, int n) {
+    if (p.raw_mode == kRawTiled) {
+        tma_prefetch_4d(&p.in_map, p.raw_x0, raw_row_origin(p, u_first) / p.raw_rowg, c0, n);
+        return;
+    }
+    const int64_t plane = (int64_t)p.OH * p.OW * p.esize;
+    const uint8_t *img = static_cast<const uint8_t *>(p.grad_out) + (int64_t)n * p.Co * plane;
+    const int chans = raw_slice_channels(p, c0);
+    if (chans == 0) return;
+    if (p.raw_mode == kRawPlanes) {
+        bulk_prefetch_l2(img + (int64_t)c0 * plane, (uint32_t)(chans * plane));
+        return;
+    }
+    int r0, r1;
+    raw_rows_inside(p, raw_row_origin(p, u_first), r0, r1);
+    if (r1 <= r0) return;
+    const int64_t row_bytes = (int64_t)p.OW * p.esize;
+    for (int c = 0; c < chans; ++c)
+        bulk_prefetch_l2(img + (int64_t)(c0 + c) * plane + r0 * row_bytes,
+                         (uint32_t)((r1 - r0) * row_bytes));
+}
+
 // Bulk copies of the resident packed weights, completing on w_full.
 __device__ void issue_weights(const TcParams &p, Shared &sh, uint32_t w_base) {
     const uint8_t *src = static_cast<const uint8_t *>(p.packed);
@@ -517,17 +646,36 @@ __device__ void issue_weights(const TcParams &p, Shared &sh, uint32_t w_base) {
 // L2 prefetch of every raw slice of tile t (if it exists): the ring's TMA
 // loads of that tile then hit L2.
 constexpr int kRawLookahead = 2;  // general mode: tiles of this CTA prefetched ahead
+template <int V>
 __device__ void prefetch_raw_tile(const TcParams &p, int64_t t) {
     if (t >= p.total_tiles) return;
-    const Tile ti = decode_tile(p, t);
+    const Tile ti = decode_tile<V>(p, t);
     const PhaseDesc &d = p.ph[ti.phase];
     if (d.Jh == 0 || ti.mt != 0) return;  // channel tiles share the window
     int n, u_first;
     row_tile_origin(p, d, ti.pt, n, u_first);
     const int slices = p.kc / p.raw_cs;
     for (int cc = 0; cc < p.n_cchunks; ++cc)
-        for (int sl = 0; sl < slices; ++sl)
-            tma_prefetch_4d(&p.in_map, p.raw_x0, u_first, cc * p.kc + sl * p.raw_cs, n);
+        for (int sl = 0; sl < slices; ++sl) {
+            if constexpr (V != kVarGeneral)  // 64-wide frame / positions-on-M: plain tiled map
+                tma_prefetch_4d(&p.in_map, p.raw_x0, u_first, cc * p.kc + sl * p.raw_cs, n);
+            else
+                prefetch_raw_slice(p, u_first, cc * p.kc + sl * p.raw_cs, n);
+        }
+}
+
+// issue_raw_slice for the kernel variant V: the 64-wide frame and
+// positions-on-M always load through the plain tiled map (kept lean: the
+// producer's time per slice sits on the raw ring's turnaround).
+template <int V>
+__device__ __forceinline__ void issue_raw(const TcParams &p, uint32_t dst, int u_first, int c0,
+                                          int n, uint32_t bar) {
+    if constexpr (V != kVarGeneral) {
+        mbar_arrive_expect_tx(bar, (uint32_t)(p.raw_cs * p.raw_br * p.raw_bw * p.esize));
+        tma_load_4d(dst, &p.in_map, p.raw_x0, u_first, c0, n, bar);
+    } else {
+        issue_raw_slice(p, dst, u_first, c0, n, bar);
+    }
 }
 
 // TMA gather producer (warp 9, lane 0): for every tile and channel chunk of
@@ -541,9 +689,9 @@ __device__ void prefetch_raw_tile(const TcParams &p, int64_t t) {
 // kRawLookahead tiles, then each later tile the one kRawLookahead after it;
 // positions-on-M mode (the ring holds a whole tile) the tile after the ring's,
 // then at each tile's end the next one.
+template <int V>
 __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, uint32_t w_base,
                              uint32_t early_base) {
-    const uint32_t box_bytes = (uint32_t)(p.raw_cs * p.raw_br * p.raw_bw * p.esize);
     const int slices = p.kc / p.raw_cs;
     const int64_t per_tile = (int64_t)slices * p.n_cchunks;
     const int64_t fill = p.raw_early + p.raw_nr;  // slices that need no free slot
@@ -556,7 +704,7 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
     // right before its first global-memory access.
     bool waited = false;
     for (int64_t t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
-        const Tile ti = decode_tile(p, t);
+        const Tile ti = decode_tile<V>(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
         int n, u_first;
@@ -591,19 +739,17 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
                     // beyond it (general) or itself (positions-on-M).
                     prefetching = true;
                     for (int k = 0; k <= (p.pos_m ? 0 : kRawLookahead); ++k)
-                        prefetch_raw_tile(p, t + (int64_t)k * gridDim.x);
+                        prefetch_raw_tile<V>(p, t + (int64_t)k * gridDim.x);
                 } else if (!p.pos_m && prefetching && cc == 0 && sl == 0) {
-                    prefetch_raw_tile(p, t + (int64_t)kRawLookahead * gridDim.x);
+                    prefetch_raw_tile<V>(p, t + (int64_t)kRawLookahead * gridDim.x);
                 }
                 if (!waited) {
                     grid_dependency_wait();
                     waited = true;
                 }
                 if (issued < p.raw_early) {  // parked in G stage 1: no slot to wait for
-                    const uint32_t full = smem_u32(&sh.full_early[issued]);
-                    mbar_arrive_expect_tx(full, box_bytes);
-                    tma_load_4d(early_base + (uint32_t)issued * p.raw_slice_bytes, &p.in_map,
-                                p.raw_x0, u_first, cc * p.kc + sl * p.raw_cs, n, full);
+                    issue_raw<V>(p, early_base + (uint32_t)issued * p.raw_slice_bytes, u_first,
+                                    cc * p.kc + sl * p.raw_cs, n, smem_u32(&sh.full_early[issued]));
                     ++issued;
                     continue;
                 }
@@ -611,10 +757,8 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
                     aborted = true;
                     break;
                 }
-                const uint32_t full = smem_u32(&sh.full_raw[slot]);
-                mbar_arrive_expect_tx(full, box_bytes);
-                tma_load_4d(raw_base + (uint32_t)slot * p.raw_slice_bytes, &p.in_map, p.raw_x0,
-                            u_first, cc * p.kc + sl * p.raw_cs, n, full);
+                issue_raw<V>(p, raw_base + (uint32_t)slot * p.raw_slice_bytes, u_first,
+                                cc * p.kc + sl * p.raw_cs, n, smem_u32(&sh.full_raw[slot]));
                 ++issued;
                 if (++slot == p.raw_nr) {
                     slot = 0;
@@ -624,7 +768,7 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
         }
         // Positions-on-M mode (the ring holds a whole tile): all of this
         // tile's slices are queued, the next tile's go to L2.
-        if (p.pos_m && prefetching && !aborted) prefetch_raw_tile(p, t + gridDim.x);
+        if (p.pos_m && prefetching && !aborted) prefetch_raw_tile<V>(p, t + gridDim.x);
     }
     if (!waited) grid_dependency_wait();
     if (!weights_issued) issue_weights(p, sh, w_base);  // fewer slices than free slots
@@ -640,13 +784,143 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
     }
 }
 
-// Warp 5, lane 0: packed weights into shared memory with bulk copies.
+// Producer for streamed weights together with the raw-slice gather (warp 9,
+// lane 0): two independent rings filled in the order the consumers drain
+// them -- raw slices for each tile / channel chunk / slice, and weight stages
+// for each tile / channel chunk / tap group -- by polling both "empty"
+// barriers without blocking, so a full ring never holds up the other.  The
+// raw slices of the CTA's first two tiles are prefetched into L2 at the start,
+// then, at each new tile, those of the CTA's next tile.  Gives up (abort flag,
+// error word) when
+// neither ring makes progress within the wait limit, then drains the copies
+// still in flight.
+__device__ __noinline__ void raw_w_producer(const TcParams &p, Shared &sh, uint32_t raw_base, uint32_t w_base) {
+    const uint8_t *wsrc = static_cast<const uint8_t *>(p.packed);
+    const int slices = p.kc / p.raw_cs;
+    // raw cursor: tile rt, chunk rcc, slice rsl; ring slot / phase
+    int64_t rt = blockIdx.x;
+    int rcc = 0, rsl = 0, rslot = 0;
+    uint32_t rph = 0;
+    int64_t r_issued = 0;
+    // weight cursor: tile wt, chunk wcc, first tap wt0; ring stage / phase
+    int64_t wt = blockIdx.x;
+    int wcc = 0, wt0 = 0, wstage = 0;
+    uint32_t wph = 0;
+    int64_t w_issued = 0;
+    auto skip_empty = [&](int64_t &t) {
+        while (t < p.total_tiles && p.ph[decode_tile(p, t).phase].Jh == 0) t += gridDim.x;
+    };
+    skip_empty(rt);
+    skip_empty(wt);
+    // The ring holds a few slices; the rest of this tile and the next one go
+    // to L2 first, so ring loads wait for L2 rather than DRAM.
+    prefetch_raw_tile<kVarGeneral>(p, rt);
+    prefetch_raw_tile<kVarGeneral>(p, rt + gridDim.x);
+    bool aborted = false;
+    uint64_t t_idle = 0, idle_spins = 0;
+    const uint64_t max_spins = p.wait_limit_ns / 16 + (1u << 20);  // backstop, as in wait_slow
+    while (rt < p.total_tiles || wt < p.total_tiles) {
+        bool progress = false;
+        if (rt < p.total_tiles && mbar_test_wait(smem_u32(&sh.empty_raw[rslot]), rph ^ 1u)) {
+            const Tile ti = decode_tile(p, rt);
+            const PhaseDesc &d = p.ph[ti.phase];
+            int n, u_first;
+            row_tile_origin(p, d, ti.pt, n, u_first);
+            issue_raw_slice(p, raw_base + (uint32_t)rslot * p.raw_slice_bytes, u_first,
+                            rcc * p.kc + rsl * p.raw_cs, n, smem_u32(&sh.full_raw[rslot]));
+            ++r_issued;
+            if (++rslot == p.raw_nr) {
+                rslot = 0;
+                rph ^= 1u;
+            }
+            if (++rsl == slices) {
+                rsl = 0;
+                if (++rcc == p.n_cchunks) {
+                    rcc = 0;
+                    rt += gridDim.x;
+                    skip_empty(rt);
+                    if (rt < p.total_tiles) prefetch_raw_tile<kVarGeneral>(p, rt + gridDim.x);
+                }
+            }
+            progress = true;
+        }
+        if (wt < p.total_tiles && mbar_test_wait(smem_u32(&sh.empty_w[wstage]), wph ^ 1u)) {
+            const Tile ti = decode_tile(p, wt);
+            const PhaseDesc &d = p.ph[ti.phase];
+            const int taps = d.Jh * d.Jw;
+            const int ng = taps - wt0 < p.taps_per_w ? taps - wt0 : p.taps_per_w;
+            const uint32_t bytes = (uint32_t)(ng * p.w_unit_bytes);
+            const uint32_t full = smem_u32(&sh.full_w[wstage]);
+            mbar_arrive_expect_tx(full, bytes);
+            bulk_g2s(w_base + (uint32_t)wstage * p.w_stage_bytes,
+                     wsrc + w_block_off(p, d, ti.mt, wcc) + (int64_t)wt0 * p.w_unit_bytes, bytes, full);
+            ++w_issued;
+            if (++wstage == p.nw) {
+                wstage = 0;
+                wph ^= 1u;
+            }
+            wt0 += p.taps_per_w;
+            if (wt0 >= taps) {
+                wt0 = 0;
+                if (++wcc == p.n_cchunks) {
+                    wcc = 0;
+                    wt += gridDim.x;
+                    skip_empty(wt);
+                }
+            }
+            progress = true;
+        }
+        if (progress) {
+            idle_spins = 0;
+            continue;
+        }
+        if (abort_raised(sh)) {
+            aborted = true;
+            break;
+        }
+        if (idle_spins == 0) t_idle = global_ns();
+        ++idle_spins;
+        __nanosleep(64);  // both rings full: back off instead of hammering the barriers
+        if (((idle_spins & 31u) == 0 && global_ns() - t_idle > p.wait_limit_ns) ||
+            idle_spins > max_spins) {
+            *reinterpret_cast<volatile int *>(&sh.abort_flag) = 1;
+            atomicOr(&g_dgrad_error_word, 1u);
+            aborted = true;
+            break;
+        }
+    }
+    if (aborted) {
+        // Let every copy that may still be landing finish before the CTA exits.
+        const int64_t rk = r_issued < p.raw_nr ? r_issued : p.raw_nr;
+        for (int64_t k = 0; k < rk; ++k) {
+            const int64_t q = r_issued - 1 - k;
+            wait_drain(smem_u32(&sh.full_raw[q % p.raw_nr]), (uint32_t)((q / p.raw_nr) & 1), p, sh);
+        }
+        const int64_t wk = w_issued < p.nw ? w_issued : p.nw;
+        for (int64_t k = 0; k < wk; ++k) {
+            const int64_t q = w_issued - 1 - k;
+            wait_drain(smem_u32(&sh.full_w[q % p.nw]), (uint32_t)((q / p.nw) & 1), p, sh);
+        }
+    }
+}
+
+// Warp 9, lane 0: packed weights into shared memory with bulk copies.
+template <int V>
 __device__ void role_weights(const TcParams &p, Shared &sh, uint32_t w_base, uint32_t raw_base,
                              uint32_t early_base) {
     const uint8_t *src = static_cast<const uint8_t *>(p.packed);
+    if constexpr (V != kVarGeneral) {  // resident weights, raw slices by TMA
+        raw_producer<V>(p, sh, raw_base, w_base, early_base);
+        wait_drain(smem_u32(&sh.w_full), 0, p, sh);
+        return;
+    }
+    if (p.nw != 0 && p.gather_tma) {
+        raw_w_producer(p, sh, raw_base, w_base);
+        return;
+    }
     if (p.nw == 0) {
         if (p.gather_tma) {
-            raw_producer(p, sh, raw_base, w_base, early_base);
+            raw_producer<V>(p, sh, raw_base, w_base, early_base);
         } else {
             issue_weights(p, sh, w_base);
         }
@@ -693,10 +967,10 @@ __device__ void role_weights(const TcParams &p, Shared &sh, uint32_t w_base, uin
     }
 }
 
-// Warp 4, lane 0: tcgen05.mma issue.  D[ci, pos] (TMEM, 256 columns per
+// Warp 8, lane 0: tcgen05.mma issue.  D[ci, pos] (TMEM, 256 columns per
 // buffer) += W_tap[ci, co] (A: packed weights) x G[co, pos + shift(tap)]
 // (B: the frame window seen from the tap's start row).
-template <bool TF32>
+template <bool TF32, int V>
 __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_t w_base,
                          uint32_t tmem) {
     int gs = 0, ws = 0, acc = 0;
@@ -704,7 +978,7 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
     bool aborted = false;
     if (p.nw == 0 && !wait_bar(smem_u32(&sh.w_full), 0, p, sh)) aborted = true;
     for (int64_t t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
-        const Tile ti = decode_tile(p, t);
+        const Tile ti = decode_tile<V>(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
         if (!wait_bar(smem_u32(&sh.acc_empty[acc]), accph ^ 1u, p, sh)) {
@@ -852,19 +1126,26 @@ __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
         const int xoff = -(d.Jw - 1) + d.qw - p.raw_x0;  // raw column of frame column 0
+        int n_img, u_first;
+        row_tile_origin(p, d, ti.pt, n_img, u_first);
+        const int roff = u_first - raw_row_origin(p, u_first);  // raw row of frame row 0
         for (int cc = 0; cc < p.n_cchunks; ++cc) {
             if (!wait_bar_warp(smem_u32(&sh.empty_g[stage]), phase ^ 1u, p, sh, lane)) return;
             if (!stage_writable(p, sh, stage, early_done, lane)) return;
             const uint32_t s_base = g_base + (uint32_t)stage * p.g_stage_bytes;
             for (int sl = 0; sl < slices; ++sl) {
+                // Channels of this slice inside grad_out (the bulk-copy modes
+                // leave the slots of the others stale).
+                const int cv = p.Co - (cc * p.kc + sl * p.raw_cs);
                 uint32_t raw;
                 if (!raw_acquire(p, sh, rc, raw_base, early_base, lane, raw)) return;
                 for (int h = gw * 32 + lane; h < p.hbp; h += kGWarps * 32) {
                     const int rho = h / d.X;
                     const int x = h - rho * d.X + xoff;
-                    const bool inside = x >= 0 && x < p.raw_bw;  // else a zero column of the frame
-                    const uint32_t src =
-                        raw + (uint32_t)rho * row_bytes + (uint32_t)(inside ? x : 0) * ESIZE;
+                    const int u = u_first + rho;
+                    // else a zero column or row of the frame
+                    const bool inside = x >= 0 && x < p.raw_bw && u >= 0 && u < p.OH;
+                    const uint32_t src = raw + (uint32_t)(inside ? (rho + roff) * (int)row_bytes + x * ESIZE : 0);
                     uint32_t q[2][4] = {};
                     if (inside) {
 #pragma unroll
@@ -881,6 +1162,17 @@ __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
                                 for (int e = 0; e < 4; ++e)
                                     q[j][e] = ld_shared_tf32(src + (uint32_t)(j * 4 + e) * ch_bytes);
                             }
+                        }
+                        if (cv < p.raw_cs) {  // ragged last slice: zero the missing channels
+#pragma unroll
+                            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    constexpr int per = 4 / ESIZE;  // channels per 32-bit word
+                                    const int c = (j * 4 + e) * per;
+                                    if (c >= cv) q[j][e] = 0u;
+                                    else if (per == 2 && c + 1 >= cv) q[j][e] &= 0xffffu;
+                                }
                         }
                     }
                     const uint32_t row = s_base + (uint32_t)h * 128u;
@@ -1037,7 +1329,7 @@ __device__ void epilogue_staged(const TcParams &p, const PhaseDesc &d, const Til
     const int ci_base = ti.mt * p.m_tile + q * ROWS;
     int ci_here = p.Ci - ci_base;  // channels of this warp that exist
     ci_here = ci_here < 0 ? 0 : (ci_here > ROWS ? ROWS : ci_here);
-    const int L0 = tile_start(p, d, ti.pt), own = tile_own(p, d);
+    const int L0 = tile_start(p, d, ti.pt), own = tile_own(p, d, ti.pt);
     FramePos f = frame_pos(d, L0 + part * kEpiChunk + lane);
     const uint32_t st_row = st_base + 4u * kEpiRowFloats * lane;  // row written by this lane
     const uint32_t st_col = st_base + 4u * lane;                  // column read by this lane
@@ -1158,6 +1450,7 @@ __device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &
     }
 }
 
+template <int V>
 __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uint32_t tmem,
                               int warp, int lane) {
     const int64_t HW = (int64_t)p.H * p.W;
@@ -1168,13 +1461,13 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
     int acc = 0;
     uint32_t accph = 0;
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-        const Tile ti = decode_tile(p, t);
+        const Tile ti = decode_tile<V>(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
-        if (d.Jh == 0) {  // no tap reaches this phase: grad_in is zero there
+        if (V == kVarGeneral && d.Jh == 0) {  // no tap reaches this phase: grad_in is zero there
             const int ci_base = ti.mt * p.m_tile + q * rows;
             int ci_here = p.Ci - ci_base;
             ci_here = ci_here < 0 ? 0 : (ci_here > rows ? rows : ci_here);
-            const int L0 = tile_start(p, d, ti.pt), own = tile_own(p, d);
+            const int L0 = tile_start(p, d, ti.pt), own = tile_own(p, d, ti.pt);
             FramePos f = frame_pos(d, L0 + part * kEpiChunk + lane);
             for (int c0 = part * kEpiChunk; c0 < own; c0 += 2 * kEpiChunk) {
                 const int64_t o = c0 + lane < own ? out_offset(p, d, f) : -1;
@@ -1187,7 +1480,7 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
         if (!wait_bar_warp(smem_u32(&sh.acc_full[acc]), accph, p, sh, lane)) break;
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.tile_p);
-        if (p.epi_tma)
+        if (V == kVarFrame64 || p.epi_tma)  // the 64-wide frame always stores through TMA
             epilogue_tma(p, d, ti, taddr, st_base, q, part, lane, bsel);
         else if (rows == 16)
             epilogue_staged<16>(p, d, ti, taddr, st_base, q, part, lane);
@@ -1463,23 +1756,28 @@ __device__ void epilogue_pm(const TcParams &p, Shared &sh, uint32_t xbase, uint3
     }
 }
 
-// Warp roles of the two kernel variants.
-template <bool PM>
+// Warp roles of the kernel variants: the general mode and the 64-wide frame
+// share a layout, positions-on-M has its own.
+template <int V>
 struct Roles {
     static constexpr int epi_warps = kEpiWarps, mma_warp = kMmaWarp, w_warp = kWWarp;
     static constexpr int g_warp0 = kGWarp0, g_warps = kGWarps, threads = kThreads;
 };
 template <>
-struct Roles<true> {
+struct Roles<kVarPosM> {
     static constexpr int epi_warps = kPmEpiWarps, mma_warp = kPmMmaWarp, w_warp = kPmWWarp;
     static constexpr int g_warp0 = kPmGWarp0, g_warps = kPmGWarps, threads = kPmThreads;
 };
 
-// PM: the positions-on-M roles and warp layout.
-template <int ESIZE, bool PM>
-__global__ void __launch_bounds__(Roles<PM>::threads, 1)
+// V (kVar*): which plan the kernel runs -- the general mode (any phase count,
+// raw-slice or register gather, resident or streamed weights, TMA-store or
+// staged epilogue), the 64-wide frame, or positions-on-M.  Each variant
+// compiles only its own roles.
+template <int ESIZE, int V>
+__global__ void __launch_bounds__(Roles<V>::threads, 1)
     dgrad_tc_kernel(const __grid_constant__ TcParams p) {
-    using R = Roles<PM>;
+    using R = Roles<V>;
+    constexpr bool PM = V == kVarPosM;
     extern __shared__ __align__(1024) uint8_t smem[];
     // Layout (smem_layout_bytes): the base rounded up to 1 KB, the barrier
     // block, then epilogue staging, raw ring, G stages and weights, each ring
@@ -1543,20 +1841,20 @@ __global__ void __launch_bounds__(Roles<PM>::threads, 1)
     if (!lazy_wait) grid_dependency_wait();
 
     if (warp == R::w_warp) {
-        if (lane == 0) role_weights(p, sh, w_base, raw_base, early_base);
+        if (lane == 0) role_weights<V>(p, sh, w_base, raw_base, early_base);
         __syncwarp();
     } else if (warp == R::mma_warp) {
         if (lane == 0) {
             if constexpr (PM)
                 role_mma_pm(p, sh, g_base, w_base, tmem);
             else
-                role_mma<ESIZE == 4>(p, sh, g_base, w_base, tmem);
+                role_mma<ESIZE == 4, V>(p, sh, g_base, w_base, tmem);
         }
         __syncwarp();
     } else if (warp >= R::g_warp0) {
         if constexpr (PM)
             gather_pm<kPmGWarps, kPmGroups>(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
-        else if (ESIZE == 2 && p.frame64)
+        else if constexpr (V == kVarFrame64)
             gather_pm<kGWarps, kF64Groups>(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
         else if (p.gather_tma)
             gather_from_raw<ESIZE>(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
@@ -1566,7 +1864,7 @@ __global__ void __launch_bounds__(Roles<PM>::threads, 1)
         if constexpr (PM)
             epilogue_pm(p, sh, epi_stage, tmem, warp, lane);
         else
-            role_epilogue(p, sh, epi_stage, tmem, warp, lane);
+            role_epilogue<V>(p, sh, epi_stage, tmem, warp, lane);
     }
     tc_fence_before();
     __syncthreads();
@@ -1579,10 +1877,10 @@ __global__ void __launch_bounds__(Roles<PM>::threads, 1)
 // Dynamic shared memory is raised once per device and variant to the full
 // limit, so no attribute call happens on later launches (e.g. during stream
 // capture).
-template <int ESIZE, bool PM>
+template <int ESIZE, int V>
 int launch_variant(const TcParams &p, int grid, cudaStream_t st, int dev) {
     static std::atomic<uint64_t> configured{0};  // bit per device
-    auto kern = dgrad_tc_kernel<ESIZE, PM>;
+    auto kern = dgrad_tc_kernel<ESIZE, V>;
     const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
     if (!bit || !(configured.load() & bit)) {
         cudaError_t e =
@@ -1594,7 +1892,7 @@ int launch_variant(const TcParams &p, int grid, cudaStream_t st, int dev) {
     // kernel may overlap the tail of the previous one (see grid_dependency_wait).
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(Roles<PM>::threads);
+    cfg.blockDim = dim3(Roles<V>::threads);
     cfg.dynamicSmemBytes = (size_t)p.smem_bytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -1628,21 +1926,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// grad_out as a 4-D tensor [N][Co][OH][OW] with a [1][raw_cs][raw_br][raw_bw]
-// load box, for the TMA gather (whole-row tiles with resident weights only).
+// grad_out as a 4-D tensor [N][Co][OH/g][g*OW] (g = raw_rowg grad_out rows
+// per map row) with a [1][raw_cs][raw_br/g][raw_bw or g*OW] load box, for the
+// tiled-mode raw gather; the bulk-copy modes need no map, only a 16-byte
+// aligned grad_out.
 bool encode_in_map(TcParams &p) {
-    if (p.raw_nr <= 0 || p.rows_per_tile <= 0 || p.nw != 0) return false;
+    if (p.raw_nr <= 0 || p.rows_per_tile <= 0 || p.raw_mode == kRawNone) return false;
     if ((reinterpret_cast<uintptr_t>(p.grad_out) & 15u) != 0) return false;
+    if (p.raw_mode != kRawTiled) return true;  // 1-D bulk copies: no tensor map
     if (((int64_t)p.OW * p.esize) % 16 != 0) return false;
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
-    const int64_t e = p.esize;
-    const cuuint64_t dims[4] = {(cuuint64_t)p.OW, (cuuint64_t)p.OH, (cuuint64_t)p.Co,
+    const int64_t e = p.esize, g = p.raw_rowg;  // g grad_out rows per map row
+    const cuuint64_t dims[4] = {(cuuint64_t)(p.OW * g), (cuuint64_t)(p.OH / g), (cuuint64_t)p.Co,
                                 (cuuint64_t)p.N};
-    const cuuint64_t strides[3] = {(cuuint64_t)(p.OW * e), (cuuint64_t)(p.OH * p.OW * e),
+    const cuuint64_t strides[3] = {(cuuint64_t)(p.OW * g * e), (cuuint64_t)(p.OH * p.OW * e),
                                    (cuuint64_t)((int64_t)p.Co * p.OH * p.OW * e)};
-    const cuuint32_t box[4] = {(cuuint32_t)p.raw_bw, (cuuint32_t)p.raw_br, (cuuint32_t)p.raw_cs,
-                               1u};
+    const cuuint32_t box[4] = {(cuuint32_t)(g > 1 ? p.OW * g : p.raw_bw), (cuuint32_t)(p.raw_br / g),
+                               (cuuint32_t)p.raw_cs, 1u};
     const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     const CUtensorMapDataType dt =
         e == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
@@ -1706,10 +2007,12 @@ int launch_tc(const Plan &plan, const void *grad_out, const void *packed, float 
     const int grid = (int)(p.total_tiles < sms ? p.total_tiles : sms);
     if (grid <= 0) return (int)cudaSuccess;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (plan.esize == 2)
-        return p.pos_m ? launch_variant<2, true>(p, grid, st, dev)
-                       : launch_variant<2, false>(p, grid, st, dev);
-    return launch_variant<4, false>(p, grid, st, dev);
+    if (plan.esize == 2) {
+        if (p.pos_m) return launch_variant<2, kVarPosM>(p, grid, st, dev);
+        if (p.frame64) return launch_variant<2, kVarFrame64>(p, grid, st, dev);
+        return launch_variant<2, kVarGeneral>(p, grid, st, dev);
+    }
+    return launch_variant<4, kVarGeneral>(p, grid, st, dev);
 }
 
 int tc_read_and_clear_error(unsigned int *out) {

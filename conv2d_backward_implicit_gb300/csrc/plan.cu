@@ -8,6 +8,7 @@
 // shared memory, or selects the CUDA-core kernel.
 #include <algorithm>
 #include <cstring>
+#include <numeric>
 
 #include "conv2d_grad_input.h"
 #include "dgrad_internal.h"
@@ -17,6 +18,82 @@ namespace {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+
+// Raw-slice geometry of the gather (tiles of whole frame rows only): each
+// slice holds raw_cs grad_out channels x raw_br rows x raw_bw columns, and the
+// gather warps turn it into the frame window.  Returns 1 and fills the raw_*
+// fields when one of the load modes applies to the shape (none: clear them).
+//  * tiled: grad_out rows a multiple of 16 bytes -- a 4-D TMA box over the
+//    columns that hold data, rows outside the grid zero-filled by the TMA unit;
+//  * planes: every tile covers whole images and raw_cs channel planes are a
+//    multiple of 16 bytes -- one 1-D bulk copy of raw_cs whole planes;
+//  * rows: channel planes a multiple of 16 bytes -- the window's rows from
+//    a row whose byte offset is a multiple of 16 (a multiple of raw_rowg
+//    rows, so a slice holds up to raw_rowg - 1 extra rows above the window):
+//    one TMA box of a map whose rows are raw_rowg grad_out rows when the
+//    planes split into whole such groups (tiled mode with raw_rowg > 1),
+//    else one 1-D bulk copy per channel of the rows inside the grid.
+int plan_raw_slices(const conv2d_grad_input_params &p, int esize, TcParams &t, bool none = false) {
+    t.raw_nr = 0;
+    t.raw_mode = kRawNone;
+    t.raw_rowg = 1;
+    t.raw_x0 = t.raw_bw = t.raw_br = t.raw_cs = t.raw_slice_bytes = 0;
+    if (none || t.rows_per_tile <= 0) return 0;
+    const int64_t OH = p.out_h, OW = p.out_w, Co = p.out_channels;
+    const int64_t row_bytes = OW * esize, plane_bytes = OH * OW * esize;
+    const int A = 16 / esize;  // elements per 16 bytes
+    const int cs = 32 / esize;  // two 16-byte channel chunks per slice
+    // Frame columns that carry grad_out data, over all phases, and the rows
+    // one window spans.
+    int64_t vmin = INT32_MAX, vmax = INT32_MIN, rows = 1;
+    bool whole = true;
+    for (int i = 0; i < t.n_phases; ++i) {
+        const PhaseDesc &d = t.ph[i];
+        if (d.Jh == 0) continue;
+        vmin = std::min<int64_t>(vmin, d.qw - (d.Jw - 1));
+        vmax = std::max<int64_t>(vmax, d.Wr - 1 + d.qw);
+        rows = std::max<int64_t>(rows, (t.hbp - 1) / d.X + 1);
+        if (t.rows_per_tile < d.Hr) whole = false;
+    }
+    if (vmin > vmax) return 0;  // no phase reads grad_out
+    int mode = kRawNone;
+    if (row_bytes % 16 == 0) {
+        const int64_t lo = std::max<int64_t>(vmin, 0), hi = std::min<int64_t>(vmax, OW - 1);
+        const int64_t x0 = lo / A * A;
+        const int64_t bw = round_up(std::max<int64_t>(hi - x0 + 1, 1), A);
+        if (bw <= 256 && rows <= 256) {
+            mode = kRawTiled;
+            t.raw_x0 = (int)x0;
+            t.raw_bw = (int)bw;
+            t.raw_br = (int)rows;
+        }
+    }
+    if (mode == kRawNone && whole && (Co * plane_bytes) % 16 == 0 && (cs * plane_bytes) % 16 == 0 &&
+        cs * plane_bytes <= kRawPlaneMaxBytes) {
+        mode = kRawPlanes;
+        t.raw_bw = (int)OW;
+        t.raw_br = (int)OH;
+    }
+    if (mode == kRawNone && plane_bytes % 16 == 0) {
+        // Windows start on a multiple of g rows (g rows = a multiple of 16
+        // bytes).  When the planes split into whole g-row groups, a TMA map
+        // over [N][Co][OH/g][g*OW] loads each slice as one box; otherwise one
+        // 1-D copy per channel.
+        const int64_t g = 16 / std::gcd<int64_t>(16, row_bytes);
+        const int64_t br = round_up(rows + g - 1, g);
+        mode = (OH % g == 0 && OW * g <= 256 && br / g <= 256) ? kRawTiled : kRawRows;
+        t.raw_rowg = (int)g;
+        t.raw_x0 = 0;
+        t.raw_bw = (int)OW;
+        t.raw_br = (int)br;
+    }
+    if (mode == kRawNone) return 0;
+    t.raw_mode = mode;
+    t.raw_cs = cs;
+    t.raw_slice_bytes = (int)round_up((int64_t)cs * t.raw_br * t.raw_bw * esize, 128);
+    t.raw_nr = 3;
+    return 1;
+}
 
 // Try to build a tensor-core plan.  Returns false when the shape is outside
 // what the tcgen05 kernel supports; the caller then uses the CUDA-core kernel.
@@ -37,21 +114,31 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
     t.m_tile = Ci <= 64 ? 64 : 128;
     t.n_mtiles = (int)cdiv(Ci, t.m_tile);
 
+    // Widest frame row and tallest phase over the stride's phases.
+    int64_t X1 = 1, Hr1 = 1;
+    for (int r = 0; r < s; ++r) {
+        const int64_t Wr = r < W ? cdiv(W - r, s) : 0, Hr = r < H ? cdiv(H - r, s) : 0;
+        const int64_t tw = (r + p.padding_w) % s;
+        const int64_t Jw = tw < kW ? cdiv(kW - tw, s) : 0;
+        X1 = std::max(X1, Jw > 0 ? Wr + Jw - 1 : Wr);
+        Hr1 = std::max(Hr1, Hr);
+    }
+
     // Output positions per tile: 256 (full-rate N); 128 when a 256-wide
     // tile's frame window would not leave room for two stages.
     bool ok = false;
     int np = 0;
     for (int cap = kTileP; cap >= 128 && !ok; cap /= 2) {
-        // Stride 1: tiles of whole frame rows (k rows of X positions, the
-        // accumulator rounded up to 16 columns), so each tile owns complete
-        // output rows.  Otherwise tiles are `cap` consecutive frame positions.
+        // Tiles of whole frame rows (k rows of the widest phase's X positions,
+        // the accumulator rounded up to 16 columns), so each tile owns
+        // complete output rows of its phase; when one row is wider than the
+        // tile, tiles are `cap` consecutive frame positions.
         int tile_p = cap, rows_per_tile = 0;
-        if (s == 1) {
-            const int64_t X1 = W + kW - 1;
+        {
             int64_t k = cap / X1;
             while (k > 0 && round_up(k * X1, 16) > cap) --k;
             if (k > 0) {
-                rows_per_tile = (int)std::min<int64_t>(k, H);
+                rows_per_tile = (int)std::min<int64_t>(k, Hr1);
                 tile_p = (int)round_up(rows_per_tile * X1, 16);
             }
         }
@@ -108,31 +195,6 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
         t.epi_stage_bytes = epi;
         t.epi_boxes = 1;
         t.epi_box_ci = kTmaBoxCi;
-        // Raw grad_out slices for the TMA gather (reserved when it can apply).
-        int raw = 0;
-        t.raw_nr = 0;
-        if (rows_per_tile > 0 && (p.out_w * (int64_t)esize) % 16 == 0) {
-            const int A = 16 / esize;                      // elements per 16 bytes
-            const int64_t vmin = -(int64_t)(kW - 1) + p.padding_w;
-            const int64_t vmax = W - 1 + p.padding_w;
-            // Only columns inside grad_out carry data: the box spans them (from
-            // an aligned start), the transpose writes zero elsewhere.
-            const int64_t lo = std::max<int64_t>(vmin, 0), hi = std::min<int64_t>(vmax, p.out_w - 1);
-            const int64_t x0 = lo / A * A;
-            t.raw_x0 = (int)x0;
-            t.raw_bw = (int)round_up(std::max<int64_t>(hi - x0 + 1, 1), A);
-            const int64_t X1 = W + kW - 1;
-            t.raw_cs = 32 / esize;                         // two 16-byte chunks per slice
-            // rows of one window: kTileP-sized tiles never exceed this
-            const int64_t hbp1 = round_up(tile_p + (kH - 1) * X1 + (kW - 1), 8);
-            t.raw_br = (int)((hbp1 - 1) / X1 + 1);
-            t.raw_slice_bytes = (int)round_up((int64_t)t.raw_cs * t.raw_br * t.raw_bw * esize, 128);
-            if (t.raw_bw <= 256 && t.raw_br <= 256) {
-                t.raw_nr = 3;
-                raw = t.raw_nr * t.raw_slice_bytes;
-            }
-        }
-        const int budget = (int)(kSmemLimit - smem_layout_bytes(epi, raw, 0));
         // Each stage carries 128 bytes of grad_out channels per frame element or
         // weight row (64 bf16/fp16 or 32 fp32 channels): one 128-byte swizzle row.
         t.kc = 128 / esize;
@@ -146,34 +208,66 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
             d.pack_off = packed;
             packed += (int64_t)t.n_mtiles * t.n_cchunks * d.Jh * d.Jw * w_unit;
         }
-        if (2 * g_stage > budget) continue;
         t.g_stage_bytes = (int)g_stage;
         t.w_unit_bytes = (int)w_unit;
         t.packed_bytes = packed;
-        const int fixed = (int)smem_layout_bytes(epi, raw, 0);
-        if (packed + (raw ? 2 : 3) * g_stage <= budget) {
-            // Resident weights: loaded once per CTA, beside at least three G
-            // stages (two when the TMA gather's raw ring also needs room).
-            t.nw = 0;
-            t.taps_per_w = std::max(max_taps, 1);
-            t.w_stage_bytes = (int)(t.taps_per_w * w_unit);
-            t.ng = (int)std::min<int64_t>(4, (budget - packed) / g_stage);
-            ok = true;
-            t.smem_bytes = fixed + (int)(packed + t.ng * g_stage);
-        } else {
-            // Streamed weights: each W stage holds a group of up to taps_per_w
-            // consecutive taps of one channel chunk; four stages when they fit.
-            const int64_t room = budget - 2 * g_stage;
-            int64_t tpw = std::min<int64_t>(std::max(max_taps, 1), room / (4 * w_unit));
-            if (tpw < 1) tpw = std::min<int64_t>(std::max(max_taps, 1), room / (2 * w_unit));
-            if (tpw >= 1) {
+        // Raw grad_out slices for the TMA / bulk-copy gather, reserved when a
+        // load mode applies (tried first; without them if G and W do not fit).
+        const int plan_raw = rows_per_tile > 0 ? plan_raw_slices(p, esize, t) : 0;
+        // Raw slices with streamed weights: two G stages (the gather turns a
+        // slice around in far less time than the MMAs of a stage take), and
+        // the rest of shared memory split between the weight ring and the raw
+        // ring -- the data in flight that covers L2 latency.
+        if (plan_raw && packed + 2 * g_stage + 2 * (int64_t)t.raw_slice_bytes >
+                            kSmemLimit - smem_layout_bytes(epi, 0, 0)) {
+            const int64_t room = kSmemLimit - smem_layout_bytes(epi, 0, 0) - 2 * g_stage - 1024;
+            const int64_t slice = t.raw_slice_bytes;
+            const int64_t tpw = 1;
+            const int64_t w_stage = tpw * w_unit;
+            const int64_t nw = std::min<int64_t>(kMaxW, std::max<int64_t>(2, room / 2 / w_stage));
+            const int64_t nr = std::min<int64_t>(kMaxRaw, (room - nw * w_stage) / slice);
+            if (nr >= 2 && room >= nw * w_stage + nr * slice) {
+                t.raw_nr = (int)nr;
+                t.nw = (int)nw;
+                t.ng = 2;
                 t.taps_per_w = (int)tpw;
-                const int64_t w_stage = tpw * w_unit;
                 t.w_stage_bytes = (int)w_stage;
-                t.nw = (int)std::min<int64_t>(4, room / w_stage);
-                t.ng = (int)std::min<int64_t>(4, (budget - t.nw * w_stage) / g_stage);
-                ok = t.ng >= 2 && t.nw >= 2;
-                t.smem_bytes = fixed + (int)(t.nw * w_stage + t.ng * g_stage);
+                t.smem_bytes = (int)(smem_layout_bytes(epi, nr * slice, 0) + nw * w_stage + 2 * g_stage);
+                ok = t.smem_bytes <= kSmemLimit;
+            }
+        }
+        // Otherwise ring depths tried: 3 raw slots, 2, then none.
+        for (int nr = plan_raw ? 3 : 0; nr >= 0 && !ok; nr = nr == 2 ? 0 : nr - 1) {
+            if (nr == 0) plan_raw_slices(p, esize, t, /*none=*/true);
+            t.raw_nr = nr;
+            const int raw = t.raw_nr * t.raw_slice_bytes;
+            const int budget = (int)(kSmemLimit - smem_layout_bytes(epi, raw, 0));
+            if (2 * g_stage > budget) continue;
+            const int fixed = (int)smem_layout_bytes(epi, raw, 0);
+            if (packed + (raw ? 2 : 3) * g_stage <= budget) {
+                // Resident weights: loaded once per CTA, beside at least three G
+                // stages (two when the raw ring also needs room).
+                t.nw = 0;
+                t.taps_per_w = std::max(max_taps, 1);
+                t.w_stage_bytes = (int)(t.taps_per_w * w_unit);
+                t.ng = (int)std::min<int64_t>(4, (budget - packed) / g_stage);
+                ok = true;
+                t.smem_bytes = fixed + (int)(packed + t.ng * g_stage);
+            } else {
+                // Streamed weights: each W stage holds a group of up to taps_per_w
+                // consecutive taps of one channel chunk; four stages when they fit.
+                const int64_t room = budget - 2 * g_stage;
+                int64_t tpw = std::min<int64_t>(std::max(max_taps, 1), room / (4 * w_unit));
+                if (tpw < 1) tpw = std::min<int64_t>(std::max(max_taps, 1), room / (2 * w_unit));
+                if (tpw >= 1) {
+                    t.taps_per_w = (int)tpw;
+                    const int64_t w_stage = tpw * w_unit;
+                    t.w_stage_bytes = (int)w_stage;
+                    t.nw = (int)std::min<int64_t>(4, room / w_stage);
+                    t.ng = (int)std::min<int64_t>(4, (budget - t.nw * w_stage) / g_stage);
+                    ok = t.ng >= 2 && t.nw >= 2;
+                    t.smem_bytes = fixed + (int)(t.nw * w_stage + t.ng * g_stage);
+                }
             }
         }
     }
@@ -183,9 +277,11 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
                       : 0;
 
     int64_t tiles = 0;
+    t.interleave = np > 1 ? 1 : 0;
     for (int i = 0; i < np; ++i) {
         t.ph[i].tile_begin = tiles;
         tiles += (int64_t)t.ph[i].p_tiles * t.n_mtiles;
+        if (t.ph[i].p_tiles != t.ph[0].p_tiles) t.interleave = 0;
     }
     t.total_tiles = tiles;
 
@@ -262,6 +358,8 @@ bool plan_pm(const conv2d_grad_input_params &p, int esize, const TcParams &g, Tc
     // Raw slices: 16 channels x raw_br rows x 56 columns from column 0; an
     // odd row count keeps the transposing ldmatrix reads free of bank
     // conflicts (channel pitch an odd number of 16-byte units).
+    t.raw_mode = kRawTiled;
+    t.raw_rowg = 1;
     t.raw_cs = 16;
     t.raw_bw = kPmPitch - kPmLeft;
     t.raw_x0 = 0;
@@ -320,6 +418,8 @@ bool plan_frame64(const conv2d_grad_input_params &p, int esize, const TcParams &
     d.hb = t.hbp;
     d.tile_begin = 0;
     t.total_tiles = (int64_t)d.p_tiles * t.n_mtiles;
+    t.raw_mode = kRawTiled;
+    t.raw_rowg = 1;
     t.raw_cs = 16;
     t.raw_bw = kPmPitch - kPmLeft;
     t.raw_x0 = 0;
