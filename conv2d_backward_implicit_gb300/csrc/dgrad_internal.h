@@ -59,9 +59,10 @@ constexpr int kEpiRowFloats = kEpiChunk + 1;  // padded staging row (conflict-fr
 constexpr int kTmaBoxCi = 8;                  // channels per TMA store box (one box per warp)
 constexpr int kMaxEarly = 4;                  // raw slices parked in G stage 1 at the start
 constexpr int kRawNone = 0, kRawTiled = 1, kRawRows = 2, kRawPlanes = 3;  // TcParams::raw_mode
-constexpr int kRawPlaneMaxBytes = 16384;      // largest whole-plane raw slice
+constexpr int kRawPlaneMaxBytes = 49152;      // largest whole-plane raw slice
 constexpr int kMaxRaw = 8;                    // raw-slice ring slots
 constexpr int kMaxW = 8;                      // streamed weight stages
+constexpr int kMaxGatherRows = 6;             // window rows per gather thread (raw-slice gather)
 constexpr int kPmPitch = 64;  // positions-on-M mode: frame positions per grad_out row
 constexpr int kPmLeft = 8;    // zero columns before grad_out column 0 in each frame row
 constexpr int kPmMaxKw = 3;   // column taps stacked on N (kW x 64 columns)

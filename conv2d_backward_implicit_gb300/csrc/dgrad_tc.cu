@@ -784,88 +784,104 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
     }
 }
 
+// A walk over this CTA's tiles (blockIdx.x, + gridDim.x, ...) that skips
+// phases no tap reaches.  Each tile is decoded once, when the walk reaches it,
+// so the per-slice and per-stage work of the producer is a few additions.
+struct TileWalk {
+    int64_t t;
+    const PhaseDesc *d;
+    int mt, n, u_first;
+};
+
+__device__ __forceinline__ bool walk_load(const TcParams &p, TileWalk &w) {
+    for (; w.t < p.total_tiles; w.t += gridDim.x) {
+        const Tile ti = decode_tile(p, w.t);
+        const PhaseDesc &d = p.ph[ti.phase];
+        if (d.Jh == 0) continue;
+        w.d = &d;
+        w.mt = ti.mt;
+        row_tile_origin(p, d, ti.pt, w.n, w.u_first);
+        return true;
+    }
+    return false;
+}
+
 // Producer for streamed weights together with the raw-slice gather (warp 9,
 // lane 0): two independent rings filled in the order the consumers drain
 // them -- raw slices for each tile / channel chunk / slice, and weight stages
 // for each tile / channel chunk / tap group -- by polling both "empty"
-// barriers without blocking, so a full ring never holds up the other.  The
-// raw slices of the CTA's first two tiles are prefetched into L2 at the start,
-// then, at each new tile, those of the CTA's next tile.  Gives up (abort flag,
-// error word) when
-// neither ring makes progress within the wait limit, then drains the copies
-// still in flight.
+// barriers without blocking, so a full ring never holds up the other.  Gives
+// up (abort flag, error word) when neither ring makes progress within the
+// wait limit, then drains the copies still in flight.
 __device__ __noinline__ void raw_w_producer(const TcParams &p, Shared &sh, uint32_t raw_base, uint32_t w_base) {
     const uint8_t *wsrc = static_cast<const uint8_t *>(p.packed);
     const int slices = p.kc / p.raw_cs;
-    // raw cursor: tile rt, chunk rcc, slice rsl; ring slot / phase
-    int64_t rt = blockIdx.x;
-    int rcc = 0, rsl = 0, rslot = 0;
+    const uint32_t w_unit = (uint32_t)p.w_unit_bytes;
+    // raw cursor: tile, chunk rcc, slice rsl; ring slot / phase
+    TileWalk rw{(int64_t)blockIdx.x, nullptr, 0, 0, 0};
+    bool r_live = walk_load(p, rw);
+    int rcc = 0, rsl = 0, rslot = 0, rc0 = 0;  // rc0: first channel of the next slice
     uint32_t rph = 0;
     int64_t r_issued = 0;
-    // weight cursor: tile wt, chunk wcc, first tap wt0; ring stage / phase
-    int64_t wt = blockIdx.x;
-    int wcc = 0, wt0 = 0, wstage = 0;
+    // weight cursor: tile, chunk wcc, first tap wt0; ring stage / phase
+    TileWalk ww{(int64_t)blockIdx.x, nullptr, 0, 0, 0};
+    bool w_live = walk_load(p, ww);
+    int wcc = 0, wt0 = 0, wstage = 0, wtaps = 0;
+    const uint8_t *wblk = nullptr;  // packed weights of (tile, chunk wcc)
+    if (w_live) {
+        wtaps = ww.d->Jh * ww.d->Jw;
+        wblk = wsrc + w_block_off(p, *ww.d, ww.mt, 0);
+    }
     uint32_t wph = 0;
     int64_t w_issued = 0;
-    auto skip_empty = [&](int64_t &t) {
-        while (t < p.total_tiles && p.ph[decode_tile(p, t).phase].Jh == 0) t += gridDim.x;
-    };
-    skip_empty(rt);
-    skip_empty(wt);
-    // The ring holds a few slices; the rest of this tile and the next one go
-    // to L2 first, so ring loads wait for L2 rather than DRAM.
-    prefetch_raw_tile<kVarGeneral>(p, rt);
-    prefetch_raw_tile<kVarGeneral>(p, rt + gridDim.x);
     bool aborted = false;
     uint64_t t_idle = 0, idle_spins = 0;
     const uint64_t max_spins = p.wait_limit_ns / 16 + (1u << 20);  // backstop, as in wait_slow
-    while (rt < p.total_tiles || wt < p.total_tiles) {
+    while (r_live || w_live) {
         bool progress = false;
-        if (rt < p.total_tiles && mbar_test_wait(smem_u32(&sh.empty_raw[rslot]), rph ^ 1u)) {
-            const Tile ti = decode_tile(p, rt);
-            const PhaseDesc &d = p.ph[ti.phase];
-            int n, u_first;
-            row_tile_origin(p, d, ti.pt, n, u_first);
-            issue_raw_slice(p, raw_base + (uint32_t)rslot * p.raw_slice_bytes, u_first,
-                            rcc * p.kc + rsl * p.raw_cs, n, smem_u32(&sh.full_raw[rslot]));
+        if (r_live && mbar_test_wait(smem_u32(&sh.empty_raw[rslot]), rph ^ 1u)) {
+            issue_raw_slice(p, raw_base + (uint32_t)rslot * p.raw_slice_bytes, rw.u_first, rc0, rw.n,
+                            smem_u32(&sh.full_raw[rslot]));
             ++r_issued;
             if (++rslot == p.raw_nr) {
                 rslot = 0;
                 rph ^= 1u;
             }
+            rc0 += p.raw_cs;
             if (++rsl == slices) {
                 rsl = 0;
                 if (++rcc == p.n_cchunks) {
                     rcc = 0;
-                    rt += gridDim.x;
-                    skip_empty(rt);
-                    if (rt < p.total_tiles) prefetch_raw_tile<kVarGeneral>(p, rt + gridDim.x);
+                    rc0 = 0;
+                    rw.t += gridDim.x;
+                    r_live = walk_load(p, rw);
                 }
             }
             progress = true;
         }
-        if (wt < p.total_tiles && mbar_test_wait(smem_u32(&sh.empty_w[wstage]), wph ^ 1u)) {
-            const Tile ti = decode_tile(p, wt);
-            const PhaseDesc &d = p.ph[ti.phase];
-            const int taps = d.Jh * d.Jw;
-            const int ng = taps - wt0 < p.taps_per_w ? taps - wt0 : p.taps_per_w;
-            const uint32_t bytes = (uint32_t)(ng * p.w_unit_bytes);
+        if (w_live && mbar_test_wait(smem_u32(&sh.empty_w[wstage]), wph ^ 1u)) {
+            const int ng = wtaps - wt0 < p.taps_per_w ? wtaps - wt0 : p.taps_per_w;
+            const uint32_t bytes = (uint32_t)ng * w_unit;
             const uint32_t full = smem_u32(&sh.full_w[wstage]);
             mbar_arrive_expect_tx(full, bytes);
-            bulk_g2s(w_base + (uint32_t)wstage * p.w_stage_bytes,
-                     wsrc + w_block_off(p, d, ti.mt, wcc) + (int64_t)wt0 * p.w_unit_bytes, bytes, full);
+            bulk_g2s(w_base + (uint32_t)wstage * p.w_stage_bytes, wblk + (size_t)wt0 * w_unit, bytes, full);
             ++w_issued;
             if (++wstage == p.nw) {
                 wstage = 0;
                 wph ^= 1u;
             }
             wt0 += p.taps_per_w;
-            if (wt0 >= taps) {
+            if (wt0 >= wtaps) {
                 wt0 = 0;
+                wblk += (size_t)wtaps * w_unit;  // chunks of a tile follow one another
                 if (++wcc == p.n_cchunks) {
                     wcc = 0;
-                    wt += gridDim.x;
-                    skip_empty(wt);
+                    ww.t += gridDim.x;
+                    w_live = walk_load(p, ww);
+                    if (w_live) {
+                        wtaps = ww.d->Jh * ww.d->Jw;
+                        wblk = wsrc + w_block_off(p, *ww.d, ww.mt, 0);
+                    }
                 }
             }
             progress = true;
@@ -880,7 +896,7 @@ __device__ __noinline__ void raw_w_producer(const TcParams &p, Shared &sh, uint3
         }
         if (idle_spins == 0) t_idle = global_ns();
         ++idle_spins;
-        __nanosleep(64);  // both rings full: back off instead of hammering the barriers
+        __nanosleep(32);  // both rings full: back off instead of hammering the barriers
         if (((idle_spins & 31u) == 0 && global_ns() - t_idle > p.wait_limit_ns) ||
             idle_spins > max_spins) {
             *reinterpret_cast<volatile int *>(&sh.abort_flag) = 1;
@@ -1107,13 +1123,17 @@ __device__ __forceinline__ bool stage_writable(const TcParams &p, Shared &sh, in
 // Gather warps, TMA variant: the frame window of each stage is assembled
 // from raw slices (raw_cs channels of whole grad_out rows) by a transpose in
 // shared memory: frame element h, channel c comes from slice row h / X,
-// column (h mod X) + vmin - raw_x0.  Each slice fills two 16-byte chunks of
-// every 128-byte window row.
+// column (h mod X) + vmin - raw_x0.  Each slice fills raw_cs / E 16-byte
+// chunks of every 128-byte window row.  A thread owns the window rows
+// h = 32 gw + lane + 32 kGWarps k; their places in a slice are worked out
+// once per tile.
 template <int ESIZE>
 __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
                                 uint32_t raw_base, uint32_t early_base, int gw, int lane) {
-    constexpr int E = 16 / ESIZE;  // elements per 16-byte chunk
+    constexpr int E = 16 / ESIZE;  // channels per 16-byte chunk
+    constexpr int kStep = kGWarps * 32;
     const int slices = p.kc / p.raw_cs;
+    const int groups = p.raw_cs / E;  // 16-byte chunks per slice and window row
     int stage = 0;
     uint32_t phase = 0;
     RawCursor rc;
@@ -1121,14 +1141,36 @@ __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
     bool withhold = (p.debug_flags & DGRAD_DEBUG_SKIP_ARRIVE) && gw == 0;
     const uint32_t row_bytes = (uint32_t)(p.raw_bw * ESIZE);
     const uint32_t ch_bytes = row_bytes * (uint32_t)p.raw_br;
+    const int h0 = gw * 32 + lane;
+    const int nrows = h0 < p.hbp ? (p.hbp - 1 - h0) / kStep + 1 : 0;  // <= kMaxGatherRows (plan)
     for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
         const Tile ti = decode_tile(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
+        const int X = d.X;
         const int xoff = -(d.Jw - 1) + d.qw - p.raw_x0;  // raw column of frame column 0
         int n_img, u_first;
         row_tile_origin(p, d, ti.pt, n_img, u_first);
         const int roff = u_first - raw_row_origin(p, u_first);  // raw row of frame row 0
+        // Byte offset inside a slice of each owned row, or -1 (zero row or
+        // column of the frame).
+        int src[kMaxGatherRows];
+        {
+            int rho = h0 / X, x = h0 - rho * X;
+            const int drho = kStep / X, dx = kStep - drho * X;
+#pragma unroll
+            for (int k = 0; k < kMaxGatherRows; ++k) {
+                const int u = u_first + rho, xc = x + xoff;
+                const bool inside = xc >= 0 && xc < p.raw_bw && u >= 0 && u < p.OH;
+                src[k] = inside ? (rho + roff) * (int)row_bytes + xc * ESIZE : -1;
+                rho += drho;
+                x += dx;
+                if (x >= X) {
+                    x -= X;
+                    ++rho;
+                }
+            }
+        }
         for (int cc = 0; cc < p.n_cchunks; ++cc) {
             if (!wait_bar_warp(smem_u32(&sh.empty_g[stage]), phase ^ 1u, p, sh, lane)) return;
             if (!stage_writable(p, sh, stage, early_done, lane)) return;
@@ -1139,47 +1181,39 @@ __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
                 const int cv = p.Co - (cc * p.kc + sl * p.raw_cs);
                 uint32_t raw;
                 if (!raw_acquire(p, sh, rc, raw_base, early_base, lane, raw)) return;
-                for (int h = gw * 32 + lane; h < p.hbp; h += kGWarps * 32) {
-                    const int rho = h / d.X;
-                    const int x = h - rho * d.X + xoff;
-                    const int u = u_first + rho;
-                    // else a zero column or row of the frame
-                    const bool inside = x >= 0 && x < p.raw_bw && u >= 0 && u < p.OH;
-                    const uint32_t src = raw + (uint32_t)(inside ? (rho + roff) * (int)row_bytes + x * ESIZE : 0);
-                    uint32_t q[2][4] = {};
-                    if (inside) {
 #pragma unroll
-                        for (int j = 0; j < 2; ++j) {
+                for (int k = 0; k < kMaxGatherRows; ++k) {
+                    if (k >= nrows) break;
+                    const int h = h0 + k * kStep;
+                    const uint32_t row = s_base + (uint32_t)h * 128u;
+                    const int off = src[k];
+                    for (int j = 0; j < groups; ++j) {
+                        uint32_t q[4] = {0u, 0u, 0u, 0u};
+                        if (off >= 0) {
+                            const uint32_t a = raw + (uint32_t)off + (uint32_t)(j * E) * ch_bytes;
                             if constexpr (ESIZE == 2) {
 #pragma unroll
-                                for (int e = 0; e < 8; e += 2) {
-                                    const uint32_t c = (uint32_t)(j * 8 + e);
-                                    q[j][e / 2] = ld_shared_u16(src + c * ch_bytes) |
-                                                  (ld_shared_u16(src + (c + 1) * ch_bytes) << 16);
-                                }
+                                for (int e = 0; e < 8; e += 2)
+                                    q[e / 2] = ld_shared_u16(a + (uint32_t)e * ch_bytes) |
+                                               (ld_shared_u16(a + (uint32_t)(e + 1) * ch_bytes) << 16);
                             } else {
 #pragma unroll
-                                for (int e = 0; e < 4; ++e)
-                                    q[j][e] = ld_shared_tf32(src + (uint32_t)(j * 4 + e) * ch_bytes);
+                                for (int e = 0; e < 4; ++e) q[e] = ld_shared_tf32(a + (uint32_t)e * ch_bytes);
                             }
-                        }
-                        if (cv < p.raw_cs) {  // ragged last slice: zero the missing channels
-#pragma unroll
-                            for (int j = 0; j < 2; ++j)
+                            const int c0 = j * E;
+                            if (c0 + E > cv) {  // ragged last slice: zero the missing channels
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
                                     constexpr int per = 4 / ESIZE;  // channels per 32-bit word
-                                    const int c = (j * 4 + e) * per;
-                                    if (c >= cv) q[j][e] = 0u;
-                                    else if (per == 2 && c + 1 >= cv) q[j][e] &= 0xffffu;
+                                    const int c = c0 + e * per;
+                                    if (c >= cv) q[e] = 0u;
+                                    else if (per == 2 && c + 1 >= cv) q[e] &= 0xffffu;
                                 }
+                            }
                         }
+                        st_shared_v4(row + (uint32_t)(((sl * groups + j) ^ (h & 7)) << 4), q[0], q[1],
+                                     q[2], q[3]);
                     }
-                    const uint32_t row = s_base + (uint32_t)h * 128u;
-#pragma unroll
-                    for (int j = 0; j < 2; ++j)
-                        st_shared_v4(row + (uint32_t)(((2 * sl + j) ^ (h & 7)) << 4), q[j][0],
-                                     q[j][1], q[j][2], q[j][3]);
                 }
                 raw_release(p, sh, rc, lane);
             }
@@ -1197,7 +1231,6 @@ __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
             }
         }
     }
-    (void)E;
 }
 
 // Gather warps: grad_out frame windows into 128-byte swizzled K-major rows
@@ -1934,7 +1967,7 @@ bool encode_in_map(TcParams &p) {
     if (p.raw_nr <= 0 || p.rows_per_tile <= 0 || p.raw_mode == kRawNone) return false;
     if ((reinterpret_cast<uintptr_t>(p.grad_out) & 15u) != 0) return false;
     if (p.raw_mode != kRawTiled) return true;  // 1-D bulk copies: no tensor map
-    if (((int64_t)p.OW * p.esize) % 16 != 0) return false;
+    if (((int64_t)p.OW * p.raw_rowg * p.esize) % 16 != 0) return false;  // map rows: raw_rowg grad_out rows
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn) return false;
     const int64_t e = p.esize, g = p.raw_rowg;  // g grad_out rows per map row

@@ -33,16 +33,19 @@ int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 //    one TMA box of a map whose rows are raw_rowg grad_out rows when the
 //    planes split into whole such groups (tiled mode with raw_rowg > 1),
 //    else one 1-D bulk copy per channel of the rows inside the grid.
-int plan_raw_slices(const conv2d_grad_input_params &p, int esize, TcParams &t, bool none = false) {
+int plan_raw_slices(const conv2d_grad_input_params &p, int esize, TcParams &t, bool none = false,
+                    int cs = 0) {
     t.raw_nr = 0;
     t.raw_mode = kRawNone;
     t.raw_rowg = 1;
     t.raw_x0 = t.raw_bw = t.raw_br = t.raw_cs = t.raw_slice_bytes = 0;
     if (none || t.rows_per_tile <= 0) return 0;
+    // Every window row a gather thread owns keeps its slice offset in a register.
+    if (t.hbp > kGWarps * 32 * kMaxGatherRows) return 0;
     const int64_t OH = p.out_h, OW = p.out_w, Co = p.out_channels;
     const int64_t row_bytes = OW * esize, plane_bytes = OH * OW * esize;
     const int A = 16 / esize;  // elements per 16 bytes
-    const int cs = 32 / esize;  // two 16-byte channel chunks per slice
+    if (cs <= 0) cs = 32 / esize;  // default: two 16-byte channel chunks per slice
     // Frame columns that carry grad_out data, over all phases, and the rows
     // one window spans.
     int64_t vmin = INT32_MAX, vmax = INT32_MIN, rows = 1;
@@ -211,14 +214,36 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
         t.g_stage_bytes = (int)g_stage;
         t.w_unit_bytes = (int)w_unit;
         t.packed_bytes = packed;
+        // When the weights cannot stay resident beside the raw ring, they are
+        // streamed, preferably with raw slices of a whole channel chunk (one
+        // copy and one hand-over per stage instead of several), when at least
+        // two such slices fit beside two G stages and two weight stages.
+        const bool narrow_raw = rows_per_tile > 0 && plan_raw_slices(p, esize, t);
+        if (narrow_raw && t.kc > 32 / esize &&
+            packed + 2 * g_stage + 2 * (int64_t)t.raw_slice_bytes > kSmemLimit - smem_layout_bytes(epi, 0, 0) &&
+            plan_raw_slices(p, esize, t, false, t.kc)) {
+            const int64_t room = kSmemLimit - smem_layout_bytes(epi, 0, 0) - 2 * g_stage - 1024;
+            const int64_t slice = t.raw_slice_bytes, w_stage = w_unit;
+            for (int64_t nw = std::min<int64_t>(kMaxW, std::max<int64_t>(2, room / 2 / w_stage)); nw >= 2 && !ok; --nw) {
+                const int64_t nr = std::min<int64_t>(kMaxRaw, (room - nw * w_stage) / slice);
+                if (nr < 2) continue;
+                t.raw_nr = (int)nr;
+                t.nw = (int)nw;
+                t.ng = 2;
+                t.taps_per_w = 1;
+                t.w_stage_bytes = (int)w_stage;
+                t.smem_bytes = (int)(smem_layout_bytes(epi, nr * slice, 0) + nw * w_stage + 2 * g_stage);
+                ok = t.smem_bytes <= kSmemLimit;
+            }
+        }
         // Raw grad_out slices for the TMA / bulk-copy gather, reserved when a
         // load mode applies (tried first; without them if G and W do not fit).
-        const int plan_raw = rows_per_tile > 0 ? plan_raw_slices(p, esize, t) : 0;
+        const int plan_raw = ok ? 1 : (rows_per_tile > 0 ? plan_raw_slices(p, esize, t) : 0);
         // Raw slices with streamed weights: two G stages (the gather turns a
         // slice around in far less time than the MMAs of a stage take), and
         // the rest of shared memory split between the weight ring and the raw
         // ring -- the data in flight that covers L2 latency.
-        if (plan_raw && packed + 2 * g_stage + 2 * (int64_t)t.raw_slice_bytes >
+        if (!ok && plan_raw && packed + 2 * g_stage + 2 * (int64_t)t.raw_slice_bytes >
                             kSmemLimit - smem_layout_bytes(epi, 0, 0)) {
             const int64_t room = kSmemLimit - smem_layout_bytes(epi, 0, 0) - 2 * g_stage - 1024;
             const int64_t slice = t.raw_slice_bytes;
