@@ -155,6 +155,14 @@ struct TcParams {
     int view0;
     int pad_w;              // padding_w: start of the row-tap views in the window
     int pm_rows;            // window rows holding grad_out data (raw_br >= pm_rows)
+    // 1x1 stride-1 convolutions whose tiles are whole images (a plain GEMM per
+    // image): the grad_out operand is read MN-major -- [channel][position], as
+    // NCHW memory holds it -- from 128-byte swizzled atoms of 8 channels x 64
+    // positions, so the gather regroups 16-byte pieces instead of transposing.
+    // Atom (channel group g, position block m) sits at g * 1024 * mn_atoms +
+    // m * 1024 in a G stage.
+    int mn_b;
+    int mn_atoms;           // 64-position atoms per channel group (tile_p <= 64 * mn_atoms)
     PhaseDesc ph[kMaxPhases];
 };
 

@@ -428,6 +428,20 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
     return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand in the 128-byte
+// swizzle layout: atoms of 8 K rows x 128 bytes (64 16-bit MN elements), the
+// 16-byte chunk c of row r at chunk position c ^ r; lbo = bytes from one
+// 64-element MN atom to the next, sbo = bytes from one 8-row K group to the
+// next.
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
 // ----------------------------------------------------------- bounded waits
 __device__ __forceinline__ bool abort_raised(Shared &sh) {
     return *reinterpret_cast<volatile int *>(&sh.abort_flag) != 0;
@@ -1030,7 +1044,11 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
                 // far from overflowing inside shared memory): a tap's view or a
                 // 32-byte K step is an add to a base descriptor.
                 const uint64_t wd0 = sw128_desc(w_grp);
-                const uint64_t gd0 = sw128_desc(g_stage + (uint32_t)(p.view0 * 128));
+                // MN-major grad_out: a 16-channel K step is two 8-row groups.
+                const uint32_t mn_sbo = (uint32_t)p.mn_atoms * 1024u;
+                const uint64_t gd0 = p.mn_b ? sw128_mn_desc(g_stage, 1024u, mn_sbo)
+                                            : sw128_desc(g_stage + (uint32_t)(p.view0 * 128));
+                const uint32_t b_kstep = p.mn_b ? (2u * mn_sbo) >> 4 : 2u;
                 const uint32_t w_step = (uint32_t)(p.w_unit_bytes >> 4);
                 int j = t0 / d.Jw, i = t0 - j * d.Jw;
                 for (int tap = t0; tap < t1; ++tap) {
@@ -1038,7 +1056,7 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
                     const uint64_t ad = wd0 + (uint64_t)((tap - t0) * w_step);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {  // four 32-byte K steps per 128-byte row
-                        tc_mma<TF32>(d_tmem, ad + 2u * k, bd + 2u * k, p.idesc, accumulate);
+                        tc_mma<TF32>(d_tmem, ad + 2u * k, bd + (uint64_t)(b_kstep * k), p.idesc, accumulate);
                         accumulate = 1;
                     }
                     if (++i == d.Jw) {
@@ -1217,6 +1235,73 @@ __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
                 }
                 raw_release(p, sh, rc, lane);
             }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+                if (withhold)
+                    withhold = false;  // failure injection: this stage is never signalled
+                else
+                    mbar_arrive(smem_u32(&sh.full_g[stage]));
+            }
+            if (++stage == p.ng) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+}
+
+// Gather warps, MN-major operand (1x1 stride-1 tiles of whole images): a raw
+// slice holds kc whole channel planes, [c][H*W] with a plane pitch of H*W
+// elements; each 16-byte piece (8 consecutive positions of one channel) goes
+// to its place in the stage's swizzled MN-major atoms.  Pieces past the end
+// of a plane hold whatever follows it: those output columns are never stored.
+// Channels past Co are zero.
+__device__ void gather_mn(const TcParams &p, Shared &sh, uint32_t g_base, uint32_t raw_base,
+                          uint32_t early_base, int gw, int lane) {
+    constexpr int kStep = kGWarps * 32;
+    const uint32_t plane = (uint32_t)(p.OH * p.OW) * 2u;  // bytes per channel plane (a multiple of 8)
+    const int pieces = p.mn_atoms * 8;                     // 16-byte pieces per channel
+    const int items = p.kc * pieces;
+    const uint32_t sbo = (uint32_t)p.mn_atoms * 1024u;
+    int stage = 0;
+    uint32_t phase = 0;
+    RawCursor rc;
+    bool early_done = false;
+    bool withhold = (p.debug_flags & DGRAD_DEBUG_SKIP_ARRIVE) && gw == 0;
+    // This thread's first piece (channel c0, piece v0) and the stride between
+    // its pieces, in channels and pieces.
+    const int i0 = gw * 32 + lane;
+    const int c0 = i0 / pieces, v0 = i0 - c0 * pieces;
+    const int dc = kStep / pieces, dv = kStep - dc * pieces;
+    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        for (int cc = 0; cc < p.n_cchunks; ++cc) {
+            if (!wait_bar_warp(smem_u32(&sh.empty_g[stage]), phase ^ 1u, p, sh, lane)) return;
+            if (!stage_writable(p, sh, stage, early_done, lane)) return;
+            const uint32_t s_base = g_base + (uint32_t)stage * p.g_stage_bytes;
+            const int cv = p.Co - cc * p.kc;  // channels of this chunk inside grad_out
+            uint32_t raw;
+            if (!raw_acquire(p, sh, rc, raw_base, early_base, lane, raw)) return;
+            int c = c0, v = v0;
+            for (int i = i0; i < items; i += kStep) {
+                uint32_t q0 = 0u, q1 = 0u, q2 = 0u, q3 = 0u;
+                if (c < cv) {
+                    const uint32_t a = raw + (uint32_t)c * plane + (uint32_t)v * 16u;
+                    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(q0), "=r"(q1) : "r"(a) : "memory");
+                    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(q2), "=r"(q3) : "r"(a + 8u) : "memory");
+                }
+                const int r = c & 7;
+                st_shared_v4(s_base + (uint32_t)(c >> 3) * sbo + (uint32_t)(v >> 3) * 1024u +
+                                 (uint32_t)r * 128u + (uint32_t)(((v & 7) ^ r) << 4),
+                             q0, q1, q2, q3);
+                c += dc;
+                v += dv;
+                if (v >= pieces) {
+                    v -= pieces;
+                    ++c;
+                }
+            }
+            raw_release(p, sh, rc, lane);
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) {
@@ -1889,6 +1974,8 @@ __global__ void __launch_bounds__(Roles<V>::threads, 1)
             gather_pm<kPmGWarps, kPmGroups>(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
         else if constexpr (V == kVarFrame64)
             gather_pm<kGWarps, kF64Groups>(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
+        else if (ESIZE == 2 && p.mn_b)
+            gather_mn(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
         else if (p.gather_tma)
             gather_from_raw<ESIZE>(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
         else
@@ -2016,11 +2103,12 @@ int launch_tc(const Plan &plan, const void *grad_out, const void *packed, float 
     p.epi_tma = 0;
     p.gather_tma = encode_in_map(p) ? 1 : 0;
     if (!p.pos_m) p.epi_tma = encode_out_map(p) ? 1 : 0;
-    if ((p.pos_m && !p.gather_tma) || (p.frame64 && !(p.gather_tma && p.epi_tma))) {
-        // The positions-on-M mode needs the TMA gather (grad_out 16-byte
-        // aligned), the 64-wide frame also the TMA store epilogue (grad_in
-        // 16-byte aligned); the general plan on the Wr + Jw - 1 frame shares
-        // their packed weights.
+    if ((p.pos_m && !p.gather_tma) || (p.frame64 && !(p.gather_tma && p.epi_tma)) ||
+        (p.mn_b && !p.gather_tma)) {
+        // The positions-on-M mode and the MN-major operand need the TMA /
+        // bulk-copy gather (grad_out 16-byte aligned), the 64-wide frame also
+        // the TMA store epilogue (grad_in 16-byte aligned); the general plan
+        // on the Wr + Jw - 1 frame shares their packed weights.
         p = plan.tc_alt;
         p.grad_out = grad_out;
         p.packed = packed;

@@ -479,6 +479,47 @@ bool plan_frame64(const conv2d_grad_input_params &p, int esize, const TcParams &
     return true;
 }
 
+// MN-major plan for 1x1, stride-1, unpadded 16-bit problems whose tiles are
+// whole images loaded as raw planes of a whole channel chunk (weights
+// streamed): derived from the
+// general plan `g` (same tiles, same packed weights).  A G stage holds kc / 8
+// channel groups x mn_atoms atoms of 1 KB; the rings are re-fitted around it.
+bool plan_mn(const conv2d_grad_input_params &p, int esize, const TcParams &g, TcParams *out) {
+    if (p.stride != 1 || p.kernel_h != 1 || p.kernel_w != 1 || p.padding_h || p.padding_w || esize != 2)
+        return false;
+    // Channel planes start 8-byte aligned in the raw slice (the gather's 8-byte loads).
+    if (((int64_t)p.out_h * p.out_w) % 4 != 0) return false;
+    // Raw slices must be whole channel planes, [c][OH][OW] with no padding:
+    // plane copies, or tensor-map boxes that span whole rows and planes.
+    const bool planes = g.raw_mode == kRawPlanes ||
+                        (g.raw_mode == kRawTiled && g.raw_rowg == 1 && g.raw_x0 == 0 &&
+                         g.raw_bw == (int)p.out_w && g.raw_br == (int)p.out_h);
+    if (g.n_phases != 1 || g.rows_per_tile < (int)p.in_h || !planes || g.raw_cs != g.kc || g.nw < 2 ||
+        g.raw_nr < 2 || g.tile_p > 256)
+        return false;
+    TcParams t = g;
+    t.mn_b = 1;
+    t.mn_atoms = (int)cdiv(t.tile_p, 64);
+    t.g_stage_bytes = (t.kc / 8) * t.mn_atoms * 1024;
+    t.hbp = t.mn_atoms * 64;
+    t.ph[0].hb = t.hbp;
+    const int64_t slice = t.raw_slice_bytes, w_stage = t.w_stage_bytes;
+    auto bytes = [&](int64_t nr, int64_t nw) {
+        return smem_layout_bytes(t.epi_stage_bytes, nr * slice, 0) + nw * w_stage + 2 * (int64_t)t.g_stage_bytes;
+    };
+    int64_t nr = t.raw_nr, nw = t.nw;
+    while (bytes(nr, nw) > kSmemLimit && (nw > 2 || nr > 2)) {
+        if (nw > 2 && (nw >= nr || nr <= 2)) --nw; else --nr;
+    }
+    if (bytes(nr, nw) > kSmemLimit) return false;
+    t.raw_nr = (int)nr;
+    t.nw = (int)nw;
+    t.smem_bytes = (int)bytes(nr, nw);
+    t.idesc |= 1u << 16;  // B (grad_out) MN-major
+    *out = t;
+    return true;
+}
+
 }  // namespace
 
 int make_plan(const void *params_v, int dtype, int forced_kernel, Plan *plan) {
@@ -526,6 +567,8 @@ int make_plan(const void *params_v, int dtype, int forced_kernel, Plan *plan) {
         if (forced_kernel == DGRAD_KERNEL_TC_POSM && plan_pm(p, plan->esize, plan->tc_alt, &v))
             plan->tc = v;
         else if (plan_frame64(p, plan->esize, plan->tc_alt, &v))
+            plan->tc = v;
+        else if (plan_mn(p, plan->esize, plan->tc_alt, &v))
             plan->tc = v;
         return DGRAD_OK;
     }

@@ -7,7 +7,9 @@ them into the frame window; how a slice is loaded depends on the shape:
 * tiled over groups of g rows (rows not a multiple of 16 bytes, planes split
   into whole g-row groups: a 28-column bf16 row needs g = 2);
 * one 1-D bulk copy per channel (the g-row group is wider than a TMA box);
-* one 1-D bulk copy of whole channel planes (tiles that cover whole images).
+* one 1-D bulk copy of whole channel planes (tiles that cover whole images);
+* 1x1 problems whose tiles are whole images: the grad_out operand is read
+  MN-major (channel rows of positions), regrouped in 16-byte pieces.
 
 Each case below is chosen (and commented) for the mode it exercises, with
 several images whose last row tile runs past the image, channel counts that
@@ -43,6 +45,10 @@ CASES = [
      "one 1-D copy per channel (a 4-row group of 150 columns exceeds a TMA box)"),
     ((3, 64, 24, 24, 136, 3, 3, 1, 1, 1), "f32",
      "tiled, TF32; rows per tile do not divide H; Co=136 ragged"),
+    ((3, 200, 12, 12, 300, 1, 1, 1, 0, 0), "bf16",
+     "MN-major grad_out operand from whole-plane copies (1x1); Co=300 leaves a 44-channel chunk"),
+    ((2, 130, 16, 16, 520, 1, 1, 1, 0, 0), "f16",
+     "MN-major operand from whole-plane tensor-map boxes; Ci=130: a 2-channel second tile"),
 ]
 
 
