@@ -311,6 +311,17 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t sm
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
+// The same for a 3-D tensor map.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t smem_src, int x, int y,
+                                             int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(z), "r"(smem_src)
+        : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
 // None of this thread's bulk groups may still be reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -1282,18 +1293,24 @@ __device__ void gather_mn(const TcParams &p, Shared &sh, uint32_t g_base, uint32
             const int cv = p.Co - cc * p.kc;  // channels of this chunk inside grad_out
             uint32_t raw;
             if (!raw_acquire(p, sh, rc, raw_base, early_base, lane, raw)) return;
+            // All of this thread's pieces are loaded first, then stored, so the
+            // loads overlap one another.
+            uint32_t q[kMaxMnPieces][4], dst[kMaxMnPieces];
             int c = c0, v = v0;
-            for (int i = i0; i < items; i += kStep) {
-                uint32_t q0 = 0u, q1 = 0u, q2 = 0u, q3 = 0u;
-                if (c < cv) {
-                    const uint32_t a = raw + (uint32_t)c * plane + (uint32_t)v * 16u;
-                    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(q0), "=r"(q1) : "r"(a) : "memory");
-                    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(q2), "=r"(q3) : "r"(a + 8u) : "memory");
+#pragma unroll
+            for (int k = 0; k < kMaxMnPieces; ++k) {
+                q[k][0] = q[k][1] = q[k][2] = q[k][3] = 0u;
+                dst[k] = ~0u;
+                if (i0 + k * kStep < items) {
+                    if (c < cv) {
+                        const uint32_t a = raw + (uint32_t)c * plane + (uint32_t)v * 16u;
+                        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(q[k][0]), "=r"(q[k][1]) : "r"(a) : "memory");
+                        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(q[k][2]), "=r"(q[k][3]) : "r"(a + 8u) : "memory");
+                    }
+                    const int r = c & 7;
+                    dst[k] = s_base + (uint32_t)(c >> 3) * sbo + (uint32_t)(v >> 3) * 1024u + (uint32_t)r * 128u +
+                             (uint32_t)(((v & 7) ^ r) << 4);
                 }
-                const int r = c & 7;
-                st_shared_v4(s_base + (uint32_t)(c >> 3) * sbo + (uint32_t)(v >> 3) * 1024u +
-                                 (uint32_t)r * 128u + (uint32_t)(((v & 7) ^ r) << 4),
-                             q0, q1, q2, q3);
                 c += dc;
                 v += dv;
                 if (v >= pieces) {
@@ -1301,6 +1318,9 @@ __device__ void gather_mn(const TcParams &p, Shared &sh, uint32_t g_base, uint32
                     ++c;
                 }
             }
+#pragma unroll
+            for (int k = 0; k < kMaxMnPieces; ++k)
+                if (dst[k] != ~0u) st_shared_v4(dst[k], q[k][0], q[k][1], q[k][2], q[k][3]);
             raw_release(p, sh, rc, lane);
             fence_proxy_async();
             __syncwarp();
@@ -1484,6 +1504,38 @@ __device__ void epilogue_staged(const TcParams &p, const PhaseDesc &d, const Til
 // grad_in is written in whole, aligned rows.
 __device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &ti,
                              uint32_t taddr, uint32_t box, int q, int part, int lane, int &bsel) {
+    if (p.mn_b) {
+        // Whole-image 1x1 tiles: accumulator column c is plane position c.
+        // Per 32 positions the warp's channels go into a [channels][32]
+        // float box, 128-byte swizzled (conflict-free writes; the box is
+        // 1 KB aligned), stored with one TMA tensor store; positions past
+        // the plane and channels past Ci are clipped by the TMA unit.
+        const int rows = p.m_tile == 64 ? 16 : 32;
+        const int ci0 = ti.mt * p.m_tile + q * rows;
+        if (ci0 >= p.Ci) return;
+        const int tpi = (d.Hr + p.rows_per_tile - 1) / p.rows_per_tile;
+        const int n = ti.pt / tpi, own = tile_own(p, d, ti.pt);
+        for (int b = part; b * 32 < own; b += 2) {
+            uint32_t v[2][16];
+            tmem_ld16(taddr + (uint32_t)(32 * b), v[0]);
+            tmem_ld16(taddr + (uint32_t)(32 * b + 16), v[1]);
+            tmem_wait_ld16x2(v);
+            if (lane == 0) bulk_wait_read_all();  // the previous store has read the box
+            __syncwarp();
+            if (lane < rows) {
+                const uint32_t row = box + (uint32_t)lane * 128u;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    st_shared_v4(row + (uint32_t)((k ^ (lane & 7)) << 4), v[k >> 2][4 * (k & 3)],
+                                 v[k >> 2][4 * (k & 3) + 1], v[k >> 2][4 * (k & 3) + 2],
+                                 v[k >> 2][4 * (k & 3) + 3]);
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) tma_store_3d(&p.out_map, box, 32 * b, ci0, n);
+        }
+        return;
+    }
     const int groups = p.m_tile == 64 ? 1 : 2;
     const int tpi = (d.Hr + p.rows_per_tile - 1) / p.rows_per_tile;
     const int n = ti.pt / tpi, a0 = (ti.pt - n * tpi) * p.rows_per_tile;
@@ -2073,8 +2125,27 @@ bool encode_in_map(TcParams &p) {
     return r == CUDA_SUCCESS;
 }
 
-// grad_in as a 4-D float32 tensor [N][Ci][H][W] with a [1][epi_box_ci][1][W] store box.
+// grad_in as a 4-D float32 tensor [N][Ci][H][W] with a [1][epi_box_ci][1][W] store box;
+// for the MN-major mode a 3-D tensor [N][Ci][H*W] with a 128-byte swizzled
+// [1][channels][32] box (one box per warp and 32 positions).
 bool encode_out_map(TcParams &p) {
+    if (p.mn_b) {
+        const int64_t HW = (int64_t)p.H * p.W;
+        const int rows = p.m_tile == 64 ? 16 : 32;
+        if ((reinterpret_cast<uintptr_t>(p.grad_in) & 15u) != 0 || (HW * 4) % 16 != 0) return false;
+        if (p.epi_stage_bytes / kEpiWarps < rows * 128 || (p.epi_stage_bytes / kEpiWarps) % 1024 != 0)
+            return false;
+        PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+        if (!fn) return false;
+        const cuuint64_t dims[3] = {(cuuint64_t)HW, (cuuint64_t)p.Ci, (cuuint64_t)p.N};
+        const cuuint64_t strides[2] = {(cuuint64_t)HW * 4, (cuuint64_t)p.Ci * HW * 4};
+        const cuuint32_t box[3] = {32u, (cuuint32_t)rows, 1u};
+        const cuuint32_t estr[3] = {1u, 1u, 1u};
+        CUresult r = fn(&p.out_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.grad_in, dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        return r == CUDA_SUCCESS;
+    }
     if (p.rows_per_tile <= 0 || p.stride != 1 || p.W % 4 != 0 || p.W > 64) return false;
     if ((reinterpret_cast<uintptr_t>(p.grad_in) & 15u) != 0) return false;
     if (p.epi_stage_bytes < kEpiWarps * p.epi_boxes * p.epi_box_ci * p.W * 4) return false;

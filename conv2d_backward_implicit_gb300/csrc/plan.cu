@@ -502,7 +502,12 @@ bool plan_mn(const conv2d_grad_input_params &p, int esize, const TcParams &g, Tc
     t.mn_atoms = (int)cdiv(t.tile_p, 64);
     t.g_stage_bytes = (t.kc / 8) * t.mn_atoms * 1024;
     t.hbp = t.mn_atoms * 64;
+    if ((int64_t)t.kc * t.mn_atoms * 8 > (int64_t)kMaxMnPieces * kGWarps * 32) return false;
     t.ph[0].hb = t.hbp;
+    // Epilogue staging per warp: a 1 KB-aligned swizzled [channels][32]
+    // float box for the plane TMA store, with room for the staged epilogue's
+    // padded block when that store cannot be used.
+    t.epi_stage_bytes = kEpiWarps * (int)round_up((int64_t)32 * kEpiRowFloats * 4, 1024);
     const int64_t slice = t.raw_slice_bytes, w_stage = t.w_stage_bytes;
     auto bytes = [&](int64_t nr, int64_t nw) {
         return smem_layout_bytes(t.epi_stage_bytes, nr * slice, 0) + nw * w_stage + 2 * (int64_t)t.g_stage_bytes;
