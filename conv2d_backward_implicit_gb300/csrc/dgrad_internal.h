@@ -164,11 +164,26 @@ struct TcParams {
     // m * 1024 in a G stage.
     int mn_b;
     int mn_atoms;           // 64-position atoms per channel group (tile_p <= 64 * mn_atoms)
+    // Stacked-phase mode (few input channels, stride > 1): 128 positions of
+    // the phase grid on the MMA M side, every phase's input channels stacked
+    // on N (column n = (rh * stride + rw) * Ci + ci, st_n columns), K = grad_out
+    // channels x the st_th x st_tw window taps (dy, dx) = (st_dy0 + t / st_tw,
+    // st_dx0 + t mod st_tw) that any phase uses.  The single frame of ph[0]
+    // holds grad_out[a + dy][b + dx] for output (a, b); A = that frame seen
+    // from the tap's shift, B = the packed weights of (channel chunk, tap),
+    // st_n rows, zero where a phase does not use the tap.
+    int stacked;
+    int st_n, st_th, st_tw, st_dy0, st_dx0;
     PhaseDesc ph[kMaxPhases];
 };
 
 struct PackParams {
     int Ci, Co, kH, kW, stride;
+    // Stacked-phase layout (TcParams::stacked): per channel chunk and window
+    // tap, st_n rows; phase k = rh * stride + rw uses tap (dy, dx) when
+    // j = qh[k] - dy and i = qw[k] - dx are taps of it.
+    int stacked, st_n, st_th, st_tw, st_dy0, st_dx0;
+    int qh[kMaxPhases], qw[kMaxPhases];
     int m_tile, n_mtiles, kc, n_cchunks, elems16;  // elems16: elements per 16 bytes
     int n_phases;
     int64_t total_elems;

@@ -1102,6 +1102,67 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
     wait_drain(smem_u32(&sh.mma_done), 0, p, sh);
 }
 
+// Warp 8, lane 0, stacked-phase mode: D[position, (phase, ci)] (TMEM, st_n
+// columns per buffer) += G[position + shift(tap), co] (A: the frame window
+// seen from the tap's start row) x W_tap[(phase, ci), co] (B: resident packed
+// weights of the chunk and tap).
+template <bool TF32>
+__device__ void role_mma_stacked(const TcParams &p, Shared &sh, uint32_t g_base, uint32_t w_base,
+                                 uint32_t tmem) {
+    int gs = 0, acc = 0;
+    uint32_t gph = 0, accph = 0;
+    bool aborted = !wait_bar(smem_u32(&sh.w_full), 0, p, sh);
+    const int X = p.ph[0].X;
+    const int taps = p.st_th * p.st_tw;
+    for (int64_t t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
+        if (!wait_bar(smem_u32(&sh.acc_empty[acc]), accph ^ 1u, p, sh)) {
+            aborted = true;
+            break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * p.st_n);
+        uint32_t accumulate = 0;
+        for (int cc = 0; cc < p.n_cchunks; ++cc) {
+            if (!wait_bar(smem_u32(&sh.full_g[gs]), gph, p, sh)) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            const uint64_t ad0 = sw128_desc(g_base + (uint32_t)gs * p.g_stage_bytes);
+            const uint64_t bd0 = sw128_desc(w_base + (uint32_t)(cc * taps) * (uint32_t)p.w_unit_bytes);
+            const uint32_t w_step = (uint32_t)(p.w_unit_bytes >> 4);
+            int dy = 0, dx = 0;
+            for (int tap = 0; tap < taps; ++tap) {
+                const uint64_t ad = ad0 + (uint64_t)((dy * X + dx) * 8);  // 128-byte rows, in 16-byte units
+                const uint64_t bd = bd0 + (uint64_t)(tap * w_step);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {  // four 32-byte K steps per 128-byte row
+                    tc_mma<TF32>(d_tmem, ad + 2u * k, bd + 2u * k, p.idesc, accumulate);
+                    accumulate = 1;
+                }
+                if (++dx == p.st_tw) {
+                    dx = 0;
+                    ++dy;
+                }
+            }
+            tc_commit(smem_u32(&sh.empty_g[gs]));
+            if (++gs == p.ng) {
+                gs = 0;
+                gph ^= 1u;
+            }
+        }
+        if (aborted) break;
+        tc_commit(smem_u32(&sh.acc_full[acc]));
+        if (++acc == 2) {
+            acc = 0;
+            accph ^= 1u;
+        }
+    }
+    // No MMA may still be running when TMEM is released.
+    tc_commit(smem_u32(&sh.mma_done));
+    wait_drain(smem_u32(&sh.mma_done), 0, p, sh);
+}
+
 // Consumer side of the raw slices (gather warps): the first raw_early come
 // from G stage 1, the rest through the ring.  After its last parked slice a
 // warp arrives on early_free; a warp waits for it before it first writes
@@ -1620,6 +1681,47 @@ __device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &
     }
 }
 
+// Stacked-phase epilogue: TMEM lane = tile position (frame row r, column b of
+// the phase grid), column n = (rh * s + rw) * Ci + ci.  Lane quadrant q holds
+// positions 32q..32q+31; the two warps of a quadrant take the phases of
+// either parity.  Each value goes to grad_in[n][ci][s (a0 + r) + rh][s b + rw];
+// consecutive lanes write consecutive columns of a phase, the other phases of
+// the row fill the columns in between.
+__device__ void epilogue_stacked(const TcParams &p, const PhaseDesc &d, const Tile &ti,
+                                 uint32_t taddr, int q, int part, int lane) {
+    uint32_t v[32];
+    tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(v));
+    if (p.st_n > 16) tmem_ld16(taddr + 16u, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+    tmem_wait_ld32(v);
+    const int tpi = (d.Hr + p.rows_per_tile - 1) / p.rows_per_tile;
+    const int n = ti.pt / tpi, a0 = (ti.pt - n * tpi) * p.rows_per_tile;
+    const int h = 32 * q + lane;
+    const int r = h / d.X, b = h - r * d.X;
+    if (r >= p.rows_per_tile || a0 + r >= d.Hr || b >= d.Wr) return;
+    const int s = p.stride, phases = s * s;
+    const int64_t HW = (int64_t)p.H * p.W;
+    float *img = p.grad_in + (int64_t)n * p.Ci * HW;
+    // Column c = k * Ci + ci, walked with (k, ci) kept alongside so that v is
+    // indexed by constants only.
+    int k = 0, ci = 0, rh = 0, rw = 0;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+        if (k >= phases) break;
+        if ((k & 1) == part) {
+            const int ih = s * (a0 + r) + rh, iw = s * b + rw;
+            if (ih < p.H && iw < p.W) img[(int64_t)ci * HW + (int64_t)ih * p.W + iw] = __uint_as_float(v[c]);
+        }
+        if (++ci == p.Ci) {
+            ci = 0;
+            ++k;
+            if (++rw == s) {
+                rw = 0;
+                ++rh;
+            }
+        }
+    }
+}
+
 template <int V>
 __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uint32_t tmem,
                               int warp, int lane) {
@@ -1650,7 +1752,10 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
         if (!wait_bar_warp(smem_u32(&sh.acc_full[acc]), accph, p, sh, lane)) break;
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.tile_p);
-        if (V == kVarFrame64 || p.epi_tma)  // the 64-wide frame always stores through TMA
+        if (V == kVarGeneral && p.stacked)
+            epilogue_stacked(p, d, ti, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.st_n), q, part,
+                             lane);
+        else if (V == kVarFrame64 || p.epi_tma)  // the 64-wide frame always stores through TMA
             epilogue_tma(p, d, ti, taddr, st_base, q, part, lane, bsel);
         else if (rows == 16)
             epilogue_staged<16>(p, d, ti, taddr, st_base, q, part, lane);
@@ -2018,7 +2123,12 @@ __global__ void __launch_bounds__(Roles<V>::threads, 1)
             if constexpr (PM)
                 role_mma_pm(p, sh, g_base, w_base, tmem);
             else
-                role_mma<ESIZE == 4, V>(p, sh, g_base, w_base, tmem);
+            {
+                if (V == kVarGeneral && p.stacked)
+                    role_mma_stacked<ESIZE == 4>(p, sh, g_base, w_base, tmem);
+                else
+                    role_mma<ESIZE == 4, V>(p, sh, g_base, w_base, tmem);
+            }
         }
         __syncwarp();
     } else if (warp >= R::g_warp0) {

@@ -10,6 +10,8 @@
 //     for each Ci tile mt, grad_out channel chunk cc, tap j, tap i:
 //       m_tile rows (ci) of 128 bytes (kc consecutive co), 128-byte swizzled
 //
+// (stacked-phase mode: for each channel chunk cc and window tap t, st_n rows
+// n = phase * Ci + ci of 128 bytes, zero where that phase has no such tap)
 // i.e. K-major [Ci, K] operand tiles in the 128-byte swizzle layout of the
 // tcgen05 shared-memory descriptors: within each group of 8 rows, the 16-byte
 // chunk c of row r is stored at chunk position c ^ (r mod 8).  Rows ci >= Ci
@@ -41,6 +43,34 @@ __global__ void __launch_bounds__(256) pack_weight_kernel(const T *__restrict__ 
     const int64_t stride_all = (int64_t)gridDim.x * blockDim.x;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < k.total_elems;
          idx += stride_all) {
+        if (k.stacked) {
+            // [chunk cc][tap t][row n][kc], rows 128-byte swizzled.
+            const int E = k.elems16;
+            int64_t r = idx;
+            const int pos = (int)(r % k.kc); r /= k.kc;
+            const int n = (int)(r % k.st_n); r /= k.st_n;
+            const int taps = k.st_th * k.st_tw;
+            const int t = (int)(r % taps);
+            const int cc = (int)(r / taps);
+            const int chunk = (pos / E) ^ (n & 7);
+            const int co = cc * k.kc + chunk * E + pos % E;
+            const int ph = n / k.Ci, ci = n - ph * k.Ci;
+            T v = T(0);
+            if (co < k.Co && ph < k.stride * k.stride) {
+                const int j = k.qh[ph] - (k.st_dy0 + t / k.st_tw);
+                const int i = k.qw[ph] - (k.st_dx0 + t % k.st_tw);
+                if (j >= 0 && j < k.Jh[ph] && i >= 0 && i < k.Jw[ph]) {
+                    const int kh = k.stride * j + k.th[ph], kw = k.stride * i + k.tw[ph];
+                    v = w[(((int64_t)co * k.Ci + ci) * k.kH + kh) * k.kW + kw];
+                }
+            }
+            if constexpr (sizeof(T) == 4) {
+                out[idx] = __uint_as_float(to_tf32_rna(v));
+            } else {
+                out[idx] = v;
+            }
+            continue;
+        }
         int ph = 0;
         while (ph + 1 < k.n_phases && idx >= k.elem_begin[ph + 1]) ++ph;
         int64_t r = idx - k.elem_begin[ph];

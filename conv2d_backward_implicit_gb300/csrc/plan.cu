@@ -525,6 +525,125 @@ bool plan_mn(const conv2d_grad_input_params &p, int esize, const TcParams &g, Tc
     return true;
 }
 
+// Stacked-phase plan (stride 2..4, stride^2 x Ci <= 32; see
+// TcParams::stacked).  Tap (j, i) of phase (rh, rw) reads grad_out
+// (a + qh - j, b + qw - i) for output (a, b) of the phase grid; the window
+// taps (dy, dx) are the union of those offsets over the phases, dy in
+// [st_dy0, st_dy0 + st_th) and dx likewise.  The frame of ph[0] (pitch
+// X = Wr + st_tw - 1) holds grad_out[a + dy][b + dx] at frame row
+// a + dy - st_dy0, column b + dx - st_dx0: the frame convention of
+// dgrad_internal.h with Jh = st_th and qh = st_th - 1 + st_dy0, so the
+// general mode's raw-slice loads and gather serve it unchanged.  Tiles are
+// whole frame rows, 128 positions at most (MMA M = 128); the weights stay
+// resident.
+bool plan_stacked(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan) {
+    const int s = (int)p.stride;
+    const int64_t H = p.in_h, W = p.in_w, kH = p.kernel_h, kW = p.kernel_w;
+    const int64_t N = p.batch, Ci = p.in_channels, Co = p.out_channels;
+    if (s < 2 || s > 4 || (int64_t)s * s * Ci > 32) return false;
+    TcParams &t = plan->tc;
+    std::memset(&t, 0, sizeof(t));
+    PackParams &k = plan->pack;
+    std::memset(&k, 0, sizeof(k));
+    t.N = (int)N; t.Ci = (int)Ci; t.H = (int)H; t.W = (int)W; t.Co = (int)Co;
+    t.OH = (int)p.out_h; t.OW = (int)p.out_w; t.stride = s;
+    t.esize = esize;
+    int64_t dy0 = INT32_MAX, dy1 = INT32_MIN, dx0 = INT32_MAX, dx1 = INT32_MIN;
+    for (int rh = 0; rh < s; ++rh) {
+        for (int rw = 0; rw < s; ++rw) {
+            const int ph = rh * s + rw;
+            k.th[ph] = (int)((rh + p.padding_h) % s);
+            k.qh[ph] = (int)((rh + p.padding_h) / s);
+            k.tw[ph] = (int)((rw + p.padding_w) % s);
+            k.qw[ph] = (int)((rw + p.padding_w) / s);
+            k.Jh[ph] = k.th[ph] < kH ? (int)cdiv(kH - k.th[ph], s) : 0;
+            k.Jw[ph] = k.tw[ph] < kW ? (int)cdiv(kW - k.tw[ph], s) : 0;
+            if (k.Jh[ph] == 0 || k.Jw[ph] == 0 || rh >= H || rw >= W) continue;
+            dy0 = std::min<int64_t>(dy0, k.qh[ph] - k.Jh[ph] + 1);
+            dy1 = std::max<int64_t>(dy1, k.qh[ph]);
+            dx0 = std::min<int64_t>(dx0, k.qw[ph] - k.Jw[ph] + 1);
+            dx1 = std::max<int64_t>(dx1, k.qw[ph]);
+        }
+    }
+    if (dy0 > dy1 || dx0 > dx1) return false;  // no phase reads grad_out
+    const int64_t Th = dy1 - dy0 + 1, Tw = dx1 - dx0 + 1;
+    const int64_t Hr = cdiv(H, s), Wr = cdiv(W, s);
+    const int64_t X = Wr + Tw - 1, R = Hr + Th - 1;
+    if (X > 128 || N * R * X + 8192 > INT32_MAX) return false;
+    const int rows_per_tile = (int)std::min<int64_t>(128 / X, Hr);
+    PhaseDesc &d = t.ph[0];
+    d.Hr = (int)Hr; d.Wr = (int)Wr;
+    d.Jh = (int)Th; d.Jw = (int)Tw;
+    d.qh = (int)(Th - 1 + dy0); d.qw = (int)(Tw - 1 + dx0);
+    d.X = (int)X; d.R = (int)R;
+    d.p_tiles = (int)(N * cdiv(Hr, rows_per_tile));
+    d.hb = (int)(128 + (Th - 1) * X + (Tw - 1));
+    t.n_phases = 1;
+    t.m_tile = 128;
+    t.n_mtiles = 1;
+    t.tile_p = 128;
+    t.rows_per_tile = rows_per_tile;
+    t.kc = 128 / esize;
+    t.n_cchunks = (int)cdiv(Co, t.kc);
+    t.hbp = (int)round_up(d.hb, 8);
+    t.stacked = 1;
+    t.st_n = (int)round_up(std::max<int64_t>((int64_t)s * s * Ci, 16), 16);
+    t.st_th = (int)Th; t.st_tw = (int)Tw;
+    t.st_dy0 = (int)dy0; t.st_dx0 = (int)dx0;
+    const int64_t g_stage = (int64_t)t.hbp * 128, w_unit = (int64_t)t.st_n * 128;
+    const int64_t packed = (int64_t)t.n_cchunks * Th * Tw * w_unit;
+    t.g_stage_bytes = (int)g_stage;
+    t.w_unit_bytes = (int)w_unit;
+    t.packed_bytes = packed;
+    t.taps_per_w = (int)(Th * Tw);
+    t.w_stage_bytes = (int)(Th * Tw * w_unit);
+    t.nw = 0;
+    t.epi_stage_bytes = 0;
+    // Raw slices when a load mode applies; resident weights beside two or
+    // three G stages and two or three raw slots.
+    const int raw = plan_raw_slices(p, esize, t);
+    bool ok = false;
+    for (int nr = raw ? 3 : 0; nr >= (raw ? 2 : 0) && !ok; --nr) {
+        for (int ng = 3; ng >= 2 && !ok; --ng) {
+            const int64_t bytes = smem_layout_bytes(0, (int64_t)nr * t.raw_slice_bytes, packed + ng * g_stage);
+            if (bytes <= kSmemLimit) {
+                ok = true;
+                t.raw_nr = nr;
+                t.ng = ng;
+                t.smem_bytes = (int)bytes;
+            }
+        }
+    }
+    if (!ok && raw) {  // without raw slices: the gather reads grad_out directly
+        plan_raw_slices(p, esize, t, /*none=*/true);
+        for (int ng = 3; ng >= 2 && !ok; --ng) {
+            const int64_t bytes = smem_layout_bytes(0, 0, packed + ng * g_stage);
+            if (bytes <= kSmemLimit) {
+                ok = true;
+                t.ng = ng;
+                t.smem_bytes = (int)bytes;
+            }
+        }
+    }
+    if (!ok) return false;
+    t.raw_early = 0;
+    t.total_tiles = d.p_tiles;
+    const uint32_t fmt = dtype == DGRAD_F32 ? 2u : (dtype == DGRAD_BF16 ? 1u : 0u);
+    t.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(t.st_n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    uint32_t cols = 32;
+    while (cols < (uint32_t)(2 * t.st_n)) cols *= 2;
+    t.tmem_cols = cols;
+    k.Ci = (int)Ci; k.Co = (int)Co; k.kH = (int)kH; k.kW = (int)kW; k.stride = s;
+    k.m_tile = t.st_n; k.n_mtiles = 1; k.kc = t.kc; k.n_cchunks = t.n_cchunks;
+    k.elems16 = 16 / esize;
+    k.n_phases = s * s;
+    k.stacked = 1;
+    k.st_n = t.st_n; k.st_th = t.st_th; k.st_tw = t.st_tw; k.st_dy0 = t.st_dy0; k.st_dx0 = t.st_dx0;
+    k.total_elems = packed / esize;
+    plan->workspace = (size_t)packed;
+    return true;
+}
+
 }  // namespace
 
 int make_plan(const void *params_v, int dtype, int forced_kernel, Plan *plan) {
@@ -563,6 +682,11 @@ int make_plan(const void *params_v, int dtype, int forced_kernel, Plan *plan) {
 
     if (forced_kernel == DGRAD_KERNEL_SIMT) {
         plan->kernel = DGRAD_KERNEL_SIMT;
+        return DGRAD_OK;
+    }
+    if (plan_stacked(p, plan->esize, dtype, plan)) {
+        plan->kernel = DGRAD_KERNEL_TC;
+        plan->tc_alt = plan->tc;
         return DGRAD_OK;
     }
     if (plan_tc(p, plan->esize, dtype, plan)) {

@@ -9,7 +9,9 @@ them into the frame window; how a slice is loaded depends on the shape:
 * one 1-D bulk copy per channel (the g-row group is wider than a TMA box);
 * one 1-D bulk copy of whole channel planes (tiles that cover whole images);
 * 1x1 problems whose tiles are whole images: the grad_out operand is read
-  MN-major (channel rows of positions), regrouped in 16-byte pieces.
+  MN-major (channel rows of positions), regrouped in 16-byte pieces;
+* few input channels and stride > 1: positions on M, every phase's channels
+  stacked on N, window taps as shifted views of one frame.
 
 Each case below is chosen (and commented) for the mode it exercises, with
 several images whose last row tile runs past the image, channel counts that
@@ -49,6 +51,14 @@ CASES = [
      "MN-major grad_out operand from whole-plane copies (1x1); Co=300 leaves a 44-channel chunk"),
     ((2, 130, 16, 16, 520, 1, 1, 1, 0, 0), "f16",
      "MN-major operand from whole-plane tensor-map boxes; Ci=130: a 2-channel second tile"),
+    ((2, 3, 30, 26, 24, 7, 7, 2, 3, 3), "f32",
+     "stacked phases (Ci=3, s=2, 7x7: 4 x 4 window taps), 8 frame rows per tile, partial last tile"),
+    ((2, 2, 25, 23, 40, 5, 3, 3, 2, 1), "bf16",
+     "stacked phases, s=3: 9 phases x 2 channels on 32 columns; odd sizes; Co=40 ragged"),
+    ((3, 1, 17, 40, 70, 4, 4, 4, 1, 2), "f16",
+     "stacked phases, s=4: 16 phases x 1 channel; rows not a multiple of the stride; Co=70"),
+    ((2, 8, 16, 16, 48, 3, 3, 2, 1, 1), "f32",
+     "stacked phases, 4 phases x 8 channels = 32 columns, TF32"),
 ]
 
 
