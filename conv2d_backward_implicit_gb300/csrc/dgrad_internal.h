@@ -174,6 +174,13 @@ struct TcParams {
     // st_n rows, zero where a phase does not use the tap.
     int stacked;
     int st_n, st_th, st_tw, st_dy0, st_dx0;
+    // A CTA takes tiles in groups of tile_group consecutive tiles (groups
+    // dealt round-robin over the grid).  pair_rw (stride 2, four phases
+    // interleaved, one channel tile): tiles 2u and 2u + 1 are the column
+    // phases rw = 0 and 1 of the same output rows; they fill the two TMEM
+    // accumulators, and one epilogue interleaves them into whole grad_in rows.
+    int tile_group;
+    int pair_rw;
     PhaseDesc ph[kMaxPhases];
 };
 

@@ -42,7 +42,11 @@ __device__ unsigned int g_dgrad_error_word = 0;
 
 namespace {
 
-constexpr int kVarGeneral = 0, kVarFrame64 = 1, kVarPosM = 2;  // kernel variants
+// Kernel variants.  Pair and Stacked are the general mode with its paired
+// column-phase epilogue or its stacked-phase MMA and epilogue compiled in
+// (separate variants keep the general one's register allocation lean).
+constexpr int kVarGeneral = 0, kVarFrame64 = 1, kVarPosM = 2, kVarPair = 3, kVarStacked = 4;
+__host__ __device__ constexpr bool is_general(int v) { return v == kVarGeneral || v == kVarPair || v == kVarStacked; }
 
 struct Shared {
     uint64_t full_g[4], empty_g[4], full_w[kMaxW], empty_w[kMaxW], full_raw[kMaxRaw],
@@ -505,7 +509,7 @@ struct Tile {
 // V: the kernel variant; only the general mode has interleaved phases.
 template <int V = kVarGeneral>
 __device__ __forceinline__ Tile decode_tile(const TcParams &p, int64_t t) {
-    if (V == kVarGeneral && p.interleave) {  // (position tile, phase, channel tile), phases side by side
+    if (is_general(V) && p.interleave) {  // (position tile, phase, channel tile), phases side by side
         const int per = p.n_phases * p.n_mtiles;
         Tile r;
         r.pt = (int)(t / per);
@@ -543,6 +547,16 @@ __device__ __forceinline__ int tile_own(const TcParams &p, const PhaseDesc &d, i
     const int tpi = (d.Hr + p.rows_per_tile - 1) / p.rows_per_tile;
     const int left = d.Hr - (pt % tpi) * p.rows_per_tile;
     return (left < p.rows_per_tile ? left : p.rows_per_tile) * d.X;
+}
+
+// This CTA's tiles: groups of tile_group consecutive tiles, the groups dealt
+// round-robin over the grid (tile_group = 1: blockIdx.x, + gridDim.x, ...).
+__device__ __forceinline__ int64_t first_tile(const TcParams &p) {
+    return (int64_t)blockIdx.x * p.tile_group;
+}
+__device__ __forceinline__ int64_t next_tile(const TcParams &p, int64_t t) {
+    if (p.tile_group == 1) return t + gridDim.x;
+    return (t + 1) % p.tile_group ? t + 1 : t + 1 + (int64_t)(gridDim.x - 1) * p.tile_group;
 }
 
 // Byte offset, inside the packed weights, of (phase, ci tile, channel chunk).
@@ -682,7 +696,7 @@ __device__ void prefetch_raw_tile(const TcParams &p, int64_t t) {
     const int slices = p.kc / p.raw_cs;
     for (int cc = 0; cc < p.n_cchunks; ++cc)
         for (int sl = 0; sl < slices; ++sl) {
-            if constexpr (V != kVarGeneral)  // 64-wide frame / positions-on-M: plain tiled map
+            if constexpr (!is_general(V))  // 64-wide frame / positions-on-M: plain tiled map
                 tma_prefetch_4d(&p.in_map, p.raw_x0, u_first, cc * p.kc + sl * p.raw_cs, n);
             else
                 prefetch_raw_slice(p, u_first, cc * p.kc + sl * p.raw_cs, n);
@@ -695,7 +709,7 @@ __device__ void prefetch_raw_tile(const TcParams &p, int64_t t) {
 template <int V>
 __device__ __forceinline__ void issue_raw(const TcParams &p, uint32_t dst, int u_first, int c0,
                                           int n, uint32_t bar) {
-    if constexpr (V != kVarGeneral) {
+    if constexpr (!is_general(V)) {
         mbar_arrive_expect_tx(bar, (uint32_t)(p.raw_cs * p.raw_br * p.raw_bw * p.esize));
         tma_load_4d(dst, &p.in_map, p.raw_x0, u_first, c0, n, bar);
     } else {
@@ -728,7 +742,7 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
     // below is cold code, run while the previous kernel finishes) and waits
     // right before its first global-memory access.
     bool waited = false;
-    for (int64_t t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
+    for (int64_t t = first_tile(p); t < p.total_tiles && !aborted; t = next_tile(p, t)) {
         const Tile ti = decode_tile<V>(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
@@ -763,10 +777,13 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
                     // From the tile this slice belongs to: kRawLookahead tiles
                     // beyond it (general) or itself (positions-on-M).
                     prefetching = true;
-                    for (int k = 0; k <= (p.pos_m ? 0 : kRawLookahead); ++k)
-                        prefetch_raw_tile<V>(p, t + (int64_t)k * gridDim.x);
+                    int64_t ahead = t;
+                    for (int k = 0; k <= (p.pos_m ? 0 : kRawLookahead); ++k, ahead = next_tile(p, ahead))
+                        prefetch_raw_tile<V>(p, ahead);
                 } else if (!p.pos_m && prefetching && cc == 0 && sl == 0) {
-                    prefetch_raw_tile<V>(p, t + (int64_t)kRawLookahead * gridDim.x);
+                    int64_t ahead = t;
+                    for (int k = 0; k < kRawLookahead; ++k) ahead = next_tile(p, ahead);
+                    prefetch_raw_tile<V>(p, ahead);
                 }
                 if (!waited) {
                     grid_dependency_wait();
@@ -793,7 +810,7 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
         }
         // Positions-on-M mode (the ring holds a whole tile): all of this
         // tile's slices are queued, the next tile's go to L2.
-        if (p.pos_m && prefetching && !aborted) prefetch_raw_tile<V>(p, t + gridDim.x);
+        if (p.pos_m && prefetching && !aborted) prefetch_raw_tile<V>(p, next_tile(p, t));
     }
     if (!waited) grid_dependency_wait();
     if (!weights_issued) issue_weights(p, sh, w_base);  // fewer slices than free slots
@@ -809,7 +826,7 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
     }
 }
 
-// A walk over this CTA's tiles (blockIdx.x, + gridDim.x, ...) that skips
+// A walk over this CTA's tiles (first_tile, next_tile, ...) that skips
 // phases no tap reaches.  Each tile is decoded once, when the walk reaches it,
 // so the per-slice and per-stage work of the producer is a few additions.
 struct TileWalk {
@@ -819,7 +836,7 @@ struct TileWalk {
 };
 
 __device__ __forceinline__ bool walk_load(const TcParams &p, TileWalk &w) {
-    for (; w.t < p.total_tiles; w.t += gridDim.x) {
+    for (; w.t < p.total_tiles; w.t = next_tile(p, w.t)) {
         const Tile ti = decode_tile(p, w.t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
@@ -843,13 +860,13 @@ __device__ __noinline__ void raw_w_producer(const TcParams &p, Shared &sh, uint3
     const int slices = p.kc / p.raw_cs;
     const uint32_t w_unit = (uint32_t)p.w_unit_bytes;
     // raw cursor: tile, chunk rcc, slice rsl; ring slot / phase
-    TileWalk rw{(int64_t)blockIdx.x, nullptr, 0, 0, 0};
+    TileWalk rw{first_tile(p), nullptr, 0, 0, 0};
     bool r_live = walk_load(p, rw);
     int rcc = 0, rsl = 0, rslot = 0, rc0 = 0;  // rc0: first channel of the next slice
     uint32_t rph = 0;
     int64_t r_issued = 0;
     // weight cursor: tile, chunk wcc, first tap wt0; ring stage / phase
-    TileWalk ww{(int64_t)blockIdx.x, nullptr, 0, 0, 0};
+    TileWalk ww{first_tile(p), nullptr, 0, 0, 0};
     bool w_live = walk_load(p, ww);
     int wcc = 0, wt0 = 0, wstage = 0, wtaps = 0;
     const uint8_t *wblk = nullptr;  // packed weights of (tile, chunk wcc)
@@ -878,7 +895,7 @@ __device__ __noinline__ void raw_w_producer(const TcParams &p, Shared &sh, uint3
                 if (++rcc == p.n_cchunks) {
                     rcc = 0;
                     rc0 = 0;
-                    rw.t += gridDim.x;
+                    rw.t = next_tile(p, rw.t);
                     r_live = walk_load(p, rw);
                 }
             }
@@ -901,7 +918,7 @@ __device__ __noinline__ void raw_w_producer(const TcParams &p, Shared &sh, uint3
                 wblk += (size_t)wtaps * w_unit;  // chunks of a tile follow one another
                 if (++wcc == p.n_cchunks) {
                     wcc = 0;
-                    ww.t += gridDim.x;
+                    ww.t = next_tile(p, ww.t);
                     w_live = walk_load(p, ww);
                     if (w_live) {
                         wtaps = ww.d->Jh * ww.d->Jw;
@@ -950,7 +967,7 @@ template <int V>
 __device__ void role_weights(const TcParams &p, Shared &sh, uint32_t w_base, uint32_t raw_base,
                              uint32_t early_base) {
     const uint8_t *src = static_cast<const uint8_t *>(p.packed);
-    if constexpr (V != kVarGeneral) {  // resident weights, raw slices by TMA
+    if constexpr (!is_general(V)) {  // resident weights, raw slices by TMA
         raw_producer<V>(p, sh, raw_base, w_base, early_base);
         wait_drain(smem_u32(&sh.w_full), 0, p, sh);
         return;
@@ -972,7 +989,7 @@ __device__ void role_weights(const TcParams &p, Shared &sh, uint32_t w_base, uin
     uint32_t phase = 0;
     int64_t issued = 0;
     bool aborted = false;
-    for (int64_t t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
+    for (int64_t t = first_tile(p); t < p.total_tiles && !aborted; t = next_tile(p, t)) {
         const Tile ti = decode_tile(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
@@ -1018,7 +1035,7 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
     uint32_t gph = 0, wph = 0, accph = 0;
     bool aborted = false;
     if (p.nw == 0 && !wait_bar(smem_u32(&sh.w_full), 0, p, sh)) aborted = true;
-    for (int64_t t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
+    for (int64_t t = first_tile(p); t < p.total_tiles && !aborted; t = next_tile(p, t)) {
         const Tile ti = decode_tile<V>(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
@@ -1114,7 +1131,7 @@ __device__ void role_mma_stacked(const TcParams &p, Shared &sh, uint32_t g_base,
     bool aborted = !wait_bar(smem_u32(&sh.w_full), 0, p, sh);
     const int X = p.ph[0].X;
     const int taps = p.st_th * p.st_tw;
-    for (int64_t t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
+    for (int64_t t = first_tile(p); t < p.total_tiles && !aborted; t = next_tile(p, t)) {
         if (!wait_bar(smem_u32(&sh.acc_empty[acc]), accph ^ 1u, p, sh)) {
             aborted = true;
             break;
@@ -1233,7 +1250,7 @@ __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
     const uint32_t ch_bytes = row_bytes * (uint32_t)p.raw_br;
     const int h0 = gw * 32 + lane;
     const int nrows = h0 < p.hbp ? (p.hbp - 1 - h0) / kStep + 1 : 0;  // <= kMaxGatherRows (plan)
-    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    for (int64_t t = first_tile(p); t < p.total_tiles; t = next_tile(p, t)) {
         const Tile ti = decode_tile(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
@@ -1346,7 +1363,7 @@ __device__ void gather_mn(const TcParams &p, Shared &sh, uint32_t g_base, uint32
     const int i0 = gw * 32 + lane;
     const int c0 = i0 / pieces, v0 = i0 - c0 * pieces;
     const int dc = kStep / pieces, dv = kStep - dc * pieces;
-    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    for (int64_t t = first_tile(p); t < p.total_tiles; t = next_tile(p, t)) {
         for (int cc = 0; cc < p.n_cchunks; ++cc) {
             if (!wait_bar_warp(smem_u32(&sh.empty_g[stage]), phase ^ 1u, p, sh, lane)) return;
             if (!stage_writable(p, sh, stage, early_done, lane)) return;
@@ -1407,7 +1424,7 @@ __device__ void role_gather(const TcParams &p, Shared &sh, uint32_t g_base, int 
     int stage = 0;
     uint32_t phase = 0;
     bool withhold = (p.debug_flags & DGRAD_DEBUG_SKIP_ARRIVE) && gw == 0;
-    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    for (int64_t t = first_tile(p); t < p.total_tiles; t = next_tile(p, t)) {
         const Tile ti = decode_tile(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
@@ -1722,6 +1739,70 @@ __device__ void epilogue_stacked(const TcParams &p, const PhaseDesc &d, const Ti
     }
 }
 
+// Paired epilogue (stride 2; the column phases rw = 0 and 1 of the same
+// output rows in TMEM buffers t0 and t1): per output row of the tile and
+// 16-lane group, each lane interleaves its channel's columns of the two
+// phases, 16 at a time, into a whole grad_in row of an [8][W] box (lanes
+// 8h..8h+7 of the group fill box h), and one lane stores both boxes with TMA
+// tensor stores, as the stride-1 rows of epilogue_tma.
+__device__ void epilogue_pair_tma(const TcParams &p, const PhaseDesc &d0, const PhaseDesc &d1,
+                                  const Tile &ti, uint32_t t0, uint32_t t1, uint32_t box, int q,
+                                  int part, int lane) {
+    const int tpi = (d0.Hr + p.rows_per_tile - 1) / p.rows_per_tile;
+    const int n = ti.pt / tpi, a0 = (ti.pt - n * tpi) * p.rows_per_tile;
+    const int W = p.W, half = W / 2;
+    const uint32_t box_bytes = (uint32_t)(kTmaBoxCi * W * 4);
+    for (int gi = 0; gi < 2; ++gi) {
+        const int ci0 = ti.mt * p.m_tile + q * 32 + 16 * gi;
+        if (ci0 >= p.Ci) break;
+        const int lg = lane - 16 * gi;
+        const bool mine = lg >= 0 && lg < 16;
+        const uint32_t my_row = box + (uint32_t)((lg >> 3) & 1) * box_bytes + 4u * (uint32_t)(W * (lg & 7));
+        for (int r = part; r < p.rows_per_tile && a0 + r < d0.Hr; r += 2) {
+            const uint32_t a0c = t0 + (uint32_t)(r * d0.X), a1c = t1 + (uint32_t)(r * d1.X);
+            if (lane == 0) bulk_wait_read_all();  // the previous stores have read both boxes
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 32; c += 16) {
+                const int rem = half - c;  // a multiple of 4
+                if (rem <= 0) break;
+                uint32_t v[32];  // v[0..16): phase rw = 0, v[16..32): rw = 1
+                if (rem >= 16) {
+                    tmem_ld16(a0c + c, *reinterpret_cast<uint32_t(*)[16]>(v));
+                    tmem_ld16(a1c + c, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+                } else {
+                    if (rem >= 8) {
+                        tmem_ld8(a0c + c, v);
+                        tmem_ld8(a1c + c, v + 16);
+                    }
+                    if (rem == 12) {
+                        tmem_ld4(a0c + c + 8, v + 8);
+                        tmem_ld4(a1c + c + 8, v + 24);
+                    } else if (rem == 4) {
+                        tmem_ld4(a0c + c, v);
+                        tmem_ld4(a1c + c, v + 16);
+                    }
+                }
+                tmem_wait_ld32(v);
+                if (mine) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)  // grad_in columns 2c + 4e .. + 3
+                        if (4 * e < 2 * rem)
+                            st_shared_v4(my_row + 4u * (uint32_t)(2 * c + 4 * e), v[2 * e], v[16 + 2 * e],
+                                         v[2 * e + 1], v[16 + 2 * e + 1]);
+                }
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+                const int ih = 2 * (a0 + r) + d0.rh;
+                tma_store_4d(&p.out_map, box, 0, ih, ci0, n);
+                if (ci0 + 8 < p.Ci) tma_store_4d(&p.out_map, box + box_bytes, 0, ih, ci0 + 8, n);
+            }
+        }
+    }
+}
+
 template <int V>
 __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uint32_t tmem,
                               int warp, int lane) {
@@ -1732,10 +1813,10 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
     int bsel = 0;  // TMA store box in use (double-buffered epilogue)
     int acc = 0;
     uint32_t accph = 0;
-    for (int64_t t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    for (int64_t t = first_tile(p); t < p.total_tiles; t = next_tile(p, t)) {
         const Tile ti = decode_tile<V>(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
-        if (V == kVarGeneral && d.Jh == 0) {  // no tap reaches this phase: grad_in is zero there
+        if (is_general(V) && d.Jh == 0) {  // no tap reaches this phase: grad_in is zero there
             const int ci_base = ti.mt * p.m_tile + q * rows;
             int ci_here = p.Ci - ci_base;
             ci_here = ci_here < 0 ? 0 : (ci_here > rows ? rows : ci_here);
@@ -1752,7 +1833,33 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
         if (!wait_bar_warp(smem_u32(&sh.acc_full[acc]), accph, p, sh, lane)) break;
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.tile_p);
-        if (V == kVarGeneral && p.stacked)
+        if constexpr (V == kVarPair) {
+            // Tiles come in pairs (rw = 0 in buffer 0, rw = 1 in buffer 1):
+            // the first waits for the second, then both are stored together.
+            if ((t & 1) == 0) {
+                acc = 1;
+                continue;
+            }
+            const Tile t0 = decode_tile(p, t - 1);
+            const PhaseDesc &d0 = p.ph[t0.phase];
+            const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+            if (p.epi_tma) {
+                epilogue_pair_tma(p, d0, d, ti, tq, tq + (uint32_t)p.tile_p, st_base, q, part, lane);
+            } else {
+                epilogue_staged<32>(p, d0, t0, tq, st_base, q, part, lane);
+                epilogue_staged<32>(p, d, ti, tq + (uint32_t)p.tile_p, st_base, q, part, lane);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(smem_u32(&sh.acc_empty[0]));
+                mbar_arrive(smem_u32(&sh.acc_empty[1]));
+            }
+            acc = 0;
+            accph ^= 1u;
+            continue;
+        }
+        if constexpr (V == kVarStacked)
             epilogue_stacked(p, d, ti, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.st_n), q, part,
                              lane);
         else if (V == kVarFrame64 || p.epi_tma)  // the 64-wide frame always stores through TMA
@@ -2124,7 +2231,7 @@ __global__ void __launch_bounds__(Roles<V>::threads, 1)
                 role_mma_pm(p, sh, g_base, w_base, tmem);
             else
             {
-                if (V == kVarGeneral && p.stacked)
+                if constexpr (V == kVarStacked)
                     role_mma_stacked<ESIZE == 4>(p, sh, g_base, w_base, tmem);
                 else
                     role_mma<ESIZE == 4, V>(p, sh, g_base, w_base, tmem);
@@ -2256,7 +2363,7 @@ bool encode_out_map(TcParams &p) {
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         return r == CUDA_SUCCESS;
     }
-    if (p.rows_per_tile <= 0 || p.stride != 1 || p.W % 4 != 0 || p.W > 64) return false;
+    if (p.rows_per_tile <= 0 || (p.stride != 1 && !p.pair_rw) || p.W % 4 != 0 || p.W > 64) return false;
     if ((reinterpret_cast<uintptr_t>(p.grad_in) & 15u) != 0) return false;
     if (p.epi_stage_bytes < kEpiWarps * p.epi_boxes * p.epi_box_ci * p.W * 4) return false;
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
@@ -2306,14 +2413,20 @@ int launch_tc(const Plan &plan, const void *grad_out, const void *packed, float 
     // At least half the shared memory of an SM, so a second CTA can never be
     // co-resident and contend for tensor memory.
     if (p.smem_bytes < kSmemLimit / 2 + 1024) p.smem_bytes = kSmemLimit / 2 + 1024;
-    const int grid = (int)(p.total_tiles < sms ? p.total_tiles : sms);
+    if (p.tile_group < 1) p.tile_group = 1;
+    const int64_t groups = (p.total_tiles + p.tile_group - 1) / p.tile_group;
+    const int grid = (int)(groups < sms ? groups : sms);
     if (grid <= 0) return (int)cudaSuccess;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (plan.esize == 2) {
         if (p.pos_m) return launch_variant<2, kVarPosM>(p, grid, st, dev);
         if (p.frame64) return launch_variant<2, kVarFrame64>(p, grid, st, dev);
+        if (p.stacked) return launch_variant<2, kVarStacked>(p, grid, st, dev);
+        if (p.pair_rw) return launch_variant<2, kVarPair>(p, grid, st, dev);
         return launch_variant<2, kVarGeneral>(p, grid, st, dev);
     }
+    if (p.stacked) return launch_variant<4, kVarStacked>(p, grid, st, dev);
+    if (p.pair_rw) return launch_variant<4, kVarPair>(p, grid, st, dev);
     return launch_variant<4, kVarGeneral>(p, grid, st, dev);
 }
 

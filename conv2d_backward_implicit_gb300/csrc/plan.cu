@@ -301,6 +301,7 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
                       ? (int)std::min<int64_t>(kMaxEarly, t.g_stage_bytes / t.raw_slice_bytes)
                       : 0;
 
+    t.tile_group = 1;
     int64_t tiles = 0;
     t.interleave = np > 1 ? 1 : 0;
     for (int i = 0; i < np; ++i) {
@@ -628,6 +629,7 @@ bool plan_stacked(const conv2d_grad_input_params &p, int esize, int dtype, Plan 
     if (!ok) return false;
     t.raw_early = 0;
     t.total_tiles = d.p_tiles;
+    t.tile_group = 1;
     const uint32_t fmt = dtype == DGRAD_F32 ? 2u : (dtype == DGRAD_BF16 ? 1u : 0u);
     t.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(t.st_n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
     uint32_t cols = 32;
@@ -641,6 +643,27 @@ bool plan_stacked(const conv2d_grad_input_params &p, int esize, int dtype, Plan 
     k.st_n = t.st_n; k.st_th = t.st_th; k.st_tw = t.st_tw; k.st_dy0 = t.st_dy0; k.st_dx0 = t.st_dx0;
     k.total_elems = packed / esize;
     plan->workspace = (size_t)packed;
+    return true;
+}
+
+// Paired column phases (see TcParams::pair_rw): stride 2 with all four phases
+// present and reached by taps, equal tile counts (interleaved order), one
+// 128-row channel tile, and grad_in rows of W = a multiple of 8 up to 64
+// floats, so that a row is two phases' W/2 columns and one [8][W] TMA box.
+bool plan_pair(const TcParams &g, TcParams *out) {
+    if (g.stride != 2 || g.n_phases != 4 || !g.interleave || g.n_mtiles != 1 || g.m_tile != 128) return false;
+    if (g.rows_per_tile <= 0 || g.W % 8 != 0 || g.W > 64 || g.mn_b || g.stacked || g.frame64 || g.pos_m)
+        return false;
+    for (int i = 0; i < 4; ++i)
+        if (g.ph[i].Jh == 0 || g.ph[i].Jw == 0 || g.ph[i].rh != i / 2 || g.ph[i].rw != i % 2 ||
+            g.ph[i].Wr * 2 != g.W)
+            return false;
+    // Two [8][W] float boxes per epilogue warp (one per 8-channel half).
+    if (g.epi_stage_bytes < kEpiWarps * 2 * kTmaBoxCi * g.W * 4 || 2 * g.tile_p > 512) return false;
+    TcParams t = g;
+    t.pair_rw = 1;
+    t.tile_group = 2;
+    *out = t;
     return true;
 }
 
@@ -699,6 +722,8 @@ int make_plan(const void *params_v, int dtype, int forced_kernel, Plan *plan) {
             plan->tc = v;
         else if (plan_mn(p, plan->esize, plan->tc_alt, &v))
             plan->tc = v;
+        else if (plan_pair(plan->tc_alt, &v))
+            plan->tc = plan->tc_alt = v;  // pairing needs no TMA (staged epilogue without it)
         return DGRAD_OK;
     }
     if (forced_kernel == DGRAD_KERNEL_TC || forced_kernel == DGRAD_KERNEL_TC_POSM)

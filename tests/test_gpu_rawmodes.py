@@ -11,7 +11,9 @@ them into the frame window; how a slice is loaded depends on the shape:
 * 1x1 problems whose tiles are whole images: the grad_out operand is read
   MN-major (channel rows of positions), regrouped in 16-byte pieces;
 * few input channels and stride > 1: positions on M, every phase's channels
-  stacked on N, window taps as shifted views of one frame.
+  stacked on N, window taps as shifted views of one frame;
+* stride 2 with one 128-row channel tile: the two column phases of the same
+  rows are taken as a pair and stored as whole grad_in rows.
 
 Each case below is chosen (and commented) for the mode it exercises, with
 several images whose last row tile runs past the image, channel counts that
@@ -59,6 +61,12 @@ CASES = [
      "stacked phases, s=4: 16 phases x 1 channel; rows not a multiple of the stride; Co=70"),
     ((2, 8, 16, 16, 48, 3, 3, 2, 1, 1), "f32",
      "stacked phases, 4 phases x 8 channels = 32 columns, TF32"),
+    ((2, 128, 24, 32, 72, 3, 3, 2, 1, 1), "bf16",
+     "paired column phases (s=2, 128 channels): rows of W=32 from two 16-column phases"),
+    ((3, 128, 20, 48, 70, 3, 3, 2, 1, 1), "f32",
+     "paired column phases, TF32, W=48, Co=70 ragged"),
+    ((2, 100, 16, 24, 64, 5, 5, 2, 2, 2), "bf16",
+     "paired column phases of a 5x5 kernel (3x3, 3x2, 2x3, 2x2 taps); Ci=100 of a 128-row tile"),
 ]
 
 
