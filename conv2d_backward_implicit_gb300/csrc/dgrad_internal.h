@@ -177,10 +177,12 @@ struct TcParams {
     // A CTA takes tiles in groups of tile_group consecutive tiles (groups
     // dealt round-robin over the grid).  pair_rw (stride 2, four phases
     // interleaved, one channel tile): tiles 2u and 2u + 1 are the column
-    // phases rw = 0 and 1 of the same output rows; they fill the two TMEM
-    // accumulators, and one epilogue interleaves them into whole grad_in rows.
+    // phases rw = 0 and 1 of the same output rows, gathered once (one frame
+    // pitch for all phases) into a pair of TMEM accumulators, and one epilogue
+    // interleaves them into whole grad_in rows.
     int tile_group;
     int pair_rw;
+    int acc_single;         // 1: one TMEM accumulator buffer (the epilogue does not overlap the MMA)
     PhaseDesc ph[kMaxPhases];
 };
 

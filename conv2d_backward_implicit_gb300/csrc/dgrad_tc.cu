@@ -687,7 +687,7 @@ __device__ void issue_weights(const TcParams &p, Shared &sh, uint32_t w_base) {
 constexpr int kRawLookahead = 2;  // general mode: tiles of this CTA prefetched ahead
 template <int V>
 __device__ void prefetch_raw_tile(const TcParams &p, int64_t t) {
-    if (t >= p.total_tiles) return;
+    if (t >= p.total_tiles || (p.pair_rw && (t & 1))) return;
     const Tile ti = decode_tile<V>(p, t);
     const PhaseDesc &d = p.ph[ti.phase];
     if (d.Jh == 0 || ti.mt != 0) return;  // channel tiles share the window
@@ -743,6 +743,7 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
     // right before its first global-memory access.
     bool waited = false;
     for (int64_t t = first_tile(p); t < p.total_tiles && !aborted; t = next_tile(p, t)) {
+        if (p.pair_rw && (t & 1)) continue;  // a pair shares its first tile's window
         const Tile ti = decode_tile<V>(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
@@ -837,6 +838,7 @@ struct TileWalk {
 
 __device__ __forceinline__ bool walk_load(const TcParams &p, TileWalk &w) {
     for (; w.t < p.total_tiles; w.t = next_tile(p, w.t)) {
+        if (p.pair_rw && (w.t & 1)) continue;  // a pair is walked at its first tile
         const Tile ti = decode_tile(p, w.t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
@@ -865,11 +867,13 @@ __device__ __noinline__ void raw_w_producer(const TcParams &p, Shared &sh, uint3
     int rcc = 0, rsl = 0, rslot = 0, rc0 = 0;  // rc0: first channel of the next slice
     uint32_t rph = 0;
     int64_t r_issued = 0;
-    // weight cursor: tile, chunk wcc, first tap wt0; ring stage / phase
+    // weight cursor: tile (a pair: member wk of it), chunk wcc, first tap wt0;
+    // ring stage / phase.  A pair's weights go chunk by chunk, both members'
+    // taps of a chunk together, the order the MMA consumes them in.
     TileWalk ww{first_tile(p), nullptr, 0, 0, 0};
     bool w_live = walk_load(p, ww);
-    int wcc = 0, wt0 = 0, wstage = 0, wtaps = 0;
-    const uint8_t *wblk = nullptr;  // packed weights of (tile, chunk wcc)
+    int wcc = 0, wk = 0, wt0 = 0, wstage = 0, wtaps = 0;
+    const uint8_t *wblk = nullptr;  // packed weights of (tile, member, chunk wcc)
     if (w_live) {
         wtaps = ww.d->Jh * ww.d->Jw;
         wblk = wsrc + w_block_off(p, *ww.d, ww.mt, 0);
@@ -915,15 +919,20 @@ __device__ __noinline__ void raw_w_producer(const TcParams &p, Shared &sh, uint3
             wt0 += p.taps_per_w;
             if (wt0 >= wtaps) {
                 wt0 = 0;
-                wblk += (size_t)wtaps * w_unit;  // chunks of a tile follow one another
-                if (++wcc == p.n_cchunks) {
-                    wcc = 0;
-                    ww.t = next_tile(p, ww.t);
-                    w_live = walk_load(p, ww);
-                    if (w_live) {
-                        wtaps = ww.d->Jh * ww.d->Jw;
-                        wblk = wsrc + w_block_off(p, *ww.d, ww.mt, 0);
+                if (p.pair_rw && wk == 0) {
+                    wk = 1;  // the pair's other column phase, same chunk
+                } else {
+                    wk = 0;
+                    if (++wcc == p.n_cchunks) {
+                        wcc = 0;
+                        ww.t = next_tile(p, ww.t);
+                        w_live = walk_load(p, ww);
                     }
+                }
+                if (w_live) {
+                    const PhaseDesc &dk = ww.d[wk];  // a pair's phases are adjacent in ph[]
+                    wtaps = dk.Jh * dk.Jw;
+                    wblk = wsrc + w_block_off(p, dk, ww.mt, wcc);
                 }
             }
             progress = true;
@@ -989,12 +998,15 @@ __device__ void role_weights(const TcParams &p, Shared &sh, uint32_t w_base, uin
     uint32_t phase = 0;
     int64_t issued = 0;
     bool aborted = false;
+    const int members = p.pair_rw ? 2 : 1;  // a pair: both column phases per chunk
     for (int64_t t = first_tile(p); t < p.total_tiles && !aborted; t = next_tile(p, t)) {
+        if (p.pair_rw && (t & 1)) continue;
         const Tile ti = decode_tile(p, t);
-        const PhaseDesc &d = p.ph[ti.phase];
-        if (d.Jh == 0) continue;
-        const int taps = d.Jh * d.Jw;
-        for (int cc = 0; cc < p.n_cchunks && !aborted; ++cc) {
+        if (p.ph[ti.phase].Jh == 0) continue;
+        for (int cc = 0; cc < p.n_cchunks && !aborted; ++cc)
+        for (int k = 0; k < members && !aborted; ++k) {
+            const PhaseDesc &d = p.ph[ti.phase + k];
+            const int taps = d.Jh * d.Jw;
             const uint8_t *blk = src + w_block_off(p, d, ti.mt, cc);
             for (int t0 = 0; t0 < taps; t0 += p.taps_per_w) {
                 if (!wait_bar(smem_u32(&sh.empty_w[stage]), phase ^ 1u, p, sh)) {
@@ -1031,11 +1043,15 @@ __device__ void role_weights(const TcParams &p, Shared &sh, uint32_t w_base, uin
 template <bool TF32, int V>
 __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_t w_base,
                          uint32_t tmem) {
+    // Paired column phases: both members of a pair (adjacent phases) consume
+    // each G stage, into the pair's two accumulators of the TMEM buffer.
+    constexpr int kMembers = V == kVarPair ? 2 : 1;
     int gs = 0, ws = 0, acc = 0;
     uint32_t gph = 0, wph = 0, accph = 0;
     bool aborted = false;
     if (p.nw == 0 && !wait_bar(smem_u32(&sh.w_full), 0, p, sh)) aborted = true;
     for (int64_t t = first_tile(p); t < p.total_tiles && !aborted; t = next_tile(p, t)) {
+        if (V == kVarPair && (t & 1)) continue;
         const Tile ti = decode_tile<V>(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
@@ -1044,9 +1060,9 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
             break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(acc * p.tile_p);
-        const int taps = d.Jh * d.Jw;
-        uint32_t accumulate = 0;
+        uint32_t accum[kMembers];
+#pragma unroll
+        for (int k = 0; k < kMembers; ++k) accum[k] = 0;
         for (int cc = 0; cc < p.n_cchunks; ++cc) {
             if (!wait_bar(smem_u32(&sh.full_g[gs]), gph, p, sh)) {
                 aborted = true;
@@ -1054,7 +1070,13 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
             }
             tc_fence_after();
             const uint32_t g_stage = g_base + (uint32_t)gs * p.g_stage_bytes;
-            const uint32_t w_res = w_base + (uint32_t)w_block_off(p, d, ti.mt, cc);
+#pragma unroll
+            for (int mb = 0; mb < kMembers; ++mb) {
+            const PhaseDesc &dk = p.ph[ti.phase + mb];
+            const uint32_t d_tmem = tmem + (uint32_t)((acc * kMembers + mb) * p.tile_p);
+            const int taps = dk.Jh * dk.Jw;
+            uint32_t accumulate = accum[mb];
+            const uint32_t w_res = w_base + (uint32_t)w_block_off(p, dk, ti.mt, cc);
             for (int t0 = 0; t0 < taps && !aborted; t0 += p.taps_per_w) {
                 const int t1 = taps - t0 < p.taps_per_w ? taps : t0 + p.taps_per_w;
                 uint32_t w_grp;
@@ -1078,16 +1100,16 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
                                             : sw128_desc(g_stage + (uint32_t)(p.view0 * 128));
                 const uint32_t b_kstep = p.mn_b ? (2u * mn_sbo) >> 4 : 2u;
                 const uint32_t w_step = (uint32_t)(p.w_unit_bytes >> 4);
-                int j = t0 / d.Jw, i = t0 - j * d.Jw;
+                int j = t0 / dk.Jw, i = t0 - j * dk.Jw;
                 for (int tap = t0; tap < t1; ++tap) {
-                    const uint64_t bd = gd0 + (uint64_t)(((d.Jh - 1 - j) * d.X + (d.Jw - 1 - i)) * 8);
+                    const uint64_t bd = gd0 + (uint64_t)(((dk.Jh - 1 - j) * dk.X + (dk.Jw - 1 - i)) * 8);
                     const uint64_t ad = wd0 + (uint64_t)((tap - t0) * w_step);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {  // four 32-byte K steps per 128-byte row
                         tc_mma<TF32>(d_tmem, ad + 2u * k, bd + (uint64_t)(b_kstep * k), p.idesc, accumulate);
                         accumulate = 1;
                     }
-                    if (++i == d.Jw) {
+                    if (++i == dk.Jw) {
                         i = 0;
                         ++j;
                     }
@@ -1100,6 +1122,8 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
                     }
                 }
             }
+            accum[mb] = accumulate;
+            }
             if (aborted) break;
             tc_commit(smem_u32(&sh.empty_g[gs]));
             if (++gs == p.ng) {
@@ -1109,7 +1133,7 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
         }
         if (aborted) break;
         tc_commit(smem_u32(&sh.acc_full[acc]));
-        if (++acc == 2) {
+        if (++acc == (p.acc_single ? 1 : 2)) {
             acc = 0;
             accph ^= 1u;
         }
@@ -1251,6 +1275,7 @@ __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
     const int h0 = gw * 32 + lane;
     const int nrows = h0 < p.hbp ? (p.hbp - 1 - h0) / kStep + 1 : 0;  // <= kMaxGatherRows (plan)
     for (int64_t t = first_tile(p); t < p.total_tiles; t = next_tile(p, t)) {
+        if (p.pair_rw && (t & 1)) continue;  // a pair shares its first tile's window
         const Tile ti = decode_tile(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
@@ -1425,6 +1450,7 @@ __device__ void role_gather(const TcParams &p, Shared &sh, uint32_t g_base, int 
     uint32_t phase = 0;
     bool withhold = (p.debug_flags & DGRAD_DEBUG_SKIP_ARRIVE) && gw == 0;
     for (int64_t t = first_tile(p); t < p.total_tiles; t = next_tile(p, t)) {
+        if (p.pair_rw && (t & 1)) continue;  // a pair shares its first tile's window
         const Tile ti = decode_tile(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
@@ -1814,6 +1840,7 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
     int acc = 0;
     uint32_t accph = 0;
     for (int64_t t = first_tile(p); t < p.total_tiles; t = next_tile(p, t)) {
+        if (V == kVarPair && (t & 1)) continue;  // a pair is stored at its first tile
         const Tile ti = decode_tile<V>(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (is_general(V) && d.Jh == 0) {  // no tap reaches this phase: grad_in is zero there
@@ -1834,31 +1861,19 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.tile_p);
         if constexpr (V == kVarPair) {
-            // Tiles come in pairs (rw = 0 in buffer 0, rw = 1 in buffer 1):
-            // the first waits for the second, then both are stored together.
-            if ((t & 1) == 0) {
-                acc = 1;
-                continue;
-            }
-            const Tile t0 = decode_tile(p, t - 1);
-            const PhaseDesc &d0 = p.ph[t0.phase];
-            const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+            // The pair's column phases rw = 0, 1 sit in accumulators 2 acc
+            // and 2 acc + 1 of the pair buffer; both are stored together.
+            const PhaseDesc &d1 = p.ph[ti.phase + 1];
+            const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(2 * acc * p.tile_p);
             if (p.epi_tma) {
-                epilogue_pair_tma(p, d0, d, ti, tq, tq + (uint32_t)p.tile_p, st_base, q, part, lane);
+                epilogue_pair_tma(p, d, d1, ti, tq, tq + (uint32_t)p.tile_p, st_base, q, part, lane);
             } else {
-                epilogue_staged<32>(p, d0, t0, tq, st_base, q, part, lane);
-                epilogue_staged<32>(p, d, ti, tq + (uint32_t)p.tile_p, st_base, q, part, lane);
+                Tile t1 = ti;
+                t1.phase = ti.phase + 1;
+                epilogue_staged<32>(p, d, ti, tq, st_base, q, part, lane);
+                epilogue_staged<32>(p, d1, t1, tq + (uint32_t)p.tile_p, st_base, q, part, lane);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(smem_u32(&sh.acc_empty[0]));
-                mbar_arrive(smem_u32(&sh.acc_empty[1]));
-            }
-            acc = 0;
-            accph ^= 1u;
-            continue;
-        }
+        } else
         if constexpr (V == kVarStacked)
             epilogue_stacked(p, d, ti, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.st_n), q, part,
                              lane);
@@ -1871,7 +1886,7 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.acc_empty[acc]));
-        if (++acc == 2) {
+        if (++acc == (p.acc_single ? 1 : 2)) {
             acc = 0;
             accph ^= 1u;
         }

@@ -100,7 +100,12 @@ int plan_raw_slices(const conv2d_grad_input_params &p, int esize, TcParams &t, b
 
 // Try to build a tensor-core plan.  Returns false when the shape is outside
 // what the tcgen05 kernel supports; the caller then uses the CUDA-core kernel.
-bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan) {
+// pair: plan paired column phases (TcParams::pair_rw) or fail: stride 2,
+// four phases with taps, one 128-row channel tile, W a multiple of 8 up to 64,
+// the two column phases of each row phase reading the same frame (equal
+// Jw - qw), tiles of at most 128 positions.  The four phases then share one
+// frame pitch X (the larger one), so a pair's window is gathered once.
+bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan, bool pair = false) {
     TcParams &t = plan->tc;
     std::memset(&t, 0, sizeof(t));
     const int s = (int)p.stride;
@@ -184,6 +189,24 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
         }
         t.n_phases = np;
         if (np == 0) return false;
+        if (pair) {
+            if (s != 2 || np != 4 || rows_per_tile <= 0 || Ci > 128 || W % 8 != 0 || W > 64) return false;
+            for (int i = 0; i < 4; ++i) {
+                const PhaseDesc &d = t.ph[i];
+                const PhaseDesc &o = t.ph[i ^ 1];  // the other column phase of the row phase
+                if (d.Jh == 0 || d.Jw == 0 || d.rh != i / 2 || d.rw != i % 2 || 2 * d.Wr != W ||
+                    d.Jw - d.qw != o.Jw - o.qw)
+                    return false;
+            }
+            max_hb = 0;
+            for (int i = 0; i < 4; ++i) {
+                PhaseDesc &d = t.ph[i];
+                d.X = (int)X1;
+                d.hb = tile_p + (d.Jh - 1) * d.X + (d.Jw - 1);
+                if ((int64_t)N * d.R * d.X + 8192 > INT32_MAX) return false;
+                max_hb = std::max(max_hb, d.hb);
+            }
+        }
         t.tile_p = tile_p;
 
         // Shared memory: barriers, 1 KB to align the rings to 1024 B, then the
@@ -317,8 +340,21 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
     t.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(t.tile_p >> 3) << 17) |
               ((uint32_t)(t.m_tile >> 4) << 24);
     uint32_t cols = 32;  // double-buffered accumulator, allocated in a power of two
-    while (cols < (uint32_t)(2 * t.tile_p)) cols *= 2;
+    while (cols < (uint32_t)((pair ? 4 : 2) * t.tile_p)) cols *= 2;
+    if (pair && cols > 512) {
+        // A pair of accumulators of the tile's columns: double-buffered when
+        // two pairs fit in TMEM's 512 columns, else one buffer.
+        t.acc_single = 1;
+        for (cols = 32; cols < (uint32_t)(2 * t.tile_p);) cols *= 2;
+    }
     t.tmem_cols = cols;
+    if (pair) {
+        if (cols > 512 || !t.interleave || t.n_mtiles != 1 || t.m_tile != 128 ||
+            t.epi_stage_bytes < kEpiWarps * 2 * kTmaBoxCi * (int)W * 4)
+            return false;
+        t.pair_rw = 1;
+        t.tile_group = 2;
+    }
 
     // Pack parameters mirror the layout above.
     PackParams &k = plan->pack;
@@ -646,27 +682,6 @@ bool plan_stacked(const conv2d_grad_input_params &p, int esize, int dtype, Plan 
     return true;
 }
 
-// Paired column phases (see TcParams::pair_rw): stride 2 with all four phases
-// present and reached by taps, equal tile counts (interleaved order), one
-// 128-row channel tile, and grad_in rows of W = a multiple of 8 up to 64
-// floats, so that a row is two phases' W/2 columns and one [8][W] TMA box.
-bool plan_pair(const TcParams &g, TcParams *out) {
-    if (g.stride != 2 || g.n_phases != 4 || !g.interleave || g.n_mtiles != 1 || g.m_tile != 128) return false;
-    if (g.rows_per_tile <= 0 || g.W % 8 != 0 || g.W > 64 || g.mn_b || g.stacked || g.frame64 || g.pos_m)
-        return false;
-    for (int i = 0; i < 4; ++i)
-        if (g.ph[i].Jh == 0 || g.ph[i].Jw == 0 || g.ph[i].rh != i / 2 || g.ph[i].rw != i % 2 ||
-            g.ph[i].Wr * 2 != g.W)
-            return false;
-    // Two [8][W] float boxes per epilogue warp (one per 8-channel half).
-    if (g.epi_stage_bytes < kEpiWarps * 2 * kTmaBoxCi * g.W * 4 || 2 * g.tile_p > 512) return false;
-    TcParams t = g;
-    t.pair_rw = 1;
-    t.tile_group = 2;
-    *out = t;
-    return true;
-}
-
 }  // namespace
 
 int make_plan(const void *params_v, int dtype, int forced_kernel, Plan *plan) {
@@ -712,6 +727,11 @@ int make_plan(const void *params_v, int dtype, int forced_kernel, Plan *plan) {
         plan->tc_alt = plan->tc;
         return DGRAD_OK;
     }
+    if (plan_tc(p, plan->esize, dtype, plan, /*pair=*/true)) {
+        plan->kernel = DGRAD_KERNEL_TC;
+        plan->tc_alt = plan->tc;  // pairing needs no TMA (staged epilogue without it)
+        return DGRAD_OK;
+    }
     if (plan_tc(p, plan->esize, dtype, plan)) {
         plan->kernel = DGRAD_KERNEL_TC;
         plan->tc_alt = plan->tc;
@@ -722,8 +742,6 @@ int make_plan(const void *params_v, int dtype, int forced_kernel, Plan *plan) {
             plan->tc = v;
         else if (plan_mn(p, plan->esize, plan->tc_alt, &v))
             plan->tc = v;
-        else if (plan_pair(plan->tc_alt, &v))
-            plan->tc = plan->tc_alt = v;  // pairing needs no TMA (staged epilogue without it)
         return DGRAD_OK;
     }
     if (forced_kernel == DGRAD_KERNEL_TC || forced_kernel == DGRAD_KERNEL_TC_POSM)

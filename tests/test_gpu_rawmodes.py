@@ -13,7 +13,8 @@ them into the frame window; how a slice is loaded depends on the shape:
 * few input channels and stride > 1: positions on M, every phase's channels
   stacked on N, window taps as shifted views of one frame;
 * stride 2 with one 128-row channel tile: the two column phases of the same
-  rows are taken as a pair and stored as whole grad_in rows.
+  rows are taken as a pair -- one shared window, two accumulators -- and
+  stored as whole grad_in rows.
 
 Each case below is chosen (and commented) for the mode it exercises, with
 several images whose last row tile runs past the image, channel counts that
@@ -65,8 +66,10 @@ CASES = [
      "paired column phases (s=2, 128 channels): rows of W=32 from two 16-column phases"),
     ((3, 128, 20, 48, 70, 3, 3, 2, 1, 1), "f32",
      "paired column phases, TF32, W=48, Co=70 ragged"),
+    ((2, 100, 16, 40, 64, 3, 3, 2, 1, 1), "bf16",
+     "paired column phases, Ci=100 of a 128-row tile, W=40"),
     ((2, 100, 16, 24, 64, 5, 5, 2, 2, 2), "bf16",
-     "paired column phases of a 5x5 kernel (3x3, 3x2, 2x3, 2x2 taps); Ci=100 of a 128-row tile"),
+     "5x5 at stride 2: the column phases read different frames, so tiles stay unpaired"),
 ]
 
 
