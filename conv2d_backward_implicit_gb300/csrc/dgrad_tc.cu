@@ -48,6 +48,28 @@ namespace {
 constexpr int kVarGeneral = 0, kVarFrame64 = 1, kVarPosM = 2, kVarPair = 3, kVarStacked = 4;
 __host__ __device__ constexpr bool is_general(int v) { return v == kVarGeneral || v == kVarPair || v == kVarStacked; }
 
+// Warp roles of each variant: epilogue warps first, then the MMA warp, the
+// producer warp and the gather warps.
+template <int V>
+struct Roles {
+    static constexpr int epi_warps = kEpiWarps, mma_warp = kMmaWarp, w_warp = kWWarp;
+    static constexpr int g_warp0 = kGWarp0, g_warps = kGWarps, threads = kThreads;
+};
+// Stacked-phase mode: a short epilogue (one TMEM read and s^2 Ci stores per
+// position) and a long gather, so four epilogue warps (one per TMEM lane
+// quadrant) and ten gather warps.
+template <>
+struct Roles<kVarStacked> {
+    static constexpr int epi_warps = 4, mma_warp = 4, w_warp = 5;
+    static constexpr int g_warp0 = 6, g_warps = 10, threads = 512;
+};
+template <>
+struct Roles<kVarPosM> {
+    static constexpr int epi_warps = kPmEpiWarps, mma_warp = kPmMmaWarp, w_warp = kPmWWarp;
+    static constexpr int g_warp0 = kPmGWarp0, g_warps = kPmGWarps, threads = kPmThreads;
+};
+
+
 struct Shared {
     uint64_t full_g[4], empty_g[4], full_w[kMaxW], empty_w[kMaxW], full_raw[kMaxRaw],
         empty_raw[kMaxRaw];
@@ -1256,13 +1278,13 @@ __device__ __forceinline__ bool stage_writable(const TcParams &p, Shared &sh, in
 // shared memory: frame element h, channel c comes from slice row h / X,
 // column (h mod X) + vmin - raw_x0.  Each slice fills raw_cs / E 16-byte
 // chunks of every 128-byte window row.  A thread owns the window rows
-// h = 32 gw + lane + 32 kGWarps k; their places in a slice are worked out
-// once per tile.
-template <int ESIZE>
+// h = 32 gw + lane + 32 GW k (GW gather warps); their places in a slice are
+// worked out once per tile.
+template <int ESIZE, int GW>
 __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
                                 uint32_t raw_base, uint32_t early_base, int gw, int lane) {
     constexpr int E = 16 / ESIZE;  // channels per 16-byte chunk
-    constexpr int kStep = kGWarps * 32;
+    constexpr int kStep = GW * 32;
     const int slices = p.kc / p.raw_cs;
     const int groups = p.raw_cs / E;  // 16-byte chunks per slice and window row
     int stage = 0;
@@ -1443,7 +1465,7 @@ __device__ void gather_mn(const TcParams &p, Shared &sh, uint32_t g_base, uint32
 
 // Gather warps: grad_out frame windows into 128-byte swizzled K-major rows
 // (one row per frame element, 128 bytes of grad_out channels).
-template <int ESIZE>
+template <int ESIZE, int GW>
 __device__ void role_gather(const TcParams &p, Shared &sh, uint32_t g_base, int gw, int lane) {
     const int64_t plane = (int64_t)p.OH * p.OW;
     int stage = 0;
@@ -1461,7 +1483,7 @@ __device__ void role_gather(const TcParams &p, Shared &sh, uint32_t g_base, int 
             const uint32_t s_base = g_base + (uint32_t)stage * p.g_stage_bytes;
             const int co0 = cc * p.kc;
             const int cleft = p.Co - co0;
-            for (int h = gw * 32 + lane; h < p.hbp; h += kGWarps * 32) {
+            for (int h = gw * 32 + lane; h < p.hbp; h += GW * 32) {
                 const int lam = L0 + h;
                 const int n = lam / img;
                 const int rem = lam - n * img;
@@ -1731,7 +1753,7 @@ __device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &
 // consecutive lanes write consecutive columns of a phase, the other phases of
 // the row fill the columns in between.
 __device__ void epilogue_stacked(const TcParams &p, const PhaseDesc &d, const Tile &ti,
-                                 uint32_t taddr, int q, int part, int lane) {
+                                 uint32_t taddr, int q, int part, int parts, int lane) {
     uint32_t v[32];
     tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(v));
     if (p.st_n > 16) tmem_ld16(taddr + 16u, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
@@ -1750,7 +1772,7 @@ __device__ void epilogue_stacked(const TcParams &p, const PhaseDesc &d, const Ti
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
         if (k >= phases) break;
-        if ((k & 1) == part) {
+        if (k % parts == part) {
             const int ih = s * (a0 + r) + rh, iw = s * b + rw;
             if (ih < p.H && iw < p.W) img[(int64_t)ci * HW + (int64_t)ih * p.W + iw] = __uint_as_float(v[c]);
         }
@@ -1876,7 +1898,7 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
         } else
         if constexpr (V == kVarStacked)
             epilogue_stacked(p, d, ti, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.st_n), q, part,
-                             lane);
+                             Roles<V>::epi_warps / 4, lane);
         else if (V == kVarFrame64 || p.epi_tma)  // the 64-wide frame always stores through TMA
             epilogue_tma(p, d, ti, taddr, st_base, q, part, lane, bsel);
         else if (rows == 16)
@@ -2155,17 +2177,6 @@ __device__ void epilogue_pm(const TcParams &p, Shared &sh, uint32_t xbase, uint3
 
 // Warp roles of the kernel variants: the general mode and the 64-wide frame
 // share a layout, positions-on-M has its own.
-template <int V>
-struct Roles {
-    static constexpr int epi_warps = kEpiWarps, mma_warp = kMmaWarp, w_warp = kWWarp;
-    static constexpr int g_warp0 = kGWarp0, g_warps = kGWarps, threads = kThreads;
-};
-template <>
-struct Roles<kVarPosM> {
-    static constexpr int epi_warps = kPmEpiWarps, mma_warp = kPmMmaWarp, w_warp = kPmWWarp;
-    static constexpr int g_warp0 = kPmGWarp0, g_warps = kPmGWarps, threads = kPmThreads;
-};
-
 // V (kVar*): which plan the kernel runs -- the general mode (any phase count,
 // raw-slice or register gather, resident or streamed weights, TMA-store or
 // staged epilogue), the 64-wide frame, or positions-on-M.  Each variant
@@ -2261,9 +2272,9 @@ __global__ void __launch_bounds__(Roles<V>::threads, 1)
         else if (ESIZE == 2 && p.mn_b)
             gather_mn(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
         else if (p.gather_tma)
-            gather_from_raw<ESIZE>(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
+            gather_from_raw<ESIZE, R::g_warps>(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
         else
-            role_gather<ESIZE>(p, sh, g_base, warp - R::g_warp0, lane);
+            role_gather<ESIZE, R::g_warps>(p, sh, g_base, warp - R::g_warp0, lane);
     } else {
         if constexpr (PM)
             epilogue_pm(p, sh, epi_stage, tmem, warp, lane);
