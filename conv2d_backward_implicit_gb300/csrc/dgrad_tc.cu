@@ -573,10 +573,15 @@ __device__ __forceinline__ int tile_own(const TcParams &p, const PhaseDesc &d, i
 
 // This CTA's tiles: groups of tile_group consecutive tiles, the groups dealt
 // round-robin over the grid (tile_group = 1: blockIdx.x, + gridDim.x, ...).
+// Only the pair variant (V) takes groups of more than one tile.
+template <int V = kVarGeneral>
 __device__ __forceinline__ int64_t first_tile(const TcParams &p) {
+    if constexpr (V != kVarPair && V != kVarGeneral) return (int64_t)blockIdx.x;
     return (int64_t)blockIdx.x * p.tile_group;
 }
+template <int V = kVarGeneral>
 __device__ __forceinline__ int64_t next_tile(const TcParams &p, int64_t t) {
+    if constexpr (V != kVarPair && V != kVarGeneral) return t + gridDim.x;
     if (p.tile_group == 1) return t + gridDim.x;
     return (t + 1) % p.tile_group ? t + 1 : t + 1 + (int64_t)(gridDim.x - 1) * p.tile_group;
 }
@@ -709,7 +714,7 @@ __device__ void issue_weights(const TcParams &p, Shared &sh, uint32_t w_base) {
 constexpr int kRawLookahead = 2;  // general mode: tiles of this CTA prefetched ahead
 template <int V>
 __device__ void prefetch_raw_tile(const TcParams &p, int64_t t) {
-    if (t >= p.total_tiles || (p.pair_rw && (t & 1))) return;
+    if (t >= p.total_tiles || (is_general(V) && p.pair_rw && (t & 1))) return;
     const Tile ti = decode_tile<V>(p, t);
     const PhaseDesc &d = p.ph[ti.phase];
     if (d.Jh == 0 || ti.mt != 0) return;  // channel tiles share the window
@@ -764,8 +769,8 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
     // below is cold code, run while the previous kernel finishes) and waits
     // right before its first global-memory access.
     bool waited = false;
-    for (int64_t t = first_tile(p); t < p.total_tiles && !aborted; t = next_tile(p, t)) {
-        if (p.pair_rw && (t & 1)) continue;  // a pair shares its first tile's window
+    for (int64_t t = first_tile<V>(p); t < p.total_tiles && !aborted; t = next_tile<V>(p, t)) {
+        if (is_general(V) && p.pair_rw && (t & 1)) continue;  // a pair shares its first tile's window
         const Tile ti = decode_tile<V>(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
         if (d.Jh == 0) continue;
@@ -801,11 +806,11 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
                     // beyond it (general) or itself (positions-on-M).
                     prefetching = true;
                     int64_t ahead = t;
-                    for (int k = 0; k <= (p.pos_m ? 0 : kRawLookahead); ++k, ahead = next_tile(p, ahead))
+                    for (int k = 0; k <= (p.pos_m ? 0 : kRawLookahead); ++k, ahead = next_tile<V>(p, ahead))
                         prefetch_raw_tile<V>(p, ahead);
                 } else if (!p.pos_m && prefetching && cc == 0 && sl == 0) {
                     int64_t ahead = t;
-                    for (int k = 0; k < kRawLookahead; ++k) ahead = next_tile(p, ahead);
+                    for (int k = 0; k < kRawLookahead; ++k) ahead = next_tile<V>(p, ahead);
                     prefetch_raw_tile<V>(p, ahead);
                 }
                 if (!waited) {
@@ -833,7 +838,7 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
         }
         // Positions-on-M mode (the ring holds a whole tile): all of this
         // tile's slices are queued, the next tile's go to L2.
-        if (p.pos_m && prefetching && !aborted) prefetch_raw_tile<V>(p, next_tile(p, t));
+        if (p.pos_m && prefetching && !aborted) prefetch_raw_tile<V>(p, next_tile<V>(p, t));
     }
     if (!waited) grid_dependency_wait();
     if (!weights_issued) issue_weights(p, sh, w_base);  // fewer slices than free slots
@@ -1072,7 +1077,7 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
     uint32_t gph = 0, wph = 0, accph = 0;
     bool aborted = false;
     if (p.nw == 0 && !wait_bar(smem_u32(&sh.w_full), 0, p, sh)) aborted = true;
-    for (int64_t t = first_tile(p); t < p.total_tiles && !aborted; t = next_tile(p, t)) {
+    for (int64_t t = first_tile<V>(p); t < p.total_tiles && !aborted; t = next_tile<V>(p, t)) {
         if (V == kVarPair && (t & 1)) continue;
         const Tile ti = decode_tile<V>(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
@@ -1117,10 +1122,11 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
                 // 32-byte K step is an add to a base descriptor.
                 const uint64_t wd0 = sw128_desc(w_grp);
                 // MN-major grad_out: a 16-channel K step is two 8-row groups.
+                const bool mn = V == kVarGeneral && p.mn_b;
                 const uint32_t mn_sbo = (uint32_t)p.mn_atoms * 1024u;
-                const uint64_t gd0 = p.mn_b ? sw128_mn_desc(g_stage, 1024u, mn_sbo)
-                                            : sw128_desc(g_stage + (uint32_t)(p.view0 * 128));
-                const uint32_t b_kstep = p.mn_b ? (2u * mn_sbo) >> 4 : 2u;
+                const uint64_t gd0 = mn ? sw128_mn_desc(g_stage, 1024u, mn_sbo)
+                                        : sw128_desc(g_stage + (uint32_t)(p.view0 * 128));
+                const uint32_t b_kstep = mn ? (2u * mn_sbo) >> 4 : 2u;
                 const uint32_t w_step = (uint32_t)(p.w_unit_bytes >> 4);
                 int j = t0 / dk.Jw, i = t0 - j * dk.Jw;
                 for (int tap = t0; tap < t1; ++tap) {
@@ -1155,7 +1161,7 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
         }
         if (aborted) break;
         tc_commit(smem_u32(&sh.acc_full[acc]));
-        if (++acc == (p.acc_single ? 1 : 2)) {
+        if (++acc == ((V == kVarPair && p.acc_single) ? 1 : 2)) {
             acc = 0;
             accph ^= 1u;
         }
@@ -1628,9 +1634,10 @@ __device__ void epilogue_staged(const TcParams &p, const PhaseDesc &d, const Til
 // row's W accumulator columns, copies them into a dense [8 channels][W] box in
 // shared memory and one lane stores the box with a TMA tensor store, so
 // grad_in is written in whole, aligned rows.
+template <int V>
 __device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &ti,
                              uint32_t taddr, uint32_t box, int q, int part, int lane, int &bsel) {
-    if (p.mn_b) {
+    if (V == kVarGeneral && p.mn_b) {
         // Whole-image 1x1 tiles: accumulator column c is plane position c.
         // Per 32 positions the warp's channels go into a [channels][32]
         // float box, 128-byte swizzled (conflict-free writes; the box is
@@ -1861,7 +1868,7 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
     int bsel = 0;  // TMA store box in use (double-buffered epilogue)
     int acc = 0;
     uint32_t accph = 0;
-    for (int64_t t = first_tile(p); t < p.total_tiles; t = next_tile(p, t)) {
+    for (int64_t t = first_tile<V>(p); t < p.total_tiles; t = next_tile<V>(p, t)) {
         if (V == kVarPair && (t & 1)) continue;  // a pair is stored at its first tile
         const Tile ti = decode_tile<V>(p, t);
         const PhaseDesc &d = p.ph[ti.phase];
@@ -1900,7 +1907,7 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
             epilogue_stacked(p, d, ti, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.st_n), q, part,
                              Roles<V>::epi_warps / 4, lane);
         else if (V == kVarFrame64 || p.epi_tma)  // the 64-wide frame always stores through TMA
-            epilogue_tma(p, d, ti, taddr, st_base, q, part, lane, bsel);
+            epilogue_tma<V>(p, d, ti, taddr, st_base, q, part, lane, bsel);
         else if (rows == 16)
             epilogue_staged<16>(p, d, ti, taddr, st_base, q, part, lane);
         else
@@ -1908,7 +1915,7 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.acc_empty[acc]));
-        if (++acc == (p.acc_single ? 1 : 2)) {
+        if (++acc == ((V == kVarPair && p.acc_single) ? 1 : 2)) {
             acc = 0;
             accph ^= 1u;
         }
