@@ -95,3 +95,37 @@ def test_raw_mode_case(dg, idx):
     assert err <= TOL[dtype], f"{what}: {err:.3g}"
     out2 = run_gpu(dg, wl, g, w, via="prepacked").cpu().numpy()
     assert np.array_equal(out1, out2), f"{what}: prepacked launch differs from the one-call API"
+
+
+def run_offset(dg, wl, g, w, g_offset, out_offset):
+    """The one-call API with grad_out / grad_in starting g_offset / out_offset
+    elements past a 16-byte boundary (aligned to the element size only)."""
+    dev = torch.device("cuda")
+    flat = torch.zeros(g.numel() + g_offset, dtype=g.dtype, device=dev)
+    flat[g_offset:] = g.reshape(-1).to(dev)
+    gd = flat[g_offset:].view(g.shape)
+    n_out = int(np.prod(wl.grad_in_shape))
+    oflat = torch.full((n_out + out_offset,), float("nan"), device=dev)
+    out = oflat[out_offset:].view(wl.grad_in_shape)
+    p = dg.params_from_shapes(g.shape, w.shape, wl.H, wl.W, wl.stride, wl.padding_h, wl.padding_w)
+    dg.conv2d_grad_input(gd, w.to(dev), out, p, dg.DTYPE_CODE[wl.dtype])
+    assert dg.conv2d_grad_input_check_errors() == 0
+    return out.cpu().numpy()
+
+
+# One case of each mode whose plan needs aligned pointers for its TMA / bulk
+# copies: the MN-major 1x1 operand, the stacked phases and the paired column
+# phases.  A misaligned grad_out (no raw-slice copies) or grad_in (no TMA
+# stores) must take the mode's fallback and still match the oracle.
+ALIGN_CASES = [8, 10, 14]
+
+
+@pytest.mark.parametrize("idx", ALIGN_CASES)
+@pytest.mark.parametrize("g_offset,out_offset", [(1, 0), (0, 1), (3, 5)])
+def test_mode_pointer_fallbacks(dg, idx, g_offset, out_offset):
+    shape, dtype, what = CASES[idx]
+    wl = make_case(shape, dtype, idx)
+    g, w = workloads.make_inputs(wl, seed=300 + idx)
+    got = run_offset(dg, wl, g, w, g_offset, out_offset)
+    err = rel_err(got, oracle_full(wl, g, w))
+    assert err <= TOL[dtype], f"{what}, offsets {g_offset}/{out_offset}: {err:.3g}"
