@@ -247,6 +247,61 @@ def workload_config(wl, key, l2_note):
 
 
 # ------------------------------------------------------------------ GPU arm
+def kernel_only(dg, workloads, wl, key, dev, stream, launches=600):
+    """Per-launch time of the dgrad kernel alone on one workload: cold L2 via
+    rotating buffer sets (> 3x L2), weights packed beforehand, a CUDA graph of
+    back-to-back launches timed with events; returns the roofline figures."""
+    import torch
+    g_cpu, w_cpu = workloads.make_inputs(wl, seed=0)
+    p = dg.params_from_shapes(g_cpu.shape, w_cpu.shape, wl.H, wl.W, wl.stride, wl.padding_h,
+                              wl.padding_w)
+    code = dg.DTYPE_CODE[wl.dtype]
+    kernel = dg.conv2d_grad_input_select_kernel(p, code)
+    ws = dg.conv2d_grad_input_workspace_size(p, code)
+    alg = algorithmic_bytes(wl)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 * 2**20)
+    # (capped: a workload of a few KB, e.g. the tiny one, is launch-latency bound
+    # and measured L2-resident)
+    n_sets = min(max(2, math.ceil(3 * l2 / alg)), 512)
+    sets = []
+    for _ in range(n_sets):
+        s = {"g": g_cpu.to(dev), "out": torch.empty(wl.grad_in_shape, device=dev, dtype=torch.float32)}
+        if kernel == dg.DGRAD_KERNEL_TC:
+            s["src"] = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+            dg.conv2d_grad_input_pack_weight(w_cpu.to(dev), s["src"], ws, p, code, stream)
+        else:
+            s["src"] = w_cpu.to(dev)
+        sets.append(s)
+    stream.synchronize()
+
+    def launch_all():
+        for s in sets:
+            dg.conv2d_grad_input_prepacked(s["g"], s["src"], s["out"], p, code, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            launch_all()
+    stream.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        launch_all()
+    reps = max(1, launches // n_sets)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        gr.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            gr.replay()
+        e1.record(stream)
+    stream.synchronize()
+    rc = dg.conv2d_grad_input_check_errors(stream)
+    if rc != 0:
+        raise RuntimeError(f"{key}: {dg.conv2d_grad_input_status_string(rc)}")
+    k_ms = e0.elapsed_time(e1) / (reps * n_sets)
+    del sets, gr
+    return k_ms, alg, kernel
+
+
 def run_gpu(args, wl, key):
     import torch
     import torch.distributed as dist
@@ -453,6 +508,22 @@ def run_gpu(args, wl, key):
                     "d2h_bytes_per_step": out_host.numel() * 4, "steps": Ke},
             "clocks": clocks,
         }
+        if world == 1 and not args.no_per_config:
+            # The metric is per workload: the dgrad kernel alone on each of the
+            # five, same cold-L2 protocol (the bench workload's own line above).
+            per = {}
+            for other_key in ("tiny", "resnet", "strided", "pointwise", "stem"):
+                owl = workloads.BY_KEY[other_key]
+                o_ms, o_alg, o_kernel = kernel_only(dg, workloads, owl, other_key, dev, stream)
+                o_peak = bf16_peak / 2 if owl.dtype == "f32" else bf16_peak
+                o_gbs = o_alg / (o_ms * 1e-3) / 1e9
+                o_tf = useful_flops(owl) / (o_ms * 1e-3) / 1e12
+                per[other_key] = {"kernel_us": o_ms * 1e3, "tflops": o_tf,
+                                  "hbm_frac": o_gbs / hbm_peak, "tensor_frac": o_tf / o_peak,
+                                  "dtype": owl.dtype,
+                                  "kernel": {1: "tcgen05", 2: "cuda-core"}.get(o_kernel, str(o_kernel)),
+                                  "traffic": recorded_traffic(other_key)}
+            out["per_config"] = per
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(wl)
         print(json.dumps(out), flush=True)
@@ -471,6 +542,8 @@ def main(argv=None):
     ap.add_argument("--config", default="resnet",
                     choices=["tiny", "resnet", "strided", "pointwise", "stem"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the kernel-only figures of the other workloads")
     args = ap.parse_args(argv)
     from conv2d_backward_implicit_gb300 import workloads
     wl = workloads.BY_KEY[args.config]
