@@ -302,6 +302,42 @@ def kernel_only(dg, workloads, wl, key, dev, stream, launches=600):
     return k_ms, alg, kernel
 
 
+def forward_call(dg, workloads, wl, dev, stream, calls=300):
+    """The stride-1 forward convolution of the layer (conv2d_forward: weight
+    flip + pack + kernel, stream-ordered workspace) on rotating buffer sets
+    (> 3x L2), back to back, timed with events; returns ms per call."""
+    import torch
+    gen = torch.Generator().manual_seed(0)
+    tdt = workloads.TORCH_DTYPE[wl.dtype]
+    x_cpu = torch.randn((wl.N, wl.Ci, wl.H, wl.W), generator=gen).to(tdt)
+    w_cpu = (torch.randn(wl.weight_shape, generator=gen) * wl.w_std).to(tdt)
+    p = dg.params_from_shapes((wl.N, wl.Co, wl.OH, wl.OW), w_cpu.shape, wl.H, wl.W, wl.stride,
+                              wl.padding_h, wl.padding_w)
+    code = dg.DTYPE_CODE[wl.dtype]
+    esize = 4 if wl.dtype == "f32" else 2
+    nbytes = x_cpu.numel() * esize + w_cpu.numel() * esize + wl.N * wl.Co * wl.OH * wl.OW * 4
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 * 2**20)
+    n_sets = min(max(2, math.ceil(3 * l2 / nbytes)), 512)
+    sets = [(x_cpu.to(dev), w_cpu.to(dev),
+             torch.empty((wl.N, wl.Co, wl.OH, wl.OW), device=dev, dtype=torch.float32))
+            for _ in range(n_sets)]
+    with torch.cuda.stream(stream):
+        for i in range(2 * n_sets):
+            x, w, o = sets[i % n_sets]
+            dg.conv2d_forward(x, w, o, p, code, stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(calls):
+            x, w, o = sets[i % n_sets]
+            dg.conv2d_forward(x, w, o, p, code, stream)
+        e1.record(stream)
+    stream.synchronize()
+    rc = dg.conv2d_grad_input_check_errors(stream)
+    if rc != 0:
+        raise RuntimeError(f"forward: {dg.conv2d_grad_input_status_string(rc)}")
+    return e0.elapsed_time(e1) / calls
+
+
 def run_gpu(args, wl, key):
     import torch
     import torch.distributed as dist
@@ -524,6 +560,12 @@ def run_gpu(args, wl, key):
                                   "kernel": {1: "tcgen05", 2: "cuda-core"}.get(o_kernel, str(o_kernel)),
                                   "traffic": recorded_traffic(other_key)}
             out["per_config"] = per
+            # The forward convolution of the bench layer (stride 1 only).
+            if wl.stride == 1:
+                f_ms = forward_call(dg, workloads, wl, dev, stream)
+                out["forward"] = {"op": "conv2d_forward (weight flip + pack + kernel)",
+                                  "workload": wl.name, "ms_per_call": f_ms,
+                                  "tflops": useful_flops(wl) / (f_ms * 1e-3) / 1e12}
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(wl)
         print(json.dumps(out), flush=True)

@@ -9,7 +9,7 @@ from .binding import (  # noqa: F401
     DGRAD_BF16, DGRAD_DEBUG_SKIP_ARRIVE, DGRAD_F16, DGRAD_F32, DGRAD_KERNEL_AUTO,
     DGRAD_KERNEL_SIMT, DGRAD_KERNEL_TC, DGRAD_KERNEL_TC_POSM, DTYPE_CODE, PARAM_FIELDS, STATUS,
     DgradError, Params,
-    conv2d_grad_input, conv2d_grad_input_check_errors, conv2d_grad_input_noalloc, conv2d_grad_input_pack_weight,
+    conv2d_forward, conv2d_grad_input, conv2d_grad_input_check_errors, conv2d_grad_input_noalloc, conv2d_grad_input_pack_weight,
     conv2d_grad_input_prepacked, conv2d_grad_input_select_kernel, conv2d_grad_input_set_debug,
     conv2d_grad_input_set_kernel, conv2d_grad_input_set_wait_limit_ns,
     conv2d_grad_input_status_string, conv2d_grad_input_workspace_size, library, library_path,

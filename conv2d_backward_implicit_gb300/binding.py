@@ -95,6 +95,8 @@ def library() -> ctypes.CDLL:
             lib.conv2d_grad_input_set_debug.restype = I
             lib.conv2d_grad_input_noalloc.argtypes = [P, P, P, PP, I, P]
             lib.conv2d_grad_input_noalloc.restype = I
+            lib.conv2d_forward.argtypes = [P, P, P, PP, I, P]
+            lib.conv2d_forward.restype = I
             _lib = lib
     return _lib
 
@@ -183,3 +185,11 @@ def conv2d_grad_input_noalloc(grad_out, weight, grad_in, params: Params, dtype: 
     rc = library().conv2d_grad_input_noalloc(_addr(grad_out), _addr(weight), _addr(grad_in),
                                              ctypes.byref(params), int(dtype), _stream(stream))
     _check(rc, "conv2d_grad_input_noalloc")
+
+
+def conv2d_forward(x, weight, out, params: Params, dtype: int, stream=None) -> None:
+    """Forward convolution of the layer ``params`` describes (stride 1): x
+    [N,Ci,H,W], weight [Co,Ci,kH,kW] -> out [N,Co,OH,OW] float32."""
+    rc = library().conv2d_forward(_addr(x), _addr(weight), _addr(out), ctypes.byref(params),
+                                  int(dtype), _stream(stream))
+    _check(rc, "conv2d_forward")

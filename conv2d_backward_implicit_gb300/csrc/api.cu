@@ -79,6 +79,53 @@ int conv2d_grad_input(const void *grad_out, const void *weight, float *grad_in,
     return rc;
 }
 
+int conv2d_forward(const void *x, const void *weight, float *out, const conv2d_grad_input_params *p,
+                   int dtype, struct CUstream_st *stream) {
+    if (!x || !weight || !out || !p) return DGRAD_ERR_INVALID_ARG;
+    // The layer itself must be valid (same checks as its input gradient).
+    dgrad::Plan layer;
+    int rc = plan_for(p, dtype, &layer);
+    if (rc != DGRAD_OK) return rc;
+    if (p->stride != 1 || p->padding_h > p->kernel_h - 1 || p->padding_w > p->kernel_w - 1)
+        return DGRAD_ERR_UNSUPPORTED;
+    // At stride 1 the forward convolution is the input gradient of the layer
+    // with the channel axes swapped, the kernel flipped and padding k - 1 - p:
+    // out plays grad_in, x plays grad_out.
+    conv2d_grad_input_params q;
+    q.batch = p->batch;
+    q.in_channels = p->out_channels;
+    q.in_h = p->out_h;
+    q.in_w = p->out_w;
+    q.out_channels = p->in_channels;
+    q.kernel_h = p->kernel_h;
+    q.kernel_w = p->kernel_w;
+    q.stride = 1;
+    q.padding_h = p->kernel_h - 1 - p->padding_h;
+    q.out_h = p->in_h;
+    q.out_w = p->in_w;
+    q.padding_w = p->kernel_w - 1 - p->padding_w;
+    dgrad::Plan plan;
+    rc = plan_for(&q, dtype, &plan);
+    if (rc != DGRAD_OK) return rc;
+    if (!aligned(x, plan.esize) || !aligned(weight, plan.esize) || !aligned(out, 4)) return DGRAD_ERR_ALIGNMENT;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t wt_bytes = ((size_t)p->out_channels * p->in_channels * p->kernel_h * p->kernel_w *
+                                 plan.esize + 255) / 256 * 256;
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, wt_bytes + plan.workspace, st);
+    if (e != cudaSuccess) return cuda_status((int)e);
+    void *packed = static_cast<char *>(ws) + wt_bytes;
+    int le = dgrad::launch_flip_transpose(weight, ws, (int)p->out_channels, (int)p->in_channels,
+                                          (int)p->kernel_h, (int)p->kernel_w, plan.esize, st);
+    if (le == (int)cudaSuccess && plan.kernel == DGRAD_KERNEL_TC && plan.workspace > 0)
+        le = dgrad::launch_pack(plan, ws, packed, st);
+    rc = le == (int)cudaSuccess ? run_main(plan, x, plan.kernel == DGRAD_KERNEL_TC ? packed : ws, out, st)
+                                : cuda_status(le);
+    e = cudaFreeAsync(ws, st);
+    if (rc == DGRAD_OK && e != cudaSuccess) rc = cuda_status((int)e);
+    return rc;
+}
+
 size_t conv2d_grad_input_workspace_size(const conv2d_grad_input_params *p, int dtype) {
     if (!p) return 0;
     dgrad::Plan plan;

@@ -224,6 +224,9 @@ int plan_with_settings(const void *params, int dtype, Plan *out);
 
 // Launchers (return cudaError_t as int).
 int launch_pack(const Plan &plan, const void *weight, void *packed, void *stream);
+// wt[ci][co][kh][kw] = w[co][ci][kH-1-kh][kW-1-kw] (pack.cu).
+int launch_flip_transpose(const void *w, void *wt, int Co, int Ci, int kH, int kW, int esize,
+                          void *stream);
 int launch_tc(const Plan &plan, const void *grad_out, const void *packed, float *grad_in,
               void *stream);
 int launch_simt(const Plan &plan, const void *grad_out, const void *weight, float *grad_in,

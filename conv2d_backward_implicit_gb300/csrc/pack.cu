@@ -102,7 +102,51 @@ __global__ void __launch_bounds__(256) pack_weight_kernel(const T *__restrict__ 
     }
 }
 
+// wt[ci][co][kh][kw] = w[co][ci][kH-1-kh][kW-1-kw]: the weights of a layer
+// seen from the other side (channel axes swapped, kernel flipped).
+template <typename T>
+__global__ void __launch_bounds__(256) flip_transpose_kernel(const T *__restrict__ w, T *__restrict__ wt,
+                                                             int Co, int Ci, int kH, int kW, int64_t total) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        int64_t r = idx;  // idx enumerates wt = [Ci][Co][kH][kW]
+        const int kw = (int)(r % kW); r /= kW;
+        const int kh = (int)(r % kH); r /= kH;
+        const int co = (int)(r % Co);
+        const int ci = (int)(r / Co);
+        wt[idx] = w[(((int64_t)co * Ci + ci) * kH + (kH - 1 - kh)) * kW + (kW - 1 - kw)];
+    }
+}
+
 }  // namespace
+
+int launch_flip_transpose(const void *w, void *wt, int Co, int Ci, int kH, int kW, int esize,
+                          void *stream) {
+    const int64_t total = (int64_t)Co * Ci * kH * kW;
+    if (total == 0) return (int)cudaSuccess;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
+    if (esize == 4)
+        e = cudaLaunchKernelEx(&cfg, flip_transpose_kernel<float>, static_cast<const float *>(w),
+                               static_cast<float *>(wt), Co, Ci, kH, kW, total);
+    else
+        e = cudaLaunchKernelEx(&cfg, flip_transpose_kernel<unsigned short>, static_cast<const unsigned short *>(w),
+                               static_cast<unsigned short *>(wt), Co, Ci, kH, kW, total);
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaGetLastError();
+}
 
 int launch_pack(const Plan &plan, const void *weight, void *packed, void *stream) {
     const PackParams &k = plan.pack;

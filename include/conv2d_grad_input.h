@@ -164,6 +164,26 @@ uint64_t conv2d_grad_input_set_wait_limit_ns(uint64_t ns);
 #define DGRAD_DEBUG_SKIP_ARRIVE 1
 int conv2d_grad_input_set_debug(int flags);
 
+/* The forward convolution of the same layer, stride 1:
+ *
+ *   out[n,co,oh,ow] = sum over ci < Ci, kh < kH, kw < kW of
+ *                     x[n,ci,oh-padding_h+kh, ow-padding_w+kw] * weight[co,ci,kh,kw]
+ *
+ * (x zero outside the image) -- the convolution whose input gradient
+ * conv2d_grad_input computes (the page's header comment defines the
+ * gradient as its adjoint).  `p` describes the layer exactly as for
+ * conv2d_grad_input: x is [batch, in_channels, in_h, in_w] of dtype, weight
+ * [out_channels, in_channels, kernel_h, kernel_w] of dtype, out [batch,
+ * out_channels, out_h, out_w] float32, overwritten.  At stride 1 this is the
+ * input gradient of a layer with the roles of the channel axes swapped, the
+ * kernel flipped and padding kernel - 1 - padding; the call flips and
+ * transposes the weights into a stream-ordered temporary buffer and runs
+ * the same kernels.  Stride > 1 or a padding above kernel - 1 returns
+ * DGRAD_ERR_UNSUPPORTED (nothing is enqueued); other argument errors as for
+ * conv2d_grad_input. */
+int conv2d_forward(const void *x, const void *weight, float *out, const conv2d_grad_input_params *p,
+                   int dtype, struct CUstream_st *stream);
+
 /* conv2d_grad_input without any device allocation.  The paper has no
  * counterpart to this entry point; it exists for callers that cannot
  * allocate device memory where they need the gradient -- code recorded into

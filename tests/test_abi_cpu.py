@@ -131,3 +131,16 @@ def test_positions_on_m_selection(lib):
 def test_stride_above_four_uses_cuda_cores(lib):
     p = dg.Params(1, 4, 20, 20, 4, 3, 3, 5, 1, 4, 4, 1)
     assert dg.conv2d_grad_input_select_kernel(p, 0) == dg.DGRAD_KERNEL_SIMT
+
+
+def test_forward_rejects_what_it_does_not_run(lib):
+    # Stride > 1 or padding above kernel - 1: unsupported, before any device work
+    # (the pointers are never touched).
+    p = dg.Params(2, 16, 10, 10, 24, 3, 3, 2, 1, 5, 5, 1)
+    assert lib.conv2d_forward(16, 16, 16, ctypes.byref(p), dg.DGRAD_BF16, None) == 4
+    p = dg.Params(2, 16, 10, 10, 24, 3, 3, 1, 3, 14, 14, 3)
+    assert lib.conv2d_forward(16, 16, 16, ctypes.byref(p), dg.DGRAD_BF16, None) == 4
+    # An inconsistent layer is a shape error, as for the input gradient.
+    p = dg.Params(2, 16, 10, 10, 24, 3, 3, 1, 1, 9, 10, 1)
+    assert lib.conv2d_forward(16, 16, 16, ctypes.byref(p), dg.DGRAD_BF16, None) == 2
+    assert lib.conv2d_forward(None, 16, 16, ctypes.byref(p), dg.DGRAD_BF16, None) == 1
