@@ -6,22 +6,30 @@
 // How it computes it is GB300-first rather than the shader's 2x2 grid of
 // cooperative-matrix tiles with two workgroup barriers per K step:
 //
-//  * M = 128 grad_in pixels of one sub-pixel phase (the frame of
-//    dgrad_internal.h), N = up to 256 input channels, K = grad_out channels x
-//    the phase's own taps.  Strided problems never multiply structural zeros.
-//  * A (the im2col operand) is never materialised per tap: for each block of
-//    grad_out channels, gather warps write one frame window of
-//    128 + (Jh-1)*X + Jw-1 pixels into shared memory as K-major,
-//    no-swizzle core matrices, and every tap is the same window read through
-//    a shared-memory descriptor whose start is shifted by that tap's offset.
-//  * B (weights) comes pre-packed (pack.cu) in exactly its shared-memory image
-//    and moves with cp.async.bulk: resident for the whole kernel when it fits,
-//    otherwise through a ring of per-channel-block stages.
+//  * The stride's sub-pixel phases (dgrad_internal.h) make every phase a
+//    dense stride-1 correlation: structural-zero products are never issued.
+//  * The im2col operand is never materialised per tap: raw grad_out slices
+//    (TMA tensor loads or 1-D bulk copies) are turned by gather warps into one
+//    frame window per stage, 128-byte K-major swizzled rows in shared memory,
+//    and every tap is that window read through a descriptor whose start is
+//    shifted by the tap's offset.  For 1x1 problems the window is kept
+//    MN-major (channel rows of positions) and only regrouped.
+//  * The weights come pre-packed (pack.cu) in exactly their shared-memory
+//    image and move with bulk copies: resident when they fit, otherwise a
+//    ring of per-(chunk, tap group) stages.
 //  * One thread issues tcgen05.mma (kind::f16 for bf16/fp16, kind::tf32 for
-//    fp32) into a double-buffered TMEM accumulator; four epilogue warps drain
-//    the other buffer with tcgen05.ld and write float32 NCHW grad_in with
-//    per-element predication, so a tile's epilogue overlaps the next tile's
-//    MMAs.  Persistent grid: one CTA per SM walking the tile list.
+//    fp32) into double-buffered TMEM accumulators; epilogue warps drain one
+//    buffer with tcgen05.ld while the next tile's MMAs fill the other, and
+//    store float32 NCHW grad_in through TMA tensor stores (whole rows or
+//    planes) or predicated stores.  Persistent grid: one CTA per SM.
+//
+// Kernel variants (one compiled kernel each, see Roles): General (input
+// channels on M -- 64 or 128 rows -- and up to 256 positions on N), Frame64
+// (stride 1, 16-bit, rows up to 56: a 64-wide frame filled by ldmatrix
+// transposes), PosM (opt-in: positions on M, kernel-row taps on N), Pair
+// (stride 2: the two column phases of the same rows from one window into two
+// accumulators, stored as whole rows) and Stacked (few input channels:
+// positions on M, every phase's channels stacked on N).
 //
 // Every mbarrier wait is bounded by a wall-clock limit (globaltimer).  On
 // expiry the CTA raises an abort flag in shared memory, sets bit 0 of the
