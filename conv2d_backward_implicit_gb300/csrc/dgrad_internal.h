@@ -174,6 +174,7 @@ struct TcParams {
     // st_n rows, zero where a phase does not use the tap.
     int stacked;
     int st_n, st_th, st_tw, st_dy0, st_dx0;
+    int st_mblocks;         // 128-position MMA M-blocks per tile (1 or 2), one accumulator each
     // A CTA takes tiles in groups of tile_group consecutive tiles (groups
     // dealt round-robin over the grid).  pair_rw (stride 2, four phases
     // interleaved, one channel tile): tiles 2u and 2u + 1 are the column

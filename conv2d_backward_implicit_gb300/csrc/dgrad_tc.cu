@@ -1186,42 +1186,69 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
 template <bool TF32>
 __device__ void role_mma_stacked(const TcParams &p, Shared &sh, uint32_t g_base, uint32_t w_base,
                                  uint32_t tmem) {
-    int gs = 0, acc = 0;
-    uint32_t gph = 0, accph = 0;
-    bool aborted = !wait_bar(smem_u32(&sh.w_full), 0, p, sh);
+    int gs = 0, ws = 0, acc = 0;
+    uint32_t gph = 0, wph = 0, accph = 0;
+    bool aborted = p.nw == 0 && !wait_bar(smem_u32(&sh.w_full), 0, p, sh);
     const int X = p.ph[0].X;
     const int taps = p.st_th * p.st_tw;
-    for (int64_t t = first_tile(p); t < p.total_tiles && !aborted; t = next_tile(p, t)) {
+    const int mblocks = p.st_mblocks;  // 128-position M-blocks of a tile, one accumulator each
+    const uint32_t w_step = (uint32_t)(p.w_unit_bytes >> 4);
+    for (int64_t t = first_tile<kVarStacked>(p); t < p.total_tiles && !aborted;
+         t = next_tile<kVarStacked>(p, t)) {
         if (!wait_bar(smem_u32(&sh.acc_empty[acc]), accph ^ 1u, p, sh)) {
             aborted = true;
             break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(acc * p.st_n);
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * mblocks * p.st_n);
         uint32_t accumulate = 0;
-        for (int cc = 0; cc < p.n_cchunks; ++cc) {
+        for (int cc = 0; cc < p.n_cchunks && !aborted; ++cc) {
             if (!wait_bar(smem_u32(&sh.full_g[gs]), gph, p, sh)) {
                 aborted = true;
                 break;
             }
             tc_fence_after();
             const uint64_t ad0 = sw128_desc(g_base + (uint32_t)gs * p.g_stage_bytes);
-            const uint64_t bd0 = sw128_desc(w_base + (uint32_t)(cc * taps) * (uint32_t)p.w_unit_bytes);
-            const uint32_t w_step = (uint32_t)(p.w_unit_bytes >> 4);
             int dy = 0, dx = 0;
-            for (int tap = 0; tap < taps; ++tap) {
-                const uint64_t ad = ad0 + (uint64_t)((dy * X + dx) * 8);  // 128-byte rows, in 16-byte units
-                const uint64_t bd = bd0 + (uint64_t)(tap * w_step);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {  // four 32-byte K steps per 128-byte row
-                    tc_mma<TF32>(d_tmem, ad + 2u * k, bd + 2u * k, p.idesc, accumulate);
-                    accumulate = 1;
+            for (int t0 = 0; t0 < taps && !aborted; t0 += p.taps_per_w) {
+                const int t1 = taps - t0 < p.taps_per_w ? taps : t0 + p.taps_per_w;
+                uint32_t w_grp;  // weights of taps t0 .. t1 - 1 of this chunk
+                if (p.nw == 0) {
+                    w_grp = w_base + (uint32_t)(cc * taps + t0) * (uint32_t)p.w_unit_bytes;
+                } else {
+                    if (!wait_bar(smem_u32(&sh.full_w[ws]), wph, p, sh)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    w_grp = w_base + (uint32_t)ws * p.w_stage_bytes;
                 }
-                if (++dx == p.st_tw) {
-                    dx = 0;
-                    ++dy;
+                const uint64_t bd0 = sw128_desc(w_grp);
+                for (int tap = t0; tap < t1; ++tap) {
+                    const uint64_t ad = ad0 + (uint64_t)((dy * X + dx) * 8);  // 128-byte rows, in 16-byte units
+                    const uint64_t bd = bd0 + (uint64_t)((tap - t0) * w_step);
+                    for (int mb = 0; mb < mblocks; ++mb) {
+                        const uint64_t adm = ad + (uint64_t)(mb * 128 * 8);  // the next 128 frame rows
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)  // four 32-byte K steps per 128-byte row
+                            tc_mma<TF32>(d_tmem + (uint32_t)(mb * p.st_n), adm + 2u * k, bd + 2u * k, p.idesc,
+                                         accumulate | (uint32_t)(k > 0));
+                    }
+                    accumulate = 1;
+                    if (++dx == p.st_tw) {
+                        dx = 0;
+                        ++dy;
+                    }
+                }
+                if (p.nw != 0) {
+                    tc_commit(smem_u32(&sh.empty_w[ws]));
+                    if (++ws == p.nw) {
+                        ws = 0;
+                        wph ^= 1u;
+                    }
                 }
             }
+            if (aborted) break;
             tc_commit(smem_u32(&sh.empty_g[gs]));
             if (++gs == p.ng) {
                 gs = 0;
@@ -1762,41 +1789,44 @@ __device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &
 }
 
 // Stacked-phase epilogue: TMEM lane = tile position (frame row r, column b of
-// the phase grid), column n = (rh * s + rw) * Ci + ci.  Lane quadrant q holds
-// positions 32q..32q+31; the two warps of a quadrant take the phases of
-// either parity.  Each value goes to grad_in[n][ci][s (a0 + r) + rh][s b + rw];
+// the phase grid) within an M-block, column n = (rh * s + rw) * Ci + ci of that
+// M-block's accumulator.  Lane quadrant q holds positions 128 mb + 32q .. +31;
+// the warps of a quadrant (`parts` of them) split the phases.  Each value goes to grad_in[n][ci][s (a0 + r) + rh][s b + rw];
 // consecutive lanes write consecutive columns of a phase, the other phases of
 // the row fill the columns in between.
 __device__ void epilogue_stacked(const TcParams &p, const PhaseDesc &d, const Tile &ti,
                                  uint32_t taddr, int q, int part, int parts, int lane) {
-    uint32_t v[32];
-    tmem_ld16(taddr, *reinterpret_cast<uint32_t(*)[16]>(v));
-    if (p.st_n > 16) tmem_ld16(taddr + 16u, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
-    tmem_wait_ld32(v);
     const int tpi = (d.Hr + p.rows_per_tile - 1) / p.rows_per_tile;
     const int n = ti.pt / tpi, a0 = (ti.pt - n * tpi) * p.rows_per_tile;
-    const int h = 32 * q + lane;
-    const int r = h / d.X, b = h - r * d.X;
-    if (r >= p.rows_per_tile || a0 + r >= d.Hr || b >= d.Wr) return;
     const int s = p.stride, phases = s * s;
     const int64_t HW = (int64_t)p.H * p.W;
     float *img = p.grad_in + (int64_t)n * p.Ci * HW;
-    // Column c = k * Ci + ci, walked with (k, ci) kept alongside so that v is
-    // indexed by constants only.
-    int k = 0, ci = 0, rh = 0, rw = 0;
+    for (int mb = 0; mb < p.st_mblocks; ++mb) {  // M-block mb: tile positions 128 mb ..
+        uint32_t v[32];
+        const uint32_t ta = taddr + (uint32_t)(mb * p.st_n);
+        tmem_ld16(ta, *reinterpret_cast<uint32_t(*)[16]>(v));
+        if (p.st_n > 16) tmem_ld16(ta + 16u, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+        tmem_wait_ld32(v);
+        const int h = 128 * mb + 32 * q + lane;
+        const int r = h / d.X, b = h - r * d.X;
+        if (r >= p.rows_per_tile || a0 + r >= d.Hr || b >= d.Wr) continue;
+        // Column c = k * Ci + ci, walked with (k, ci) kept alongside so that v
+        // is indexed by constants only.
+        int k = 0, ci = 0, rh = 0, rw = 0;
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-        if (k >= phases) break;
-        if (k % parts == part) {
-            const int ih = s * (a0 + r) + rh, iw = s * b + rw;
-            if (ih < p.H && iw < p.W) img[(int64_t)ci * HW + (int64_t)ih * p.W + iw] = __uint_as_float(v[c]);
-        }
-        if (++ci == p.Ci) {
-            ci = 0;
-            ++k;
-            if (++rw == s) {
-                rw = 0;
-                ++rh;
+        for (int c = 0; c < 32; ++c) {
+            if (k >= phases) break;
+            if (k % parts == part) {
+                const int ih = s * (a0 + r) + rh, iw = s * b + rw;
+                if (ih < p.H && iw < p.W) img[(int64_t)ci * HW + (int64_t)ih * p.W + iw] = __uint_as_float(v[c]);
+            }
+            if (++ci == p.Ci) {
+                ci = 0;
+                ++k;
+                if (++rw == s) {
+                    rw = 0;
+                    ++rh;
+                }
             }
         }
     }
@@ -1912,8 +1942,8 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
             }
         } else
         if constexpr (V == kVarStacked)
-            epilogue_stacked(p, d, ti, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.st_n), q, part,
-                             Roles<V>::epi_warps / 4, lane);
+            epilogue_stacked(p, d, ti, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.st_mblocks * p.st_n),
+                             q, part, Roles<V>::epi_warps / 4, lane);
         else if (V == kVarFrame64 || p.epi_tma)  // the 64-wide frame always stores through TMA
             epilogue_tma<V>(p, d, ti, taddr, st_base, q, part, lane, bsel);
         else if (rows == 16)

@@ -607,57 +607,79 @@ bool plan_stacked(const conv2d_grad_input_params &p, int esize, int dtype, Plan 
     const int64_t Hr = cdiv(H, s), Wr = cdiv(W, s);
     const int64_t X = Wr + Tw - 1, R = Hr + Th - 1;
     if (X > 128 || N * R * X + 8192 > INT32_MAX) return false;
-    const int rows_per_tile = (int)std::min<int64_t>(128 / X, Hr);
     PhaseDesc &d = t.ph[0];
     d.Hr = (int)Hr; d.Wr = (int)Wr;
     d.Jh = (int)Th; d.Jw = (int)Tw;
     d.qh = (int)(Th - 1 + dy0); d.qw = (int)(Tw - 1 + dx0);
     d.X = (int)X; d.R = (int)R;
-    d.p_tiles = (int)(N * cdiv(Hr, rows_per_tile));
-    d.hb = (int)(128 + (Th - 1) * X + (Tw - 1));
     t.n_phases = 1;
     t.m_tile = 128;
     t.n_mtiles = 1;
     t.tile_p = 128;
-    t.rows_per_tile = rows_per_tile;
     t.kc = 128 / esize;
     t.n_cchunks = (int)cdiv(Co, t.kc);
-    t.hbp = (int)round_up(d.hb, 8);
     t.stacked = 1;
     t.st_n = (int)round_up(std::max<int64_t>((int64_t)s * s * Ci, 16), 16);
     t.st_th = (int)Th; t.st_tw = (int)Tw;
     t.st_dy0 = (int)dy0; t.st_dx0 = (int)dx0;
-    const int64_t g_stage = (int64_t)t.hbp * 128, w_unit = (int64_t)t.st_n * 128;
+    const int64_t w_unit = (int64_t)t.st_n * 128;
     const int64_t packed = (int64_t)t.n_cchunks * Th * Tw * w_unit;
-    t.g_stage_bytes = (int)g_stage;
     t.w_unit_bytes = (int)w_unit;
     t.packed_bytes = packed;
-    t.taps_per_w = (int)(Th * Tw);
-    t.w_stage_bytes = (int)(Th * Tw * w_unit);
-    t.nw = 0;
     t.epi_stage_bytes = 0;
-    // Raw slices when a load mode applies; resident weights beside two or
-    // three G stages and two or three raw slots.
-    const int raw = plan_raw_slices(p, esize, t);
+    // Tile shapes tried in turn: two M-blocks of 128 positions (whole frame
+    // rows up to 256 positions; the window's halo rows are then shared by
+    // twice the outputs) with the weights streamed in tap groups, then one
+    // M-block with the weights resident.  Each with raw slices when a load
+    // mode applies (two or three slots), else the gather reads grad_out
+    // directly.
     bool ok = false;
-    for (int nr = raw ? 3 : 0; nr >= (raw ? 2 : 0) && !ok; --nr) {
-        for (int ng = 3; ng >= 2 && !ok; --ng) {
-            const int64_t bytes = smem_layout_bytes(0, (int64_t)nr * t.raw_slice_bytes, packed + ng * g_stage);
-            if (bytes <= kSmemLimit) {
-                ok = true;
+    for (int mblocks = 2; mblocks >= 1 && !ok; --mblocks) {
+        const int rows = (int)std::min<int64_t>(mblocks * 128 / X, Hr);
+        if (mblocks == 2 && rows <= 128 / X) continue;  // no more rows than one M-block holds
+        t.st_mblocks = mblocks;
+        t.rows_per_tile = rows;
+        d.p_tiles = (int)(N * cdiv(Hr, rows));
+        d.hb = (int)(mblocks * 128 + (Th - 1) * X + (Tw - 1));
+        t.hbp = (int)round_up(d.hb, 8);
+        const int64_t g_stage = (int64_t)t.hbp * 128;
+        t.g_stage_bytes = (int)g_stage;
+        const int raw = plan_raw_slices(p, esize, t);
+        // (two M-blocks: two raw slots, the rest of shared memory for weights)
+        for (int nr = raw ? (mblocks == 2 ? 2 : 3) : 0; nr >= (raw ? 2 : 0) && !ok; --nr) {
+            const int64_t fixed = smem_layout_bytes(0, (int64_t)nr * t.raw_slice_bytes, 2 * g_stage);
+            if (mblocks == 1) {  // resident weights
+                if (fixed + packed <= kSmemLimit) {
+                    ok = true;
+                    t.nw = 0;
+                    t.taps_per_w = (int)(Th * Tw);
+                    t.w_stage_bytes = (int)(Th * Tw * w_unit);
+                    t.smem_bytes = (int)(fixed + packed);
+                }
+            } else {  // two weight stages of as many taps as fit
+                const int64_t tpw = std::min<int64_t>(Th * Tw, (kSmemLimit - fixed) / (2 * w_unit));
+                if (tpw >= 1) {
+                    ok = true;
+                    t.nw = 2;
+                    t.taps_per_w = (int)tpw;
+                    t.w_stage_bytes = (int)(tpw * w_unit);
+                    t.smem_bytes = (int)(fixed + 2 * tpw * w_unit);
+                }
+            }
+            if (ok) {
                 t.raw_nr = nr;
-                t.ng = ng;
-                t.smem_bytes = (int)bytes;
+                t.ng = 2;
             }
         }
-    }
-    if (!ok && raw) {  // without raw slices: the gather reads grad_out directly
-        plan_raw_slices(p, esize, t, /*none=*/true);
-        for (int ng = 3; ng >= 2 && !ok; --ng) {
-            const int64_t bytes = smem_layout_bytes(0, 0, packed + ng * g_stage);
+        if (!ok && raw && mblocks == 1) {  // without raw slices: the gather reads grad_out directly
+            plan_raw_slices(p, esize, t, /*none=*/true);
+            const int64_t bytes = smem_layout_bytes(0, 0, packed + 2 * g_stage);
             if (bytes <= kSmemLimit) {
                 ok = true;
-                t.ng = ng;
+                t.nw = 0;
+                t.taps_per_w = (int)(Th * Tw);
+                t.w_stage_bytes = (int)(Th * Tw * w_unit);
+                t.ng = 2;
                 t.smem_bytes = (int)bytes;
             }
         }
@@ -668,8 +690,8 @@ bool plan_stacked(const conv2d_grad_input_params &p, int esize, int dtype, Plan 
     t.tile_group = 1;
     const uint32_t fmt = dtype == DGRAD_F32 ? 2u : (dtype == DGRAD_BF16 ? 1u : 0u);
     t.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(t.st_n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-    uint32_t cols = 32;
-    while (cols < (uint32_t)(2 * t.st_n)) cols *= 2;
+    uint32_t cols = 32;  // two buffers of st_mblocks accumulators of st_n columns
+    while (cols < (uint32_t)(2 * t.st_mblocks * t.st_n)) cols *= 2;
     t.tmem_cols = cols;
     k.Ci = (int)Ci; k.Co = (int)Co; k.kH = (int)kH; k.kW = (int)kW; k.stride = s;
     k.m_tile = t.st_n; k.n_mtiles = 1; k.kc = t.kc; k.n_cchunks = t.n_cchunks;
