@@ -6,7 +6,8 @@ the kernel's roofline, on the ResNet 3x3 workload (N=32, Ci=Co=64, 56x56,
 stride 1, pad 1, bf16 in, float32 out) unless --config names another.
 
 One step = one pass of the whole path over one batch: the weight pre-pack
-kernel, then the dgrad kernel.  Inputs are resident in HBM; every step uses
+kernel, then the dgrad kernel (or the dgrad kernel alone where it packs the
+weights in shared memory itself: the workspace size is then 0).  Inputs are resident in HBM; every step uses
 the next of several buffer sets whose total exceeds 3x the L2 cache, so each
 step starts cold.  The timed region replays a CUDA graph of exactly K such
 steps (no event nodes inside the graph, so each kernel's prologue can overlap
@@ -266,10 +267,10 @@ def kernel_only(dg, workloads, wl, key, dev, stream, launches=600):
     sets = []
     for _ in range(n_sets):
         s = {"g": g_cpu.to(dev), "out": torch.empty(wl.grad_in_shape, device=dev, dtype=torch.float32)}
-        if kernel == dg.DGRAD_KERNEL_TC:
-            s["src"] = torch.empty(max(ws, 16), dtype=torch.uint8, device=dev)
+        if ws > 0:
+            s["src"] = torch.empty(ws, dtype=torch.uint8, device=dev)
             dg.conv2d_grad_input_pack_weight(w_cpu.to(dev), s["src"], ws, p, code, stream)
-        else:
+        else:  # CUDA-core kernel, or a kernel that packs the weights itself
             s["src"] = w_cpu.to(dev)
         sets.append(s)
     stream.synchronize()
@@ -304,7 +305,8 @@ def kernel_only(dg, workloads, wl, key, dev, stream, launches=600):
 
 def forward_call(dg, workloads, wl, dev, stream, calls=300):
     """The stride-1 forward convolution of the layer (conv2d_forward: weight
-    flip + pack + kernel, stream-ordered workspace) on rotating buffer sets
+    flip, pack unless the kernel packs itself, kernel; stream-ordered workspace)
+    on rotating buffer sets
     (> 3x L2), back to back, timed with events; returns ms per call."""
     import torch
     gen = torch.Generator().manual_seed(0)
@@ -374,7 +376,7 @@ def run_gpu(args, wl, key):
 
     def step(i, st, ev=None):
         s = sets[i % n_sets]
-        if kernel == dg.DGRAD_KERNEL_TC:
+        if ws > 0:
             dg.conv2d_grad_input_pack_weight(s["w"], s["packed"], ws, p, code, st)
             if ev is not None:
                 ev[0].record(st)
@@ -386,7 +388,7 @@ def run_gpu(args, wl, key):
         if ev is not None:
             ev[1].record(st)
 
-    launches_per_step = 2 if kernel == dg.DGRAD_KERNEL_TC else 1
+    launches_per_step = 2 if ws > 0 else 1  # pack + dgrad, or dgrad alone
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
             step(i, stream)
@@ -412,14 +414,14 @@ def run_gpu(args, wl, key):
 
     def main_only(i, st, ev=None):
         s = sets[i % n_sets]
-        src = s["packed"] if kernel == dg.DGRAD_KERNEL_TC else s["w"]
+        src = s["packed"] if ws > 0 else s["w"]
         if ev is not None:
             ev[0].record(st)
         dg.conv2d_grad_input_prepacked(s["g"], src, s["out"], p, code, st)
         if ev is not None:
             ev[1].record(st)
 
-    if kernel == dg.DGRAD_KERNEL_TC:  # weights packed once per set for the kernel-only region
+    if ws > 0:  # weights packed once per set for the kernel-only region
         for i in range(n_sets):
             s = sets[i]
             dg.conv2d_grad_input_pack_weight(s["w"], s["packed"], ws, p, code, stream)
@@ -442,7 +444,7 @@ def run_gpu(args, wl, key):
     torch.cuda.synchronize(dev)
     wall0 = time.time()
     with torch.cuda.stream(stream):
-        # Timed region 1: exactly K steps (pack + dgrad each).
+        # Timed region 1: exactly K steps (pack + dgrad, or dgrad alone, each).
         ev[0].record(stream)
         for _ in range(reps):
             step_graph.replay()
@@ -585,7 +587,7 @@ def run_gpu(args, wl, key):
             # The forward convolution of the bench layer (stride 1 only).
             if wl.stride == 1:
                 f_ms = forward_call(dg, workloads, wl, dev, stream)
-                out["forward"] = {"op": "conv2d_forward (weight flip + pack + kernel)",
+                out["forward"] = {"op": "conv2d_forward (weight flip + kernel, pack in the kernel or before it)",
                                   "workload": wl.name, "ms_per_call": f_ms,
                                   "tflops": useful_flops(wl) / (f_ms * 1e-3) / 1e12}
         if world == 1 and not args.no_cpu_baseline:

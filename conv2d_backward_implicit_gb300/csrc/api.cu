@@ -71,7 +71,7 @@ int conv2d_grad_input(const void *grad_out, const void *weight, float *grad_in,
             return cuda_status(le);
         }
     }
-    rc = run_main(plan, grad_out, ws, grad_in, st);
+    rc = run_main(plan, grad_out, ws ? ws : weight, grad_in, st);  // no workspace: the kernel packs
     if (ws) {
         cudaError_t e = cudaFreeAsync(ws, st);
         if (rc == DGRAD_OK && e != cudaSuccess) rc = cuda_status((int)e);
@@ -119,8 +119,8 @@ int conv2d_forward(const void *x, const void *weight, float *out, const conv2d_g
                                           (int)p->kernel_h, (int)p->kernel_w, plan.esize, st);
     if (le == (int)cudaSuccess && plan.kernel == DGRAD_KERNEL_TC && plan.workspace > 0)
         le = dgrad::launch_pack(plan, ws, packed, st);
-    rc = le == (int)cudaSuccess ? run_main(plan, x, plan.kernel == DGRAD_KERNEL_TC ? packed : ws, out, st)
-                                : cuda_status(le);
+    const bool prepacked = plan.kernel == DGRAD_KERNEL_TC && plan.workspace > 0;
+    rc = le == (int)cudaSuccess ? run_main(plan, x, prepacked ? packed : ws, out, st) : cuda_status(le);
     e = cudaFreeAsync(ws, st);
     if (rc == DGRAD_OK && e != cudaSuccess) rc = cuda_status((int)e);
     return rc;
@@ -154,10 +154,9 @@ int conv2d_grad_input_prepacked(const void *grad_out, const void *packed, float 
     dgrad::Plan plan;
     int rc = plan_for(p, dtype, &plan);
     if (rc != DGRAD_OK) return rc;
-    if (!packed && (plan.kernel == DGRAD_KERNEL_SIMT || plan.workspace > 0))
-        return DGRAD_ERR_INVALID_ARG;
-    const uintptr_t pa = plan.kernel == DGRAD_KERNEL_TC ? 16 : (uintptr_t)plan.esize;
-    if (!aligned(grad_out, plan.esize) || !aligned(grad_in, 4) || (packed && !aligned(packed, pa)))
+    if (!packed) return DGRAD_ERR_INVALID_ARG;  // packed weights, or the weights themselves
+    const uintptr_t pa = plan.workspace > 0 ? 16 : (uintptr_t)plan.esize;
+    if (!aligned(grad_out, plan.esize) || !aligned(grad_in, 4) || !aligned(packed, pa))
         return DGRAD_ERR_ALIGNMENT;
     return run_main(plan, grad_out, packed, grad_in, reinterpret_cast<cudaStream_t>(stream));
 }

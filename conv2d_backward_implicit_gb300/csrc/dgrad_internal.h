@@ -184,6 +184,11 @@ struct TcParams {
     int tile_group;
     int pair_rw;
     int acc_single;         // 1: one TMEM accumulator buffer (the epilogue does not overlap the MMA)
+    // 1: `packed` is the weight tensor itself ([Co][Ci][kH][kW], 16-bit, one
+    // stride-1 phase, resident weights): the epilogue warps build the packed
+    // image in shared memory while the first grad_out tile loads, so no pack
+    // kernel runs before the launch.
+    int w_raw;
     PhaseDesc ph[kMaxPhases];
 };
 
@@ -215,7 +220,7 @@ struct Plan {
                          // used when tc needs TMA (gather or store) that the pointers rule out
     PackParams pack;     // valid when kernel == TC
     SimtParams simt;
-    size_t workspace;    // packed-weight bytes (TC), 0 otherwise
+    size_t workspace;    // packed-weight bytes (TC without w_raw), 0 otherwise
 };
 
 // plan.cu: validation + planning.  Returns a dgrad_status.

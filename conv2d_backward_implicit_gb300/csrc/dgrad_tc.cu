@@ -706,8 +706,10 @@ __device__ __noinline__ void prefetch_raw_slice(const TcParams &p, int u_first, 
                          (uint32_t)((r1 - r0) * row_bytes));
 }
 
-// Bulk copies of the resident packed weights, completing on w_full.
+// Bulk copies of the resident packed weights, completing on w_full (none
+// when the epilogue warps pack them: w_raw).
 __device__ void issue_weights(const TcParams &p, Shared &sh, uint32_t w_base) {
+    if (p.w_raw) return;
     const uint8_t *src = static_cast<const uint8_t *>(p.packed);
     const uint32_t bar = smem_u32(&sh.w_full);
     mbar_arrive_expect_tx(bar, (uint32_t)p.packed_bytes);
@@ -715,6 +717,118 @@ __device__ void issue_weights(const TcParams &p, Shared &sh, uint32_t w_base) {
         const int64_t left = p.packed_bytes - off;
         bulk_g2s(w_base + (uint32_t)off, src + off, (uint32_t)(left < 32768 ? left : 32768), bar);
     }
+}
+
+// Resident weights packed in the kernel (w_raw: p.packed is the weight tensor
+// [Co][Ci][kH][kW], 16-bit, one stride-1 phase, so tap (j, i) is (kh, kw)).
+// Threads tid < nt write the packed image that issue_weights would copy:
+// per (Ci tile mt, channel chunk cc, tap j, tap i) m_tile rows ci of 128
+// bytes (64 consecutive co), 16-byte chunk c of row r at chunk slot c ^ (r & 7),
+// zero for ci >= Ci and co >= Co.  With 16-byte aligned weight rows each item
+// is 8 co rows x one 16-byte column of the [Co][Ci*kH*kW] matrix: eight vector
+// loads, an 8x8 transpose of 16-bit values in registers, and eight 16-byte
+// stores, one per (ci, tap) of the column.  Otherwise every 16-byte chunk of
+// the image takes eight scalar loads.  The writes are made visible to the
+// tensor core (async proxy) before each warp's arrival on w_full.
+__device__ void pack_resident_weights(const TcParams &p, Shared &sh, uint32_t w_base, int tid,
+                                      int nt) {
+    const uint16_t *w = static_cast<const uint16_t *>(p.packed);
+    const PhaseDesc &d = p.ph[0];
+    const int Ci = p.Ci, Co = p.Co, KK = d.Jh * d.Jw, kW = d.Jw;
+    const int64_t row_elems = (int64_t)Ci * KK;  // elements per co row of the weight tensor
+    const uint32_t base = w_base + (uint32_t)d.pack_off;
+    // Byte offset of 16-byte chunk `chunk` (64 co per chunk row) of (ci, tap, cc).
+    auto slot_off = [&](int ci, int t, int cc, int chunk) -> uint32_t {
+        const int mt = ci / p.m_tile, row = ci - mt * p.m_tile;
+        const int64_t r = (((int64_t)(mt * p.n_cchunks + cc) * KK + t) * p.m_tile + row);
+        return (uint32_t)(r * 128 + ((chunk ^ (row & 7)) << 4));
+    };
+    const bool vec = (reinterpret_cast<uintptr_t>(w) & 15u) == 0 && row_elems % 8 == 0;
+    if (vec) {
+        const int cols = (int)(row_elems / 8);  // 16-byte columns per co row
+        const int total = p.n_cchunks * 8 * cols;  // co groups of 8 (whole chunks) x columns
+        const int mshift = p.m_tile == 128 ? 7 : 6;
+        auto load = [&](uint4 (&v)[8], int it) {
+            const int g8 = it / cols, c = it - g8 * cols;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int co = g8 * 8 + e;
+                v[e] = co < Co ? __ldg(reinterpret_cast<const uint4 *>(w + (int64_t)co * row_elems) + c)
+                               : make_uint4(0u, 0u, 0u, 0u);
+            }
+        };
+        // Items dealt round-robin; the next item's loads are in flight while
+        // this one is transposed and stored.
+        uint4 cur[8];
+        if (tid < total) load(cur, tid);
+        for (int it = tid; it < total; it += nt) {
+            uint4 nxt[8];
+            if (it + nt < total) load(nxt, it + nt);
+            const int g8 = it / cols, c = it - g8 * cols;
+            const int cc = g8 >> 3, chunk = g8 & 7;
+            int ci = (c * 8) / KK, t = c * 8 - ci * KK;  // (ci, tap) of element 0 of the column
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                // Element k of each co row: the halves of word k / 2.
+                const uint32_t sel = (k & 1) ? 0x7632u : 0x5410u;
+                auto word = [&](const uint4 &u) -> uint32_t {
+                    const int q = k >> 1;
+                    return q == 0 ? u.x : q == 1 ? u.y : q == 2 ? u.z : u.w;
+                };
+                const uint32_t o0 = __byte_perm(word(cur[0]), word(cur[1]), sel);
+                const uint32_t o1 = __byte_perm(word(cur[2]), word(cur[3]), sel);
+                const uint32_t o2 = __byte_perm(word(cur[4]), word(cur[5]), sel);
+                const uint32_t o3 = __byte_perm(word(cur[6]), word(cur[7]), sel);
+                const int mt = ci >> mshift, row = ci & (p.m_tile - 1);
+                const uint32_t r = (uint32_t)(((mt * p.n_cchunks + cc) * KK + t) * p.m_tile + row);
+                st_shared_v4(base + r * 128u + (uint32_t)((chunk ^ (row & 7)) << 4), o0, o1, o2, o3);
+                if (++t == KK) {
+                    t = 0;
+                    ++ci;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) cur[e] = nxt[e];
+        }
+        // Rows of the last Ci tile past Ci: zero.
+        const int pad0 = Ci, pad1 = p.n_mtiles * p.m_tile;
+        const int per_row = p.n_cchunks * KK * 8;  // 16-byte chunks of one ci over (cc, tap)
+        for (int it = tid; it < (pad1 - pad0) * per_row; it += nt) {
+            const int ci = pad0 + it / per_row;
+            int r = it % per_row;
+            const int chunk = r & 7;
+            r >>= 3;
+            const int t = r % KK, cc = r / KK;
+            st_shared_v4(base + slot_off(ci, t, cc, chunk), 0u, 0u, 0u, 0u);
+        }
+    } else {
+        const int64_t chunks = p.packed_bytes / 16;
+        for (int64_t it = tid; it < chunks; it += nt) {
+            int64_t r = it;
+            const int slot = (int)(r & 7); r >>= 3;
+            const int row = (int)(r % p.m_tile); r /= p.m_tile;
+            const int t = (int)(r % KK); r /= KK;
+            const int cc = (int)(r % p.n_cchunks);
+            const int mt = (int)(r / p.n_cchunks);
+            const int ci = mt * p.m_tile + row, chunk = slot ^ (row & 7);
+            const int kh = t / kW, kw = t - kh * kW;
+            uint32_t o[4];
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+                uint32_t lo = 0, hi = 0;
+                const int co = cc * 64 + chunk * 8 + 2 * e2;
+                if (ci < Ci && co < Co)
+                    lo = w[(((int64_t)co * Ci + ci) * d.Jh + kh) * kW + kw];
+                if (ci < Ci && co + 1 < Co)
+                    hi = w[(((int64_t)(co + 1) * Ci + ci) * d.Jh + kh) * kW + kw];
+                o[e2] = lo | (hi << 16);
+            }
+            st_shared_v4(base + (uint32_t)(it * 16), o[0], o[1], o[2], o[3]);
+        }
+    }
+    fence_proxy_async();
+    __syncwarp();
+    if ((tid & 31) == 0) mbar_arrive(smem_u32(&sh.w_full));
 }
 
 // L2 prefetch of every raw slice of tile t (if it exists): the ring's TMA
@@ -2268,7 +2382,7 @@ __global__ void __launch_bounds__(Roles<V>::threads, 1)
         }
         for (int s = 0; s < kMaxEarly; ++s) mbar_init(smem_u32(&sh.full_early[s]), 1);
         mbar_init(smem_u32(&sh.early_free), R::g_warps);
-        mbar_init(smem_u32(&sh.w_full), 1);
+        mbar_init(smem_u32(&sh.w_full), p.w_raw ? R::epi_warps : 1);
         mbar_init(smem_u32(&sh.mma_done), 1);
         sh.abort_flag = 0;
         fence_barrier_init();
@@ -2321,6 +2435,9 @@ __global__ void __launch_bounds__(Roles<V>::threads, 1)
         else
             role_gather<ESIZE, R::g_warps>(p, sh, g_base, warp - R::g_warp0, lane);
     } else {
+        if constexpr (ESIZE == 2 && (V == kVarGeneral || V == kVarFrame64)) {
+            if (p.w_raw) pack_resident_weights(p, sh, w_base, (int)threadIdx.x, R::epi_warps * 32);
+        }
         if constexpr (PM)
             epilogue_pm(p, sh, epi_stage, tmem, warp, lane);
         else

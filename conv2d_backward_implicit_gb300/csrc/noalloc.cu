@@ -7,8 +7,8 @@
 // cudaMalloc/cudaMallocAsync on their execution path, and latency-critical
 // loops where an allocation's implicit synchronisation is not acceptable.
 // This entry point serves them: it keeps the packed weights (the only scratch
-// the tensor-core path needs) in a fixed, file-scope device array instead of a
-// stream-ordered allocation.  The caller still owns and passes grad_out,
+// the tensor-core path needs, unless its kernel packs the weights itself) in a
+// fixed, file-scope device array instead of a stream-ordered allocation.  The caller still owns and passes grad_out,
 // weight and grad_in.
 //
 // Costs and rules:
@@ -86,5 +86,6 @@ extern "C" int conv2d_grad_input_noalloc(const void *grad_out, const void *weigh
         e = dgrad::launch_pack(plan, weight, scratch, st);
         if (e != (int)cudaSuccess) return cuda_status(e);
     }
-    return cuda_status(dgrad::launch_tc(plan, grad_out, scratch, grad_in, st));
+    // No workspace: the kernel packs the weights itself from the weight tensor.
+    return cuda_status(dgrad::launch_tc(plan, grad_out, scratch ? scratch : weight, grad_in, st));
 }

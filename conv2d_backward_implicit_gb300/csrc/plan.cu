@@ -760,8 +760,13 @@ int make_plan(const void *params_v, int dtype, int forced_kernel, Plan *plan) {
         TcParams v;
         if (forced_kernel == DGRAD_KERNEL_TC_POSM && plan_pm(p, plan->esize, plan->tc_alt, &v))
             plan->tc = v;
-        else if (plan_frame64(p, plan->esize, plan->tc_alt, &v))
+        else if (plan_frame64(p, plan->esize, plan->tc_alt, &v)) {
             plan->tc = v;
+            // One stride-1 phase with resident weights (the general plan's
+            // too): the kernel packs them from the weight tensor itself.
+            plan->tc.w_raw = plan->tc_alt.w_raw = 1;
+            plan->workspace = 0;
+        }
         else if (plan_mn(p, plan->esize, plan->tc_alt, &v))
             plan->tc = v;
         return DGRAD_OK;

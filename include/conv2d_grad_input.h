@@ -102,15 +102,19 @@ typedef enum dgrad_kernel {
 
 /* The whole operation: packs the weights into a stream-ordered temporary
  * buffer (cudaMallocAsync / cudaFreeAsync on `stream`) and runs the dgrad
- * kernel.  grad_out and weight are read, grad_in is overwritten. */
+ * kernel; when conv2d_grad_input_workspace_size is 0 the kernel reads the
+ * weights as they are (one launch, no allocation).  grad_out and weight are
+ * read, grad_in is overwritten. */
 int conv2d_grad_input(const void *grad_out, const void *weight, float *grad_in,
                       const conv2d_grad_input_params *p, int dtype, struct CUstream_st *stream);
 
 /* Bytes of the packed-weight buffer that conv2d_grad_input_pack_weight
  * writes and conv2d_grad_input_prepacked reads for these params and dtype,
  * for the kernel that the current selection would run.  0 when the
- * selected kernel reads the weights unpacked (the CUDA-core kernel) or when
- * the arguments are invalid. */
+ * selected kernel reads the weights unpacked -- the CUDA-core kernel, and the
+ * tensor-core kernel on 16-bit stride-1 layers whose packed weights stay
+ * resident in shared memory (its epilogue warps pack them there while the
+ * first grad_out tile loads) -- or when the arguments are invalid. */
 size_t conv2d_grad_input_workspace_size(const conv2d_grad_input_params *p, int dtype);
 
 /* The weight pre-pack: transposes weight [Co,Ci,kH,kW] into per-phase,
@@ -119,15 +123,18 @@ size_t conv2d_grad_input_workspace_size(const conv2d_grad_input_params *p, int d
  * DGRAD_F32 rounds to TF32 (nearest, ties away from zero).  `packed` is a
  * device buffer of at least packed_bytes >= conv2d_grad_input_workspace_size
  * bytes, 16-byte aligned.  A pack depends only on weight, p and dtype, so it
- * can be reused across calls with the same weights. */
+ * can be reused across calls with the same weights.  When
+ * conv2d_grad_input_workspace_size is 0 there is nothing to pack: the call
+ * returns DGRAD_OK and launches nothing. */
 int conv2d_grad_input_pack_weight(const void *weight, void *packed, size_t packed_bytes,
                                   const conv2d_grad_input_params *p, int dtype,
                                   struct CUstream_st *stream);
 
 /* The dgrad kernel alone, reading weights packed by
  * conv2d_grad_input_pack_weight with the same p and dtype (and the same
- * kernel selection).  When the CUDA-core kernel is selected, `packed` must be
- * the original weight tensor instead. */
+ * kernel selection).  When conv2d_grad_input_workspace_size is 0 (the
+ * CUDA-core kernel, or a kernel that packs in shared memory), `packed` must be
+ * the original weight tensor instead, aligned to its element size. */
 int conv2d_grad_input_prepacked(const void *grad_out, const void *packed, float *grad_in,
                                 const conv2d_grad_input_params *p, int dtype,
                                 struct CUstream_st *stream);

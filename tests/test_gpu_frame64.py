@@ -5,7 +5,10 @@ W a multiple of 4) -- ragged row tiles, channel counts that are not multiples
 of 16, one and two 128-row input-channel tiles, several 64-channel grad_out
 chunks, 1x1 to 3x3 kernels, paddings 0..2 -- and the
 fallback to the Wr + Jw - 1 frame when grad_out or grad_in is not 16-byte
-aligned.  Bar: max|gpu - oracle| / max|oracle| <= 2e-3."""
+aligned.  The kernel packs these layers' weights in shared memory itself
+(workspace size 0): with 16-byte vector loads when the weight rows allow it,
+else with scalar loads, and both give the same bits.
+Bar: max|gpu - oracle| / max|oracle| <= 2e-3."""
 import numpy as np
 import pytest
 import torch
@@ -42,16 +45,19 @@ def case(shape, dtype):
                               "uniform")
 
 
-def run(dg, wl, g, w, g_offset=0, out_offset=0):
+def run(dg, wl, g, w, g_offset=0, out_offset=0, w_offset=0):
     dev = torch.device("cuda")
     flat = torch.zeros(g.numel() + g_offset, dtype=g.dtype, device=dev)
     flat[g_offset:] = g.reshape(-1).to(dev)
     gd = flat[g_offset:].view(g.shape)
+    wflat = torch.zeros(w.numel() + w_offset, dtype=w.dtype, device=dev)
+    wflat[w_offset:] = w.reshape(-1).to(dev)
+    wd = wflat[w_offset:].view(w.shape)
     n_out = int(np.prod(wl.grad_in_shape))
     oflat = torch.full((n_out + out_offset,), float("nan"), device=dev)
     out = oflat[out_offset:].view(wl.grad_in_shape)
     p = dg.params_from_shapes(g.shape, w.shape, wl.H, wl.W, wl.stride, wl.padding_h, wl.padding_w)
-    dg.conv2d_grad_input(gd, w.to(dev), out, p, dg.DTYPE_CODE[wl.dtype])
+    dg.conv2d_grad_input(gd, wd, out, p, dg.DTYPE_CODE[wl.dtype])
     rc = dg.conv2d_grad_input_check_errors()
     assert rc == 0, dg.conv2d_grad_input_status_string(rc)
     return out
@@ -96,3 +102,46 @@ def test_pointer_alignment_fallback(dg, g_offset, out_offset):
     g, w = workloads.make_inputs(wl, seed=3)
     out = run(dg, wl, g, w, g_offset=g_offset, out_offset=out_offset)
     assert rel_err(out.cpu().numpy(), oracle_of(wl, g, w)) <= TOL
+
+
+@pytest.mark.parametrize("name", ["resnet_rows_ragged", "channels_not_16", "pointwise_two_m_tiles"])
+def test_in_kernel_pack_vector_and_scalar_loads_agree(dg, name):
+    # A weight pointer 16 bytes past a boundary keeps the vector loads; 2 bytes
+    # past one takes the scalar loads.  Both write the same packed image, so
+    # grad_in matches bit for bit (and the oracle within the bar).
+    wl = case(SHAPES[name], "bf16")
+    g, w = workloads.make_inputs(wl, seed=7)
+    p = dg.params_from_shapes(g.shape, w.shape, wl.H, wl.W, wl.stride, wl.padding_h, wl.padding_w)
+    assert dg.conv2d_grad_input_workspace_size(p, dg.DGRAD_BF16) == 0
+    ref = run(dg, wl, g, w).cpu().numpy()
+    assert rel_err(ref, oracle_of(wl, g, w)) <= TOL
+    for w_offset in (8, 1):
+        out = run(dg, wl, g, w, w_offset=w_offset).cpu().numpy()
+        assert np.array_equal(out, ref), (name, w_offset)
+
+
+def test_in_kernel_pack_with_the_alignment_fallback(dg):
+    # grad_out off a 16-byte boundary: the general plan on the Wr + Jw - 1 frame
+    # runs, and it too packs the weights in the kernel (scalar loads here).
+    wl = case((2, 64, 9, 16, 64, 3, 3, 1, 1, 1), "f16")
+    g, w = workloads.make_inputs(wl, seed=9)
+    out = run(dg, wl, g, w, g_offset=1, w_offset=3)
+    assert rel_err(out.cpu().numpy(), oracle_of(wl, g, w)) <= TOL
+
+
+def test_prepacked_takes_the_weights_when_nothing_is_packed(dg):
+    wl = case(SHAPES["resnet_rows_ragged"], "bf16")
+    g, w = workloads.make_inputs(wl, seed=11)
+    dev = torch.device("cuda")
+    p = dg.params_from_shapes(g.shape, w.shape, wl.H, wl.W, wl.stride, wl.padding_h, wl.padding_w)
+    assert dg.conv2d_grad_input_workspace_size(p, dg.DGRAD_BF16) == 0
+    gd, wd = g.to(dev), w.to(dev)
+    buf = torch.full((64,), 7, dtype=torch.uint8, device=dev)
+    dg.conv2d_grad_input_pack_weight(wd, buf, 0, p, dg.DGRAD_BF16)  # nothing to pack
+    out = torch.full(wl.grad_in_shape, float("nan"), device=dev)
+    dg.conv2d_grad_input_prepacked(gd, wd, out, p, dg.DGRAD_BF16)
+    assert dg.conv2d_grad_input_check_errors() == 0
+    torch.cuda.synchronize()
+    assert torch.all(buf == 7)
+    ref = run(dg, wl, g, w)
+    assert torch.equal(out, ref)

@@ -74,9 +74,12 @@ def run(dg, wl, g, w, via="call", g_offset=0):
         dg.conv2d_grad_input(gd, wd, out, p, code)
     else:
         ws = dg.conv2d_grad_input_workspace_size(p, code)
-        packed = torch.empty(ws, dtype=torch.uint8, device=dev)
-        dg.conv2d_grad_input_pack_weight(wd, packed, ws, p, code)
-        dg.conv2d_grad_input_prepacked(gd, packed, out, p, code)
+        if ws:
+            packed = torch.empty(ws, dtype=torch.uint8, device=dev)
+            dg.conv2d_grad_input_pack_weight(wd, packed, ws, p, code)
+            dg.conv2d_grad_input_prepacked(gd, packed, out, p, code)
+        else:  # the kernel packs the weights itself
+            dg.conv2d_grad_input_prepacked(gd, wd, out, p, code)
     rc = dg.conv2d_grad_input_check_errors()
     assert rc == 0, dg.conv2d_grad_input_status_string(rc)
     return out
