@@ -758,12 +758,17 @@ __device__ void pack_resident_weights(const TcParams &p, Shared &sh, uint32_t w_
             }
         };
         // Items dealt round-robin; the next item's loads are in flight while
-        // this one is transposed and stored.
+        // this one is transposed and stored.  Each CTA starts at its own
+        // offset (the item order rotated by the CTA index), so the CTAs' first
+        // reads of the usually cold weights ask for different lines.
+        const int rot = (int)(((int64_t)blockIdx.x * total) / gridDim.x);
+        auto item = [&](int i) { return i + rot < total ? i + rot : i + rot - total; };
         uint4 cur[8];
-        if (tid < total) load(cur, tid);
-        for (int it = tid; it < total; it += nt) {
+        if (tid < total) load(cur, item(tid));
+        for (int i = tid; i < total; i += nt) {
             uint4 nxt[8];
-            if (it + nt < total) load(nxt, it + nt);
+            if (i + nt < total) load(nxt, item(i + nt));
+            const int it = item(i);
             const int g8 = it / cols, c = it - g8 * cols;
             const int cc = g8 >> 3, chunk = g8 & 7;
             int ci = (c * 8) / KK, t = c * 8 - ci * KK;  // (ci, tap) of element 0 of the column
