@@ -769,6 +769,12 @@ int make_plan(const void *params_v, int dtype, int forced_kernel, Plan *plan) {
         }
         else if (plan_mn(p, plan->esize, plan->tc_alt, &v))
             plan->tc = v;
+        else if (plan->esize == 2 && p.stride == 1 && plan->tc.nw == 0 && !plan->tc.pos_m) {
+            // General mode, one stride-1 phase, resident weights: packed in
+            // the kernel as on the 64-wide frame.
+            plan->tc.w_raw = plan->tc_alt.w_raw = 1;
+            plan->workspace = 0;
+        }
         return DGRAD_OK;
     }
     if (forced_kernel == DGRAD_KERNEL_TC || forced_kernel == DGRAD_KERNEL_TC_POSM)
