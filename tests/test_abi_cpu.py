@@ -146,3 +146,29 @@ def test_forward_rejects_what_it_does_not_run(lib):
     p = dg.Params(2, 16, 10, 10, 24, 3, 3, 1, 1, 9, 10, 1)
     assert lib.conv2d_forward(16, 16, 16, ctypes.byref(p), dg.DGRAD_BF16, None) == 2
     assert lib.conv2d_forward(None, 16, 16, ctypes.byref(p), dg.DGRAD_BF16, None) == 1
+
+
+def test_in_kernel_weight_pack_selection(lib):
+    # The kernel packs the weights itself (workspace 0) exactly for 16-bit
+    # stride-1 tensor-core plans whose packed weights stay resident in shared
+    # memory; fp32 (TF32 rounding), strided layers and streamed weights keep
+    # the pack kernel and its workspace.
+    def params_of(shape):
+        N, Ci, H, W, Co, kH, kW, s, ph, pw = shape
+        oh, ow = (H + 2 * ph - kH) // s + 1, (W + 2 * pw - kW) // s + 1
+        return dg.Params(N, Ci, H, W, Co, kH, kW, s, ph, oh, ow, pw)
+
+    def ws(shape, code):
+        return dg.conv2d_grad_input_workspace_size(params_of(shape), code)
+    packed_in_kernel = [(32, 64, 56, 56, 64, 3, 3, 1, 1, 1),   # the ResNet layer (64-wide frame)
+                        (3, 40, 13, 17, 33, 3, 3, 1, 1, 1),     # odd width: the general frame
+                        (2, 6, 3, 3, 5, 3, 3, 1, 0, 0)]
+    for shape in packed_in_kernel:
+        for code in (dg.DGRAD_BF16, dg.DGRAD_F16):
+            assert dg.conv2d_grad_input_select_kernel(params_of(shape), code) == dg.DGRAD_KERNEL_TC
+            assert ws(shape, code) == 0, shape
+        assert ws(shape, dg.DGRAD_F32) > 0, shape
+    assert ws((32, 128, 56, 56, 256, 3, 3, 2, 1, 1), dg.DGRAD_BF16) > 0      # stride 2
+    for streamed in [(1, 1024, 8, 8, 1024, 3, 3, 1, 1, 1), (1, 8, 4, 300, 16, 3, 3, 1, 1, 1),
+                     (1, 64, 28, 112, 64, 3, 3, 1, 1, 1), (1, 16, 20, 20, 16, 7, 7, 1, 3, 3)]:
+        assert ws(streamed, dg.DGRAD_BF16) > 0, streamed                     # streamed weights
