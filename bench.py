@@ -28,6 +28,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -69,11 +70,19 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_of(source: str) -> str:
+    """The source without comments and blank lines: edits to comments alone
+    leave the compiled kernel, and so its fingerprint, unchanged."""
+    source = re.sub(r"/\*.*?\*/", "", source, flags=re.S)
+    lines = (re.sub(r"//.*", "", ln).rstrip() for ln in source.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_fingerprint() -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(code_of(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -874,9 +874,10 @@ __device__ __forceinline__ void issue_raw(const TcParams &p, uint32_t dst, int u
 // TMA gather producer (warp 9, lane 0): for every tile and channel chunk of
 // this CTA, the raw grad_out slices of the tile's window -- raw_cs channels x
 // raw_br rows x raw_bw columns from column raw_x0 -- into the raw ring.  Rows
-// and columns outside grad_out are zero-filled by the TMA unit.  The first
-// tile's slices go out first, then the resident weights, then slices into the
-// remaining free slots.  Once those are all queued and the first tile's last
+// and columns outside grad_out are zero-filled by the TMA unit.  The resident
+// weights go out first (bulk copies; none when the epilogue warps pack them in
+// shared memory), then the first tile's slices, then slices into the remaining
+// free slots.  Once those are all queued and the first tile's last
 // slice has landed (earlier, prefetches would compete with it for DRAM), the
 // L2 prefetch starts: general mode (a ring shorter than a tile) the next
 // kRawLookahead tiles, then each later tile the one kRawLookahead after it;
@@ -907,7 +908,8 @@ __device__ void raw_producer(const TcParams &p, Shared &sh, uint32_t raw_base, u
             for (int sl = 0; sl < slices; ++sl) {
                 // The weights first: every CTA reads the same packed weights,
                 // so they mostly come from L2 while the first slices' DRAM reads
-                // are in flight.
+                // are in flight (issue_weights does nothing when the epilogue
+                // warps pack them: w_raw).
                 if (!weights_issued) {
                     if (!waited) {
                         grid_dependency_wait();

@@ -172,3 +172,11 @@ def test_in_kernel_weight_pack_selection(lib):
     for streamed in [(1, 1024, 8, 8, 1024, 3, 3, 1, 1, 1), (1, 8, 4, 300, 16, 3, 3, 1, 1, 1),
                      (1, 64, 28, 112, 64, 3, 3, 1, 1, 1), (1, 16, 20, 20, 16, 7, 7, 1, 3, 3)]:
         assert ws(streamed, dg.DGRAD_BF16) > 0, streamed                     # streamed weights
+
+
+def test_kernel_fingerprint_ignores_comments():
+    import bench
+    code = "int a; // note\n/* block\n comment */\nint b;  \n\n"
+    assert bench.code_of(code) == "int a;\nint b;"
+    assert bench.code_of(code) == bench.code_of(code.replace("note", "other note"))
+    assert bench.code_of(code) != bench.code_of(code.replace("int b", "int c"))
