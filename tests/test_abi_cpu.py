@@ -180,3 +180,27 @@ def test_kernel_fingerprint_ignores_comments():
     assert bench.code_of(code) == "int a;\nint b;"
     assert bench.code_of(code) == bench.code_of(code.replace("note", "other note"))
     assert bench.code_of(code) != bench.code_of(code.replace("int b", "int c"))
+
+
+def test_planner_accepts_every_valid_shape(lib):
+    # Host-side planning over a random sweep of valid layers (strides 1-6,
+    # kernels 1-7, paddings up to past the kernel, channels 1-300, all three
+    # dtypes): every call plans a kernel -- tensor-core, or the CUDA-core
+    # fallback -- never an error, and only tensor-core plans can ask for a
+    # workspace.
+    import random
+    rng = random.Random(20240611)
+    for _ in range(1500):
+        s = rng.choice([1, 1, 2, 2, 3, 4, 5, 6])
+        kH, kW = rng.randint(1, 7), rng.randint(1, 7)
+        ph, pw = rng.randint(0, kH), rng.randint(0, kW)
+        H = rng.randint(max(1, kH - 2 * ph), 80)
+        W = rng.randint(max(1, kW - 2 * pw), 80)
+        N, Ci, Co = rng.randint(1, 4), rng.randint(1, 300), rng.randint(1, 300)
+        oh, ow = (H + 2 * ph - kH) // s + 1, (W + 2 * pw - kW) // s + 1
+        p = dg.Params(N, Ci, H, W, Co, kH, kW, s, ph, oh, ow, pw)
+        for code in (dg.DGRAD_F32, dg.DGRAD_BF16, dg.DGRAD_F16):
+            k = dg.conv2d_grad_input_select_kernel(p, code)
+            assert k in (dg.DGRAD_KERNEL_TC, dg.DGRAD_KERNEL_SIMT), (p, code, k)
+            if k == dg.DGRAD_KERNEL_SIMT:
+                assert dg.conv2d_grad_input_workspace_size(p, code) == 0
