@@ -101,12 +101,30 @@ def library() -> ctypes.CDLL:
     return _lib
 
 
-def _addr(x) -> int | None:
+_TORCH_DTYPE_NAME = {DGRAD_F32: "float32", DGRAD_BF16: "bfloat16", DGRAD_F16: "float16"}
+
+
+def _addr(x, name: str = "buffer", dtype: str | None = None) -> int | None:
+    """Device address of a buffer argument.  Integers pass through unchecked;
+    a tensor must live on a CUDA device, be contiguous (the C ABI reads dense
+    NCHW / [Co,Ci,kH,kW] memory) and, when ``dtype`` is given, have that
+    element type -- checked here, on the host, before the library is called."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
+    dev = getattr(x, "device", None)
+    if dev is not None and getattr(dev, "type", "cuda") != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (got one on {dev})")
+    if hasattr(x, "is_contiguous") and not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and hasattr(x, "dtype") and str(x.dtype).replace("torch.", "") != dtype:
+        raise ValueError(f"{name} must be {dtype} (got {x.dtype})")
     return x.data_ptr()
+
+
+def _in_dtype(code: int) -> str | None:
+    return _TORCH_DTYPE_NAME.get(int(code))
 
 
 def _stream(stream) -> int | None:
@@ -124,7 +142,9 @@ def _check(rc: int, where: str) -> int:
 
 
 def conv2d_grad_input(grad_out, weight, grad_in, params: Params, dtype: int, stream=None) -> None:
-    rc = library().conv2d_grad_input(_addr(grad_out), _addr(weight), _addr(grad_in),
+    rc = library().conv2d_grad_input(_addr(grad_out, "grad_out", _in_dtype(dtype)),
+                                     _addr(weight, "weight", _in_dtype(dtype)),
+                                     _addr(grad_in, "grad_in", "float32"),
                                      ctypes.byref(params), int(dtype), _stream(stream))
     _check(rc, "conv2d_grad_input")
 
@@ -135,14 +155,17 @@ def conv2d_grad_input_workspace_size(params: Params, dtype: int) -> int:
 
 def conv2d_grad_input_pack_weight(weight, packed, packed_bytes: int, params: Params, dtype: int,
                                   stream=None) -> None:
-    rc = library().conv2d_grad_input_pack_weight(_addr(weight), _addr(packed), int(packed_bytes),
+    rc = library().conv2d_grad_input_pack_weight(_addr(weight, "weight", _in_dtype(dtype)),
+                                                 _addr(packed, "packed"), int(packed_bytes),
                                                  ctypes.byref(params), int(dtype), _stream(stream))
     _check(rc, "conv2d_grad_input_pack_weight")
 
 
 def conv2d_grad_input_prepacked(grad_out, packed, grad_in, params: Params, dtype: int,
                                 stream=None) -> None:
-    rc = library().conv2d_grad_input_prepacked(_addr(grad_out), _addr(packed), _addr(grad_in),
+    rc = library().conv2d_grad_input_prepacked(_addr(grad_out, "grad_out", _in_dtype(dtype)),
+                                               _addr(packed, "packed"),
+                                               _addr(grad_in, "grad_in", "float32"),
                                                ctypes.byref(params), int(dtype), _stream(stream))
     _check(rc, "conv2d_grad_input_prepacked")
 
@@ -182,7 +205,9 @@ def conv2d_grad_input_noalloc(grad_out, weight, grad_in, params: Params, dtype: 
     ordered by the caller, and problems whose packed weights exceed 8 MiB
     raise DgradError(DGRAD_ERR_WORKSPACE).
     """
-    rc = library().conv2d_grad_input_noalloc(_addr(grad_out), _addr(weight), _addr(grad_in),
+    rc = library().conv2d_grad_input_noalloc(_addr(grad_out, "grad_out", _in_dtype(dtype)),
+                                             _addr(weight, "weight", _in_dtype(dtype)),
+                                             _addr(grad_in, "grad_in", "float32"),
                                              ctypes.byref(params), int(dtype), _stream(stream))
     _check(rc, "conv2d_grad_input_noalloc")
 
@@ -190,6 +215,7 @@ def conv2d_grad_input_noalloc(grad_out, weight, grad_in, params: Params, dtype: 
 def conv2d_forward(x, weight, out, params: Params, dtype: int, stream=None) -> None:
     """Forward convolution of the layer ``params`` describes (stride 1): x
     [N,Ci,H,W], weight [Co,Ci,kH,kW] -> out [N,Co,OH,OW] float32."""
-    rc = library().conv2d_forward(_addr(x), _addr(weight), _addr(out), ctypes.byref(params),
+    rc = library().conv2d_forward(_addr(x, "x", _in_dtype(dtype)), _addr(weight, "weight", _in_dtype(dtype)),
+                                  _addr(out, "out", "float32"), ctypes.byref(params),
                                   int(dtype), _stream(stream))
     _check(rc, "conv2d_forward")

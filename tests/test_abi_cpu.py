@@ -204,3 +204,40 @@ def test_planner_accepts_every_valid_shape(lib):
             assert k in (dg.DGRAD_KERNEL_TC, dg.DGRAD_KERNEL_SIMT), (p, code, k)
             if k == dg.DGRAD_KERNEL_SIMT:
                 assert dg.conv2d_grad_input_workspace_size(p, code) == 0
+
+
+class _FakeCudaTensor:
+    """Just enough of a tensor for the binding's host-side checks."""
+
+    def __init__(self, dtype="bfloat16", contiguous=True, device="cuda"):
+        self.dtype = f"torch.{dtype}"
+        self.device = type("Dev", (), {"type": device, "__str__": lambda s: device})()
+        self._contiguous = contiguous
+
+    def is_contiguous(self):
+        return self._contiguous
+
+    def data_ptr(self):
+        return 1 << 20
+
+
+def test_binding_checks_tensors_before_calling_the_library(lib):
+    import torch
+    p = params(workloads.RESNET)
+    good_g, good_w = _FakeCudaTensor(), _FakeCudaTensor()
+    out = _FakeCudaTensor("float32")
+    cases = [
+        (torch.zeros(4), good_w, out, "CUDA tensor"),                       # host memory
+        (_FakeCudaTensor(contiguous=False), good_w, out, "contiguous"),     # a strided view
+        (good_g, _FakeCudaTensor("float16"), out, "bfloat16"),              # dtype vs code
+        (good_g, good_w, _FakeCudaTensor("bfloat16"), "float32"),           # grad_in is fp32
+    ]
+    for g, w, o, msg in cases:
+        with pytest.raises(ValueError, match=msg):
+            dg.conv2d_grad_input(g, w, o, p, dg.DGRAD_BF16)
+        with pytest.raises(ValueError, match=msg):
+            dg.conv2d_grad_input_noalloc(g, w, o, p, dg.DGRAD_BF16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        dg.conv2d_grad_input_prepacked(good_g, torch.zeros(4), out, p, dg.DGRAD_BF16)
+    with pytest.raises(ValueError, match="float32"):
+        dg.conv2d_forward(good_g, good_w, _FakeCudaTensor("float16"), p, dg.DGRAD_BF16)
