@@ -89,13 +89,13 @@ typedef enum dgrad_status {
 
 typedef enum dgrad_kernel {
     DGRAD_KERNEL_AUTO = 0, /* tensor-core kernel where it applies, else the CUDA-core kernel */
-    DGRAD_KERNEL_TC = 1,   /* tcgen05 implicit GEMM (weights pre-packed) */
+    DGRAD_KERNEL_TC = 1,   /* tcgen05 implicit GEMM (weights pre-packed, or packed by the kernel itself) */
     DGRAD_KERNEL_SIMT = 2, /* direct CUDA-core kernel, one thread per grad_in element */
     /* tcgen05 implicit GEMM with the output positions on the MMA M side and
      * the kW taps of a kernel row side by side on N, for stride 1, bf16 or
      * fp16, in_channels and out_channels <= 64, kernel_w <= 3, in_w and
      * out_w <= 56 with 16-byte grad_out rows; other shapes run as
-     * DGRAD_KERNEL_TC.  Same packed weights as DGRAD_KERNEL_TC.  Opt-in:
+     * DGRAD_KERNEL_TC.  Weights pre-packed by conv2d_grad_input_pack_weight.  Opt-in:
      * its epilogue writes grad_in with plain stores from the epilogue warps. */
     DGRAD_KERNEL_TC_POSM = 3
 } dgrad_kernel;
@@ -191,7 +191,7 @@ int conv2d_grad_input_set_debug(int flags);
 int conv2d_forward(const void *x, const void *weight, float *out, const conv2d_grad_input_params *p,
                    int dtype, struct CUstream_st *stream);
 
-/* conv2d_grad_input without any device allocation.  The paper has no
+/* conv2d_grad_input without any device allocation.  The pages have no
  * counterpart to this entry point; it exists for callers that cannot
  * allocate device memory where they need the gradient -- code recorded into
  * a CUDA graph whose capture mode forbids allocation calls, runtimes whose
