@@ -17,9 +17,16 @@ synchronisation on both sides.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle (the
 only reference there is) on a bounded sample of the same workload instead.
-Multi-GPU (torchrun): every rank runs the full workload on its own GPU
-(weak scaling, no collective on the data path); value = all ranks' FLOPs / the
-slowest rank's time.
+Multi-GPU (torchrun): data parallel over the batch.  The global batch is
+N x world images; rank r takes its own shard of N of them (shard_bounds), a
+replica of the weights, and writes its own slice of grad_in -- no collective on
+the data path (weak scaling: per-rank work is fixed).  value = all ranks' FLOPs
+/ the slowest rank's time.
+
+``--profile-launches L`` only launches the dgrad kernel L times over the
+rotating buffer sets (for an ncu capture of per-launch DRAM traffic), and
+``--record-traffic CSV`` turns that capture's CSV into the workload's traffic
+record under profiles/.
 """
 from __future__ import annotations
 
@@ -97,6 +104,108 @@ def recorded_traffic(config_key: str):
     if d.get("kernel_fingerprint") != kernel_fingerprint():
         return None
     return d.get("dram_bytes_per_launch")
+
+
+def shard_bounds(global_n: int, world: int, rank: int):
+    """[lo, hi) of the global batch that `rank` processes: contiguous shards,
+    sizes differing by at most one, together covering [0, global_n) once."""
+    base, extra = divmod(global_n, world)
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
+
+
+def measure_tf32_peak(dev, n: int = 8192, reps: int = 10) -> float:
+    """Dense TF32 tensor-core rate (TFLOP/s): torch.matmul of float32 n x n
+    matrices with TF32 allowed, best of `reps` after a warm-up (the method of
+    the measured bf16 peak, for the dtype the fp32 workloads compute in)."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        a = torch.randn(n, n, device=dev)
+        b = torch.randn(n, n, device=dev)
+        c = torch.empty(n, n, device=dev)
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        torch.cuda.synchronize(dev)
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b, c
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+_UNIT = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "nsecond": 1e-9,
+         "usecond": 1e-6, "msecond": 1e-3, "second": 1.0}
+
+
+def traffic_from_ncu_csv(text: str, kernel_pattern: str = "dgrad_tc_kernel"):
+    """Per-launch DRAM bytes of the kernel from an ncu --csv log of the metrics
+    dram__bytes_read.sum, dram__bytes_write.sum and gpu__time_duration.sum:
+    [(launch id, kernel name, read bytes, write bytes, seconds)], in launch order."""
+    import csv
+    import io
+    lines = [ln for ln in text.splitlines() if ln.startswith('"')]
+    rows = list(csv.DictReader(io.StringIO("\n".join(lines))))
+    per = {}
+    for r in rows:
+        name = r.get("Kernel Name", "")
+        if kernel_pattern not in name:
+            continue
+        metric, unit = r.get("Metric Name", ""), r.get("Metric Unit", "").strip().lower()
+        try:
+            value = float(r.get("Metric Value", "").replace(",", ""))
+        except ValueError:
+            continue
+        value *= _UNIT.get(unit, 1.0)
+        key = int(r["ID"])
+        d = per.setdefault(key, {"name": name})
+        if metric == "dram__bytes_read.sum":
+            d["read"] = value
+        elif metric == "dram__bytes_write.sum":
+            d["write"] = value
+        elif metric == "gpu__time_duration.sum":
+            d["seconds"] = value
+    out = []
+    for key in sorted(per):
+        d = per[key]
+        if "read" in d and "write" in d:
+            out.append((key, d["name"], int(d["read"]), int(d["write"]), d.get("seconds")))
+    return out
+
+
+def traffic_record(launches, wl, key, command: str):
+    """The traffic record of a workload: DRAM bytes per launch averaged over
+    the captured launches after the first (steady state: a launch's grad_in
+    writes leave L2 during later launches, so the first one shows only reads)."""
+    steady = launches[1:] if len(launches) > 1 else launches
+    rd = sum(x[2] for x in steady) / len(steady)
+    wr = sum(x[3] for x in steady) / len(steady)
+    alg = algorithmic_bytes(wl)
+    return {
+        "kernel": launches[0][1].split("(")[0].replace("void ", "").strip(),
+        "workload": workload_config(wl, key, "")["workload"],
+        "kernel_fingerprint": kernel_fingerprint(),
+        "dram_bytes_per_launch": int(round(rd + wr)),
+        "dram_read_bytes": int(round(rd)),
+        "dram_write_bytes": int(round(wr)),
+        "algorithmic_bytes": alg,
+        "traffic_over_algorithmic": (rd + wr) / alg,
+        "launches_averaged": len(steady),
+        "per_launch": [{"id": x[0], "read": x[2], "write": x[3], "us": (x[4] or 0) * 1e6}
+                       for x in launches],
+        "note": "steady-state DRAM traffic per launch: ncu with --cache-control none over "
+                "back-to-back launches on rotating buffer sets, averaged over the launches "
+                "after the first (whose grad_in writes are still in L2 when it ends)",
+        "command": command,
+    }
 
 
 def reduce_max(value: float, dist_on: bool, device=None) -> float:
@@ -366,7 +475,13 @@ def run_gpu(args, wl, key):
         dist.init_process_group("nccl", device_id=dev)
     dg.library()
 
-    g_cpu, w_cpu = workloads.make_inputs(wl, seed=0)
+    # Data parallel over the batch: this rank's shard [lo, hi) of the global
+    # batch of N x world images (its own seeded grad_out), the same weights on
+    # every rank, its own grad_in slice; no exchange step.
+    lo, hi = shard_bounds(wl.N * world, world, rank)
+    assert hi - lo == wl.N
+    g_cpu, _ = workloads.make_inputs(wl, seed=rank)
+    _, w_cpu = workloads.make_inputs(wl, seed=0)
     p = dg.params_from_shapes(g_cpu.shape, w_cpu.shape, wl.H, wl.W, wl.stride, wl.padding_h,
                               wl.padding_w)
     code = dg.DTYPE_CODE[wl.dtype]
@@ -447,7 +562,8 @@ def run_gpu(args, wl, key):
     sampler.start()
     time.sleep(0.3)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    main_reps = max(1, reps // 2)
+    # The kernel-only region: at least 200 back-to-back launches whatever --steps is.
+    main_reps = max(1, math.ceil(200 / n_sets))
     if dist_on:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -543,8 +659,16 @@ def run_gpu(args, wl, key):
     peaks, peak_src = load_peaks()
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    # fp32 inputs run on TF32 tensor cores: nominal TF32 rate is half the bf16 rate.
-    tc_peak = bf16_peak / 2 if wl.dtype == "f32" else bf16_peak
+    # fp32 inputs run on TF32 tensor cores: their peak is a TF32 matmul timed here.
+    need_tf32 = wl.dtype == "f32" or (world == 1 and not args.no_per_config)
+    tf32_peak = measure_tf32_peak(dev) if need_tf32 else None
+    tf32_src = ("measured by bench.py on this GPU: torch.matmul float32 8192^3 with TF32 "
+                "allowed, best of 10")
+
+    def tc_peak_of(dtype):
+        return (tf32_peak, tf32_src) if dtype == "f32" else (bf16_peak, peak_src)
+
+    tc_peak, tc_src = tc_peak_of(wl.dtype)
     achieved_gbs = alg / (k_ms * 1e-3) / 1e9
     achieved_tflops = flops / (k_ms * 1e-3) / 1e12
     traffic = recorded_traffic(key)
@@ -557,20 +681,25 @@ def run_gpu(args, wl, key):
             "scaling": "weak", "vs_baseline": None,
             "dtype": {"bf16": "bf16", "f16": "f16", "f32": "tf32"}[wl.dtype] + " in, f32 accumulate/out",
             "data": "synthetic (seeded torch.Generator, recipe of the workload)",
-            "config": workload_config(
+            "config": dict(workload_config(
                 wl, key, l2_note=f"rotating {n_sets} buffer sets of {alg / 1e6:.1f} MB "
                                  f"({n_sets * alg / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)"),
+                global_batch=wl.N * world, per_rank_batch=wl.N,
+                parallelism=f"dp{world} (batch shards of {wl.N} images, weights replicated, "
+                            "no collective)"),
             "kernel": {1: "tcgen05", 2: "cuda-core"}.get(kernel, str(kernel)),
             "gpu_launches": K * launches_per_step + main_reps * n_sets,
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak,
                          "unit": "GB/s", "frac": achieved_gbs / hbm_peak,
-                         "traffic": traffic, "kernel_ms": k_ms,
+                         "traffic": traffic,
+                         "traffic_over_algorithmic": traffic / alg if traffic else None,
+                         "kernel_ms": k_ms,
                          "kernel_ms_isolated": k_ms_isolated,
                          "kernel_timing": f"{main_reps * n_sets} back-to-back dgrad launches "
                                           "in the timed region (graph replay, events around it)",
                          "algorithmic_bytes": alg, "peak_source": peak_src},
             "tensor_roofline": {"achieved": achieved_tflops, "peak": tc_peak, "unit": "TFLOP/s",
-                                "frac": achieved_tflops / tc_peak, "peak_source": peak_src},
+                                "frac": achieved_tflops / tc_peak, "peak_source": tc_src},
             "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": g_cpu.numel() * g_cpu.element_size()
                     + w_cpu.numel() * w_cpu.element_size(),
@@ -584,15 +713,18 @@ def run_gpu(args, wl, key):
             for other_key in ("tiny", "resnet", "strided", "pointwise", "stem"):
                 owl = workloads.BY_KEY[other_key]
                 o_ms, o_alg, o_kernel = kernel_only(dg, workloads, owl, other_key, dev, stream)
-                o_peak = bf16_peak / 2 if owl.dtype == "f32" else bf16_peak
+                o_peak, o_src = tc_peak_of(owl.dtype)
                 o_gbs = o_alg / (o_ms * 1e-3) / 1e9
                 o_tf = useful_flops(owl) / (o_ms * 1e-3) / 1e12
+                o_traffic = recorded_traffic(other_key)
                 per[other_key] = {"kernel_us": o_ms * 1e3, "tflops": o_tf,
                                   "hbm_frac": o_gbs / hbm_peak, "tensor_frac": o_tf / o_peak,
-                                  "dtype": owl.dtype,
+                                  "tensor_peak": o_peak, "dtype": owl.dtype,
                                   "kernel": {1: "tcgen05", 2: "cuda-core"}.get(o_kernel, str(o_kernel)),
-                                  "traffic": recorded_traffic(other_key)}
+                                  "traffic": o_traffic,
+                                  "traffic_over_algorithmic": o_traffic / o_alg if o_traffic else None}
             out["per_config"] = per
+            out["tf32_peak"] = {"value": tf32_peak, "unit": "TFLOP/s", "source": tf32_src}
             # The forward convolution of the bench layer (stride 1 only).
             if wl.stride == 1:
                 f_ms = forward_call(dg, workloads, wl, dev, stream)
@@ -608,6 +740,71 @@ def run_gpu(args, wl, key):
     return 0
 
 
+def ncu_traffic_command(key: str) -> str:
+    """The ncu capture whose CSV --record-traffic reads (one pass: DRAM bytes
+    and duration only; no cache flush between launches, so the counts are
+    steady-state traffic; one GPU, a few launches, no clock control)."""
+    return ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum "
+            "--print-units base --cache-control none --clock-control none "
+            f"-k regex:dgrad_tc_kernel -s 2 -c 6 --csv --log-file traffic_{key}.csv "
+            f"python bench.py --config {key} --profile-launches 10")
+
+
+def profile_run(args, wl, key):
+    """Only the dgrad kernel, args.profile_launches times back to back over the
+    rotating buffer sets (weights packed beforehand), for an ncu capture."""
+    import torch
+    import conv2d_backward_implicit_gb300 as dg
+    from conv2d_backward_implicit_gb300 import workloads
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    g_cpu, w_cpu = workloads.make_inputs(wl, seed=0)
+    p = dg.params_from_shapes(g_cpu.shape, w_cpu.shape, wl.H, wl.W, wl.stride, wl.padding_h,
+                              wl.padding_w)
+    code = dg.DTYPE_CODE[wl.dtype]
+    ws = dg.conv2d_grad_input_workspace_size(p, code)
+    alg = algorithmic_bytes(wl)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 * 2**20)
+    n_sets = min(max(2, math.ceil(3 * l2 / alg)), 64)
+    stream = torch.cuda.Stream(dev)
+    sets = []
+    for _ in range(n_sets):
+        s = {"g": g_cpu.to(dev), "out": torch.empty(wl.grad_in_shape, device=dev)}
+        if ws > 0:
+            s["src"] = torch.empty(ws, dtype=torch.uint8, device=dev)
+            dg.conv2d_grad_input_pack_weight(w_cpu.to(dev), s["src"], ws, p, code, stream)
+        else:
+            s["src"] = w_cpu.to(dev)
+        sets.append(s)
+    for i in range(args.profile_launches):
+        s = sets[i % n_sets]
+        dg.conv2d_grad_input_prepacked(s["g"], s["src"], s["out"], p, code, stream)
+    stream.synchronize()
+    rc = dg.conv2d_grad_input_check_errors(stream)
+    if rc != 0:
+        raise RuntimeError(f"profile launches failed: {dg.conv2d_grad_input_status_string(rc)}")
+    print(json.dumps({"profile_launches": args.profile_launches, "workload": wl.name,
+                      "buffer_sets": n_sets}), flush=True)
+    return 0
+
+
+def record_traffic_file(args, wl, key):
+    """Writes profiles/dgrad_tc_<key>.traffic.json from the CSV of ncu_traffic_command."""
+    with open(args.record_traffic) as f:
+        launches = traffic_from_ncu_csv(f.read())
+    if not launches:
+        raise SystemExit(f"no dgrad_tc_kernel launches with DRAM counters in {args.record_traffic}")
+    rec = traffic_record(launches, wl, key, ncu_traffic_command(key))
+    path = os.path.join(ROOT, "profiles", f"dgrad_tc_{key}.traffic.json")
+    with open(path, "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    print(json.dumps({"written": os.path.relpath(path, ROOT),
+                      "dram_bytes_per_launch": rec["dram_bytes_per_launch"],
+                      "traffic_over_algorithmic": rec["traffic_over_algorithmic"]}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -619,9 +816,17 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the kernel-only figures of the other workloads")
+    ap.add_argument("--profile-launches", type=int, default=0, metavar="L",
+                    help="only launch the dgrad kernel L times (for an ncu capture)")
+    ap.add_argument("--record-traffic", metavar="CSV", default=None,
+                    help="write profiles/dgrad_tc_<config>.traffic.json from an ncu CSV")
     args = ap.parse_args(argv)
     from conv2d_backward_implicit_gb300 import workloads
     wl = workloads.BY_KEY[args.config]
+    if args.record_traffic:
+        return record_traffic_file(args, wl, args.config)
+    if args.profile_launches > 0:
+        return profile_run(args, wl, args.config)
     if args.impl == "reference":
         args.steps = 10 if args.steps is None else args.steps
         args.warmup = 1 if args.warmup is None else args.warmup

@@ -102,13 +102,23 @@ def library() -> ctypes.CDLL:
 
 
 _TORCH_DTYPE_NAME = {DGRAD_F32: "float32", DGRAD_BF16: "bfloat16", DGRAD_F16: "float16"}
+_ESIZE = {DGRAD_F32: 4, DGRAD_BF16: 2, DGRAD_F16: 2}
 
 
-def _addr(x, name: str = "buffer", dtype: str | None = None) -> int | None:
+def _current_device() -> int:
+    import torch
+    return int(torch.cuda.current_device())
+
+
+def _addr(x, name: str = "buffer", dtype: str | None = None, numel: int | None = None,
+          min_bytes: int | None = None) -> int | None:
     """Device address of a buffer argument.  Integers pass through unchecked;
-    a tensor must live on a CUDA device, be contiguous (the C ABI reads dense
-    NCHW / [Co,Ci,kH,kW] memory) and, when ``dtype`` is given, have that
-    element type -- checked here, on the host, before the library is called."""
+    a tensor must live on the current CUDA device (the library launches there),
+    be contiguous (the C ABI reads dense NCHW / [Co,Ci,kH,kW] memory), have the
+    element type ``dtype`` and exactly ``numel`` elements when those are given,
+    and hold at least ``min_bytes`` bytes -- all checked here, on the host,
+    before the library is called, so a tensor smaller than the Params describe
+    never reaches a kernel."""
     if x is None:
         return None
     if isinstance(x, int):
@@ -116,11 +126,29 @@ def _addr(x, name: str = "buffer", dtype: str | None = None) -> int | None:
     dev = getattr(x, "device", None)
     if dev is not None and getattr(dev, "type", "cuda") != "cuda":
         raise ValueError(f"{name} must be a CUDA tensor (got one on {dev})")
+    index = getattr(dev, "index", None) if dev is not None else None
+    if index is not None and int(index) != _current_device():
+        raise ValueError(f"{name} is on cuda:{index} but the current device is "
+                         f"cuda:{_current_device()}: the library launches on the current device")
     if hasattr(x, "is_contiguous") and not x.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and hasattr(x, "dtype") and str(x.dtype).replace("torch.", "") != dtype:
         raise ValueError(f"{name} must be {dtype} (got {x.dtype})")
+    if numel is not None and hasattr(x, "numel") and int(x.numel()) != int(numel):
+        raise ValueError(f"{name} must have {numel} elements for these params (got {x.numel()})")
+    if min_bytes is not None and hasattr(x, "numel") and hasattr(x, "element_size"):
+        have = int(x.numel()) * int(x.element_size())
+        if have < int(min_bytes):
+            raise ValueError(f"{name} must hold at least {min_bytes} bytes (got {have})")
     return x.data_ptr()
+
+
+def _sizes(params: Params):
+    """Element counts of grad_out, weight and grad_in that ``params`` describe."""
+    p = params
+    return (p.batch * p.out_channels * p.out_h * p.out_w,
+            p.out_channels * p.in_channels * p.kernel_h * p.kernel_w,
+            p.batch * p.in_channels * p.in_h * p.in_w)
 
 
 def _in_dtype(code: int) -> str | None:
@@ -128,10 +156,16 @@ def _in_dtype(code: int) -> str | None:
 
 
 def _stream(stream) -> int | None:
+    """The cudaStream_t of a torch stream (or an integer handle, passed through).
+    A torch stream must belong to the current device."""
     if stream is None:
         return None
     if isinstance(stream, int):
         return stream
+    dev = getattr(stream, "device", None)
+    index = getattr(dev, "index", None) if dev is not None else None
+    if index is not None and int(index) != _current_device():
+        raise ValueError(f"stream is on cuda:{index} but the current device is cuda:{_current_device()}")
     return stream.cuda_stream
 
 
@@ -142,9 +176,10 @@ def _check(rc: int, where: str) -> int:
 
 
 def conv2d_grad_input(grad_out, weight, grad_in, params: Params, dtype: int, stream=None) -> None:
-    rc = library().conv2d_grad_input(_addr(grad_out, "grad_out", _in_dtype(dtype)),
-                                     _addr(weight, "weight", _in_dtype(dtype)),
-                                     _addr(grad_in, "grad_in", "float32"),
+    n_go, n_w, n_gi = _sizes(params)
+    rc = library().conv2d_grad_input(_addr(grad_out, "grad_out", _in_dtype(dtype), n_go),
+                                     _addr(weight, "weight", _in_dtype(dtype), n_w),
+                                     _addr(grad_in, "grad_in", "float32", n_gi),
                                      ctypes.byref(params), int(dtype), _stream(stream))
     _check(rc, "conv2d_grad_input")
 
@@ -155,17 +190,25 @@ def conv2d_grad_input_workspace_size(params: Params, dtype: int) -> int:
 
 def conv2d_grad_input_pack_weight(weight, packed, packed_bytes: int, params: Params, dtype: int,
                                   stream=None) -> None:
-    rc = library().conv2d_grad_input_pack_weight(_addr(weight, "weight", _in_dtype(dtype)),
-                                                 _addr(packed, "packed"), int(packed_bytes),
-                                                 ctypes.byref(params), int(dtype), _stream(stream))
+    _, n_w, _ = _sizes(params)
+    rc = library().conv2d_grad_input_pack_weight(_addr(weight, "weight", _in_dtype(dtype), n_w),
+                                                 _addr(packed, "packed", min_bytes=int(packed_bytes)),
+                                                 int(packed_bytes), ctypes.byref(params), int(dtype),
+                                                 _stream(stream))
     _check(rc, "conv2d_grad_input_pack_weight")
 
 
 def conv2d_grad_input_prepacked(grad_out, packed, grad_in, params: Params, dtype: int,
                                 stream=None) -> None:
-    rc = library().conv2d_grad_input_prepacked(_addr(grad_out, "grad_out", _in_dtype(dtype)),
-                                               _addr(packed, "packed"),
-                                               _addr(grad_in, "grad_in", "float32"),
+    """``packed``: the buffer conv2d_grad_input_pack_weight filled, or -- when
+    the workspace size is 0 -- the weight tensor itself."""
+    n_go, n_w, n_gi = _sizes(params)
+    ws = conv2d_grad_input_workspace_size(params, dtype)
+    packed_addr = (_addr(packed, "packed", min_bytes=ws) if ws > 0
+                   else _addr(packed, "packed (the weight tensor)", _in_dtype(dtype), n_w))
+    rc = library().conv2d_grad_input_prepacked(_addr(grad_out, "grad_out", _in_dtype(dtype), n_go),
+                                               packed_addr,
+                                               _addr(grad_in, "grad_in", "float32", n_gi),
                                                ctypes.byref(params), int(dtype), _stream(stream))
     _check(rc, "conv2d_grad_input_prepacked")
 
@@ -205,17 +248,20 @@ def conv2d_grad_input_noalloc(grad_out, weight, grad_in, params: Params, dtype: 
     ordered by the caller, and problems whose packed weights exceed 8 MiB
     raise DgradError(DGRAD_ERR_WORKSPACE).
     """
-    rc = library().conv2d_grad_input_noalloc(_addr(grad_out, "grad_out", _in_dtype(dtype)),
-                                             _addr(weight, "weight", _in_dtype(dtype)),
-                                             _addr(grad_in, "grad_in", "float32"),
+    n_go, n_w, n_gi = _sizes(params)
+    rc = library().conv2d_grad_input_noalloc(_addr(grad_out, "grad_out", _in_dtype(dtype), n_go),
+                                             _addr(weight, "weight", _in_dtype(dtype), n_w),
+                                             _addr(grad_in, "grad_in", "float32", n_gi),
                                              ctypes.byref(params), int(dtype), _stream(stream))
     _check(rc, "conv2d_grad_input_noalloc")
 
 
 def conv2d_forward(x, weight, out, params: Params, dtype: int, stream=None) -> None:
-    """Forward convolution of the layer ``params`` describes (stride 1): x
-    [N,Ci,H,W], weight [Co,Ci,kH,kW] -> out [N,Co,OH,OW] float32."""
-    rc = library().conv2d_forward(_addr(x, "x", _in_dtype(dtype)), _addr(weight, "weight", _in_dtype(dtype)),
-                                  _addr(out, "out", "float32"), ctypes.byref(params),
+    """Forward convolution of the layer ``params`` describes: x [N,Ci,H,W],
+    weight [Co,Ci,kH,kW] -> out [N,Co,OH,OW] float32."""
+    n_out, n_w, n_x = _sizes(params)
+    rc = library().conv2d_forward(_addr(x, "x", _in_dtype(dtype), n_x),
+                                  _addr(weight, "weight", _in_dtype(dtype), n_w),
+                                  _addr(out, "out", "float32", n_out), ctypes.byref(params),
                                   int(dtype), _stream(stream))
     _check(rc, "conv2d_forward")

@@ -179,7 +179,7 @@ const char *conv2d_grad_input_status_string(int status) {
     case DGRAD_ERR_UNSUPPORTED: return "unsupported size or kernel choice";
     case DGRAD_ERR_CUDA: return "CUDA runtime error";
     case DGRAD_ERR_TIMEOUT: return "device wait timed out";
-    case DGRAD_ERR_WORKSPACE: return "packed-weight buffer too small";
+    case DGRAD_ERR_WORKSPACE: return "packed-weight buffer too small (the one passed in, or the 8 MiB array of the no-alloc entry point)";
     default: return "unknown status";
     }
 }

@@ -12,8 +12,11 @@
 // weight and grad_in.
 //
 // Costs and rules:
-//  * Every GPU that loads this library holds kNoAllocScratchBytes (8 MiB) of
-//    device memory for this array until the process exits.
+//  * The array is device memory of this library's module: kNoAllocScratchBytes
+//    (8 MiB) are committed on a device when the module is loaded there.
+//    Under CUDA's lazy module loading (the default) that is the first call of
+//    this entry point on the device (its cudaGetSymbolAddress loads the
+//    module); the memory then stays until the process exits.
 //  * All calls share the one array.  Calls whose work overlaps on the GPU
 //    (different streams without ordering, or several host threads) race on
 //    it; order such calls on one stream or serialise them.

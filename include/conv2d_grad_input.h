@@ -27,8 +27,10 @@
  * after a call returns; the work it enqueued reads and writes them
  * asynchronously on `stream`, so they must stay alive until that work is done.
  *
- * Streams: `stream` is a cudaStream_t (NULL = the legacy default stream) of
- * the current device.  Every entry point that takes one is asynchronous with
+ * Streams and devices: `stream` is a cudaStream_t (NULL = the legacy default
+ * stream) of the current device, the kernels run on the current device, and
+ * every buffer must be memory of that device (the library does not check
+ * which device a pointer belongs to; the Python binding does).  Every entry point that takes one is asynchronous with
  * respect to the host, except conv2d_grad_input_check_errors.
  *
  * Errors: every entry point returns a dgrad_status (0 = success) and never
@@ -84,7 +86,8 @@ typedef enum dgrad_status {
     DGRAD_ERR_UNSUPPORTED = 4, /* a size beyond the library's limits (e.g. > 2^31-1 per index) */
     DGRAD_ERR_CUDA = 5,        /* a CUDA runtime call failed */
     DGRAD_ERR_TIMEOUT = 6,     /* a device-side wait ran out of time (kernel returned early) */
-    DGRAD_ERR_WORKSPACE = 7    /* the packed-weight buffer passed in is too small */
+    DGRAD_ERR_WORKSPACE = 7    /* the packed-weight buffer is too small: the one passed in, or the
+                                  fixed 8 MiB internal array of conv2d_grad_input_noalloc */
 } dgrad_status;
 
 typedef enum dgrad_kernel {
@@ -200,8 +203,11 @@ int conv2d_forward(const void *x, const void *weight, float *out, const conv2d_g
  * allocation's synchronisation.  Same arguments, semantics and results as
  * conv2d_grad_input, but the packed weights live in a fixed 8 MiB device
  * array inside the library instead of a temporary allocation:
- *  - every GPU that loads the library holds those 8 MiB until the process
- *    exits;
+ *  - the 8 MiB are device memory of the library's module: they are
+ *    committed on a device when the module is loaded there -- under CUDA's
+ *    lazy module loading (the default) at the first conv2d_grad_input_noalloc
+ *    call on that device, whose address lookup loads it -- and stay until the
+ *    process exits;
  *  - a problem whose packed weights exceed 8 MiB
  *    (conv2d_grad_input_workspace_size > 8388608) is rejected with
  *    DGRAD_ERR_WORKSPACE before anything is enqueued;

@@ -209,10 +209,14 @@ def test_planner_accepts_every_valid_shape(lib):
 class _FakeCudaTensor:
     """Just enough of a tensor for the binding's host-side checks."""
 
-    def __init__(self, dtype="bfloat16", contiguous=True, device="cuda"):
+    def __init__(self, dtype="bfloat16", contiguous=True, device="cuda", numel=None, index=None):
         self.dtype = f"torch.{dtype}"
-        self.device = type("Dev", (), {"type": device, "__str__": lambda s: device})()
+        self.device = type("Dev", (), {"type": device, "index": index,
+                                       "__str__": lambda s: device})()
         self._contiguous = contiguous
+        self._numel = numel
+        if numel is None:  # no size known: the size checks are skipped
+            del self.__dict__["_numel"]
 
     def is_contiguous(self):
         return self._contiguous
@@ -220,10 +224,22 @@ class _FakeCudaTensor:
     def data_ptr(self):
         return 1 << 20
 
+    def __getattr__(self, name):
+        if name in ("numel", "element_size") and "_numel" in self.__dict__:
+            esize = 4 if "32" in self.dtype else (1 if "uint8" in self.dtype else 2)
+            return (lambda: self._numel) if name == "numel" else (lambda: esize)
+        raise AttributeError(name)
 
-def test_binding_checks_tensors_before_calling_the_library(lib):
+
+def test_binding_checks_tensors_before_calling_the_library(lib, monkeypatch):
     import torch
-    p = params(workloads.RESNET)
+    import conv2d_backward_implicit_gb300.binding as binding
+    monkeypatch.setattr(binding, "_current_device", lambda: 0)
+    wl = workloads.RESNET
+    p = params(wl)
+    n_go = wl.N * wl.Co * wl.OH * wl.OW
+    n_w = wl.Co * wl.Ci * wl.kH * wl.kW
+    n_gi = wl.N * wl.Ci * wl.H * wl.W
     good_g, good_w = _FakeCudaTensor(), _FakeCudaTensor()
     out = _FakeCudaTensor("float32")
     cases = [
@@ -231,13 +247,39 @@ def test_binding_checks_tensors_before_calling_the_library(lib):
         (_FakeCudaTensor(contiguous=False), good_w, out, "contiguous"),     # a strided view
         (good_g, _FakeCudaTensor("float16"), out, "bfloat16"),              # dtype vs code
         (good_g, good_w, _FakeCudaTensor("bfloat16"), "float32"),           # grad_in is fp32
+        # tensors smaller (or larger) than the params describe never reach a kernel
+        (_FakeCudaTensor(numel=n_go - 1), good_w, out, "elements"),
+        (good_g, _FakeCudaTensor(numel=n_w // 2), out, "elements"),
+        (good_g, good_w, _FakeCudaTensor("float32", numel=n_gi - 56), "elements"),
+        (good_g, good_w, _FakeCudaTensor("float32", numel=n_gi + 1), "elements"),
+        # a tensor on another GPU than the current one
+        (_FakeCudaTensor(index=1), good_w, out, "current device"),
+        (good_g, good_w, _FakeCudaTensor("float32", index=3), "current device"),
     ]
     for g, w, o, msg in cases:
         with pytest.raises(ValueError, match=msg):
             dg.conv2d_grad_input(g, w, o, p, dg.DGRAD_BF16)
         with pytest.raises(ValueError, match=msg):
             dg.conv2d_grad_input_noalloc(g, w, o, p, dg.DGRAD_BF16)
+        with pytest.raises(ValueError, match=msg):
+            dg.conv2d_grad_input_prepacked(g, w, o, p, dg.DGRAD_BF16)  # ResNet packs in the kernel
     with pytest.raises(ValueError, match="CUDA tensor"):
         dg.conv2d_grad_input_prepacked(good_g, torch.zeros(4), out, p, dg.DGRAD_BF16)
     with pytest.raises(ValueError, match="float32"):
         dg.conv2d_forward(good_g, good_w, _FakeCudaTensor("float16"), p, dg.DGRAD_BF16)
+    with pytest.raises(ValueError, match="elements"):
+        dg.conv2d_forward(_FakeCudaTensor(numel=n_gi - 1), good_w, out, p, dg.DGRAD_BF16)
+    # A packed-weight buffer smaller than the workspace the layer needs.
+    s = params(workloads.STRIDED)
+    ws = dg.conv2d_grad_input_workspace_size(s, dg.DGRAD_BF16)
+    assert ws > 0
+    with pytest.raises(ValueError, match="bytes"):
+        dg.conv2d_grad_input_prepacked(good_g, _FakeCudaTensor("uint8", numel=ws - 16), out, s,
+                                       dg.DGRAD_BF16)
+    with pytest.raises(ValueError, match="bytes"):
+        dg.conv2d_grad_input_pack_weight(good_w, _FakeCudaTensor("uint8", numel=ws - 1), ws, s,
+                                         dg.DGRAD_BF16)
+    # A stream of another device.
+    other = type("S", (), {"device": type("D", (), {"index": 2})(), "cuda_stream": 0})()
+    with pytest.raises(ValueError, match="stream"):
+        dg.conv2d_grad_input(good_g, good_w, out, p, dg.DGRAD_BF16, other)

@@ -41,3 +41,52 @@ def test_recorded_traffic_needs_the_same_kernel_source(monkeypatch, tmp_path):
     assert bench.recorded_traffic("resnet") is None
     assert bench.recorded_traffic("no-such-workload") is None
 
+
+
+_NCU_HEADER = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",'
+               '"Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit",'
+               '"Metric Value"')
+
+
+def _ncu_row(i, name, metric, unit, value):
+    return (f'"{i}","77","python3","127.0.0.1","{name}","1","13","(512, 1, 1)","(152, 1, 1)",'
+            f'"0","10.3","Command line profiler metrics","{metric}","{unit}","{value}"')
+
+
+def test_traffic_record_from_an_ncu_csv():
+    k = "void dgrad::(anonymous namespace)::dgrad_tc_kernel<2, 1>(dgrad::TcParams)"
+    rows = ["==PROF== Connected to process 77", _NCU_HEADER]
+    # Launch 0 (cold: grad_in still in L2 at its end), then two steady launches.
+    per = [(13_000_000, 2_304, 25_400), (13_100_000, 25_600_000, 17_900), (13_200_000, 25_800_000, 18_100)]
+    for i, (rd, wr, ns) in enumerate(per):
+        rows.append(_ncu_row(i, k, "dram__bytes_read.sum", "byte", f"{rd:,}"))
+        rows.append(_ncu_row(i, k, "dram__bytes_write.sum", "byte", str(wr)))
+        rows.append(_ncu_row(i, k, "gpu__time_duration.sum", "nsecond", str(ns)))
+    rows.append(_ncu_row(9, "void other_kernel()", "dram__bytes_read.sum", "byte", "5"))
+    launches = bench.traffic_from_ncu_csv("\n".join(rows))
+    assert [x[0] for x in launches] == [0, 1, 2]
+    assert launches[1][2:4] == (13_100_000, 25_600_000)
+    assert launches[2][4] == pytest.approx(18.1e-6)
+    rec = bench.traffic_record(launches, workloads.RESNET, "resnet", "cmd")
+    # averaged over the launches after the first
+    assert rec["dram_read_bytes"] == 13_150_000
+    assert rec["dram_write_bytes"] == 25_700_000
+    assert rec["dram_bytes_per_launch"] == 38_850_000
+    assert rec["traffic_over_algorithmic"] == pytest.approx(38_850_000 / 38_608_896)
+    assert rec["kernel"].startswith("dgrad::")
+    # scaled units
+    m = bench.traffic_from_ncu_csv("\n".join([
+        _NCU_HEADER, _ncu_row(3, k, "dram__bytes_read.sum", "Mbyte", "1.5"),
+        _ncu_row(3, k, "dram__bytes_write.sum", "Kbyte", "2")]))
+    assert m[0][2:4] == (1_500_000, 2_000)
+
+
+def test_shard_bounds_cover_the_batch_once():
+    for n in (1, 7, 32, 64, 100):
+        for world in (1, 2, 3, 4, 8):
+            spans = [bench.shard_bounds(n, world, r) for r in range(world)]
+            assert spans[0][0] == 0 and spans[-1][1] == n
+            for (a, b), (c, d) in zip(spans, spans[1:]):
+                assert b == c
+            sizes = [b - a for a, b in spans]
+            assert max(sizes) - min(sizes) <= 1

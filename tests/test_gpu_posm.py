@@ -98,21 +98,17 @@ def test_resnet_reduced_batch(dg):
     assert rel_err(out.cpu().numpy(), full_oracle(wl, g, w)) <= TOL
 
 
-def test_resnet_full_size_sampled(dg):
+def test_resnet_full_size_every_element(dg, parity_log):
+    # 448 tiles on at most 152 CTAs: every CTA takes several tiles, so both
+    # TMEM accumulator buffers, the ring wrap-around and the next-tile
+    # prefetch run under an element-by-element check against the oracle.
     wl = workloads.RESNET
     g, w = workloads.make_inputs(wl, seed=0)
+    assert dg.conv2d_grad_input_select_kernel(params(dg, wl, g, w), 1) == dg.DGRAD_KERNEL_TC_POSM
     out = run(dg, wl, g, w, via="prepacked")
-    # The general mode computes the same sums in another order: close, not equal.
-    dg.conv2d_grad_input_set_kernel(dg.DGRAD_KERNEL_TC)
-    out_tc = run(dg, wl, g, w, via="prepacked")
-    assert rel_err(out.cpu().numpy(), out_tc.cpu().numpy()) <= TOL
-    rng = np.random.default_rng(5)
-    pts = np.stack([rng.integers(0, d, 4000) for d in wl.grad_in_shape], axis=1)
-    edge = [[n, c, ih, iw] for n in (0, wl.N - 1) for c in (0, 63) for ih in (0, 1, 54, 55)
-            for iw in (0, 1, 22, 23, 24, 25, 26, 54, 55)]
-    pts = np.unique(np.concatenate([pts, np.array(edge)]).astype(np.int64), axis=0)
-    ref = oracle.dgrad_points(g.double().numpy(), w.double().numpy(), pts, wl.H, wl.W, 1, 1, 1)
-    assert rel_err(out.cpu().numpy()[tuple(pts.T)], ref) <= TOL
+    err = rel_err(out.cpu().numpy(), full_oracle(wl, g, w))
+    parity_log("positions-on-M, resnet full size", err, TOL)
+    assert err <= TOL
 
 
 SHAPES = {

@@ -7,6 +7,8 @@ call reuses the same fixed scratch array left over from the previous one.
 Collected last on purpose, so that a run stopping at its first failure has
 already run every other test; it also passes on its own in a fresh process.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -65,3 +67,59 @@ def test_noalloc_rejects_packs_above_its_limit():
     assert ei.value.status == 7
     torch.cuda.synchronize()
     assert torch.all(out == 3.0)
+
+
+def _pool_high_water():
+    """Read and reset functions for the used-memory high-water mark of the
+    current device's memory pool -- the pool cudaMallocAsync draws from (driver
+    API, so no particular CUDA runtime copy is involved)."""
+    cu = ctypes.CDLL("libcuda.so.1")
+    dev = ctypes.c_int()
+    assert cu.cuCtxGetDevice(ctypes.byref(dev)) == 0
+    pool = ctypes.c_void_p()
+    assert cu.cuDeviceGetMemPool(ctypes.byref(pool), dev) == 0
+    used_mem_high = 8  # CU_MEMPOOL_ATTR_USED_MEM_HIGH
+
+    def high():
+        v = ctypes.c_uint64()
+        assert cu.cuMemPoolGetAttribute(pool, used_mem_high, ctypes.byref(v)) == 0
+        return v.value
+
+    def reset():
+        z = ctypes.c_uint64(0)  # resets the mark to the memory in use now
+        assert cu.cuMemPoolSetAttribute(pool, used_mem_high, ctypes.byref(z)) == 0
+
+    return high, reset
+
+
+def test_noalloc_takes_no_device_memory_after_its_first_call():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import conv2d_backward_implicit_gb300 as dg
+    dev = torch.device("cuda")
+    high, reset = _pool_high_water()
+    for wl in (workloads.STRIDED.with_batch(1), workloads.STEM.with_batch(1)):
+        g, w = workloads.make_inputs(wl, seed=3)
+        gd, wd = g.to(dev), w.to(dev)
+        p = dg.params_from_shapes(g.shape, w.shape, wl.H, wl.W, wl.stride, wl.padding_h,
+                                  wl.padding_w)
+        code = dg.DTYPE_CODE[wl.dtype]
+        ws = dg.conv2d_grad_input_workspace_size(p, code)
+        assert ws > 0  # a layer whose weights are packed into scratch memory
+        out = torch.empty(wl.grad_in_shape, device=dev)
+        dg.conv2d_grad_input_noalloc(gd, wd, out, p, code)  # first call: address set-up
+        torch.cuda.synchronize()
+        # The probe sees the allocating entry point's stream-ordered workspace ...
+        reset()
+        before = high()
+        dg.conv2d_grad_input(gd, wd, out, p, code)
+        torch.cuda.synchronize()
+        assert high() >= before + ws, wl.name
+        # ... and nothing from the allocation-free one.
+        reset()
+        before = high()
+        for _ in range(3):
+            dg.conv2d_grad_input_noalloc(gd, wd, out, p, code)
+        torch.cuda.synchronize()
+        assert high() == before, wl.name
+        assert dg.conv2d_grad_input_check_errors() == 0
