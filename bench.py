@@ -142,8 +142,8 @@ def measure_tf32_peak(dev, n: int = 8192, reps: int = 10) -> float:
         torch.backends.cuda.matmul.allow_tf32 = prev
 
 
-_UNIT = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "nsecond": 1e-9,
-         "usecond": 1e-6, "msecond": 1e-3, "second": 1.0}
+_UNIT = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "nsecond": 1e-9, "ns": 1e-9,
+         "usecond": 1e-6, "us": 1e-6, "msecond": 1e-3, "ms": 1e-3, "second": 1.0, "s": 1.0}
 
 
 def traffic_from_ncu_csv(text: str, kernel_pattern: str = "dgrad_tc_kernel"):
@@ -186,16 +186,16 @@ def traffic_record(launches, wl, key, command: str):
     the captured launches after the first (steady state: a launch's grad_in
     writes leave L2 during later launches, so the first one shows only reads)."""
     steady = launches[1:] if len(launches) > 1 else launches
-    rd = sum(x[2] for x in steady) / len(steady)
-    wr = sum(x[3] for x in steady) / len(steady)
+    rd = round(sum(x[2] for x in steady) / len(steady))
+    wr = round(sum(x[3] for x in steady) / len(steady))
     alg = algorithmic_bytes(wl)
     return {
         "kernel": launches[0][1].split("(")[0].replace("void ", "").strip(),
         "workload": workload_config(wl, key, "")["workload"],
         "kernel_fingerprint": kernel_fingerprint(),
-        "dram_bytes_per_launch": int(round(rd + wr)),
-        "dram_read_bytes": int(round(rd)),
-        "dram_write_bytes": int(round(wr)),
+        "dram_bytes_per_launch": int(rd + wr),
+        "dram_read_bytes": int(rd),
+        "dram_write_bytes": int(wr),
         "algorithmic_bytes": alg,
         "traffic_over_algorithmic": (rd + wr) / alg,
         "launches_averaged": len(steady),

@@ -61,7 +61,7 @@ def test_traffic_record_from_an_ncu_csv():
     for i, (rd, wr, ns) in enumerate(per):
         rows.append(_ncu_row(i, k, "dram__bytes_read.sum", "byte", f"{rd:,}"))
         rows.append(_ncu_row(i, k, "dram__bytes_write.sum", "byte", str(wr)))
-        rows.append(_ncu_row(i, k, "gpu__time_duration.sum", "nsecond", str(ns)))
+        rows.append(_ncu_row(i, k, "gpu__time_duration.sum", "ns", str(ns)))
     rows.append(_ncu_row(9, "void other_kernel()", "dram__bytes_read.sum", "byte", "5"))
     launches = bench.traffic_from_ncu_csv("\n".join(rows))
     assert [x[0] for x in launches] == [0, 1, 2]
