@@ -64,6 +64,7 @@ constexpr int kMaxRaw = 8;                    // raw-slice ring slots
 constexpr int kMaxW = 8;                      // streamed weight stages
 constexpr int kMaxGatherRows = 6;             // window rows per gather thread (raw-slice gather)
 constexpr int kMaxMnPieces = 11;              // 16-byte pieces per gather thread and stage (MN-major)
+constexpr int kStMaxTw = 4;                   // stacked mode: column taps stacked on N (at most)
 constexpr int kPmPitch = 64;  // positions-on-M mode: frame positions per grad_out row
 constexpr int kPmLeft = 8;    // zero columns before grad_out column 0 in each frame row
 constexpr int kPmMaxKw = 3;   // column taps stacked on N (kW x 64 columns)
@@ -74,7 +75,7 @@ constexpr int kPmGWarp0 = 18;
 constexpr int kPmGWarps = 4;
 constexpr int kPmThreads = 32 * (kPmGWarp0 + kPmGWarps);
 constexpr int kPmGroups = 6;  // ldmatrix.x4 groups per gather warp and raw slice (at most)
-constexpr int kF64Groups = 4; // the same with the general mode's kGWarps gather warps
+constexpr int kF64Groups = 7; // the same with the general mode's kGWarps gather warps
 // Boundary-exchange buffer of the positions-on-M epilogue: 8 warp pairs x 2
 // slots x 3 (tap, lane) values x 16 floats: block 1 of lane 31, block 2 of
 // lanes 30 and 31.
@@ -175,6 +176,15 @@ struct TcParams {
     int stacked;
     int st_n, st_th, st_tw, st_dy0, st_dx0;
     int st_mblocks;         // 128-position MMA M-blocks per tile (1 or 2), one accumulator each
+    // > 0: the stacked mode with the column taps on N as well (N = st_tw x
+    // st_n: column block i of lane e holds the window tap dx = st_dx0 + i of
+    // frame element e), on a quadrant-halo frame: X = 128 elements per frame
+    // row, element e = 32q + l holding frame column (32 - st_qhalo) q + l, so
+    // each 32-lane TMEM quadrant covers 32 - st_qhalo outputs plus st_qhalo =
+    // st_tw - 1 halo columns, and the epilogue adds block i of lane l + i
+    // within the warp.  An M-block is one frame row (one output row of the
+    // phase grid); K = grad_out channels x the st_th row taps.
+    int st_qhalo;
     // A CTA takes tiles in groups of tile_group consecutive tiles (groups
     // dealt round-robin over the grid).  pair_rw (stride 2, four phases
     // interleaved, one channel tile): tiles 2u and 2u + 1 are the column
@@ -191,6 +201,12 @@ struct TcParams {
     int w_raw;
     PhaseDesc ph[kMaxPhases];
 };
+
+// Frame column held by frame element x of a row: x itself, or on the
+// quadrant-halo frame (TcParams::st_qhalo) (32 - halo) * (x / 32) + x mod 32.
+__host__ __device__ __forceinline__ int frame_column(int x, int qhalo) {
+    return qhalo > 0 ? (32 - qhalo) * (x >> 5) + (x & 31) : x;
+}
 
 struct PackParams {
     int Ci, Co, kH, kW, stride;

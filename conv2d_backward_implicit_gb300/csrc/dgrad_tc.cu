@@ -214,6 +214,14 @@ __device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
     return v;
 }
 
+// float32 bits rounded to TF32 (nearest, ties away from zero): the operand
+// precision of kind::tf32.
+__device__ __forceinline__ uint32_t to_tf32(uint32_t bits) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(__uint_as_float(bits)));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t ld_shared_tf32(uint32_t addr) {
     float v;
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
@@ -254,12 +262,10 @@ __device__ __forceinline__ uint32_t ldg_u16(const unsigned short *p) {
     return v;
 }
 
-__device__ __forceinline__ uint32_t ldg_tf32(const float *p) {
-    float v;
-    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
-    return r;
+__device__ __forceinline__ uint32_t ldg_b32(const float *p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -425,6 +431,11 @@ __device__ __forceinline__ void tmem_wait_ld3(uint32_t (&r)[3][16]) {
                  : "+r"(r[0][0]), "+r"(r[0][1]), "+r"(r[0][2]), "+r"(r[0][3]), "+r"(r[0][4]), "+r"(r[0][5]), "+r"(r[0][6]), "+r"(r[0][7]), "+r"(r[0][8]), "+r"(r[0][9]), "+r"(r[0][10]), "+r"(r[0][11]), "+r"(r[0][12]), "+r"(r[0][13]), "+r"(r[0][14]), "+r"(r[0][15]), "+r"(r[1][0]), "+r"(r[1][1]), "+r"(r[1][2]), "+r"(r[1][3]), "+r"(r[1][4]), "+r"(r[1][5]), "+r"(r[1][6]), "+r"(r[1][7]), "+r"(r[1][8]), "+r"(r[1][9]), "+r"(r[1][10]), "+r"(r[1][11]), "+r"(r[1][12]), "+r"(r[1][13]), "+r"(r[1][14]), "+r"(r[1][15]), "+r"(r[2][0]), "+r"(r[2][1]), "+r"(r[2][2]), "+r"(r[2][3]), "+r"(r[2][4]), "+r"(r[2][5]), "+r"(r[2][6]), "+r"(r[2][7]), "+r"(r[2][8]), "+r"(r[2][9]), "+r"(r[2][10]), "+r"(r[2][11]), "+r"(r[2][12]), "+r"(r[2][13]), "+r"(r[2][14]), "+r"(r[2][15])
                  :
                  : "memory");
+}
+
+// Waits for this thread's outstanding TMEM loads into r[0..3][0..15].
+__device__ __forceinline__ void tmem_wait_ld16x4(uint32_t (&r)[4][16]) {
+    tmem_wait_ld4(r);
 }
 
 // Waits for this thread's outstanding TMEM loads into r[0..1][0..15].
@@ -1300,6 +1311,12 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
     wait_drain(smem_u32(&sh.mma_done), 0, p, sh);
 }
 
+// Accumulator columns of one stacked-mode M-block: st_n, or st_tw x st_n with
+// the column taps on N.
+__device__ __forceinline__ int st_cols(const TcParams &p) {
+    return p.st_qhalo ? p.st_tw * p.st_n : p.st_n;
+}
+
 // Warp 8, lane 0, stacked-phase mode: D[position, (phase, ci)] (TMEM, st_n
 // columns per buffer) += G[position + shift(tap), co] (A: the frame window
 // seen from the tap's start row) x W_tap[(phase, ci), co] (B: resident packed
@@ -1314,6 +1331,76 @@ __device__ void role_mma_stacked(const TcParams &p, Shared &sh, uint32_t g_base,
     const int taps = p.st_th * p.st_tw;
     const int mblocks = p.st_mblocks;  // 128-position M-blocks of a tile, one accumulator each
     const uint32_t w_step = (uint32_t)(p.w_unit_bytes >> 4);
+    const uint32_t ncols = (uint32_t)st_cols(p);
+    if (p.st_qhalo) {
+        // Column taps on N: for each grad_out chunk and row tap dy, one MMA
+        // group per M-block (frame row mb of the tile) with A = the window
+        // from frame row mb + dy (row taps are whole 128-element frame rows)
+        // and B = the st_tw taps (dy, 0..st_tw-1) of the chunk, st_tw x st_n
+        // rows; weights streamed one row tap per stage, or resident.
+        for (int64_t t = first_tile<kVarStacked>(p); t < p.total_tiles && !aborted;
+             t = next_tile<kVarStacked>(p, t)) {
+            if (!wait_bar(smem_u32(&sh.acc_empty[acc]), accph ^ 1u, p, sh)) {
+                aborted = true;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + (uint32_t)acc * (uint32_t)mblocks * ncols;
+            uint32_t accumulate = 0;
+            for (int cc = 0; cc < p.n_cchunks && !aborted; ++cc) {
+                if (!wait_bar(smem_u32(&sh.full_g[gs]), gph, p, sh)) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t ad0 = sw128_desc(g_base + (uint32_t)gs * p.g_stage_bytes);
+                for (int dy = 0; dy < p.st_th; ++dy) {
+                    uint32_t w_grp;  // taps (dy, 0 .. st_tw - 1) of this chunk
+                    if (p.nw == 0) {
+                        w_grp = w_base + (uint32_t)(cc * taps + dy * p.st_tw) * (uint32_t)p.w_unit_bytes;
+                    } else {
+                        if (!wait_bar(smem_u32(&sh.full_w[ws]), wph, p, sh)) {
+                            aborted = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        w_grp = w_base + (uint32_t)ws * p.w_stage_bytes;
+                    }
+                    const uint64_t bd = sw128_desc(w_grp);
+                    for (int mb = 0; mb < mblocks; ++mb) {
+                        const uint64_t ad = ad0 + (uint64_t)((mb + dy) * X * 8);  // frame rows of 128 B rows
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)  // four 32-byte K steps per 128-byte row
+                            tc_mma<TF32>(d_tmem + (uint32_t)mb * ncols, ad + 2u * k, bd + 2u * k, p.idesc,
+                                         accumulate | (uint32_t)(k > 0));
+                    }
+                    accumulate = 1;
+                    if (p.nw != 0) {
+                        tc_commit(smem_u32(&sh.empty_w[ws]));
+                        if (++ws == p.nw) {
+                            ws = 0;
+                            wph ^= 1u;
+                        }
+                    }
+                }
+                if (aborted) break;
+                tc_commit(smem_u32(&sh.empty_g[gs]));
+                if (++gs == p.ng) {
+                    gs = 0;
+                    gph ^= 1u;
+                }
+            }
+            if (aborted) break;
+            tc_commit(smem_u32(&sh.acc_full[acc]));
+            if (++acc == 2) {
+                acc = 0;
+                accph ^= 1u;
+            }
+        }
+        tc_commit(smem_u32(&sh.mma_done));
+        wait_drain(smem_u32(&sh.mma_done), 0, p, sh);
+        return;
+    }
     for (int64_t t = first_tile<kVarStacked>(p); t < p.total_tiles && !aborted;
          t = next_tile<kVarStacked>(p, t)) {
         if (!wait_bar(smem_u32(&sh.acc_empty[acc]), accph ^ 1u, p, sh)) {
@@ -1476,7 +1563,7 @@ __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
             const int drho = kStep / X, dx = kStep - drho * X;
 #pragma unroll
             for (int k = 0; k < kMaxGatherRows; ++k) {
-                const int u = u_first + rho, xc = x + xoff;
+                const int u = u_first + rho, xc = frame_column(x, p.st_qhalo) + xoff;
                 const bool inside = xc >= 0 && xc < p.raw_bw && u >= 0 && u < p.OH;
                 src[k] = inside ? (rho + roff) * (int)row_bytes + xc * ESIZE : -1;
                 rho += drho;
@@ -1503,32 +1590,52 @@ __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
                     const int h = h0 + k * kStep;
                     const uint32_t row = s_base + (uint32_t)h * 128u;
                     const int off = src[k];
-                    for (int j = 0; j < groups; ++j) {
-                        uint32_t q[4] = {0u, 0u, 0u, 0u};
-                        if (off >= 0) {
-                            const uint32_t a = raw + (uint32_t)off + (uint32_t)(j * E) * ch_bytes;
-                            if constexpr (ESIZE == 2) {
+                    // Batches of kGB 16-byte chunks: every shared-memory load
+                    // of a batch is issued before any of them is used, so the
+                    // loads overlap instead of each one waiting on the last.
+                    constexpr int kGB = ESIZE == 2 ? 1 : 2;  // 16-bit: one chunk (measured faster on the paired mode)
+                    for (int j0 = 0; j0 < groups; j0 += kGB) {
+                        uint32_t v[kGB][E];  // raw elements: 16-bit values or float32 bits
 #pragma unroll
-                                for (int e = 0; e < 8; e += 2)
-                                    q[e / 2] = ld_shared_u16(a + (uint32_t)e * ch_bytes) |
-                                               (ld_shared_u16(a + (uint32_t)(e + 1) * ch_bytes) << 16);
-                            } else {
+                        for (int jj = 0; jj < kGB; ++jj) {
+                            if (j0 + jj < groups && off >= 0) {
+                                const uint32_t a = raw + (uint32_t)off + (uint32_t)((j0 + jj) * E) * ch_bytes;
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) q[e] = ld_shared_tf32(a + (uint32_t)e * ch_bytes);
-                            }
-                            const int c0 = j * E;
-                            if (c0 + E > cv) {  // ragged last slice: zero the missing channels
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    constexpr int per = 4 / ESIZE;  // channels per 32-bit word
-                                    const int c = c0 + e * per;
-                                    if (c >= cv) q[e] = 0u;
-                                    else if (per == 2 && c + 1 >= cv) q[e] &= 0xffffu;
+                                for (int e = 0; e < E; ++e) {
+                                    if constexpr (ESIZE == 2)
+                                        v[jj][e] = ld_shared_u16(a + (uint32_t)e * ch_bytes);
+                                    else
+                                        v[jj][e] = __float_as_uint(ld_shared_f32(a + (uint32_t)e * ch_bytes));
                                 }
                             }
                         }
-                        st_shared_v4(row + (uint32_t)(((sl * groups + j) ^ (h & 7)) << 4), q[0], q[1],
-                                     q[2], q[3]);
+#pragma unroll
+                        for (int jj = 0; jj < kGB; ++jj) {
+                            const int j = j0 + jj;
+                            if (j >= groups) break;
+                            uint32_t q[4] = {0u, 0u, 0u, 0u};
+                            if (off >= 0) {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    if constexpr (ESIZE == 2)
+                                        q[e] = v[jj][2 * e] | (v[jj][2 * e + 1] << 16);
+                                    else
+                                        q[e] = to_tf32(v[jj][e]);
+                                }
+                                const int c0 = j * E;
+                                if (c0 + E > cv) {  // ragged last slice: zero the missing channels
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        constexpr int per = 4 / ESIZE;  // channels per 32-bit word
+                                        const int c = c0 + e * per;
+                                        if (c >= cv) q[e] = 0u;
+                                        else if (per == 2 && c + 1 >= cv) q[e] &= 0xffffu;
+                                    }
+                                }
+                            }
+                            st_shared_v4(row + (uint32_t)(((sl * groups + j) ^ (h & 7)) << 4), q[0], q[1],
+                                         q[2], q[3]);
+                        }
                     }
                 }
                 raw_release(p, sh, rc, lane);
@@ -1645,48 +1752,61 @@ __device__ void role_gather(const TcParams &p, Shared &sh, uint32_t g_base, int 
             const uint32_t s_base = g_base + (uint32_t)stage * p.g_stage_bytes;
             const int co0 = cc * p.kc;
             const int cleft = p.Co - co0;
-            for (int h = gw * 32 + lane; h < p.hbp; h += GW * 32) {
-                const int lam = L0 + h;
-                const int n = lam / img;
-                const int rem = lam - n * img;
-                const int rho = rem / d.X;
-                const int kap = rem - rho * d.X;
-                const int u = rho - (d.Jh - 1) + d.qh;
-                const int v = kap - (d.Jw - 1) + d.qw;
-                const bool ok = n < p.N && u >= 0 && u < p.OH && v >= 0 && v < p.OW;
-                const int cvalid = ok ? (cleft < p.kc ? cleft : p.kc) : 0;
-                const int64_t off =
-                    ok ? ((int64_t)n * p.Co + co0) * plane + (int64_t)u * p.OW + v : 0;
-                constexpr int CHUNKS = 8;
-                uint32_t q[CHUNKS][4];
-                if constexpr (ESIZE == 2) {
-                    const unsigned short *g = static_cast<const unsigned short *>(p.grad_out) + off;
+            // Rows of this thread in batches of RB: all loads of a batch are
+            // issued before any is used, so many are in flight at once.
+            constexpr int RB = ESIZE == 4 ? 2 : 1;  // rows per batch (64 registers of loads)
+            constexpr int CHUNKS = 8;                // 16-byte chunks per 128-byte row
+            constexpr int E = 16 / ESIZE;            // elements per chunk
+            for (int h0 = gw * 32 + lane; h0 < p.hbp; h0 += RB * GW * 32) {
+                int64_t off[RB];
+                int cvalid[RB];
 #pragma unroll
-                    for (int kc = 0; kc < CHUNKS; ++kc) {
+                for (int r = 0; r < RB; ++r) {
+                    const int h = h0 + r * GW * 32;
+                    const int lam = L0 + h;
+                    const int n = lam / img;
+                    const int rem = lam - n * img;
+                    const int rho = rem / d.X;
+                    const int kap = rem - rho * d.X;
+                    const int u = rho - (d.Jh - 1) + d.qh;
+                    const int v = frame_column(kap, p.st_qhalo) - (d.Jw - 1) + d.qw;
+                    const bool ok = h < p.hbp && n < p.N && u >= 0 && u < p.OH && v >= 0 && v < p.OW;
+                    cvalid[r] = ok ? (cleft < p.kc ? cleft : p.kc) : 0;
+                    off[r] = ok ? ((int64_t)n * p.Co + co0) * plane + (int64_t)u * p.OW + v : 0;
+                }
+                uint32_t x[RB][CHUNKS * E];  // raw elements: 16-bit values or float32 bits
 #pragma unroll
-                        for (int e = 0; e < 8; e += 2) {
-                            const int c = kc * 8 + e;
-                            const uint32_t lo = c < cvalid ? ldg_u16(g + c * plane) : 0u;
-                            const uint32_t hi = c + 1 < cvalid ? ldg_u16(g + (c + 1) * plane) : 0u;
-                            q[kc][e / 2] = lo | (hi << 16);
-                        }
-                    }
-                } else {
-                    const float *g = static_cast<const float *>(p.grad_out) + off;
+                for (int r = 0; r < RB; ++r) {
 #pragma unroll
-                    for (int kc = 0; kc < CHUNKS; ++kc) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int c = kc * 4 + e;
-                            q[kc][e] = c < cvalid ? ldg_tf32(g + c * plane) : 0u;
-                        }
+                    for (int c = 0; c < CHUNKS * E; ++c) {
+                        if constexpr (ESIZE == 2)
+                            x[r][c] = c < cvalid[r]
+                                          ? ldg_u16(static_cast<const unsigned short *>(p.grad_out) + off[r] + c * plane)
+                                          : 0u;
+                        else
+                            x[r][c] = c < cvalid[r]
+                                          ? ldg_b32(static_cast<const float *>(p.grad_out) + off[r] + c * plane)
+                                          : 0u;
                     }
                 }
-                const uint32_t row = s_base + (uint32_t)h * 128u;
 #pragma unroll
-                for (int kc = 0; kc < CHUNKS; ++kc)
-                    st_shared_v4(row + (uint32_t)((kc ^ (h & 7)) << 4), q[kc][0], q[kc][1],
-                                 q[kc][2], q[kc][3]);
+                for (int r = 0; r < RB; ++r) {
+                    const int h = h0 + r * GW * 32;
+                    if (h >= p.hbp) break;
+                    const uint32_t row = s_base + (uint32_t)h * 128u;
+#pragma unroll
+                    for (int kc = 0; kc < CHUNKS; ++kc) {
+                        uint32_t q[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if constexpr (ESIZE == 2)
+                                q[e] = x[r][kc * 8 + 2 * e] | (x[r][kc * 8 + 2 * e + 1] << 16);
+                            else
+                                q[e] = to_tf32(x[r][kc * 4 + e]);
+                        }
+                        st_shared_v4(row + (uint32_t)((kc ^ (h & 7)) << 4), q[0], q[1], q[2], q[3]);
+                    }
+                }
             }
             fence_proxy_async();
             __syncwarp();
@@ -1922,6 +2042,49 @@ __device__ void epilogue_stacked(const TcParams &p, const PhaseDesc &d, const Ti
     const int s = p.stride, phases = s * s;
     const int64_t HW = (int64_t)p.H * p.W;
     float *img = p.grad_in + (int64_t)n * p.Ci * HW;
+    if (p.st_qhalo) {
+        // Column taps on N: M-block mb is frame row a = a0 + mb; lane l of
+        // quadrant q is frame element 32q + l, output column b = (32 - halo) q
+        // + l for l < 32 - halo.  Column block i (window tap dx = st_dx0 + i)
+        // of lane l + i holds that tap's term for b, so the output is the sum
+        // over i of block i shifted down by i lanes -- within the warp.
+        const int halo = p.st_qhalo, ncols = st_cols(p);
+        const int b = (32 - halo) * q + lane;
+        for (int mb = 0; mb < p.st_mblocks; ++mb) {
+            const int a = a0 + mb;
+            const bool row_ok = a < d.Hr;
+            for (int g0 = 0; g0 < p.st_n; g0 += 16) {  // 16 columns (phase, ci) at a time
+                uint32_t v[kStMaxTw][16];
+#pragma unroll
+                for (int i = 0; i < kStMaxTw; ++i)
+                    if (i < p.st_tw) tmem_ld16(taddr + (uint32_t)(mb * ncols + i * p.st_n + g0), v[i]);
+                tmem_wait_ld16x4(v);
+                float out[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) out[c] = __uint_as_float(v[0][c]);
+#pragma unroll
+                for (int i = 1; i < kStMaxTw; ++i) {
+                    if (i < p.st_tw) {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c)
+                            out[c] += __shfl_down_sync(0xffffffffu, __uint_as_float(v[i][c]), i);
+                    }
+                }
+                if (row_ok && lane < 32 - halo && b < d.Wr) {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const int col = g0 + c, k = col / p.Ci, ci = col - k * p.Ci;
+                        if (k >= phases) break;
+                        if (k % parts != part) continue;
+                        const int ih = s * a + k / s, iw = s * b + k % s;
+                        if (ih < p.H && iw < p.W) img[(int64_t)ci * HW + (int64_t)ih * p.W + iw] = out[c];
+                    }
+                }
+                __syncwarp();  // converge before the next (warp-collective) TMEM loads
+            }
+        }
+        return;
+    }
     for (int mb = 0; mb < p.st_mblocks; ++mb) {  // M-block mb: tile positions 128 mb ..
         uint32_t v[32];
         const uint32_t ta = taddr + (uint32_t)(mb * p.st_n);
@@ -2063,7 +2226,7 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
             }
         } else
         if constexpr (V == kVarStacked)
-            epilogue_stacked(p, d, ti, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.st_mblocks * p.st_n),
+            epilogue_stacked(p, d, ti, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.st_mblocks * st_cols(p)),
                              q, part, Roles<V>::epi_warps / 4, lane);
         else if (V == kVarFrame64 || p.epi_tma)  // the 64-wide frame always stores through TMA
             epilogue_tma<V>(p, d, ti, taddr, st_base, q, part, lane, bsel);
@@ -2144,17 +2307,19 @@ __device__ void role_mma_pm(const TcParams &p, Shared &sh, uint32_t g_base, uint
 // mode's frame64 plans): the frame columns b < kPmLeft of every window row are
 // zero in every tile, so they are cleared once per G stage (before its first
 // use); each raw slice (16
-// channels x raw_br rows x 56 columns) then lands in the window by 8x8 block
-// transposes: ldmatrix.trans reads 8 channels x 8 columns, stmatrix writes 8
-// window rows x 16 bytes (the slice's two 16-byte channel chunks, swizzled).
+// or 32 channels x raw_br rows x 56 columns) then lands in the window by 8x8
+// block transposes: ldmatrix.trans reads 8 channels x 8 columns, stmatrix
+// writes 8 window rows x 16 bytes (the slice's 16-byte channel chunks,
+// swizzled).
 template <int GW, int NG>  // gather warps, ldmatrix.x4 groups per warp and slice
 __device__ void gather_pm(const TcParams &p, Shared &sh, uint32_t g_base, uint32_t raw_base,
                           uint32_t early_base, int gw, int lane) {
     const int slices = p.kc / p.raw_cs;
+    const int cgs = p.raw_cs / 8;                      // 8-channel groups per slice (2 or 4)
     const uint32_t row_bytes = (uint32_t)(p.raw_bw * 2);
     const uint32_t ch_bytes = row_bytes * (uint32_t)p.raw_br;
     const int nb_col = p.raw_bw / 8;                   // 8-column blocks per grad_out row
-    const int blocks = 2 * p.pm_rows * nb_col;         // per slice: 2 channel groups
+    const int blocks = cgs * p.pm_rows * nb_col;       // 8x8 blocks per slice
     const int groups = (blocks + 3) / 4;               // ldmatrix.x4 per slice
     const int zrows = (p.hbp + kPmPitch - 1) / kPmPitch * kPmLeft;
     int stage = 0;
@@ -2207,7 +2372,7 @@ __device__ void gather_pm(const TcParams &p, Shared &sh, uint32_t g_base, uint32
 #pragma unroll
             for (int j = 0; j < NG; ++j)
                 if (j < ng_mine)
-                    stmatrix_x4(s_base + dst_row[j] + (uint32_t)(((2 * sl) ^ cgk[j]) << 4), r[j]);
+                    stmatrix_x4(s_base + dst_row[j] + (uint32_t)(((cgs * sl) ^ cgk[j]) << 4), r[j]);
             raw_release(p, sh, rc, lane);
         }
         fence_proxy_async();

@@ -17,6 +17,7 @@ namespace dgrad {
 namespace {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t Co_of(const conv2d_grad_input_params &p) { return p.out_channels; }
 int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 
 // Raw-slice geometry of the gather (tiles of whole frame rows only): each
@@ -471,7 +472,7 @@ bool plan_frame64(const conv2d_grad_input_params &p, int esize, const TcParams &
     const int64_t view_end = kPmPitch * (kH - 1) + p.padding_w + kPmLeft + t.tile_p;
     t.pm_rows = (int)(t.rows_per_tile + kH - 1);
     t.hbp = (int)round_up(std::max<int64_t>(view_end, (int64_t)kPmPitch * t.pm_rows), 8);
-    if (2 * t.pm_rows * ((kPmPitch - kPmLeft) / 8) > 4 * kGWarps * kF64Groups) return false;
+
     t.g_stage_bytes = t.hbp * 128;
     PhaseDesc &d = t.ph[0];
     d.X = kPmPitch;
@@ -482,11 +483,9 @@ bool plan_frame64(const conv2d_grad_input_params &p, int esize, const TcParams &
     t.total_tiles = (int64_t)d.p_tiles * t.n_mtiles;
     t.raw_mode = kRawTiled;
     t.raw_rowg = 1;
-    t.raw_cs = 16;
     t.raw_bw = kPmPitch - kPmLeft;
     t.raw_x0 = 0;
     t.raw_br = t.pm_rows | 1;
-    t.raw_slice_bytes = (int)round_up((int64_t)t.raw_cs * t.raw_br * t.raw_bw * esize, 128);
     // TMA store boxes only: 64-row tiles read a quadrant's 16 channels with
     // the 16x256b TMEM shape (all 32 threads busy) into one 16-channel box
     // per warp; 128-row tiles use 8-channel boxes, two per warp when that
@@ -496,13 +495,24 @@ bool plan_frame64(const conv2d_grad_input_params &p, int esize, const TcParams &
     t.ng = 2;
     const int64_t gw = t.packed_bytes + 2 * (int64_t)t.g_stage_bytes;
     t.raw_nr = 0;
-    for (int boxes = t.epi_box_ci == 16 ? 1 : 2; boxes >= 1 && !t.raw_nr; --boxes) {
-        const int64_t epi = round_up(kEpiWarps * boxes * box, kEpiWarps * 128);
-        for (int r = 3; r >= 2 && !t.raw_nr; --r) {
-            if (smem_layout_bytes(epi, (int64_t)r * t.raw_slice_bytes, gw) <= kSmemLimit) {
-                t.raw_nr = r;
-                t.epi_boxes = boxes;
-                t.epi_stage_bytes = (int)epi;
+    // Raw slices of 32 channels (one TMA load per half chunk) when a ring of
+    // at least one such slice fits, else 16: a TMA load costs about the same
+    // time whatever its size up to tens of KB, so fewer, larger loads move
+    // the window in far less time.  The ldmatrix groups per gather warp
+    // (kF64Groups) bound the slice's 8x8 blocks.
+    for (int cs = 16; cs >= 16 && !t.raw_nr; cs /= 2) {
+        if ((cs / 8) * t.pm_rows * ((kPmPitch - kPmLeft) / 8) > 4 * kGWarps * kF64Groups) continue;
+        if (Co_of(p) % cs != 0 && cs == 32) continue;  // whole slices of the chunk's channels
+        t.raw_cs = cs;
+        t.raw_slice_bytes = (int)round_up((int64_t)t.raw_cs * t.raw_br * t.raw_bw * esize, 128);
+        for (int boxes = t.epi_box_ci == 16 ? 1 : 2; boxes >= 1 && !t.raw_nr; --boxes) {
+            const int64_t epi = round_up(kEpiWarps * boxes * box, kEpiWarps * 128);
+            for (int r = cs == 32 ? 2 : 3; r >= (cs == 32 ? 1 : 2) && !t.raw_nr; --r) {
+                if (smem_layout_bytes(epi, (int64_t)r * t.raw_slice_bytes, gw) <= kSmemLimit) {
+                    t.raw_nr = r;
+                    t.epi_boxes = boxes;
+                    t.epi_stage_bytes = (int)epi;
+                }
             }
         }
     }
@@ -606,7 +616,7 @@ bool plan_stacked(const conv2d_grad_input_params &p, int esize, int dtype, Plan 
     const int64_t Th = dy1 - dy0 + 1, Tw = dx1 - dx0 + 1;
     const int64_t Hr = cdiv(H, s), Wr = cdiv(W, s);
     const int64_t X = Wr + Tw - 1, R = Hr + Th - 1;
-    if (X > 128 || N * R * X + 8192 > INT32_MAX) return false;
+    if (X > 128 || N * R * 128 + 8192 > INT32_MAX) return false;
     PhaseDesc &d = t.ph[0];
     d.Hr = (int)Hr; d.Wr = (int)Wr;
     d.Jh = (int)Th; d.Jw = (int)Tw;
@@ -627,13 +637,60 @@ bool plan_stacked(const conv2d_grad_input_params &p, int esize, int dtype, Plan 
     t.w_unit_bytes = (int)w_unit;
     t.packed_bytes = packed;
     t.epi_stage_bytes = 0;
-    // Tile shapes tried in turn: two M-blocks of 128 positions (whole frame
-    // rows up to 256 positions; the window's halo rows are then shared by
-    // twice the outputs) with the weights streamed in tap groups, then one
-    // M-block with the weights resident.  Each with raw slices when a load
-    // mode applies (two or three slots), else the gather reads grad_out
-    // directly.
     bool ok = false;
+    // First choice: the column taps on N as well (TcParams::st_qhalo), so an
+    // MMA covers st_tw taps at once (N = st_tw x st_n) and a tile issues
+    // st_tw times fewer of them.  The quadrant-halo frame (X = 128, each
+    // 32-element quadrant covering 32 - (st_tw - 1) output columns) keeps the
+    // epilogue's column shifts inside one warp; it needs st_tw - 1 <= 3 and
+    // Wr <= 4 (33 - st_tw).  Tiles of two frame rows (two M-blocks).  The
+    // gather warps read grad_out straight from global memory (no raw slices:
+    // a frame row is consecutive grad_out columns, so the loads coalesce, and
+    // the two 80 KB-class G stages leave room for only two raw slots, too few
+    // loads in flight); the weights stay resident when they fit, else stream
+    // one row tap (st_tw taps) per stage.
+    const int64_t nq = Tw * t.st_n;
+    if (Tw >= 2 && Tw <= kStMaxTw && nq <= 256 && 4 * (33 - Tw) >= Wr) {
+        const int rows = (int)std::min<int64_t>(2, Hr);
+        t.st_qhalo = (int)(Tw - 1);
+        t.st_mblocks = rows;
+        t.rows_per_tile = rows;
+        d.X = 128;
+        d.p_tiles = (int)(N * cdiv(Hr, rows));
+        d.hb = (int)((rows + Th - 1) * 128);
+        t.hbp = d.hb;
+        const int64_t g_stage = (int64_t)t.hbp * 128;
+        t.g_stage_bytes = (int)g_stage;
+        plan_raw_slices(p, esize, t, /*none=*/true);
+        const int64_t w_stage = Tw * w_unit;  // one row tap: st_tw taps
+        const int64_t fixed = smem_layout_bytes(0, 0, 2 * g_stage);
+        const int64_t nw = std::min<int64_t>(std::min<int64_t>(kMaxW, Th * t.n_cchunks),
+                                             (kSmemLimit - fixed) / w_stage);
+        if (fixed + packed <= kSmemLimit) {  // resident weights
+            ok = true;
+            t.ng = 2;
+            t.nw = 0;
+            t.taps_per_w = (int)(Th * Tw);
+            t.w_stage_bytes = (int)(Th * Tw * w_unit);
+            t.smem_bytes = (int)(fixed + packed);
+        } else if (nw >= 2) {
+            ok = true;
+            t.ng = 2;
+            t.nw = (int)nw;
+            t.taps_per_w = (int)Tw;
+            t.w_stage_bytes = (int)w_stage;
+            t.smem_bytes = (int)(fixed + nw * w_stage);
+        } else {
+            t.st_qhalo = 0;
+            d.X = (int)X;
+        }
+    }
+    // Otherwise, tile shapes tried in turn: two M-blocks of 128 positions
+    // (whole frame rows up to 256 positions; the window's halo rows are then
+    // shared by twice the outputs) with the weights streamed in tap groups,
+    // then one M-block with the weights resident.  Each with raw slices when
+    // a load mode applies (two or three slots), else the gather reads
+    // grad_out directly.
     for (int mblocks = 2; mblocks >= 1 && !ok; --mblocks) {
         const int rows = (int)std::min<int64_t>(mblocks * 128 / X, Hr);
         if (mblocks == 2 && rows <= 128 / X) continue;  // no more rows than one M-block holds
@@ -689,9 +746,10 @@ bool plan_stacked(const conv2d_grad_input_params &p, int esize, int dtype, Plan 
     t.total_tiles = d.p_tiles;
     t.tile_group = 1;
     const uint32_t fmt = dtype == DGRAD_F32 ? 2u : (dtype == DGRAD_BF16 ? 1u : 0u);
-    t.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(t.st_n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-    uint32_t cols = 32;  // two buffers of st_mblocks accumulators of st_n columns
-    while (cols < (uint32_t)(2 * t.st_mblocks * t.st_n)) cols *= 2;
+    const int ncols = t.st_qhalo ? (int)nq : t.st_n;  // MMA N = accumulator columns per M-block
+    t.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(ncols >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    uint32_t cols = 32;  // two buffers of st_mblocks accumulators of ncols columns
+    while (cols < (uint32_t)(2 * t.st_mblocks * ncols)) cols *= 2;
     t.tmem_cols = cols;
     k.Ci = (int)Ci; k.Co = (int)Co; k.kH = (int)kH; k.kW = (int)kW; k.stride = s;
     k.m_tile = t.st_n; k.n_mtiles = 1; k.kc = t.kc; k.n_cchunks = t.n_cchunks;
