@@ -725,12 +725,20 @@ def run_gpu(args, wl, key):
                                   "traffic_over_algorithmic": o_traffic / o_alg if o_traffic else None}
             out["per_config"] = per
             out["tf32_peak"] = {"value": tf32_peak, "unit": "TFLOP/s", "source": tf32_src}
-            # The forward convolution of the bench layer (stride 1 only).
+            # The forward convolution of the bench layer, and of the strided
+            # layer (stride 2: space-to-depth copy of x + weight split, then
+            # the stride-1 path).
+            f_ms = forward_call(dg, workloads, wl, dev, stream)
+            out["forward"] = {"op": "conv2d_forward (weight flip + kernel, pack in the kernel or before it)",
+                              "workload": wl.name, "ms_per_call": f_ms,
+                              "tflops": useful_flops(wl) / (f_ms * 1e-3) / 1e12}
             if wl.stride == 1:
-                f_ms = forward_call(dg, workloads, wl, dev, stream)
-                out["forward"] = {"op": "conv2d_forward (weight flip + kernel, pack in the kernel or before it)",
-                                  "workload": wl.name, "ms_per_call": f_ms,
-                                  "tflops": useful_flops(wl) / (f_ms * 1e-3) / 1e12}
+                swl = workloads.STRIDED
+                fs_ms = forward_call(dg, workloads, swl, dev, stream)
+                out["forward_strided"] = {
+                    "op": "conv2d_forward at stride 2 (space-to-depth of x, weight split, stride-1 path)",
+                    "workload": swl.name, "ms_per_call": fs_ms,
+                    "tflops": useful_flops(swl) / (fs_ms * 1e-3) / 1e12}
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(wl)
         print(json.dumps(out), flush=True)

@@ -257,8 +257,8 @@ def conv2d_grad_input_noalloc(grad_out, weight, grad_in, params: Params, dtype: 
 
 
 def conv2d_forward(x, weight, out, params: Params, dtype: int, stream=None) -> None:
-    """Forward convolution of the layer ``params`` describes: x [N,Ci,H,W],
-    weight [Co,Ci,kH,kW] -> out [N,Co,OH,OW] float32."""
+    """Forward convolution of the layer ``params`` describes (stride 1 to 8):
+    x [N,Ci,H,W], weight [Co,Ci,kH,kW] -> out [N,Co,OH,OW] float32."""
     n_out, n_w, n_x = _sizes(params)
     rc = library().conv2d_forward(_addr(x, "x", _in_dtype(dtype), n_x),
                                   _addr(weight, "weight", _in_dtype(dtype), n_w),

@@ -40,6 +40,73 @@ int run_main(const dgrad::Plan &plan, const void *grad_out, const void *packed_o
     return cuda_status(dgrad::launch_tc(plan, grad_out, packed_or_weight, grad_in, stream));
 }
 
+// The stride-1 forward convolution of layer p (padding at most kernel - 1):
+// the input gradient of the layer with the channel axes swapped, the kernel
+// flipped and padding k - 1 - p, so out plays grad_in and x plays grad_out.
+// The weights are flipped and transposed into a stream-ordered temporary
+// buffer (and packed there unless the kernel packs them itself).
+int forward_stride1(const void *x, const void *weight, float *out, const conv2d_grad_input_params *p,
+                    int dtype, cudaStream_t st) {
+    conv2d_grad_input_params q;
+    q.batch = p->batch;
+    q.in_channels = p->out_channels;
+    q.in_h = p->out_h;
+    q.in_w = p->out_w;
+    q.out_channels = p->in_channels;
+    q.kernel_h = p->kernel_h;
+    q.kernel_w = p->kernel_w;
+    q.stride = 1;
+    q.padding_h = p->kernel_h - 1 - p->padding_h;
+    q.out_h = p->in_h;
+    q.out_w = p->in_w;
+    q.padding_w = p->kernel_w - 1 - p->padding_w;
+    dgrad::Plan plan;
+    int rc = plan_for(&q, dtype, &plan);
+    if (rc != DGRAD_OK) return rc;
+    const size_t wt_bytes = ((size_t)p->out_channels * p->in_channels * p->kernel_h * p->kernel_w *
+                                 plan.esize + 255) / 256 * 256;
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocAsync(&ws, wt_bytes + plan.workspace, st);
+    if (e != cudaSuccess) return cuda_status((int)e);
+    void *packed = static_cast<char *>(ws) + wt_bytes;
+    int le = dgrad::launch_flip_transpose(weight, ws, (int)p->out_channels, (int)p->in_channels,
+                                          (int)p->kernel_h, (int)p->kernel_w, plan.esize, st);
+    if (le == (int)cudaSuccess && plan.kernel == DGRAD_KERNEL_TC && plan.workspace > 0)
+        le = dgrad::launch_pack(plan, ws, packed, st);
+    const bool prepacked = plan.kernel == DGRAD_KERNEL_TC && plan.workspace > 0;
+    rc = le == (int)cudaSuccess ? run_main(plan, x, prepacked ? packed : ws, out, st) : cuda_status(le);
+    e = cudaFreeAsync(ws, st);
+    if (rc == DGRAD_OK && e != cudaSuccess) rc = cuda_status((int)e);
+    return rc;
+}
+
+// The split of a stride > 1 forward convolution (FwdSplit): false when the
+// stride is above kMaxFwdStride.
+bool forward_split(const conv2d_grad_input_params *p, dgrad::FwdSplit *f) {
+    const int s = (int)p->stride;
+    if (s < 2 || s > dgrad::kMaxFwdStride) return false;
+    f->N = (int)p->batch; f->Ci = (int)p->in_channels; f->H = (int)p->in_h; f->W = (int)p->in_w;
+    f->Co = (int)p->out_channels; f->kH = (int)p->kernel_h; f->kW = (int)p->kernel_w;
+    f->s = s; f->ph = (int)p->padding_h; f->pw = (int)p->padding_w;
+    f->OH = (int)p->out_h; f->OW = (int)p->out_w;
+    auto floor_div = [](int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); };
+    bool rh[dgrad::kMaxFwdStride] = {}, rw[dgrad::kMaxFwdStride] = {};
+    for (int t = 0; t < f->kH; ++t) rh[((t - f->ph) % s + s) % s] = true;
+    for (int t = 0; t < f->kW; ++t) rw[((t - f->pw) % s + s) % s] = true;
+    f->nr = f->nc = 0;
+    for (int r = 0; r < s; ++r) {
+        if (rh[r]) f->R[f->nr++] = r;
+        if (rw[r]) f->C[f->nc++] = r;
+    }
+    f->jmin = floor_div(-f->ph, s);
+    f->imin = floor_div(-f->pw, s);
+    f->KH = floor_div(f->kH - 1 - f->ph, s) - f->jmin + 1;
+    f->KW = floor_div(f->kW - 1 - f->pw, s) - f->imin + 1;
+    f->Hx = f->OH + f->KH - 1;
+    f->Wx = f->OW + f->KW - 1;
+    return true;
+}
+
 }  // namespace
 
 namespace dgrad {
@@ -86,42 +153,45 @@ int conv2d_forward(const void *x, const void *weight, float *out, const conv2d_g
     dgrad::Plan layer;
     int rc = plan_for(p, dtype, &layer);
     if (rc != DGRAD_OK) return rc;
-    if (p->stride != 1 || p->padding_h > p->kernel_h - 1 || p->padding_w > p->kernel_w - 1)
-        return DGRAD_ERR_UNSUPPORTED;
-    // At stride 1 the forward convolution is the input gradient of the layer
-    // with the channel axes swapped, the kernel flipped and padding k - 1 - p:
-    // out plays grad_in, x plays grad_out.
+    if (!aligned(x, layer.esize) || !aligned(weight, layer.esize) || !aligned(out, 4)) return DGRAD_ERR_ALIGNMENT;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (p->stride == 1) {
+        if (p->padding_h > p->kernel_h - 1 || p->padding_w > p->kernel_w - 1) return DGRAD_ERR_UNSUPPORTED;
+        return forward_stride1(x, weight, out, p, dtype, st);
+    }
+    // Stride s > 1: the same output as a stride-1 valid correlation of the
+    // space-to-depth copy X'' of x with the rearranged weights W'' (FwdSplit
+    // in dgrad_internal.h): with kh - ph = s j + r, input row s oh - ph + kh
+    // is row oh + j - jmin of residue r's decimated image.
+    dgrad::FwdSplit f;
+    if (!forward_split(p, &f)) return DGRAD_ERR_UNSUPPORTED;
     conv2d_grad_input_params q;
     q.batch = p->batch;
-    q.in_channels = p->out_channels;
-    q.in_h = p->out_h;
-    q.in_w = p->out_w;
-    q.out_channels = p->in_channels;
-    q.kernel_h = p->kernel_h;
-    q.kernel_w = p->kernel_w;
+    q.in_channels = (uint32_t)(f.nr * f.nc) * p->in_channels;
+    q.in_h = (uint32_t)f.Hx;
+    q.in_w = (uint32_t)f.Wx;
+    q.out_channels = p->out_channels;
+    q.kernel_h = (uint32_t)f.KH;
+    q.kernel_w = (uint32_t)f.KW;
     q.stride = 1;
-    q.padding_h = p->kernel_h - 1 - p->padding_h;
-    q.out_h = p->in_h;
-    q.out_w = p->in_w;
-    q.padding_w = p->kernel_w - 1 - p->padding_w;
-    dgrad::Plan plan;
-    rc = plan_for(&q, dtype, &plan);
+    q.padding_h = 0;
+    q.out_h = p->out_h;
+    q.out_w = p->out_w;
+    q.padding_w = 0;
+    dgrad::Plan inner;
+    rc = plan_for(&q, dtype, &inner);
     if (rc != DGRAD_OK) return rc;
-    if (!aligned(x, plan.esize) || !aligned(weight, plan.esize) || !aligned(out, 4)) return DGRAD_ERR_ALIGNMENT;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const size_t wt_bytes = ((size_t)p->out_channels * p->in_channels * p->kernel_h * p->kernel_w *
-                                 plan.esize + 255) / 256 * 256;
-    void *ws = nullptr;
-    cudaError_t e = cudaMallocAsync(&ws, wt_bytes + plan.workspace, st);
+    const size_t es = (size_t)layer.esize;
+    const size_t xs_bytes = ((size_t)q.batch * q.in_channels * q.in_h * q.in_w * es + 255) / 256 * 256;
+    const size_t ws_bytes = ((size_t)q.out_channels * q.in_channels * q.kernel_h * q.kernel_w * es + 255) / 256 * 256;
+    void *buf = nullptr;
+    cudaError_t e = cudaMallocAsync(&buf, xs_bytes + ws_bytes, st);
     if (e != cudaSuccess) return cuda_status((int)e);
-    void *packed = static_cast<char *>(ws) + wt_bytes;
-    int le = dgrad::launch_flip_transpose(weight, ws, (int)p->out_channels, (int)p->in_channels,
-                                          (int)p->kernel_h, (int)p->kernel_w, plan.esize, st);
-    if (le == (int)cudaSuccess && plan.kernel == DGRAD_KERNEL_TC && plan.workspace > 0)
-        le = dgrad::launch_pack(plan, ws, packed, st);
-    const bool prepacked = plan.kernel == DGRAD_KERNEL_TC && plan.workspace > 0;
-    rc = le == (int)cudaSuccess ? run_main(plan, x, prepacked ? packed : ws, out, st) : cuda_status(le);
-    e = cudaFreeAsync(ws, st);
+    void *xs = buf, *wsplit = static_cast<char *>(buf) + xs_bytes;
+    int le = dgrad::launch_space_to_depth(f, x, xs, layer.esize, st);
+    if (le == (int)cudaSuccess) le = dgrad::launch_split_weights(f, weight, wsplit, layer.esize, st);
+    rc = le == (int)cudaSuccess ? forward_stride1(xs, wsplit, out, &q, dtype, st) : cuda_status(le);
+    e = cudaFreeAsync(buf, st);
     if (rc == DGRAD_OK && e != cudaSuccess) rc = cuda_status((int)e);
     return rc;
 }

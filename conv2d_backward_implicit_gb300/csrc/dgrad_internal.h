@@ -222,6 +222,19 @@ struct PackParams {
     int th[kMaxPhases], tw[kMaxPhases], Jh[kMaxPhases], Jw[kMaxPhases];
 };
 
+// The strided forward convolution as a stride-1 valid correlation (api.cu,
+// pack.cu): residues r of kh - ph (c of kw - pw) modulo the stride that some
+// tap reaches, X''[n][(pr, pc, ci)][a][b] = x[n][ci][s (a + jmin) + R[pr]]
+// [s (b + imin) + C[pc]] (zero outside the image), W''[co][(pr, pc, ci)][j][i]
+// = w[co][ci][s (j + jmin) + R[pr] + ph][s (i + imin) + C[pc] + pw] (zero
+// outside the kernel).
+constexpr int kMaxFwdStride = 8;
+struct FwdSplit {
+    int N, Ci, H, W, Co, kH, kW, s, ph, pw;
+    int nr, nc, R[kMaxFwdStride], C[kMaxFwdStride];
+    int jmin, imin, KH, KW, Hx, Wx, OH, OW;
+};
+
 struct SimtParams {
     int N, Ci, H, W, Co, kH, kW, stride, ph, pw, OH, OW;
 };
@@ -249,6 +262,9 @@ int launch_pack(const Plan &plan, const void *weight, void *packed, void *stream
 // wt[ci][co][kh][kw] = w[co][ci][kH-1-kh][kW-1-kw] (pack.cu).
 int launch_flip_transpose(const void *w, void *wt, int Co, int Ci, int kH, int kW, int esize,
                           void *stream);
+// X'' and W'' of a FwdSplit (esize 2 or 4), in `stream` order.
+int launch_space_to_depth(const FwdSplit &f, const void *x, void *xs, int esize, void *stream);
+int launch_split_weights(const FwdSplit &f, const void *w, void *ws, int esize, void *stream);
 int launch_tc(const Plan &plan, const void *grad_out, const void *packed, float *grad_in,
               void *stream);
 int launch_simt(const Plan &plan, const void *grad_out, const void *weight, float *grad_in,

@@ -120,7 +120,91 @@ __global__ void __launch_bounds__(256) flip_transpose_kernel(const T *__restrict
     }
 }
 
+// X''[n][(pr, pc, ci)][a][b] of a FwdSplit, one element per thread (writes
+// coalesced along b; the reads stride by s along x's rows).
+template <typename T>
+__global__ void __launch_bounds__(256) space_to_depth_kernel(const T *__restrict__ x, T *__restrict__ xs,
+                                                             const __grid_constant__ FwdSplit f,
+                                                             int64_t total) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        int64_t r = idx;
+        const int b = (int)(r % f.Wx); r /= f.Wx;
+        const int a = (int)(r % f.Hx); r /= f.Hx;
+        const int ch = (int)(r % ((int64_t)f.nr * f.nc * f.Ci));
+        const int n = (int)(r / ((int64_t)f.nr * f.nc * f.Ci));
+        const int ci = ch % f.Ci, pc = (ch / f.Ci) % f.nc, pr = ch / (f.Ci * f.nc);
+        const int ih = f.s * (a + f.jmin) + f.R[pr], iw = f.s * (b + f.imin) + f.C[pc];
+        xs[idx] = (ih >= 0 && ih < f.H && iw >= 0 && iw < f.W)
+                      ? x[(((int64_t)n * f.Ci + ci) * f.H + ih) * f.W + iw]
+                      : T(0);
+    }
+}
+
+// W''[co][(pr, pc, ci)][j][i] of a FwdSplit.
+template <typename T>
+__global__ void __launch_bounds__(256) split_weights_kernel(const T *__restrict__ w, T *__restrict__ ws,
+                                                            const __grid_constant__ FwdSplit f,
+                                                            int64_t total) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        int64_t r = idx;
+        const int i = (int)(r % f.KW); r /= f.KW;
+        const int j = (int)(r % f.KH); r /= f.KH;
+        const int ch = (int)(r % ((int64_t)f.nr * f.nc * f.Ci));
+        const int co = (int)(r / ((int64_t)f.nr * f.nc * f.Ci));
+        const int ci = ch % f.Ci, pc = (ch / f.Ci) % f.nc, pr = ch / (f.Ci * f.nc);
+        const int kh = f.s * (j + f.jmin) + f.R[pr] + f.ph, kw = f.s * (i + f.imin) + f.C[pc] + f.pw;
+        ws[idx] = (kh >= 0 && kh < f.kH && kw >= 0 && kw < f.kW)
+                      ? w[(((int64_t)co * f.Ci + ci) * f.kH + kh) * f.kW + kw]
+                      : T(0);
+    }
+}
+
+// One launch of an elementwise kernel over `total` elements with programmatic
+// stream serialization (the next kernel's prologue may overlap this one).
+template <typename K, typename... A>
+int launch_elementwise(K kern, int64_t total, void *stream, A... args) {
+    if (total == 0) return (int)cudaSuccess;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 8192) blocks = 8192;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args..., total);
+    if (e != cudaSuccess) return (int)e;
+    return (int)cudaGetLastError();
+}
+
 }  // namespace
+
+int launch_space_to_depth(const FwdSplit &f, const void *x, void *xs, int esize, void *stream) {
+    const int64_t total = (int64_t)f.N * f.nr * f.nc * f.Ci * f.Hx * f.Wx;
+    if (esize == 4)
+        return launch_elementwise(space_to_depth_kernel<float>, total, stream, static_cast<const float *>(x),
+                                  static_cast<float *>(xs), f);
+    return launch_elementwise(space_to_depth_kernel<unsigned short>, total, stream,
+                              static_cast<const unsigned short *>(x), static_cast<unsigned short *>(xs), f);
+}
+
+int launch_split_weights(const FwdSplit &f, const void *w, void *ws, int esize, void *stream) {
+    const int64_t total = (int64_t)f.Co * f.nr * f.nc * f.Ci * f.KH * f.KW;
+    if (esize == 4)
+        return launch_elementwise(split_weights_kernel<float>, total, stream, static_cast<const float *>(w),
+                                  static_cast<float *>(ws), f);
+    return launch_elementwise(split_weights_kernel<unsigned short>, total, stream,
+                              static_cast<const unsigned short *>(w), static_cast<unsigned short *>(ws), f);
+}
 
 int launch_flip_transpose(const void *w, void *wt, int Co, int Ci, int kH, int kW, int esize,
                           void *stream) {

@@ -174,22 +174,32 @@ uint64_t conv2d_grad_input_set_wait_limit_ns(uint64_t ns);
 #define DGRAD_DEBUG_SKIP_ARRIVE 1
 int conv2d_grad_input_set_debug(int flags);
 
-/* The forward convolution of the same layer, stride 1:
+/* The forward convolution of the same layer:
  *
  *   out[n,co,oh,ow] = sum over ci < Ci, kh < kH, kw < kW of
- *                     x[n,ci,oh-padding_h+kh, ow-padding_w+kw] * weight[co,ci,kh,kw]
+ *                     x[n,ci,stride*oh-padding_h+kh, stride*ow-padding_w+kw] * weight[co,ci,kh,kw]
  *
  * (x zero outside the image) -- the convolution whose input gradient
  * conv2d_grad_input computes (the page's header comment defines the
  * gradient as its adjoint).  `p` describes the layer exactly as for
  * conv2d_grad_input: x is [batch, in_channels, in_h, in_w] of dtype, weight
  * [out_channels, in_channels, kernel_h, kernel_w] of dtype, out [batch,
- * out_channels, out_h, out_w] float32, overwritten.  At stride 1 this is the
- * input gradient of a layer with the roles of the channel axes swapped, the
- * kernel flipped and padding kernel - 1 - padding; the call flips and
- * transposes the weights into a stream-ordered temporary buffer and runs
- * the same kernels.  Stride > 1 or a padding above kernel - 1 returns
- * DGRAD_ERR_UNSUPPORTED (nothing is enqueued); other argument errors as for
+ * out_channels, out_h, out_w] float32, overwritten.
+ *  - Stride 1: the input gradient of a layer with the roles of the channel
+ *    axes swapped, the kernel flipped and padding kernel - 1 - padding; the
+ *    call flips and transposes the weights into a stream-ordered temporary
+ *    buffer and runs the same kernels.  A padding above kernel - 1 returns
+ *    DGRAD_ERR_UNSUPPORTED.
+ *  - Stride s from 2 to 8: one stride-1 correlation without padding of a
+ *    space-to-depth copy of x (one channel group per residue r of kh -
+ *    padding_h and c of kw - padding_w modulo s that a tap reaches:
+ *    [batch][(r, c, ci)][out_h + KH - 1][out_w + KW - 1], KH = floor((kH - 1
+ *    - padding_h) / s) - floor(-padding_h / s) + 1) with the weights
+ *    rearranged to match ([out_channels][(r, c, ci)][KH][KW], zero where a
+ *    residue has no tap); both go to one stream-ordered temporary buffer and
+ *    the stride-1 path runs on them.  Stride above 8 returns
+ *    DGRAD_ERR_UNSUPPORTED.
+ * Nothing is enqueued on an error; other argument errors as for
  * conv2d_grad_input. */
 int conv2d_forward(const void *x, const void *weight, float *out, const conv2d_grad_input_params *p,
                    int dtype, struct CUstream_st *stream);

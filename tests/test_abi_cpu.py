@@ -136,9 +136,9 @@ def test_stride_above_four_uses_cuda_cores(lib):
 
 
 def test_forward_rejects_what_it_does_not_run(lib):
-    # Stride > 1 or padding above kernel - 1: unsupported, before any device work
-    # (the pointers are never touched).
-    p = dg.Params(2, 16, 10, 10, 24, 3, 3, 2, 1, 5, 5, 1)
+    # Stride above 8, or padding above kernel - 1 at stride 1: unsupported,
+    # before any device work (the pointers are never touched).
+    p = dg.Params(2, 16, 40, 40, 24, 3, 3, 9, 1, 5, 5, 1)
     assert lib.conv2d_forward(16, 16, 16, ctypes.byref(p), dg.DGRAD_BF16, None) == 4
     p = dg.Params(2, 16, 10, 10, 24, 3, 3, 1, 3, 14, 14, 3)
     assert lib.conv2d_forward(16, 16, 16, ctypes.byref(p), dg.DGRAD_BF16, None) == 4
