@@ -813,6 +813,25 @@ def record_traffic_file(args, wl, key):
     return 0
 
 
+PROBES = {"mma": "mma_rate.cu", "tma": "tma_rate.cu", "tma_store": "tma_store_rate.cu"}
+
+
+def run_probe(name: str) -> int:
+    """Builds (nvcc, sm_103a) and runs one of the probes beside the package:
+    tcgen05.mma issue rate per shape, TMA load and TMA store throughput per
+    copy shape and number of issuing threads -- the device rates the kernels'
+    design rests on.  Prints the probe's own report."""
+    import shutil
+    src = os.path.join(ROOT, "conv2d_backward_implicit_gb300", "probes", PROBES[name])
+    out_dir = os.path.join(ROOT, "conv2d_backward_implicit_gb300", "_build", "probes")
+    os.makedirs(out_dir, exist_ok=True)
+    exe = os.path.join(out_dir, name)
+    nvcc = os.environ.get("NVCC") or shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", src, "-o", exe],
+                   check=True)
+    return subprocess.run([exe]).returncode
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -828,7 +847,11 @@ def main(argv=None):
                     help="only launch the dgrad kernel L times (for an ncu capture)")
     ap.add_argument("--record-traffic", metavar="CSV", default=None,
                     help="write profiles/dgrad_tc_<config>.traffic.json from an ncu CSV")
+    ap.add_argument("--probe", choices=sorted(PROBES), default=None,
+                    help="build and run a device-rate probe (tcgen05.mma, TMA loads or stores)")
     args = ap.parse_args(argv)
+    if args.probe:
+        return run_probe(args.probe)
     from conv2d_backward_implicit_gb300 import workloads
     wl = workloads.BY_KEY[args.config]
     if args.record_traffic:

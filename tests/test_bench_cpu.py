@@ -90,3 +90,17 @@ def test_shard_bounds_cover_the_batch_once():
                 assert b == c
             sizes = [b - a for a, b in spans]
             assert max(sizes) - min(sizes) <= 1
+
+
+def test_probes_compile_for_sm103a():
+    # The device-rate probes bench.py --probe runs (cross-compiled here, no GPU).
+    import shutil
+    import subprocess
+    import tempfile
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    for name, src in bench.PROBES.items():
+        path = bench.ROOT + "/conv2d_backward_implicit_gb300/probes/" + src
+        with tempfile.TemporaryDirectory() as d:
+            r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
+                                path, "-o", d + "/" + name], capture_output=True, text=True)
+            assert r.returncode == 0, r.stderr
