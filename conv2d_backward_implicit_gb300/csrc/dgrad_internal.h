@@ -63,7 +63,7 @@ constexpr int kRawPlaneMaxBytes = 49152;      // largest whole-plane raw slice
 constexpr int kMaxRaw = 8;                    // raw-slice ring slots
 constexpr int kMaxW = 8;                      // streamed weight stages
 constexpr int kMaxGatherRows = 6;             // window rows per gather thread (raw-slice gather)
-constexpr int kMaxMnPieces = 11;              // 16-byte pieces per gather thread and stage (MN-major)
+constexpr int kMaxMnPieces = 13;              // 16-byte pieces per gather thread and stage (MN-major)
 constexpr int kStMaxTw = 4;                   // stacked mode: column taps stacked on N (at most)
 constexpr int kPmPitch = 64;  // positions-on-M mode: frame positions per grad_out row
 constexpr int kPmLeft = 8;    // zero columns before grad_out column 0 in each frame row

@@ -53,27 +53,45 @@ namespace {
 // Kernel variants.  Pair and Stacked are the general mode with its paired
 // column-phase epilogue or its stacked-phase MMA and epilogue compiled in
 // (separate variants keep the general one's register allocation lean).
-constexpr int kVarGeneral = 0, kVarFrame64 = 1, kVarPosM = 2, kVarPair = 3, kVarStacked = 4;
-__host__ __device__ constexpr bool is_general(int v) { return v == kVarGeneral || v == kVarPair || v == kVarStacked; }
+constexpr int kVarGeneral = 0, kVarFrame64 = 1, kVarPosM = 2, kVarPair = 3, kVarStacked = 4, kVarMN = 5;
+__host__ __device__ constexpr bool is_general(int v) {
+    return v == kVarGeneral || v == kVarPair || v == kVarStacked || v == kVarMN;
+}
 
 // Warp roles of each variant: epilogue warps first, then the MMA warp, the
-// producer warp and the gather warps.
+// producer warp(s) and the gather warps.  w2_warp >= 0: a second producer
+// warp -- with streamed weights and raw slices, one warp issues the raw
+// slices and the other the weight stages, because one thread's bulk copies
+// run one after another (each about 1.1K cycles, whatever its size) while
+// copies issued by different warps overlap.
 template <int V>
 struct Roles {
-    static constexpr int epi_warps = kEpiWarps, mma_warp = kMmaWarp, w_warp = kWWarp;
+    static constexpr int epi_warps = kEpiWarps, mma_warp = kMmaWarp, w_warp = kWWarp, w2_warp = -1;
     static constexpr int g_warp0 = kGWarp0, g_warps = kGWarps, threads = kThreads;
+};
+// Paired column phases and the MN-major 1x1 mode stream their weights: two
+// producer warps and five gather warps.
+template <>
+struct Roles<kVarPair> {
+    static constexpr int epi_warps = kEpiWarps, mma_warp = kMmaWarp, w_warp = kWWarp, w2_warp = kWWarp + 1;
+    static constexpr int g_warp0 = kGWarp0 + 1, g_warps = kGWarps - 1, threads = kThreads;
+};
+template <>
+struct Roles<kVarMN> {
+    static constexpr int epi_warps = kEpiWarps, mma_warp = kMmaWarp, w_warp = kWWarp, w2_warp = kWWarp + 1;
+    static constexpr int g_warp0 = kGWarp0 + 1, g_warps = kGWarps - 1, threads = kThreads;
 };
 // Stacked-phase mode: a short epilogue (one TMEM read and s^2 Ci stores per
 // position) and a long gather, so four epilogue warps (one per TMEM lane
 // quadrant) and ten gather warps.
 template <>
 struct Roles<kVarStacked> {
-    static constexpr int epi_warps = 4, mma_warp = 4, w_warp = 5;
+    static constexpr int epi_warps = 4, mma_warp = 4, w_warp = 5, w2_warp = -1;
     static constexpr int g_warp0 = 6, g_warps = 10, threads = 512;
 };
 template <>
 struct Roles<kVarPosM> {
-    static constexpr int epi_warps = kPmEpiWarps, mma_warp = kPmMmaWarp, w_warp = kPmWWarp;
+    static constexpr int epi_warps = kPmEpiWarps, mma_warp = kPmMmaWarp, w_warp = kPmWWarp, w2_warp = -1;
     static constexpr int g_warp0 = kPmGWarp0, g_warps = kPmGWarps, threads = kPmThreads;
 };
 
@@ -1119,6 +1137,110 @@ __device__ __noinline__ void raw_w_producer(const TcParams &p, Shared &sh, uint3
     }
 }
 
+// The two streams of raw_w_producer, each on its own producer warp (lane 0)
+// for the variants with two (Roles::w2_warp): raw slices for each tile /
+// channel chunk / slice, and weight stages for each tile / channel chunk /
+// tap group (a pair: both members' taps of a chunk together), each in the
+// order its consumers drain it.  Each gives up on the wait limit (abort flag,
+// error word) and then waits for its own copies still in flight.
+__device__ __noinline__ void raw_stream_producer(const TcParams &p, Shared &sh, uint32_t raw_base) {
+    const int slices = p.kc / p.raw_cs;
+    TileWalk rw{first_tile(p), nullptr, 0, 0, 0};
+    bool live = walk_load(p, rw);
+    int rcc = 0, rsl = 0, rc0 = 0, slot = 0;
+    uint32_t ph = 0;
+    int64_t issued = 0;
+    bool aborted = false;
+    while (live) {
+        if (!wait_bar(smem_u32(&sh.empty_raw[slot]), ph ^ 1u, p, sh)) {
+            aborted = true;
+            break;
+        }
+        issue_raw_slice(p, raw_base + (uint32_t)slot * p.raw_slice_bytes, rw.u_first, rc0, rw.n,
+                        smem_u32(&sh.full_raw[slot]));
+        ++issued;
+        if (++slot == p.raw_nr) {
+            slot = 0;
+            ph ^= 1u;
+        }
+        rc0 += p.raw_cs;
+        if (++rsl == slices) {
+            rsl = 0;
+            if (++rcc == p.n_cchunks) {
+                rcc = 0;
+                rc0 = 0;
+                rw.t = next_tile(p, rw.t);
+                live = walk_load(p, rw);
+            }
+        }
+    }
+    if (aborted) {
+        const int64_t k_end = issued < p.raw_nr ? issued : p.raw_nr;
+        for (int64_t k = 0; k < k_end; ++k) {
+            const int64_t q = issued - 1 - k;
+            wait_drain(smem_u32(&sh.full_raw[q % p.raw_nr]), (uint32_t)((q / p.raw_nr) & 1), p, sh);
+        }
+    }
+}
+
+__device__ __noinline__ void weight_stream_producer(const TcParams &p, Shared &sh, uint32_t w_base) {
+    const uint8_t *wsrc = static_cast<const uint8_t *>(p.packed);
+    const uint32_t w_unit = (uint32_t)p.w_unit_bytes;
+    TileWalk ww{first_tile(p), nullptr, 0, 0, 0};
+    bool live = walk_load(p, ww);
+    int wcc = 0, wk = 0, wt0 = 0, wtaps = 0, stage = 0;
+    uint32_t ph = 0;
+    const uint8_t *wblk = nullptr;  // packed weights of (tile, member, chunk wcc)
+    if (live) {
+        wtaps = ww.d->Jh * ww.d->Jw;
+        wblk = wsrc + w_block_off(p, *ww.d, ww.mt, 0);
+    }
+    int64_t issued = 0;
+    bool aborted = false;
+    while (live) {
+        if (!wait_bar(smem_u32(&sh.empty_w[stage]), ph ^ 1u, p, sh)) {
+            aborted = true;
+            break;
+        }
+        const int ng = wtaps - wt0 < p.taps_per_w ? wtaps - wt0 : p.taps_per_w;
+        const uint32_t bytes = (uint32_t)ng * w_unit;
+        const uint32_t full = smem_u32(&sh.full_w[stage]);
+        mbar_arrive_expect_tx(full, bytes);
+        bulk_g2s(w_base + (uint32_t)stage * p.w_stage_bytes, wblk + (size_t)wt0 * w_unit, bytes, full);
+        ++issued;
+        if (++stage == p.nw) {
+            stage = 0;
+            ph ^= 1u;
+        }
+        wt0 += p.taps_per_w;
+        if (wt0 >= wtaps) {
+            wt0 = 0;
+            if (p.pair_rw && wk == 0) {
+                wk = 1;  // the pair's other column phase, same chunk
+            } else {
+                wk = 0;
+                if (++wcc == p.n_cchunks) {
+                    wcc = 0;
+                    ww.t = next_tile(p, ww.t);
+                    live = walk_load(p, ww);
+                }
+            }
+            if (live) {
+                const PhaseDesc &dk = ww.d[wk];  // a pair's phases are adjacent in ph[]
+                wtaps = dk.Jh * dk.Jw;
+                wblk = wsrc + w_block_off(p, dk, ww.mt, wcc);
+            }
+        }
+    }
+    if (aborted) {
+        const int64_t k_end = issued < p.nw ? issued : p.nw;
+        for (int64_t k = 0; k < k_end; ++k) {
+            const int64_t q = issued - 1 - k;
+            wait_drain(smem_u32(&sh.full_w[q % p.nw]), (uint32_t)((q / p.nw) & 1), p, sh);
+        }
+    }
+}
+
 // Warp 9, lane 0: packed weights into shared memory with bulk copies.
 template <int V>
 __device__ void role_weights(const TcParams &p, Shared &sh, uint32_t w_base, uint32_t raw_base,
@@ -1243,7 +1365,7 @@ __device__ void role_mma(const TcParams &p, Shared &sh, uint32_t g_base, uint32_
                 // 32-byte K step is an add to a base descriptor.
                 const uint64_t wd0 = sw128_desc(w_grp);
                 // MN-major grad_out: a 16-channel K step is two 8-row groups.
-                const bool mn = V == kVarGeneral && p.mn_b;
+                const bool mn = (V == kVarGeneral || V == kVarMN) && p.mn_b;
                 const uint32_t mn_sbo = (uint32_t)p.mn_atoms * 1024u;
                 const uint64_t gd0 = mn ? sw128_mn_desc(g_stage, 1024u, mn_sbo)
                                         : sw128_desc(g_stage + (uint32_t)(p.view0 * 128));
@@ -1643,9 +1765,10 @@ __device__ void gather_from_raw(const TcParams &p, Shared &sh, uint32_t g_base,
 // to its place in the stage's swizzled MN-major atoms.  Pieces past the end
 // of a plane hold whatever follows it: those output columns are never stored.
 // Channels past Co are zero.
+template <int GW>
 __device__ void gather_mn(const TcParams &p, Shared &sh, uint32_t g_base, uint32_t raw_base,
                           uint32_t early_base, int gw, int lane) {
-    constexpr int kStep = kGWarps * 32;
+    constexpr int kStep = GW * 32;
     const uint32_t plane = (uint32_t)(p.OH * p.OW) * 2u;  // bytes per channel plane (a multiple of 8)
     const int pieces = p.mn_atoms * 8;                     // 16-byte pieces per channel
     const int items = p.kc * pieces;
@@ -1894,7 +2017,7 @@ __device__ void epilogue_staged(const TcParams &p, const PhaseDesc &d, const Til
 template <int V>
 __device__ void epilogue_tma(const TcParams &p, const PhaseDesc &d, const Tile &ti,
                              uint32_t taddr, uint32_t box, int q, int part, int lane, int &bsel) {
-    if (V == kVarGeneral && p.mn_b) {
+    if ((V == kVarGeneral || V == kVarMN) && p.mn_b) {
         // Whole-image 1x1 tiles: accumulator column c is plane position c.
         // Per 32 positions the warp's channels go into a [channels][32]
         // float box, 128-byte swizzled (conflict-free writes; the box is
@@ -2561,7 +2684,15 @@ __global__ void __launch_bounds__(Roles<V>::threads, 1)
     if (!lazy_wait) grid_dependency_wait();
 
     if (warp == R::w_warp) {
-        if (lane == 0) role_weights<V>(p, sh, w_base, raw_base, early_base);
+        if (lane == 0) {
+            if (R::w2_warp >= 0 && p.nw != 0 && p.gather_tma)  // raw slices here, weights on w2_warp
+                raw_stream_producer(p, sh, raw_base);
+            else
+                role_weights<V>(p, sh, w_base, raw_base, early_base);
+        }
+        __syncwarp();
+    } else if (R::w2_warp >= 0 && warp == R::w2_warp) {
+        if (lane == 0 && p.nw != 0 && p.gather_tma) weight_stream_producer(p, sh, w_base);
         __syncwarp();
     } else if (warp == R::mma_warp) {
         if (lane == 0) {
@@ -2582,7 +2713,7 @@ __global__ void __launch_bounds__(Roles<V>::threads, 1)
         else if constexpr (V == kVarFrame64)
             gather_pm<kGWarps, kF64Groups>(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
         else if (ESIZE == 2 && p.mn_b)
-            gather_mn(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
+            gather_mn<R::g_warps>(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
         else if (p.gather_tma)
             gather_from_raw<ESIZE, R::g_warps>(p, sh, g_base, raw_base, early_base, warp - R::g_warp0, lane);
         else
@@ -2764,6 +2895,7 @@ int launch_tc(const Plan &plan, const void *grad_out, const void *packed, float 
         if (p.frame64) return launch_variant<2, kVarFrame64>(p, grid, st, dev);
         if (p.stacked) return launch_variant<2, kVarStacked>(p, grid, st, dev);
         if (p.pair_rw) return launch_variant<2, kVarPair>(p, grid, st, dev);
+        if (p.mn_b) return launch_variant<2, kVarMN>(p, grid, st, dev);
         return launch_variant<2, kVarGeneral>(p, grid, st, dev);
     }
     if (p.stacked) return launch_variant<4, kVarStacked>(p, grid, st, dev);

@@ -192,6 +192,8 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
         if (np == 0) return false;
         if (pair) {
             if (s != 2 || np != 4 || rows_per_tile <= 0 || Ci > 128 || W % 8 != 0 || W > 64) return false;
+            // (the pair variant runs kGWarps - 1 gather warps beside two producers)
+            if (round_up(tile_p + 2 * X1 + 8, 8) > (int64_t)(kGWarps - 1) * 32 * kMaxGatherRows) return false;
             for (int i = 0; i < 4; ++i) {
                 const PhaseDesc &d = t.ph[i];
                 const PhaseDesc &o = t.ph[i ^ 1];  // the other column phase of the row phase
@@ -549,7 +551,8 @@ bool plan_mn(const conv2d_grad_input_params &p, int esize, const TcParams &g, Tc
     t.mn_atoms = (int)cdiv(t.tile_p, 64);
     t.g_stage_bytes = (t.kc / 8) * t.mn_atoms * 1024;
     t.hbp = t.mn_atoms * 64;
-    if ((int64_t)t.kc * t.mn_atoms * 8 > (int64_t)kMaxMnPieces * kGWarps * 32) return false;
+    // (the MN-major variant runs kGWarps - 1 gather warps beside two producers)
+    if ((int64_t)t.kc * t.mn_atoms * 8 > (int64_t)kMaxMnPieces * (kGWarps - 1) * 32) return false;
     t.ph[0].hb = t.hbp;
     // Epilogue staging per warp: a 1 KB-aligned swizzled [channels][32]
     // float box for the plane TMA store, with room for the staged epilogue's
