@@ -2221,65 +2221,63 @@ __device__ void epilogue_stacked(const TcParams &p, const PhaseDesc &d, const Ti
 }
 
 // Paired epilogue (stride 2; the column phases rw = 0 and 1 of the same
-// output rows in TMEM buffers t0 and t1): per output row of the tile and
-// 16-lane group, each lane interleaves its channel's columns of the two
-// phases, 16 at a time, into a whole grad_in row of an [8][W] box (lanes
-// 8h..8h+7 of the group fill box h), and one lane stores both boxes with TMA
-// tensor stores, as the stride-1 rows of epilogue_tma.
+// output rows in TMEM buffers t0 and t1): per output row of the tile, the
+// warp reads both phases' row once for all 32 lanes of its quadrant (one
+// grad_in channel per lane), then in two halves of 16 lanes interleaves each
+// lane's columns of the two phases into a whole grad_in row of a [16][W] box
+// (p.epi_box_ci = 16) and stores the box with one TMA tensor store -- half the
+// TMEM reads and half the stores of 8-channel boxes, whose per-store issue
+// cost dominates this epilogue.
 __device__ void epilogue_pair_tma(const TcParams &p, const PhaseDesc &d0, const PhaseDesc &d1,
                                   const Tile &ti, uint32_t t0, uint32_t t1, uint32_t box, int q,
                                   int part, int lane) {
     const int tpi = (d0.Hr + p.rows_per_tile - 1) / p.rows_per_tile;
     const int n = ti.pt / tpi, a0 = (ti.pt - n * tpi) * p.rows_per_tile;
-    const int W = p.W, half = W / 2;
-    const uint32_t box_bytes = (uint32_t)(kTmaBoxCi * W * 4);
-    for (int gi = 0; gi < 2; ++gi) {
-        const int ci0 = ti.mt * p.m_tile + q * 32 + 16 * gi;
-        if (ci0 >= p.Ci) break;
-        const int lg = lane - 16 * gi;
-        const bool mine = lg >= 0 && lg < 16;
-        const uint32_t my_row = box + (uint32_t)((lg >> 3) & 1) * box_bytes + 4u * (uint32_t)(W * (lg & 7));
-        for (int r = part; r < p.rows_per_tile && a0 + r < d0.Hr; r += 2) {
-            const uint32_t a0c = t0 + (uint32_t)(r * d0.X), a1c = t1 + (uint32_t)(r * d1.X);
-            if (lane == 0) bulk_wait_read_all();  // the previous stores have read both boxes
+    const int W = p.W, half = W / 2;  // frame columns of a member row (a multiple of 4, <= 32)
+    const int ci_q = ti.mt * p.m_tile + q * 32;
+    if (ci_q >= p.Ci) return;
+    const uint32_t my_row = box + 4u * (uint32_t)(W * (lane & 15));
+    for (int r = part; r < p.rows_per_tile && a0 + r < d0.Hr; r += 2) {
+        const uint32_t a0c = t0 + (uint32_t)(r * d0.X), a1c = t1 + (uint32_t)(r * d1.X);
+        uint32_t v[64];  // [0, 32): phase rw = 0, [32, 64): rw = 1, frame column c at c
+#pragma unroll
+        for (int c = 0; c < 32; c += 16) {
+            const int rem = half - c;  // a multiple of 4
+            if (rem >= 16) {
+                tmem_ld16(a0c + c, *reinterpret_cast<uint32_t(*)[16]>(v + c));
+                tmem_ld16(a1c + c, *reinterpret_cast<uint32_t(*)[16]>(v + 32 + c));
+            } else if (rem > 0) {
+                if (rem >= 8) {
+                    tmem_ld8(a0c + c, v + c);
+                    tmem_ld8(a1c + c, v + 32 + c);
+                }
+                if (rem == 12) {
+                    tmem_ld4(a0c + c + 8, v + c + 8);
+                    tmem_ld4(a1c + c + 8, v + 32 + c + 8);
+                } else if (rem == 4) {
+                    tmem_ld4(a0c + c, v + c);
+                    tmem_ld4(a1c + c, v + 32 + c);
+                }
+            }
+        }
+        tmem_wait_ld64(v);
+        const int ih = 2 * (a0 + r) + d0.rh;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // lanes 16h .. 16h + 15: channels ci_q + 16h ..
+            const int ci0 = ci_q + 16 * h;
+            if (ci0 >= p.Ci) break;
+            if (lane == 0) bulk_wait_read_all();  // the previous store has read the box
             __syncwarp();
+            if ((lane >> 4) == h) {
 #pragma unroll
-            for (int c = 0; c < 32; c += 16) {
-                const int rem = half - c;  // a multiple of 4
-                if (rem <= 0) break;
-                uint32_t v[32];  // v[0..16): phase rw = 0, v[16..32): rw = 1
-                if (rem >= 16) {
-                    tmem_ld16(a0c + c, *reinterpret_cast<uint32_t(*)[16]>(v));
-                    tmem_ld16(a1c + c, *reinterpret_cast<uint32_t(*)[16]>(v + 16));
-                } else {
-                    if (rem >= 8) {
-                        tmem_ld8(a0c + c, v);
-                        tmem_ld8(a1c + c, v + 16);
-                    }
-                    if (rem == 12) {
-                        tmem_ld4(a0c + c + 8, v + 8);
-                        tmem_ld4(a1c + c + 8, v + 24);
-                    } else if (rem == 4) {
-                        tmem_ld4(a0c + c, v);
-                        tmem_ld4(a1c + c, v + 16);
-                    }
-                }
-                tmem_wait_ld32(v);
-                if (mine) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)  // grad_in columns 2c + 4e .. + 3
-                        if (4 * e < 2 * rem)
-                            st_shared_v4(my_row + 4u * (uint32_t)(2 * c + 4 * e), v[2 * e], v[16 + 2 * e],
-                                         v[2 * e + 1], v[16 + 2 * e + 1]);
-                }
+                for (int e = 0; e < 16; ++e)  // grad_in columns 4e .. 4e + 3
+                    if (2 * e < half)
+                        st_shared_v4(my_row + 16u * (uint32_t)e, v[2 * e], v[32 + 2 * e], v[2 * e + 1],
+                                     v[32 + 2 * e + 1]);
             }
             fence_proxy_async();
             __syncwarp();
-            if (lane == 0) {
-                const int ih = 2 * (a0 + r) + d0.rh;
-                tma_store_4d(&p.out_map, box, 0, ih, ci0, n);
-                if (ci0 + 8 < p.Ci) tma_store_4d(&p.out_map, box + box_bytes, 0, ih, ci0 + 8, n);
-            }
+            if (lane == 0) tma_store_4d(&p.out_map, box, 0, ih, ci0, n);
         }
     }
 }

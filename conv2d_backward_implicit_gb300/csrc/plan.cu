@@ -357,6 +357,7 @@ bool plan_tc(const conv2d_grad_input_params &p, int esize, int dtype, Plan *plan
             return false;
         t.pair_rw = 1;
         t.tile_group = 2;
+        t.epi_box_ci = 2 * kTmaBoxCi;  // the paired epilogue stores 16-channel boxes
     }
 
     // Pack parameters mirror the layout above.
