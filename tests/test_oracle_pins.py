@@ -42,7 +42,7 @@ SWEEP = workloads.random_small_shapes(160, seed=7)
 
 
 # --------------------------------------------------------------------------
-@pytest.mark.parametrize("path", sorted(glob.glob(os.path.join(GOLDEN, "*.json"))),
+@pytest.mark.parametrize("path", sorted(glob.glob(os.path.join(GOLDEN, "hand_*.json"))),
                          ids=lambda p: os.path.basename(p))
 def test_golden_fixture(path):
     fx = json.load(open(path))
@@ -233,7 +233,7 @@ MUTANTS = {
 
 def _pins_pass(lib) -> bool:
     """Run a compact set of the pins above against another build of the oracle."""
-    for path in sorted(glob.glob(os.path.join(GOLDEN, "*.json"))):
+    for path in sorted(glob.glob(os.path.join(GOLDEN, "hand_*.json"))):
         fx = json.load(open(path))
         p = fx["params"]
         got = oracle.dgrad(np.array(fx["grad_out"], float), np.array(fx["weight"], float),
