@@ -1,4 +1,5 @@
-"""GB300-native conv2d input gradient (dgrad) as an implicit GEMM.
+"""GB300-native conv2d input gradient (dgrad) as an implicit GEMM, with the
+strided forward convolution and the fused RMSNorm + matmul beside it.
 
 The compute path is the C-ABI library ``libconv2d_grad_input.so`` built from
 ``csrc/`` for sm_103a; :mod:`.binding` marshals arguments to it.  Importing
@@ -14,4 +15,6 @@ from .binding import (  # noqa: F401
     conv2d_grad_input_set_kernel, conv2d_grad_input_set_wait_limit_ns,
     conv2d_grad_input_status_string, conv2d_grad_input_workspace_size, library, library_path,
     params_from_shapes,
+    RmsParams, rmsnorm_matmul, rmsnorm_matmul_check_errors, rmsnorm_matmul_select_kernel,
+    rmsnorm_matmul_set_kernel,
 )

@@ -1,4 +1,5 @@
-"""ctypes binding for the C ABI in include/conv2d_grad_input.h (argument marshalling only).
+"""ctypes binding for the C ABI in include/conv2d_grad_input.h and include/rmsnorm_matmul.h
+(argument marshalling only).
 
 Every function here has the name of the C entry point it calls, accepts torch
 tensors (or raw integer addresses) for the buffers, and raises
@@ -34,6 +35,12 @@ class Params(ctypes.Structure):
 
     def as_dict(self):
         return {k: int(getattr(self, k)) for k in PARAM_FIELDS}
+
+
+class RmsParams(ctypes.Structure):
+    """rmsnorm_matmul_params: m, n, k (uint32) and eps (float)."""
+    _fields_ = [("m", ctypes.c_uint32), ("n", ctypes.c_uint32), ("k", ctypes.c_uint32),
+                ("eps", ctypes.c_float)]
 
 
 class DgradError(RuntimeError):
@@ -97,6 +104,15 @@ def library() -> ctypes.CDLL:
             lib.conv2d_grad_input_noalloc.restype = I
             lib.conv2d_forward.argtypes = [P, P, P, PP, I, P]
             lib.conv2d_forward.restype = I
+            RP = ctypes.POINTER(RmsParams)
+            lib.rmsnorm_matmul.argtypes = [P, P, P, P, RP, I, P]
+            lib.rmsnorm_matmul.restype = I
+            lib.rmsnorm_matmul_select_kernel.argtypes = [P, P, P, P, RP, I]
+            lib.rmsnorm_matmul_select_kernel.restype = I
+            lib.rmsnorm_matmul_set_kernel.argtypes = [I]
+            lib.rmsnorm_matmul_set_kernel.restype = I
+            lib.rmsnorm_matmul_check_errors.argtypes = [P]
+            lib.rmsnorm_matmul_check_errors.restype = I
             _lib = lib
     return _lib
 
@@ -265,3 +281,32 @@ def conv2d_forward(x, weight, out, params: Params, dtype: int, stream=None) -> N
                                   _addr(out, "out", "float32", n_out), ctypes.byref(params),
                                   int(dtype), _stream(stream))
     _check(rc, "conv2d_forward")
+
+
+def _rms_args(x, w_norm, w_proj, c, params: RmsParams, dtype: int):
+    m, n, k = int(params.m), int(params.n), int(params.k)
+    t = _in_dtype(dtype)
+    return (_addr(x, "x", t, m * k), _addr(w_norm, "w_norm", t, k), _addr(w_proj, "w_proj", t, k * n),
+            _addr(c, "c", "float32", m * n))
+
+
+def rmsnorm_matmul(x, w_norm, w_proj, c, params: RmsParams, dtype: int, stream=None) -> None:
+    """C [m, n] = RmsNorm(X [m, k], W_norm [k]) x W_proj [k, n] (include/rmsnorm_matmul.h)."""
+    rc = library().rmsnorm_matmul(*_rms_args(x, w_norm, w_proj, c, params, dtype), ctypes.byref(params),
+                                  int(dtype), _stream(stream))
+    _check(rc, "rmsnorm_matmul")
+
+
+def rmsnorm_matmul_select_kernel(x, w_norm, w_proj, c, params: RmsParams, dtype: int) -> int:
+    """DGRAD_KERNEL_TC (1) or DGRAD_KERNEL_SIMT (2) for these buffers, or a negative status."""
+    return int(library().rmsnorm_matmul_select_kernel(*_rms_args(x, w_norm, w_proj, c, params, dtype),
+                                                      ctypes.byref(params), int(dtype)))
+
+
+def rmsnorm_matmul_set_kernel(kernel: int) -> int:
+    return int(library().rmsnorm_matmul_set_kernel(int(kernel)))
+
+
+def rmsnorm_matmul_check_errors(stream=None) -> int:
+    """Returns the status (0, DGRAD_ERR_TIMEOUT = 6 or DGRAD_ERR_CUDA = 5) without raising."""
+    return int(library().rmsnorm_matmul_check_errors(_stream(stream)))

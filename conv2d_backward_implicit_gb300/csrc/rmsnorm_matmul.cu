@@ -1,0 +1,762 @@
+// rmsnorm_matmul.cu -- the fused RMSNorm + matmul
+//
+//     C[i, j] = sum_t X[i, t] * r[i] * W_norm[t] * W_proj[t, j],
+//     r[i]    = 1 / sqrt(sum_t X[i, t]^2 / K + eps)
+//
+// (matmul_rms_norm.wgsl, meganeura 0.2.0: header comment, row-scale prologue
+// and normalised A-tile load), declared in include/rmsnorm_matmul.h.
+//
+// Tensor-core kernel (bf16 / fp16, sm_103a).  One CTA per SM walks output
+// tiles of 128 rows x 256 columns; the K loop runs in stages of 64.  Row
+// scale r[i] is a per-row factor of the whole product, so it is applied to
+// the float32 accumulator in the epilogue rather than to the operand: X is
+// read once, its sum of squares accumulated while the stages stream through.
+//   * warp 5 (one thread): TMA loads of the X tile [128 rows][64 K], 128-byte
+//     swizzled, which is the K-major A operand layout;
+//   * warp 6 (one thread): TMA loads of the W_proj tile [64 K][256 N] through a
+//     3-D view [N/64][K][64] of W_proj, giving the MN-major B operand layout
+//     (atoms of 8 K rows x 64 N, 1 KB, N-block stride 8 KB) in one copy;
+//   * warps 7-10 (the transform): thread r owns tile row r; per stage it reads
+//     its row's eight 16-byte chunks in place, accumulates x^2 in float32,
+//     writes x * W_norm[t] rounded to the input type back, and signals the
+//     stage; after a tile's last stage it stores r[i] for the epilogue;
+//   * warp 4 (one thread): tcgen05.mma M128 N256 K16 into a double-buffered
+//     TMEM accumulator (2 x 256 columns);
+//   * warps 0-3 (the epilogue, one per TMEM lane quadrant): 32 rows x 32
+//     columns at a time from TMEM, scaled by r[i], into a 128-byte swizzled
+//     staging box, stored with a TMA tensor store (two boxes per warp, so one
+//     is filled while the other's store reads it).
+// Every wait is bounded (global timer); on timeout the kernel raises its
+// error flag, lets the copies and MMAs in flight finish, frees TMEM and
+// returns.
+//
+// CUDA-core kernel (any dtype, any shape): 64 x 64 output tiles, 256 threads
+// with 4 x 4 outputs each; the block first computes r[i] for its rows, then
+// runs a shared-memory-tiled product of (X * W_norm) and W_proj in float32
+// and scales each row by r[i] at the end.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "rmsnorm_matmul.h"
+
+namespace rmsmm {
+
+__device__ unsigned int g_rmsnorm_error_word = 0;
+
+namespace {
+
+constexpr int kBM = 128, kBN = 256, kBK = 64;  // tile rows, tile columns, K per stage (16-bit)
+constexpr int kStages = 4;
+constexpr int kEpiWarps = 4, kMmaWarp = 4, kAWarp = 5, kBWarp = 6, kTWarp0 = 7, kTWarps = 4;
+constexpr int kThreads = 32 * (kTWarp0 + kTWarps);
+constexpr uint32_t kAStage = kBM * kBK * 2;  // 16 KB
+constexpr uint32_t kBStage = kBK * kBN * 2;  // 32 KB
+constexpr uint32_t kBoxBytes = 32 * 32 * 4;  // one epilogue store box: 32 rows x 32 floats
+constexpr uint32_t kCtl = 2048;              // barriers + row scales
+constexpr uint32_t kOffA = kCtl, kOffB = kOffA + kStages * kAStage, kOffEpi = kOffB + kStages * kBStage;
+constexpr uint32_t kSmemBytes = 1024 + kOffEpi + kEpiWarps * 2 * kBoxBytes;  // + 1 KB alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory over the per-block limit");
+
+struct Params {
+    CUtensorMap a_map;  // X as [M][K], box [128][64], 128-byte swizzle
+    CUtensorMap b_map;  // W_proj as [N/64][K][64], box [4][64][64], 128-byte swizzle
+    CUtensorMap c_map;  // C as [M][N] float32, box [32][32], 128-byte swizzle
+    const void *w_norm;
+    int m, n, k, kt, nt;  // kt: K stages, nt: column tiles
+    int64_t tiles;
+    float eps;
+    uint32_t idesc;
+    int f16;  // 1: float16 inputs, 0: bfloat16
+    uint64_t wait_limit_ns;
+};
+
+struct Ctl {
+    uint64_t a_full[kStages], b_full[kStages], a_ready[kStages], empty[kStages];
+    uint64_t acc_full[2], acc_empty[2], rs_full[2], rs_empty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+static_assert(sizeof(Ctl) <= 1024, "control block too large");
+
+// ------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t su32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint32_t bar) {
+    asm volatile("{\n\t.reg .b64 s;\n\tmbarrier.arrive.shared::cta.b64 s, [%0];\n\t}" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void bar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("{\n\t.reg .b64 s;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 s, [%0], %1;\n\t}" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t now_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void fence_async_proxy() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_alloc(uint32_t dst, uint32_t cols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t cols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+__device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit_to(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// 32 lanes x 32 consecutive 32-bit columns; completes at tc_wait_ld.
+__device__ __forceinline__ void tc_ld_32x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                   "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]),
+                   "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]),
+                   "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+// Shared-memory matrix descriptors (128-byte swizzle): K-major rows of 128
+// bytes in groups of 8 (stride 1 KB), and MN-major atoms of 8 K rows x 128
+// bytes with the given MN-atom (leading) and K-group (stride) byte offsets.
+__device__ __forceinline__ uint64_t desc_k(uint32_t addr) {
+    uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+__device__ __forceinline__ uint64_t desc_mn(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// --------------------------------------------------------- bounded waits
+__device__ __noinline__ bool wait_long(uint32_t bar, uint32_t parity, const Params &p, Ctl &c, bool honour_abort) {
+    const uint64_t t0 = now_ns();
+    const uint64_t max_spins = p.wait_limit_ns / 16 + (1u << 20);
+    for (uint64_t spin = 1;; ++spin) {
+        if (bar_try(bar, parity)) return true;
+        if (honour_abort && *reinterpret_cast<volatile int *>(&c.abort_flag)) return false;
+        if (((spin & 31u) == 0 && now_ns() - t0 > p.wait_limit_ns) || spin > max_spins) {
+            *reinterpret_cast<volatile int *>(&c.abort_flag) = 1;
+            atomicOr(&g_rmsnorm_error_word, 1u);
+            return false;
+        }
+    }
+}
+// false: the CTA is aborting.
+__device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, const Params &p, Ctl &c) {
+    return bar_try(bar, parity) || wait_long(bar, parity, p, c, true);
+}
+// For work already in flight (copies, MMAs): ends even while aborting.
+__device__ __forceinline__ void drain(uint32_t bar, uint32_t parity, const Params &p, Ctl &c) {
+    if (!bar_try(bar, parity)) wait_long(bar, parity, p, c, false);
+}
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Params &p, Ctl &c, int lane) {
+    int ok = 0;
+    if (lane == 0) ok = wait(bar, parity, p, c) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// 16-bit element <-> float32 for the input type.
+__device__ __forceinline__ float lo_f(uint32_t w, bool f16) {
+    return f16 ? __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)))
+               : __bfloat162float(__ushort_as_bfloat16((unsigned short)(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float hi_f(uint32_t w, bool f16) {
+    return f16 ? __half2float(__ushort_as_half((unsigned short)(w >> 16)))
+               : __bfloat162float(__ushort_as_bfloat16((unsigned short)(w >> 16)));
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b, bool f16) {
+    if (f16) {
+        const __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// ----------------------------------------------------------------- roles
+// Producer of one operand (A: X tiles, B: W_proj tiles) for every tile and
+// stage of this CTA, into the stage ring; drains its copies when aborting.
+template <bool IS_A>
+__device__ void role_load(const Params &p, Ctl &c, uint32_t smem) {
+    int s = 0;
+    uint32_t ph = 0;
+    int64_t issued = 0;
+    bool aborted = false;
+    for (int64_t t = blockIdx.x; t < p.tiles && !aborted; t += gridDim.x) {
+        const int m0 = (int)(t / p.nt) * kBM, n0 = (int)(t % p.nt) * kBN;
+        for (int kk = 0; kk < p.kt; ++kk) {
+            if (!wait(su32(&c.empty[s]), ph ^ 1u, p, c)) {
+                aborted = true;
+                break;
+            }
+            if (IS_A) {
+                bar_expect_tx(su32(&c.a_full[s]), kAStage);
+                tma_load_2d(smem + kOffA + (uint32_t)s * kAStage, &p.a_map, kk * kBK, m0, su32(&c.a_full[s]));
+            } else {
+                bar_expect_tx(su32(&c.b_full[s]), kBStage);
+                tma_load_3d(smem + kOffB + (uint32_t)s * kBStage, &p.b_map, 0, kk * kBK, n0 / 64,
+                            su32(&c.b_full[s]));
+            }
+            ++issued;
+            if (++s == kStages) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+    }
+    if (aborted) {  // every copy still landing must finish before the CTA exits
+        const int64_t k_end = issued < kStages ? issued : kStages;
+        for (int64_t q = issued - k_end; q < issued; ++q)
+            drain(su32(IS_A ? &c.a_full[q % kStages] : &c.b_full[q % kStages]), (uint32_t)((q / kStages) & 1), p,
+                  c);
+    }
+}
+
+// Transform warps: thread r owns row r of every X tile in the ring.
+__device__ void role_transform(const Params &p, Ctl &c, uint32_t smem, float *rs, int r, int lane) {
+    const bool f16 = p.f16 != 0;
+    const uint16_t *wn = static_cast<const uint16_t *>(p.w_norm);
+    const bool wn_vec = (reinterpret_cast<uintptr_t>(wn) & 15u) == 0;
+    int s = 0, acc = 0;
+    uint32_t ph = 0, rph = 0;
+    for (int64_t t = blockIdx.x; t < p.tiles; t += gridDim.x) {
+        float ss = 0.f;
+        for (int kk = 0; kk < p.kt; ++kk) {
+            if (!wait_warp(su32(&c.a_full[s]), ph, p, c, lane)) return;
+            const uint32_t row = smem + kOffA + (uint32_t)s * kAStage + (uint32_t)r * 128u;
+#pragma unroll 2
+            for (int ch = 0; ch < 8; ++ch) {  // logical 16-byte chunk ch: columns kk*64 + 8ch .. + 7
+                const int t0 = kk * kBK + 8 * ch;
+                uint32_t w[4];
+                if (wn_vec && t0 + 8 <= p.k) {
+                    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(wn + t0));
+                    w[0] = u.x, w[1] = u.y, w[2] = u.z, w[3] = u.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t lo = t0 + 2 * e < p.k ? (uint32_t)__ldg(wn + t0 + 2 * e) : 0u;
+                        const uint32_t hi = t0 + 2 * e + 1 < p.k ? (uint32_t)__ldg(wn + t0 + 2 * e + 1) : 0u;
+                        w[e] = lo | (hi << 16);
+                    }
+                }
+                const uint32_t a = row + (uint32_t)((ch ^ (r & 7)) << 4);
+                const uint4 x = lds128(a);
+                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float x0 = lo_f(xs[e], f16), x1 = hi_f(xs[e], f16);
+                    ss = fmaf(x0, x0, ss);
+                    ss = fmaf(x1, x1, ss);
+                    o[e] = pack2(x0 * lo_f(w[e], f16), x1 * hi_f(w[e], f16), f16);
+                }
+                sts128(a, o[0], o[1], o[2], o[3]);
+            }
+            fence_async_proxy();  // the MMA (async proxy) reads what these threads wrote
+            __syncwarp();
+            if (lane == 0) bar_arrive(su32(&c.a_ready[s]));
+            if (++s == kStages) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+        // Row scale of this tile, for the epilogue (buffer acc, free once the
+        // epilogue of the tile two back has read it).
+        if (!wait_warp(su32(&c.rs_empty[acc]), rph ^ 1u, p, c, lane)) return;
+        rs[acc * kBM + r] = 1.0f / sqrtf(ss / (float)p.k + p.eps);
+        __syncwarp();
+        if (lane == 0) bar_arrive(su32(&c.rs_full[acc]));
+        if (++acc == 2) {
+            acc = 0;
+            rph ^= 1u;
+        }
+    }
+}
+
+// MMA issue (one thread).
+__device__ void role_mma(const Params &p, Ctl &c, uint32_t smem, uint32_t tmem) {
+    int s = 0, acc = 0;
+    uint32_t ph = 0, aph = 0;
+    bool aborted = false;
+    for (int64_t t = blockIdx.x; t < p.tiles && !aborted; t += gridDim.x) {
+        if (!wait(su32(&c.acc_empty[acc]), aph ^ 1u, p, c)) break;
+        tc_after();
+        const uint32_t d = tmem + (uint32_t)(acc * kBN);
+        for (int kk = 0; kk < p.kt; ++kk) {
+            if (!wait(su32(&c.a_ready[s]), ph, p, c) || !wait(su32(&c.b_full[s]), ph, p, c)) {
+                aborted = true;
+                break;
+            }
+            tc_after();
+            const uint64_t ad = desc_k(smem + kOffA + (uint32_t)s * kAStage);
+            const uint64_t bd = desc_mn(smem + kOffB + (uint32_t)s * kBStage, 8192u, 1024u);
+#pragma unroll
+            for (int k16 = 0; k16 < 4; ++k16)  // A: +32 bytes of each row; B: +2 K groups (2 KB)
+                tc_mma_f16(d, ad + 2u * k16, bd + 128u * k16, p.idesc, (kk | k16) != 0);
+            tc_commit_to(su32(&c.empty[s]));
+            if (++s == kStages) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+        if (aborted) break;
+        tc_commit_to(su32(&c.acc_full[acc]));
+        if (++acc == 2) {
+            acc = 0;
+            aph ^= 1u;
+        }
+    }
+    tc_commit_to(su32(&c.mma_done));  // no MMA may still run when TMEM is released
+    drain(su32(&c.mma_done), 0, p, c);
+}
+
+// Epilogue warp q: rows 32q .. 32q + 31 of each tile.
+__device__ void role_epilogue(const Params &p, Ctl &c, uint32_t smem, const float *rs, uint32_t tmem, int q,
+                              int lane) {
+    const uint32_t stage0 = smem + kOffEpi + (uint32_t)q * 2u * kBoxBytes;
+    int acc = 0, box = 0;
+    uint32_t aph = 0;
+    for (int64_t t = blockIdx.x; t < p.tiles; t += gridDim.x) {
+        const int m0 = (int)(t / p.nt) * kBM, n0 = (int)(t % p.nt) * kBN;
+        if (!wait_warp(su32(&c.acc_full[acc]), aph, p, c, lane)) break;
+        if (!wait_warp(su32(&c.rs_full[acc]), aph, p, c, lane)) break;
+        tc_after();
+        const float scale = rs[acc * kBM + 32 * q + lane];
+        const bool rows_live = m0 + 32 * q < p.m;
+        for (int cg = 0; cg < kBN / 32 && rows_live && n0 + 32 * cg < p.n; ++cg) {
+            uint32_t v[32];
+            tc_ld_32x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(acc * kBN + 32 * cg), v);
+            tc_wait_ld(v);
+            const uint32_t stg = stage0 + (uint32_t)box * kBoxBytes;
+            if (lane == 0) bulk_wait_read_1();  // this box's previous store has read it
+            __syncwarp();
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)  // row `lane`, logical chunk ch at slot ch ^ (lane & 7)
+                sts128(stg + (uint32_t)lane * 128u + (uint32_t)((ch ^ (lane & 7)) << 4),
+                       __float_as_uint(__uint_as_float(v[4 * ch]) * scale),
+                       __float_as_uint(__uint_as_float(v[4 * ch + 1]) * scale),
+                       __float_as_uint(__uint_as_float(v[4 * ch + 2]) * scale),
+                       __float_as_uint(__uint_as_float(v[4 * ch + 3]) * scale));
+            fence_async_proxy();
+            __syncwarp();
+            if (lane == 0) tma_store_2d(&p.c_map, stg, n0 + 32 * cg, m0 + 32 * q);
+            box ^= 1;
+        }
+        tc_before();
+        __syncwarp();
+        if (lane == 0) {
+            bar_arrive(su32(&c.acc_empty[acc]));
+            bar_arrive(su32(&c.rs_empty[acc]));
+        }
+        if (++acc == 2) {
+            acc = 0;
+            aph ^= 1u;
+        }
+    }
+    if (lane == 0) bulk_wait_all();  // every store complete before the CTA exits
+    __syncwarp();
+}
+
+__global__ void __launch_bounds__(kThreads, 1) rmsnorm_matmul_tc_kernel(const __grid_constant__ Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t smem = (su32(smem_raw) + 1023u) & ~1023u;
+    Ctl &c = *reinterpret_cast<Ctl *>(smem_raw + (smem - su32(smem_raw)));
+    float *rs = reinterpret_cast<float *>(smem_raw + (smem - su32(smem_raw)) + 1024);  // [2][128]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            bar_init(su32(&c.a_full[s]), 1);
+            bar_init(su32(&c.b_full[s]), 1);
+            bar_init(su32(&c.a_ready[s]), kTWarps);
+            bar_init(su32(&c.empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            bar_init(su32(&c.acc_full[a]), 1);
+            bar_init(su32(&c.acc_empty[a]), kEpiWarps);
+            bar_init(su32(&c.rs_full[a]), kTWarps);
+            bar_init(su32(&c.rs_empty[a]), kEpiWarps);
+        }
+        bar_init(su32(&c.mma_done), 1);
+        c.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) tc_alloc(su32(&c.tmem_base), 512);
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const uint32_t tmem = c.tmem_base;
+    if ((warp == kAWarp || warp == kBWarp) && lane == 0) {
+        const CUtensorMap *m = warp == kAWarp ? &p.a_map : &p.b_map;
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+    }
+    // Only this CTA's own shared memory and TMEM were touched so far.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    if (warp == kAWarp) {
+        if (lane == 0) role_load<true>(p, c, smem);
+        __syncwarp();
+    } else if (warp == kBWarp) {
+        if (lane == 0) role_load<false>(p, c, smem);
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) role_mma(p, c, smem, tmem);
+        __syncwarp();
+    } else if (warp >= kTWarp0) {
+        role_transform(p, c, smem, rs, (warp - kTWarp0) * 32 + lane, lane);
+    } else {
+        role_epilogue(p, c, smem, rs, tmem, warp, lane);
+    }
+    tc_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_after();
+        tc_dealloc(tmem, 512);
+    }
+}
+
+// --------------------------------------------------- CUDA-core kernel
+template <typename T>
+__device__ __forceinline__ float to_f(T v) {
+    if constexpr (sizeof(T) == 4) {
+        return v;
+    } else {
+        return (float)v;
+    }
+}
+
+// 64 x 64 tile of C per block of 16 x 16 threads, 4 x 4 outputs per thread.
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_matmul_simt_kernel(const T *__restrict__ x, const T *__restrict__ wn,
+                                                                  const T *__restrict__ wp, float *__restrict__ c,
+                                                                  int m, int n, int k, float eps) {
+    __shared__ float a_s[32][65];  // [t][row] of X * W_norm
+    __shared__ float b_s[32][65];  // [t][col] of W_proj
+    __shared__ float r_s[64];
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4, tid = threadIdx.x;
+    const int row0 = blockIdx.y * 64, col0 = blockIdx.x * 64;
+    // Row scales: warp w sums the squares of rows w, w + 8, ...
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int rr = warp; rr < 64; rr += 8) {
+        const int row = row0 + rr;
+        float ss = 0.f;
+        if (row < m)
+            for (int t = lane; t < k; t += 32) {
+                const float v = to_f(x[(int64_t)row * k + t]);
+                ss = fmaf(v, v, ss);
+            }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) r_s[rr] = 1.0f / sqrtf(ss / (float)k + eps);
+    }
+    float acc[4][4] = {};
+    for (int t0 = 0; t0 < k; t0 += 32) {
+        for (int e = tid; e < 64 * 32; e += 256) {
+            const int rr = e >> 5, tt = e & 31, row = row0 + rr, t = t0 + tt;
+            a_s[tt][rr] = (row < m && t < k) ? to_f(x[(int64_t)row * k + t]) * to_f(wn[t]) : 0.f;
+            const int kr = e >> 6, cc = e & 63, col = col0 + cc, tk = t0 + kr;
+            b_s[kr][cc] = (tk < k && col < n) ? to_f(wp[(int64_t)tk * n + col]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int tt = 0; tt < 32; ++tt) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = a_s[tt][ty + 16 * i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = b_s[tt][tx + 16 * j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int rr = ty + 16 * i, row = row0 + rr;
+        if (row >= m) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int col = col0 + tx + 16 * j;
+            if (col < n) c[(int64_t)row * n + col] = acc[i][j] * r_s[rr];
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            ptr = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }();
+    return fn;
+}
+
+std::atomic<int> g_kernel_choice{DGRAD_KERNEL_AUTO};
+
+int esize_of(int dtype) { return dtype == DGRAD_F32 ? 4 : 2; }
+
+bool aligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
+
+// Validation shared by the entry points: DGRAD_OK or a dgrad_status.
+int validate(const void *x, const void *wn, const void *wp, const float *c, const rmsnorm_matmul_params *p,
+             int dtype) {
+    if (!x || !wn || !wp || !c || !p) return DGRAD_ERR_INVALID_ARG;
+    if (dtype != DGRAD_F32 && dtype != DGRAD_BF16 && dtype != DGRAD_F16) return DGRAD_ERR_INVALID_ARG;
+    if (!std::isfinite(p->eps) || p->eps < 0.f) return DGRAD_ERR_INVALID_ARG;
+    if (p->m == 0 || p->n == 0 || p->k == 0) return DGRAD_ERR_SHAPE;
+    const int64_t lim = INT32_MAX;
+    if ((int64_t)p->m * p->k > lim || (int64_t)p->k * p->n > lim || (int64_t)p->m * p->n > lim)
+        return DGRAD_ERR_UNSUPPORTED;
+    const uintptr_t e = (uintptr_t)esize_of(dtype);
+    if (!aligned(x, e) || !aligned(wn, e) || !aligned(wp, e) || !aligned(c, 4)) return DGRAD_ERR_ALIGNMENT;
+    return DGRAD_OK;
+}
+
+bool tc_applies(const void *x, const void *wp, const float *c, const rmsnorm_matmul_params *p, int dtype) {
+    return dtype != DGRAD_F32 && p->k % 8 == 0 && p->n % 64 == 0 && aligned(x, 16) && aligned(wp, 16) &&
+           aligned(c, 16);
+}
+
+int select(const void *x, const void *wn, const void *wp, const float *c, const rmsnorm_matmul_params *p,
+           int dtype) {
+    const int v = validate(x, wn, wp, c, p, dtype);
+    if (v != DGRAD_OK) return -v;
+    const int choice = g_kernel_choice.load();
+    const bool tc = tc_applies(x, wp, c, p, dtype);
+    if (choice == DGRAD_KERNEL_SIMT) return DGRAD_KERNEL_SIMT;
+    if (choice == DGRAD_KERNEL_TC) return tc ? DGRAD_KERNEL_TC : -DGRAD_ERR_UNSUPPORTED;
+    return tc ? DGRAD_KERNEL_TC : DGRAD_KERNEL_SIMT;
+}
+
+bool encode_maps(Params &q, const void *x, const void *wp, float *c) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn) return false;
+    const CUtensorMapDataType dt16 = CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)q.k, (cuuint64_t)q.m};
+        const cuuint64_t strides[1] = {(cuuint64_t)q.k * 2};
+        const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBM};
+        const cuuint32_t es[2] = {1, 1};
+        if (fn(&q.a_map, dt16, 2, const_cast<void *>(x), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    {
+        // W_proj [K][N] seen as [N/64][K][64]: element (b, t, e) = W_proj[t][64 b + e].
+        const cuuint64_t dims[3] = {64, (cuuint64_t)q.k, (cuuint64_t)(q.n / 64)};
+        const cuuint64_t strides[2] = {(cuuint64_t)q.n * 2, 128};
+        const cuuint32_t box[3] = {64, (cuuint32_t)kBK, (cuuint32_t)(kBN / 64)};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (fn(&q.b_map, dt16, 3, const_cast<void *>(wp), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)q.n, (cuuint64_t)q.m};
+        const cuuint64_t strides[1] = {(cuuint64_t)q.n * 4};
+        const cuuint32_t box[2] = {32, 32};
+        const cuuint32_t es[2] = {1, 1};
+        if (fn(&q.c_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, c, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
+}
+
+int launch_tc(const void *x, const void *wn, const void *wp, float *c, const rmsnorm_matmul_params *p, int dtype,
+              cudaStream_t st) {
+    Params q{};
+    q.w_norm = wn;
+    q.m = (int)p->m;
+    q.n = (int)p->n;
+    q.k = (int)p->k;
+    q.kt = (q.k + kBK - 1) / kBK;
+    q.nt = (q.n + kBN - 1) / kBN;
+    q.tiles = (int64_t)((q.m + kBM - 1) / kBM) * q.nt;
+    q.eps = p->eps;
+    q.f16 = dtype == DGRAD_F16 ? 1 : 0;
+    const uint32_t fmt = dtype == DGRAD_BF16 ? 1u : 0u;
+    // D float32, A and B of the input type, B MN-major, N = 256, M = 128.
+    q.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | (1u << 16) | ((uint32_t)(kBN >> 3) << 17) |
+              ((uint32_t)(kBM >> 4) << 24);
+    q.wait_limit_ns = 2000000000ull;  // 2 s: far beyond any stage of any valid problem
+    if (!encode_maps(q, x, wp, c)) return DGRAD_ERR_UNSUPPORTED;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DGRAD_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return DGRAD_ERR_CUDA;
+    static std::atomic<uint64_t> configured{0};  // bit per device: shared-memory limit raised
+    const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+    if (!bit || !(configured.load() & bit)) {
+        if (cudaFuncSetAttribute(rmsnorm_matmul_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSmemBytes) != cudaSuccess)
+            return DGRAD_ERR_CUDA;
+        configured.fetch_or(bit);
+    }
+    const int grid = (int)(q.tiles < sms ? q.tiles : sms);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, rmsnorm_matmul_tc_kernel, q) == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
+}
+
+template <typename T>
+int launch_simt(const void *x, const void *wn, const void *wp, float *c, const rmsnorm_matmul_params *p,
+                cudaStream_t st) {
+    const dim3 grid((p->n + 63) / 64, (p->m + 63) / 64);
+    if (grid.y > 65535u) return DGRAD_ERR_UNSUPPORTED;
+    rmsnorm_matmul_simt_kernel<T><<<grid, 256, 0, st>>>(static_cast<const T *>(x), static_cast<const T *>(wn),
+                                                          static_cast<const T *>(wp), c, (int)p->m, (int)p->n,
+                                                          (int)p->k, p->eps);
+    return cudaGetLastError() == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace rmsmm
+
+extern "C" {
+
+int rmsnorm_matmul(const void *x, const void *w_norm, const void *w_proj, float *c, const rmsnorm_matmul_params *p,
+                   int dtype, struct CUstream_st *stream) {
+    using namespace rmsmm;
+    const int k = select(x, w_norm, w_proj, c, p, dtype);
+    if (k < 0) return -k;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (k == DGRAD_KERNEL_TC) return launch_tc(x, w_norm, w_proj, c, p, dtype, st);
+    if (dtype == DGRAD_F32) return launch_simt<float>(x, w_norm, w_proj, c, p, st);
+    if (dtype == DGRAD_BF16) return launch_simt<__nv_bfloat16>(x, w_norm, w_proj, c, p, st);
+    return launch_simt<__half>(x, w_norm, w_proj, c, p, st);
+}
+
+int rmsnorm_matmul_select_kernel(const void *x, const void *w_norm, const void *w_proj, const float *c,
+                                 const rmsnorm_matmul_params *p, int dtype) {
+    return rmsmm::select(x, w_norm, w_proj, c, p, dtype);
+}
+
+int rmsnorm_matmul_set_kernel(int kernel) {
+    if (kernel != DGRAD_KERNEL_AUTO && kernel != DGRAD_KERNEL_TC && kernel != DGRAD_KERNEL_SIMT)
+        return DGRAD_ERR_INVALID_ARG;
+    return rmsmm::g_kernel_choice.exchange(kernel);
+}
+
+int rmsnorm_matmul_check_errors(struct CUstream_st *stream) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    unsigned int word = 0;
+    const unsigned int zero = 0;
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&word, rmsmm::g_rmsnorm_error_word, sizeof(word));
+    if (e == cudaSuccess && word) e = cudaMemcpyToSymbol(rmsmm::g_rmsnorm_error_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return DGRAD_ERR_CUDA;
+    }
+    return word ? DGRAD_ERR_TIMEOUT : DGRAD_OK;
+}
+
+}  // extern "C"

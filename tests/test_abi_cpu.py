@@ -9,8 +9,8 @@ import pytest
 import conv2d_backward_implicit_gb300 as dg
 from conv2d_backward_implicit_gb300 import build_ext, workloads
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
-                      "conv2d_grad_input.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADER = os.path.join(INCLUDE, "conv2d_grad_input.h")
 
 
 @pytest.fixture(scope="module")
@@ -21,18 +21,26 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(conv2d_grad_input\w*)\s*\(",
-                                 text, flags=re.M)))
+    """Every function declared in include/*.h (a return type, a name, an open parenthesis)."""
+    names = set()
+    for h in sorted(os.listdir(INCLUDE)):
+        if not h.endswith(".h"):
+            continue
+        text = re.sub(r"/\*.*?\*/", "", open(os.path.join(INCLUDE, h)).read(), flags=re.S)
+        names.update(re.findall(r"^\s*(?:const\s+)?(?:int|size_t|void|uint64_t|const char)\s*\*?\s*"
+                                r"([a-z_0-9]+)\s*\(", text, flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_abi():
     names = declared_functions()
     for must in ("conv2d_grad_input", "conv2d_grad_input_workspace_size",
                  "conv2d_grad_input_pack_weight", "conv2d_grad_input_prepacked",
-                 "conv2d_grad_input_check_errors", "conv2d_grad_input_status_string"):
-        assert must in names
+                 "conv2d_grad_input_check_errors", "conv2d_grad_input_status_string",
+                 "conv2d_grad_input_noalloc", "conv2d_forward", "rmsnorm_matmul",
+                 "rmsnorm_matmul_select_kernel", "rmsnorm_matmul_set_kernel",
+                 "rmsnorm_matmul_check_errors"):
+        assert must in names, must
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -283,3 +291,58 @@ def test_binding_checks_tensors_before_calling_the_library(lib, monkeypatch):
     other = type("S", (), {"device": type("D", (), {"index": 2})(), "cuda_stream": 0})()
     with pytest.raises(ValueError, match="stream"):
         dg.conv2d_grad_input(good_g, good_w, out, p, dg.DGRAD_BF16, other)
+
+
+# ---------------------------------------------------------------- rmsnorm_matmul (host logic)
+def test_rmsnorm_matmul_selection_and_validation(lib):
+    sel = dg.rmsnorm_matmul_select_kernel
+    A, W, B, C = 0x10000, 0x20000, 0x30000, 0x40000  # 16-byte aligned raw addresses
+    p = dg.RmsParams(300, 320, 520, 1e-5)
+    assert sel(A, W, B, C, p, dg.DGRAD_BF16) == dg.DGRAD_KERNEL_TC
+    assert sel(A, W, B, C, p, dg.DGRAD_F16) == dg.DGRAD_KERNEL_TC
+    assert sel(A, W, B, C, p, dg.DGRAD_F32) == dg.DGRAD_KERNEL_SIMT      # float32: CUDA cores
+    assert sel(A, W, B, C + 4, p, dg.DGRAD_BF16) == dg.DGRAD_KERNEL_SIMT  # C off 16 bytes
+    assert sel(A + 2, W, B, C, p, dg.DGRAD_BF16) == dg.DGRAD_KERNEL_SIMT  # X off 16 bytes
+    assert sel(A, W, B, C, dg.RmsParams(300, 330, 520, 1e-5), dg.DGRAD_BF16) == dg.DGRAD_KERNEL_SIMT
+    assert sel(A, W, B, C, dg.RmsParams(300, 320, 521, 1e-5), dg.DGRAD_BF16) == dg.DGRAD_KERNEL_SIMT
+    assert sel(0, W, B, C, p, dg.DGRAD_BF16) == -1                        # NULL
+    assert sel(A, W, B, C, p, 7) == -1                                    # dtype
+    assert sel(A, W, B, C, dg.RmsParams(300, 320, 520, -1.0), dg.DGRAD_BF16) == -1
+    assert sel(A, W, B, C, dg.RmsParams(300, 320, 520, float("nan")), dg.DGRAD_BF16) == -1
+    assert sel(A, W, B, C, dg.RmsParams(0, 320, 520, 0.0), dg.DGRAD_BF16) == -2
+    assert sel(A + 1, W, B, C, p, dg.DGRAD_BF16) == -3                    # element alignment
+    assert sel(A, W, B, C + 2, p, dg.DGRAD_F32) == -3
+    assert sel(A, W, B, C, dg.RmsParams(1 << 16, 1 << 16, 8, 0.0), dg.DGRAD_BF16) == -4  # 2^32 outputs
+    assert dg.rmsnorm_matmul_set_kernel(dg.DGRAD_KERNEL_TC) == dg.DGRAD_KERNEL_AUTO
+    try:
+        assert sel(A, W, B, C, p, dg.DGRAD_BF16) == dg.DGRAD_KERNEL_TC
+        assert sel(A, W, B, C, p, dg.DGRAD_F32) == -4                     # forced but not applicable
+        assert dg.rmsnorm_matmul_set_kernel(dg.DGRAD_KERNEL_SIMT) == dg.DGRAD_KERNEL_TC
+        assert sel(A, W, B, C, p, dg.DGRAD_BF16) == dg.DGRAD_KERNEL_SIMT
+        assert dg.rmsnorm_matmul_set_kernel(3) == 1                       # DGRAD_ERR_INVALID_ARG
+    finally:
+        dg.rmsnorm_matmul_set_kernel(dg.DGRAD_KERNEL_AUTO)
+
+
+def test_rmsnorm_matmul_binding_checks_tensors(lib, monkeypatch):
+    """Sizes, dtypes and devices of the four buffers are checked on the host
+    before the library is called (fake CUDA tensors: nothing reaches a GPU)."""
+    import torch
+    import conv2d_backward_implicit_gb300.binding as binding
+    monkeypatch.setattr(binding, "_current_device", lambda: 0)
+    p = dg.RmsParams(4, 64, 8, 0.0)
+    x = _FakeCudaTensor(numel=32)
+    wn = _FakeCudaTensor(numel=8)
+    wp = _FakeCudaTensor(numel=512)
+    c = _FakeCudaTensor("float32", numel=256)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        dg.rmsnorm_matmul(torch.zeros(4, 8, dtype=torch.bfloat16), wn, wp, c, p, dg.DGRAD_BF16)
+    for bad, what in (((_FakeCudaTensor(numel=33), wn, wp, c), "x must have 32"),
+                      ((x, _FakeCudaTensor(numel=9), wp, c), "w_norm must have 8"),
+                      ((x, wn, _FakeCudaTensor(numel=511), c), "w_proj must have 512"),
+                      ((x, wn, wp, _FakeCudaTensor("float32", numel=255)), "c must have 256"),
+                      ((x, wn, wp, _FakeCudaTensor("bfloat16", numel=256)), "float32"),
+                      ((_FakeCudaTensor("float16", numel=32), wn, wp, c), "bfloat16"),
+                      ((x, wn, wp, _FakeCudaTensor("float32", numel=256, index=1)), "current device")):
+        with pytest.raises(ValueError, match=what):
+            dg.rmsnorm_matmul(*bad, p, dg.DGRAD_BF16)
