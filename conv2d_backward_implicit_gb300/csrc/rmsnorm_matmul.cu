@@ -16,10 +16,12 @@
 //   * warp 6 (one thread): TMA loads of the W_proj tile [64 K][256 N] through a
 //     3-D view [N/64][K][64] of W_proj, giving the MN-major B operand layout
 //     (atoms of 8 K rows x 64 N, 1 KB, N-block stride 8 KB) in one copy;
-//   * warps 7-10 (the transform): thread r owns tile row r; per stage it reads
-//     its row's eight 16-byte chunks in place, accumulates x^2 in float32,
-//     writes x * W_norm[t] rounded to the input type back, and signals the
-//     stage; after a tile's last stage it stores r[i] for the epilogue;
+//   * warps 7-22 (the transform): threads 4r .. 4r + 3 own tile row r, two
+//     of its eight 16-byte chunks each; per stage they read them in place,
+//     accumulate x^2 in float32, write x * W_norm[t] back (one packed 16-bit
+//     multiply per pair: the exact product rounded once to the input type)
+//     and signal the stage; after a tile's last stage the four add their
+//     sums and store r[i] for the epilogue;
 //   * warp 4 (one thread): tcgen05.mma M128 N256 K16 into a double-buffered
 //     TMEM accumulator (2 x 256 columns);
 //   * warps 0-3 (the epilogue, one per TMEM lane quadrant): 32 rows x 32
@@ -54,7 +56,7 @@ namespace {
 
 constexpr int kBM = 128, kBN = 256, kBK = 64;  // tile rows, tile columns, K per stage (16-bit)
 constexpr int kStages = 4;
-constexpr int kEpiWarps = 4, kMmaWarp = 4, kAWarp = 5, kBWarp = 6, kTWarp0 = 7, kTWarps = 4;
+constexpr int kEpiWarps = 4, kMmaWarp = 4, kAWarp = 5, kBWarp = 6, kTWarp0 = 7, kTWarps = 16;
 constexpr int kThreads = 32 * (kTWarp0 + kTWarps);
 constexpr uint32_t kAStage = kBM * kBK * 2;  // 16 KB
 constexpr uint32_t kBStage = kBK * kBN * 2;  // 32 KB
@@ -245,24 +247,6 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const P
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// 16-bit element <-> float32 for the input type.
-__device__ __forceinline__ float lo_f(uint32_t w, bool f16) {
-    return f16 ? __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)))
-               : __bfloat162float(__ushort_as_bfloat16((unsigned short)(w & 0xFFFFu)));
-}
-__device__ __forceinline__ float hi_f(uint32_t w, bool f16) {
-    return f16 ? __half2float(__ushort_as_half((unsigned short)(w >> 16)))
-               : __bfloat162float(__ushort_as_bfloat16((unsigned short)(w >> 16)));
-}
-__device__ __forceinline__ uint32_t pack2(float a, float b, bool f16) {
-    if (f16) {
-        const __half2 h = __floats2half2_rn(a, b);
-        return *reinterpret_cast<const uint32_t *>(&h);
-    }
-    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<const uint32_t *>(&h);
-}
-
 // ----------------------------------------------------------------- roles
 // Producer of one operand (A: X tiles, B: W_proj tiles) for every tile and
 // stage of this CTA, into the stage ring; drains its copies when aborting.
@@ -302,45 +286,72 @@ __device__ void role_load(const Params &p, Ctl &c, uint32_t smem) {
     }
 }
 
-// Transform warps: thread r owns row r of every X tile in the ring.
-__device__ void role_transform(const Params &p, Ctl &c, uint32_t smem, float *rs, int r, int lane) {
+// 16-bit pair (low, high) -> two floats.
+__device__ __forceinline__ float2 unpack2(uint32_t v, bool f16) {
+    if (f16) return __half22float2(*reinterpret_cast<const __half2 *>(&v));
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+// Product of two 16-bit pairs, rounded once to the input type (the exact
+// float32 product rounded to nearest: a 16-bit product fits float32 exactly).
+__device__ __forceinline__ uint32_t mul2(uint32_t a, uint32_t b, bool f16) {
+    uint32_t r;
+    if (f16) {
+        const __half2 h = __hmul2(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&b));
+        r = *reinterpret_cast<const uint32_t *>(&h);
+    } else {
+        const __nv_bfloat162 h = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&a),
+                                         *reinterpret_cast<const __nv_bfloat162 *>(&b));
+        r = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    return r;
+}
+
+// Transform warps: threads 4r .. 4r + 3 (h = 0 .. 3) own row r of every X
+// tile in the ring, logical chunks 2h and 2h + 1 of it.
+__device__ void role_transform(const Params &p, Ctl &c, uint32_t smem, float *rs, int tid, int lane) {
     const bool f16 = p.f16 != 0;
     const uint16_t *wn = static_cast<const uint16_t *>(p.w_norm);
     const bool wn_vec = (reinterpret_cast<uintptr_t>(wn) & 15u) == 0;
+    constexpr int J = 8 * kBM / (32 * kTWarps);  // chunks per thread
+    const int r = tid / (8 / J), h = tid % (8 / J);
     int s = 0, acc = 0;
     uint32_t ph = 0, rph = 0;
     for (int64_t t = blockIdx.x; t < p.tiles; t += gridDim.x) {
-        float ss = 0.f;
+        float2 ss = make_float2(0.f, 0.f);
         for (int kk = 0; kk < p.kt; ++kk) {
             if (!wait_warp(su32(&c.a_full[s]), ph, p, c, lane)) return;
             const uint32_t row = smem + kOffA + (uint32_t)s * kAStage + (uint32_t)r * 128u;
-#pragma unroll 2
-            for (int ch = 0; ch < 8; ++ch) {  // logical 16-byte chunk ch: columns kk*64 + 8ch .. + 7
-                const int t0 = kk * kBK + 8 * ch;
-                uint32_t w[4];
+            // All of this thread's chunk loads (W_norm from L1, the row from
+            // shared memory) are issued before any is used.
+            uint32_t w[J][4];
+            uint4 xv[J];
+#pragma unroll
+            for (int j = 0; j < J; ++j) {  // logical chunk J h + j: columns kk*64 + 8(J h + j) .. + 7
+                const int t0 = kk * kBK + 8 * (J * h + j);
                 if (wn_vec && t0 + 8 <= p.k) {
                     const uint4 u = __ldg(reinterpret_cast<const uint4 *>(wn + t0));
-                    w[0] = u.x, w[1] = u.y, w[2] = u.z, w[3] = u.w;
+                    w[j][0] = u.x, w[j][1] = u.y, w[j][2] = u.z, w[j][3] = u.w;
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const uint32_t lo = t0 + 2 * e < p.k ? (uint32_t)__ldg(wn + t0 + 2 * e) : 0u;
                         const uint32_t hi = t0 + 2 * e + 1 < p.k ? (uint32_t)__ldg(wn + t0 + 2 * e + 1) : 0u;
-                        w[e] = lo | (hi << 16);
+                        w[j][e] = lo | (hi << 16);
                     }
                 }
-                const uint32_t a = row + (uint32_t)((ch ^ (r & 7)) << 4);
-                const uint4 x = lds128(a);
-                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+                xv[j] = lds128(row + (uint32_t)(((J * h + j) ^ (r & 7)) << 4));
+            }
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const uint32_t xs[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
                 uint32_t o[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float x0 = lo_f(xs[e], f16), x1 = hi_f(xs[e], f16);
-                    ss = fmaf(x0, x0, ss);
-                    ss = fmaf(x1, x1, ss);
-                    o[e] = pack2(x0 * lo_f(w[e], f16), x1 * hi_f(w[e], f16), f16);
+                    const float2 f = unpack2(xs[e], f16);
+                    ss = __ffma2_rn(f, f, ss);
+                    o[e] = mul2(xs[e], w[j][e], f16);
                 }
-                sts128(a, o[0], o[1], o[2], o[3]);
+                sts128(row + (uint32_t)(((J * h + j) ^ (r & 7)) << 4), o[0], o[1], o[2], o[3]);
             }
             fence_async_proxy();  // the MMA (async proxy) reads what these threads wrote
             __syncwarp();
@@ -352,8 +363,11 @@ __device__ void role_transform(const Params &p, Ctl &c, uint32_t smem, float *rs
         }
         // Row scale of this tile, for the epilogue (buffer acc, free once the
         // epilogue of the tile two back has read it).
+        float sum = ss.x + ss.y;
+#pragma unroll
+        for (int o = 1; o < 8 / J; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);  // the row's other parts
         if (!wait_warp(su32(&c.rs_empty[acc]), rph ^ 1u, p, c, lane)) return;
-        rs[acc * kBM + r] = 1.0f / sqrtf(ss / (float)p.k + p.eps);
+        if (h == 0) rs[acc * kBM + r] = 1.0f / sqrtf(sum / (float)p.k + p.eps);
         __syncwarp();
         if (lane == 0) bar_arrive(su32(&c.rs_full[acc]));
         if (++acc == 2) {
