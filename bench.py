@@ -458,6 +458,49 @@ def forward_call(dg, workloads, wl, dev, stream, calls=300):
     return e0.elapsed_time(e1) / calls
 
 
+# The fused RMSNorm + matmul (include/rmsnorm_matmul.h): an LLM projection
+# shape -- 8192 tokens, hidden size 4096, 4096 outputs -- in bf16.
+RMS_SHAPE = {"m": 8192, "n": 4096, "k": 4096, "dtype": "bf16", "eps": 1e-6}
+
+
+def rmsnorm_flops_bytes(m: int, n: int, k: int, esize: int = 2):
+    """Useful FLOPs (2 m n k: the products; the norm adds O(m k)) and
+    algorithmic bytes (X, W_norm and W_proj read once, C float32 written once)."""
+    return 2.0 * m * n * k, float(m * k * esize + k * esize + k * n * esize + m * n * 4)
+
+
+def rmsnorm_call(dg, dev, stream, calls=40):
+    """The fused RMSNorm + matmul of RMS_SHAPE, back to back (its 224 MB of
+    operands and result exceed L2, so every call streams from HBM), timed with
+    events; returns (ms per call, kernel id)."""
+    import torch
+    sh = RMS_SHAPE
+    m, n, k = sh["m"], sh["n"], sh["k"]
+    gen = torch.Generator().manual_seed(0)
+    x = (torch.randn(m, k, generator=gen) * torch.exp(torch.empty(m, 1).uniform_(-2.3, 2.3, generator=gen)))
+    wn = torch.empty(k).uniform_(0.5, 1.5, generator=gen)
+    wp = torch.randn(k, n, generator=gen) / math.sqrt(k)
+    tdt = torch.bfloat16
+    x, wn, wp = x.to(tdt).to(dev), wn.to(tdt).to(dev), wp.to(tdt).to(dev)
+    c = torch.empty(m, n, device=dev)
+    p = dg.RmsParams(m, n, k, sh["eps"])
+    code = dg.DTYPE_CODE[sh["dtype"]]
+    kernel = dg.rmsnorm_matmul_select_kernel(x, wn, wp, c, p, code)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            dg.rmsnorm_matmul(x, wn, wp, c, p, code, stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(calls):
+            dg.rmsnorm_matmul(x, wn, wp, c, p, code, stream)
+        e1.record(stream)
+    stream.synchronize()
+    rc = dg.rmsnorm_matmul_check_errors(stream)
+    if rc != 0:
+        raise RuntimeError(f"rmsnorm_matmul: {dg.STATUS.get(rc, rc)}")
+    return e0.elapsed_time(e1) / calls, kernel
+
+
 def run_gpu(args, wl, key):
     import torch
     import torch.distributed as dist
@@ -739,6 +782,19 @@ def run_gpu(args, wl, key):
                     "op": "conv2d_forward at stride 2 (space-to-depth of x, weight split, stride-1 path)",
                     "workload": swl.name, "ms_per_call": fs_ms,
                     "tflops": useful_flops(swl) / (fs_ms * 1e-3) / 1e12}
+            # The fused RMSNorm + matmul (a second operation of the library).
+            r_ms, r_kernel = rmsnorm_call(dg, dev, stream)
+            r_flops, r_bytes = rmsnorm_flops_bytes(RMS_SHAPE["m"], RMS_SHAPE["n"], RMS_SHAPE["k"])
+            r_tf = r_flops / (r_ms * 1e-3) / 1e12
+            sustained = float(peaks.get("bf16_tflops_sustained", bf16_peak))
+            out["rmsnorm_matmul"] = {
+                "op": "rmsnorm_matmul: C = RmsNorm(X, W_norm) x W_proj, norm fused (one pass over X)",
+                "workload": "m={m} n={n} k={k} {dtype} in, f32 out, eps={eps}".format(**RMS_SHAPE),
+                "kernel": {1: "tcgen05", 2: "cuda-core"}.get(r_kernel, str(r_kernel)),
+                "us_per_call": r_ms * 1e3, "tflops": r_tf,
+                "tensor_frac": r_tf / bf16_peak, "tensor_peak": bf16_peak,
+                "tensor_frac_sustained": r_tf / sustained, "tensor_peak_sustained": sustained,
+                "hbm_frac": r_bytes / (r_ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": r_bytes}
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(wl)
         print(json.dumps(out), flush=True)

@@ -104,3 +104,12 @@ def test_probes_compile_for_sm103a():
             r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
                                 path, "-o", d + "/" + name], capture_output=True, text=True)
             assert r.returncode == 0, r.stderr
+
+
+def test_rmsnorm_flops_and_bytes():
+    import bench
+    f, b = bench.rmsnorm_flops_bytes(8192, 4096, 4096)
+    assert f == 2.0 * 8192 * 4096 * 4096
+    # X and W_proj bf16, W_norm bf16, C float32
+    assert b == 8192 * 4096 * 2 + 4096 * 2 + 4096 * 4096 * 2 + 8192 * 4096 * 4
+    assert bench.RMS_SHAPE["dtype"] == "bf16" and bench.RMS_SHAPE["n"] % 64 == 0 and bench.RMS_SHAPE["k"] % 8 == 0
