@@ -852,6 +852,29 @@ def profile_run(args, wl, key):
     return 0
 
 
+def profile_rmsnorm(args):
+    """Only the fused RMSNorm + matmul, args.profile_rmsnorm times back to back
+    on an m x 4096 x 4096 bf16 problem (m = args.rmsnorm_m), for an ncu capture."""
+    import torch
+    import conv2d_backward_implicit_gb300 as dg
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    m, n, k = args.rmsnorm_m, RMS_SHAPE["n"], RMS_SHAPE["k"]
+    gen = torch.Generator().manual_seed(0)
+    x = torch.randn(m, k, generator=gen).to(torch.bfloat16).to(dev)
+    wn = torch.empty(k).uniform_(0.5, 1.5, generator=gen).to(torch.bfloat16).to(dev)
+    wp = (torch.randn(k, n, generator=gen) / math.sqrt(k)).to(torch.bfloat16).to(dev)
+    c = torch.empty(m, n, device=dev)
+    p = dg.RmsParams(m, n, k, RMS_SHAPE["eps"])
+    for _ in range(args.profile_rmsnorm):
+        dg.rmsnorm_matmul(x, wn, wp, c, p, dg.DGRAD_BF16)
+    rc = dg.rmsnorm_matmul_check_errors()
+    if rc != 0:
+        raise RuntimeError(f"rmsnorm_matmul: {dg.STATUS.get(rc, rc)}")
+    print(json.dumps({"profile_rmsnorm": args.profile_rmsnorm, "m": m, "n": n, "k": k}), flush=True)
+    return 0
+
+
 def record_traffic_file(args, wl, key):
     """Writes profiles/dgrad_tc_<key>.traffic.json from the CSV of ncu_traffic_command."""
     with open(args.record_traffic) as f:
@@ -903,6 +926,10 @@ def main(argv=None):
                     help="only launch the dgrad kernel L times (for an ncu capture)")
     ap.add_argument("--record-traffic", metavar="CSV", default=None,
                     help="write profiles/dgrad_tc_<config>.traffic.json from an ncu CSV")
+    ap.add_argument("--profile-rmsnorm", type=int, default=0, metavar="L",
+                    help="only launch the fused RMSNorm + matmul L times on an m x 4096 x 4096 bf16 "
+                         "problem (for an ncu capture; m from --rmsnorm-m)")
+    ap.add_argument("--rmsnorm-m", type=int, default=2048, help="rows of X for --profile-rmsnorm")
     ap.add_argument("--probe", choices=sorted(PROBES), default=None,
                     help="build and run a device-rate probe (tcgen05.mma, TMA loads or stores)")
     args = ap.parse_args(argv)
@@ -914,6 +941,8 @@ def main(argv=None):
         return record_traffic_file(args, wl, args.config)
     if args.profile_launches > 0:
         return profile_run(args, wl, args.config)
+    if args.profile_rmsnorm > 0:
+        return profile_rmsnorm(args)
     if args.impl == "reference":
         args.steps = 10 if args.steps is None else args.steps
         args.warmup = 1 if args.warmup is None else args.warmup

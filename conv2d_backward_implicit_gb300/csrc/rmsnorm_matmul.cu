@@ -319,12 +319,9 @@ __device__ void role_transform(const Params &p, Ctl &c, uint32_t smem, float *rs
     for (int64_t t = blockIdx.x; t < p.tiles; t += gridDim.x) {
         float2 ss = make_float2(0.f, 0.f);
         for (int kk = 0; kk < p.kt; ++kk) {
-            if (!wait_warp(su32(&c.a_full[s]), ph, p, c, lane)) return;
-            const uint32_t row = smem + kOffA + (uint32_t)s * kAStage + (uint32_t)r * 128u;
-            // All of this thread's chunk loads (W_norm from L1, the row from
-            // shared memory) are issued before any is used.
+            // This stage's W_norm values (from L1) are loaded before the wait
+            // for its X tile, so their latency hides behind it.
             uint32_t w[J][4];
-            uint4 xv[J];
 #pragma unroll
             for (int j = 0; j < J; ++j) {  // logical chunk J h + j: columns kk*64 + 8(J h + j) .. + 7
                 const int t0 = kk * kBK + 8 * (J * h + j);
@@ -339,8 +336,12 @@ __device__ void role_transform(const Params &p, Ctl &c, uint32_t smem, float *rs
                         w[j][e] = lo | (hi << 16);
                     }
                 }
-                xv[j] = lds128(row + (uint32_t)(((J * h + j) ^ (r & 7)) << 4));
             }
+            if (!wait_warp(su32(&c.a_full[s]), ph, p, c, lane)) return;
+            const uint32_t row = smem + kOffA + (uint32_t)s * kAStage + (uint32_t)r * 128u;
+            uint4 xv[J];
+#pragma unroll
+            for (int j = 0; j < J; ++j) xv[j] = lds128(row + (uint32_t)(((J * h + j) ^ (r & 7)) << 4));
 #pragma unroll
             for (int j = 0; j < J; ++j) {
                 const uint32_t xs[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
