@@ -1,5 +1,6 @@
 """GB300-native conv2d input gradient (dgrad) as an implicit GEMM, with the
-strided forward convolution and the fused RMSNorm + matmul beside it.
+strided forward convolution, the fused RMSNorm + matmul and the attention
+gradient with respect to V beside it.
 
 The compute path is the C-ABI library ``libconv2d_grad_input.so`` built from
 ``csrc/`` for sm_103a; :mod:`.binding` marshals arguments to it.  Importing
@@ -17,4 +18,5 @@ from .binding import (  # noqa: F401
     params_from_shapes,
     RmsParams, rmsnorm_matmul, rmsnorm_matmul_check_errors, rmsnorm_matmul_select_kernel,
     rmsnorm_matmul_set_kernel,
+    MhaParams, mha_grad_v, mha_grad_v_check_errors, mha_grad_v_select_kernel, mha_grad_v_set_kernel,
 )

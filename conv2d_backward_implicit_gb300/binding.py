@@ -1,5 +1,5 @@
-"""ctypes binding for the C ABI in include/conv2d_grad_input.h and include/rmsnorm_matmul.h
-(argument marshalling only).
+"""ctypes binding for the C ABI in include/conv2d_grad_input.h, include/rmsnorm_matmul.h
+and include/mha_grad_v.h (argument marshalling only).
 
 Every function here has the name of the C entry point it calls, accepts torch
 tensors (or raw integer addresses) for the buffers, and raises
@@ -41,6 +41,14 @@ class RmsParams(ctypes.Structure):
     """rmsnorm_matmul_params: m, n, k (uint32) and eps (float)."""
     _fields_ = [("m", ctypes.c_uint32), ("n", ctypes.c_uint32), ("k", ctypes.c_uint32),
                 ("eps", ctypes.c_float)]
+
+
+MHA_FIELDS = ("q_seq", "kv_seq", "num_heads", "num_kv_heads", "head_dim", "window_size")
+
+
+class MhaParams(ctypes.Structure):
+    """mha_grad_v_params: six uint32 fields in the header's order."""
+    _fields_ = [(name, ctypes.c_uint32) for name in MHA_FIELDS]
 
 
 class DgradError(RuntimeError):
@@ -113,6 +121,15 @@ def library() -> ctypes.CDLL:
             lib.rmsnorm_matmul_set_kernel.restype = I
             lib.rmsnorm_matmul_check_errors.argtypes = [P]
             lib.rmsnorm_matmul_check_errors.restype = I
+            MP = ctypes.POINTER(MhaParams)
+            lib.mha_grad_v.argtypes = [P, P, P, P, P, MP, I, P]
+            lib.mha_grad_v.restype = I
+            lib.mha_grad_v_select_kernel.argtypes = [P, P, P, P, P, MP, I]
+            lib.mha_grad_v_select_kernel.restype = I
+            lib.mha_grad_v_set_kernel.argtypes = [I]
+            lib.mha_grad_v_set_kernel.restype = I
+            lib.mha_grad_v_check_errors.argtypes = [P]
+            lib.mha_grad_v_check_errors.restype = I
             _lib = lib
     return _lib
 
@@ -310,3 +327,33 @@ def rmsnorm_matmul_set_kernel(kernel: int) -> int:
 def rmsnorm_matmul_check_errors(stream=None) -> int:
     """Returns the status (0, DGRAD_ERR_TIMEOUT = 6 or DGRAD_ERR_CUDA = 5) without raising."""
     return int(library().rmsnorm_matmul_check_errors(_stream(stream)))
+
+
+def _mha_args(q, k, d_out, lse, dv, params: MhaParams, dtype: int):
+    qs, nh, nkv, hd = int(params.q_seq), int(params.num_heads), int(params.num_kv_heads), int(params.head_dim)
+    kv = qs if int(params.kv_seq) == 0 else int(params.kv_seq)
+    t = _in_dtype(dtype)
+    return (_addr(q, "q", t, qs * nh * hd), _addr(k, "k", t, kv * nkv * hd), _addr(d_out, "d_out", t, qs * nh * hd),
+            _addr(lse, "lse", "float32", qs * nh * 2), _addr(dv, "dv", "float32", kv * nkv * hd))
+
+
+def mha_grad_v(q, k, d_out, lse, dv, params: MhaParams, dtype: int, stream=None) -> None:
+    """dV [kv, num_kv_heads, head_dim] of attention (include/mha_grad_v.h)."""
+    rc = library().mha_grad_v(*_mha_args(q, k, d_out, lse, dv, params, dtype), ctypes.byref(params), int(dtype),
+                              _stream(stream))
+    _check(rc, "mha_grad_v")
+
+
+def mha_grad_v_select_kernel(q, k, d_out, lse, dv, params: MhaParams, dtype: int) -> int:
+    """DGRAD_KERNEL_TC (1) or DGRAD_KERNEL_SIMT (2) for these buffers, or a negative status."""
+    return int(library().mha_grad_v_select_kernel(*_mha_args(q, k, d_out, lse, dv, params, dtype),
+                                                  ctypes.byref(params), int(dtype)))
+
+
+def mha_grad_v_set_kernel(kernel: int) -> int:
+    return int(library().mha_grad_v_set_kernel(int(kernel)))
+
+
+def mha_grad_v_check_errors(stream=None) -> int:
+    """Returns the status (0, DGRAD_ERR_TIMEOUT = 6 or DGRAD_ERR_CUDA = 5) without raising."""
+    return int(library().mha_grad_v_check_errors(_stream(stream)))

@@ -346,3 +346,46 @@ def test_rmsnorm_matmul_binding_checks_tensors(lib, monkeypatch):
                       ((x, wn, wp, _FakeCudaTensor("float32", numel=256, index=1)), "current device")):
         with pytest.raises(ValueError, match=what):
             dg.rmsnorm_matmul(*bad, p, dg.DGRAD_BF16)
+
+
+# ---------------------------------------------------------------- mha_grad_v (host logic)
+def test_mha_grad_v_validation_and_selection(lib):
+    sel = dg.mha_grad_v_select_kernel
+    Q, K, O, L, V = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
+    p = dg.MhaParams(128, 0, 8, 2, 64, 0)
+    assert sel(Q, K, O, L, V, p, dg.DGRAD_F32) == dg.DGRAD_KERNEL_SIMT
+    assert sel(0, K, O, L, V, p, dg.DGRAD_BF16) == -1                          # NULL
+    assert sel(Q, K, O, L, V, p, 9) == -1                                      # dtype
+    assert sel(Q, K, O, L, V, dg.MhaParams(0, 0, 8, 2, 64, 0), dg.DGRAD_BF16) == -2
+    assert sel(Q, K, O, L, V, dg.MhaParams(128, 0, 6, 4, 64, 0), dg.DGRAD_BF16) == -2   # 6 % 4
+    assert sel(Q, K, O, L, V, dg.MhaParams(128, 0, 8, 2, 0, 0), dg.DGRAD_BF16) == -2
+    assert sel(Q + 1, K, O, L, V, p, dg.DGRAD_BF16) == -3                      # element alignment
+    assert sel(Q, K, O, L + 2, V, p, dg.DGRAD_BF16) == -3
+    assert sel(Q, K, O, L, V, dg.MhaParams(128, 0, 8, 2, 512, 0), dg.DGRAD_BF16) == -4  # head_dim
+    assert dg.mha_grad_v_set_kernel(dg.DGRAD_KERNEL_SIMT) == dg.DGRAD_KERNEL_AUTO
+    try:
+        assert sel(Q, K, O, L, V, p, dg.DGRAD_BF16) == dg.DGRAD_KERNEL_SIMT
+        assert dg.mha_grad_v_set_kernel(dg.DGRAD_KERNEL_TC) == dg.DGRAD_KERNEL_SIMT
+        assert sel(Q, K, O, L, V, p, dg.DGRAD_F32) == -4                       # forced, not applicable
+        assert dg.mha_grad_v_set_kernel(7) == 1
+    finally:
+        dg.mha_grad_v_set_kernel(dg.DGRAD_KERNEL_AUTO)
+
+
+def test_mha_grad_v_binding_checks_tensors(lib, monkeypatch):
+    import conv2d_backward_implicit_gb300.binding as binding
+    monkeypatch.setattr(binding, "_current_device", lambda: 0)
+    p = dg.MhaParams(10, 0, 4, 2, 8, 0)   # kv = 10
+    q = _FakeCudaTensor(numel=320)
+    k = _FakeCudaTensor(numel=160)
+    go = _FakeCudaTensor(numel=320)
+    lse = _FakeCudaTensor("float32", numel=80)
+    dv = _FakeCudaTensor("float32", numel=160)
+    for bad, what in (((_FakeCudaTensor(numel=321), k, go, lse, dv), "q must have 320"),
+                      ((q, _FakeCudaTensor(numel=159), go, lse, dv), "k must have 160"),
+                      ((q, k, _FakeCudaTensor(numel=10), lse, dv), "d_out must have 320"),
+                      ((q, k, go, _FakeCudaTensor("float32", numel=40), dv), "lse must have 80"),
+                      ((q, k, go, lse, _FakeCudaTensor("bfloat16", numel=160)), "float32"),
+                      ((q, k, go, lse, _FakeCudaTensor("float32", numel=160, index=3)), "current device")):
+        with pytest.raises(ValueError, match=what):
+            dg.mha_grad_v(*bad, p, dg.DGRAD_BF16)
