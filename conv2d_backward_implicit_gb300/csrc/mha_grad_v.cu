@@ -146,14 +146,15 @@ int validate(const void *q, const void *k, const void *go, const float *lse, con
     return DGRAD_OK;
 }
 
-bool tc_applies(const void *q, const void *k, const void *go, const mha_grad_v_params *p, int dtype);
+bool tc_applies(const void *q, const void *k, const void *go, const float *lse, const float *dv,
+                const mha_grad_v_params *p, int dtype);
 
 int select(const void *q, const void *k, const void *go, const float *lse, const float *dv,
            const mha_grad_v_params *p, int dtype) {
     const int v = validate(q, k, go, lse, dv, p, dtype);
     if (v != DGRAD_OK) return -v;
     const int choice = g_kernel_choice.load();
-    const bool tc = tc_applies(q, k, go, p, dtype);
+    const bool tc = tc_applies(q, k, go, lse, dv, p, dtype);
     if (choice == DGRAD_KERNEL_SIMT) return DGRAD_KERNEL_SIMT;
     if (choice == DGRAD_KERNEL_TC) return tc ? DGRAD_KERNEL_TC : -DGRAD_ERR_UNSUPPORTED;
     return tc ? DGRAD_KERNEL_TC : DGRAD_KERNEL_SIMT;

@@ -1,13 +1,466 @@
 // mha_grad_v_tc.cuh -- tensor-core kernel of the attention dV (included by
-// mha_grad_v.cu).
+// mha_grad_v.cu): bf16 / fp16 Q, K, dO with head_dim 64, sm_103a.
+//
+// Work unit: 128 key positions t of one KV head g (units ordered by key tile,
+// so under a causal mask the units with the most query blocks start first),
+// one persistent CTA per SM.  For every block of 128 query positions that can
+// reach the unit and every head h of the group (a "step"):
+//   GEMM1  S^T[t][pos] = K_tile (128 x 64) . Q_block^T        tcgen05 M128 N128 K16 x4
+//   P^T[t][pos]        = exp(min(S^T / sqrt(64) - max[pos], 0) - log_sum[pos]), masked
+//   GEMM2  dV[t][:]   += P^T (128 x 128) . dO_block (128 x 64)  tcgen05 M128 N64 K16 x8
+// with dV accumulating in TMEM over all the unit's steps.
+//   * warp 5 (one thread): TMA loads -- the unit's K tile, then per step the
+//     Q and dO blocks of head h through 3-D views [q_seq][H][64] (box
+//     [128][1][64], 128-byte swizzle): Q lands as GEMM1's K-major B operand,
+//     dO as GEMM2's MN-major B operand (atoms of 8 positions x 64 elements);
+//   * warp 4 (one thread): GEMM1 of step i into one of two TMEM score buffers,
+//     then GEMM2 of step i - 1 (so the softmax of step i overlaps it);
+//   * warps 0-3 (one per TMEM lane quadrant, lane = key t): per step they read
+//     the step's 128 (max, log_sum) pairs into shared memory, read their score
+//     row from TMEM, form P with the page's clamp and the causal / window mask,
+//     round it to the input type and write it as GEMM2's K-major A operand (two
+//     128-byte swizzled chunks of 64 positions); after the unit's last step
+//     they store dV from TMEM to global memory.
+// Every wait is bounded; on timeout the kernel raises its error flag, drains
+// its copies and MMAs, frees TMEM and returns.
+#include <cudaTypedefs.h>
+
+#include "tc_helpers.cuh"
+
 namespace mhadv {
 namespace {
 
-bool tc_applies(const void *, const void *, const void *, const mha_grad_v_params *, int) { return false; }
+using namespace tch;
 
-int launch_tc(const void *, const void *, const void *, const float *, float *, const mha_grad_v_params *, int,
-              cudaStream_t) {
-    return DGRAD_ERR_UNSUPPORTED;
+constexpr int kTcT = 128, kTcP = 128, kTcD = 64;  // keys per unit, queries per step, head_dim
+constexpr int kTcStages = 4;
+constexpr int kTcSoftWarps = 4, kTcMmaWarp = 4, kTcLoadWarp = 5;
+constexpr int kTcThreads = 32 * 6;
+constexpr uint32_t kTile = 128 * 128;  // bytes of a [128][64] 16-bit tile
+constexpr uint32_t kOffLse = 1024, kOffK = 4096, kOffStage = kOffK + kTile;
+constexpr uint32_t kOffP = kOffStage + kTcStages * 2 * kTile;
+constexpr uint32_t kTcSmem = 1024 + kOffP + 2 * 2 * kTile;  // + 1 KB alignment slack
+static_assert(kTcSmem <= 232448, "shared memory over the per-block limit");
+
+struct TcArgs {
+    CUtensorMap q_map, k_map, o_map;  // [len][heads][64] views, box [128][1][64], 128-byte swizzle
+    const float *lse;
+    float *dv;
+    int q_seq, kv, nh, nkv, hpk, window, causal, t_tiles;
+    int64_t units;
+    float scale;
+    uint32_t idesc1, idesc2;
+    int f16;
+    uint64_t wait_limit_ns;
+};
+
+struct TcCtl {
+    uint64_t full[kTcStages], empty[kTcStages];
+    uint64_t k_full, k_empty;
+    uint64_t s_full[2], s_empty[2], p_ready[2], p_empty[2];
+    uint64_t dv_full, dv_empty, mma_done;
+    uint64_t lse_full[2];  // the softmax warps' shared (max, log_sum) buffer of a step
+    uint32_t tmem_base;
+    int abort_flag;
+};
+static_assert(sizeof(TcCtl) <= 1024, "control block too large");
+
+__device__ __noinline__ bool tc_wait_long(uint32_t bar, uint32_t parity, const TcArgs &a, TcCtl &c, bool honour) {
+    const uint64_t t0 = now_ns();
+    const uint64_t max_spins = a.wait_limit_ns / 16 + (1u << 20);
+    for (uint64_t spin = 1;; ++spin) {
+        if (bar_try(bar, parity)) return true;
+        if (honour && *reinterpret_cast<volatile int *>(&c.abort_flag)) return false;
+        if (((spin & 31u) == 0 && now_ns() - t0 > a.wait_limit_ns) || spin > max_spins) {
+            *reinterpret_cast<volatile int *>(&c.abort_flag) = 1;
+            atomicOr(&g_mha_error_word, 1u);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, const TcArgs &a, TcCtl &c) {
+    return bar_try(bar, parity) || tc_wait_long(bar, parity, a, c, true);
+}
+__device__ __forceinline__ void tc_drain(uint32_t bar, uint32_t parity, const TcArgs &a, TcCtl &c) {
+    if (!bar_try(bar, parity)) tc_wait_long(bar, parity, a, c, false);
+}
+__device__ __forceinline__ bool tc_wait_warp(uint32_t bar, uint32_t parity, const TcArgs &a, TcCtl &c, int lane) {
+    int ok = 0;
+    if (lane == 0) ok = tc_wait(bar, parity, a, c) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// The query blocks of a unit: [lo, hi) in steps of 128 (then the heads of the group).
+__device__ __forceinline__ void unit_range(const TcArgs &a, int64_t u, int &t0, int &g, int &lo, int &nblk) {
+    t0 = (int)(u / a.nkv) * kTcT;
+    g = (int)(u % a.nkv);
+    const int t_last = t0 + kTcT - 1 < a.kv ? t0 + kTcT - 1 : a.kv - 1;
+    lo = a.causal ? t0 : 0;
+    int hi = a.q_seq;
+    if (a.window > 0 && t_last + a.window < hi) hi = t_last + a.window;
+    nblk = hi > lo ? (hi - lo + kTcP - 1) / kTcP : 0;
+}
+
+__device__ void tc_role_load(const TcArgs &a, TcCtl &c, uint32_t smem) {
+    int s = 0;
+    uint32_t ph = 0, kph = 0;
+    int64_t issued = 0, k_issued = 0;
+    bool aborted = false;
+    for (int64_t u = blockIdx.x; u < a.units && !aborted; u += gridDim.x) {
+        int t0, g, lo, nblk;
+        unit_range(a, u, t0, g, lo, nblk);
+        if (nblk == 0) continue;  // no query reaches these keys: nothing to load
+        if (!tc_wait(su32(&c.k_empty), kph ^ 1u, a, c)) break;
+        bar_expect_tx(su32(&c.k_full), kTile);
+        tma_load_3d(smem + kOffK, &a.k_map, 0, g, t0, su32(&c.k_full));
+        ++k_issued;
+        kph ^= 1u;
+        for (int b = 0; b < nblk && !aborted; ++b)
+            for (int r = 0; r < a.hpk; ++r) {
+                if (!tc_wait(su32(&c.empty[s]), ph ^ 1u, a, c)) {
+                    aborted = true;
+                    break;
+                }
+                const int h = g * a.hpk + r, p0 = lo + b * kTcP;
+                const uint32_t st = smem + kOffStage + (uint32_t)s * 2u * kTile;
+                bar_expect_tx(su32(&c.full[s]), 2 * kTile);
+                tma_load_3d(st, &a.q_map, 0, h, p0, su32(&c.full[s]));
+                tma_load_3d(st + kTile, &a.o_map, 0, h, p0, su32(&c.full[s]));
+                ++issued;
+                if (++s == kTcStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+    }
+    // Copies still landing must finish before the CTA exits.
+    const int64_t k_end = issued < kTcStages ? issued : kTcStages;
+    for (int64_t q = issued - k_end; q < issued; ++q)
+        tc_drain(su32(&c.full[q % kTcStages]), (uint32_t)((q / kTcStages) & 1), a, c);
+    if (k_issued) tc_drain(su32(&c.k_full), (uint32_t)((k_issued - 1) & 1), a, c);
+}
+
+__device__ void tc_role_mma(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t tmem) {
+    int s = 0, sb = 0;
+    uint32_t ph = 0, sph = 0, kph = 0, dph = 0;
+    int64_t gstep = 0;  // this CTA's steps so far: score / P buffer gstep % 2, its use gstep / 2
+    bool aborted = false;
+    for (int64_t u = blockIdx.x; u < a.units && !aborted; u += gridDim.x) {
+        int t0, g, lo, nblk;
+        unit_range(a, u, t0, g, lo, nblk);
+        const int n = nblk * a.hpk;
+        if (n == 0) continue;
+        if (!tc_wait(su32(&c.k_full), kph, a, c)) break;
+        kph ^= 1u;
+        tc_after();
+        const uint64_t kd = desc_k(smem + kOffK);
+        int s_prev = 0, sb_prev = 0;
+        int64_t g_prev = 0;
+        for (int i = 0; i <= n && !aborted; ++i) {
+            if (i < n) {  // GEMM1 of step i
+                if (!tc_wait(su32(&c.full[s]), ph, a, c) || !tc_wait(su32(&c.s_empty[sb]), sph ^ 1u, a, c)) {
+                    aborted = true;
+                    break;
+                }
+                tc_after();
+                const uint64_t qd = desc_k(smem + kOffStage + (uint32_t)s * 2u * kTile);
+#pragma unroll
+                for (int k16 = 0; k16 < 4; ++k16)
+                    tc_mma_f16(tmem + (uint32_t)(sb * kTcP), kd + 2u * k16, qd + 2u * k16, a.idesc1, k16 != 0);
+                tc_commit_to(su32(&c.s_full[sb]));
+                if (i == n - 1) tc_commit_to(su32(&c.k_empty));  // the unit's last read of its K tile
+            }
+            if (i >= 1) {  // GEMM2 of step i - 1
+                const int j = i - 1;
+                if (!tc_wait(su32(&c.p_ready[sb_prev]), (uint32_t)((g_prev >> 1) & 1), a, c) ||
+                    (j == 0 && !tc_wait(su32(&c.dv_empty), dph ^ 1u, a, c))) {
+                    aborted = true;
+                    break;
+                }
+                tc_after();
+                const uint32_t pbuf = smem + kOffP + (uint32_t)sb_prev * 2u * kTile;
+                const uint64_t od = desc_mn(smem + kOffStage + (uint32_t)s_prev * 2u * kTile + kTile, 1024u, 1024u);
+#pragma unroll
+                for (int k16 = 0; k16 < 8; ++k16)
+                    tc_mma_f16(tmem + 2u * kTcP, desc_k(pbuf + (uint32_t)(k16 >> 2) * kTile) + 2u * (k16 & 3),
+                               od + 128u * k16, a.idesc2, (j | k16) != 0);
+                tc_commit_to(su32(&c.p_empty[sb_prev]));
+                tc_commit_to(su32(&c.empty[s_prev]));
+            }
+            if (i < n) {
+                s_prev = s;
+                sb_prev = sb;
+                g_prev = gstep++;
+                if (++s == kTcStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+                if (++sb == 2) {
+                    sb = 0;
+                    sph ^= 1u;
+                }
+            }
+        }
+        if (aborted) break;
+        tc_commit_to(su32(&c.dv_full));
+        dph ^= 1u;
+    }
+    tc_commit_to(su32(&c.mma_done));
+    tc_drain(su32(&c.mma_done), 0, a, c);
+}
+
+// Softmax and dV store warps: thread u = 32 w + lane is key row t0 + u.
+__device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, float2 *lse_s, uint32_t tmem, int w,
+                             int lane) {
+    const int u = 32 * w + lane;
+    const bool f16 = a.f16 != 0;
+    const float l2e = 1.4426950408889634f;  // log2(e): exp(x) = 2^(x log2(e))
+    int sb = 0, lb = 0;
+    uint32_t sph = 0, dph = 0;
+    int64_t steps = 0;  // this CTA's steps so far (P buffer parity)
+    for (int64_t un = blockIdx.x; un < a.units; un += gridDim.x) {
+        int t0, g, lo, nblk;
+        unit_range(a, un, t0, g, lo, nblk);
+        const int t = t0 + u;
+        const int start = a.causal ? t : 0;
+        int end = a.q_seq;
+        if (a.window > 0 && t + a.window < end) end = t + a.window;
+        const bool t_live = t < a.kv;
+        for (int b = 0; b < nblk; ++b)
+            for (int r = 0; r < a.hpk; ++r, ++steps) {
+                const int h = g * a.hpk + r, p0 = lo + b * kTcP;
+                // The step's forward statistics, one pair per thread, shared
+                // through buffer lb (free again once every warp has reached the
+                // next step's exchange, which it does only after this step).
+                {
+                    const int pos = p0 + u;
+                    float2 st = make_float2(0.f, 0.f);
+                    if (pos < a.q_seq) st = *reinterpret_cast<const float2 *>(a.lse + ((int64_t)pos * a.nh + h) * 2);
+                    lse_s[lb * kTcP + u] = make_float2(st.x * l2e, st.y * l2e);
+                    __syncwarp();
+                    if (lane == 0) bar_arrive(su32(&c.lse_full[lb]));
+                    if (!tc_wait_warp(su32(&c.lse_full[lb]), (uint32_t)((steps >> 1) & 1), a, c, lane)) return;
+                }
+                if (!tc_wait_warp(su32(&c.s_full[sb]), sph, a, c, lane)) return;
+                tc_after();
+                const uint32_t srow = tmem + ((uint32_t)(32 * w) << 16) + (uint32_t)(sb * kTcP);
+                if (!tc_wait_warp(su32(&c.p_empty[sb]), (uint32_t)(((steps >> 1) & 1) ^ 1), a, c, lane)) return;
+                const uint32_t prow = smem + kOffP + (uint32_t)sb * 2u * kTile + (uint32_t)u * 128u;
+#pragma unroll 1
+                for (int q32 = 0; q32 < kTcP / 32; ++q32) {  // 32 query positions at a time
+                    uint32_t v[32];
+                    tc_ld_32x32(srow + (uint32_t)(32 * q32), v);
+                    tc_wait_ld(v);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float pr[2];
+#pragma unroll
+                        for (int z = 0; z < 2; ++z) {
+                            const int pi = 32 * q32 + e + z, pos = p0 + pi;
+                            const float2 st = lse_s[lb * kTcP + pi];
+                            const float x = fminf(__uint_as_float(v[e + z]) * (a.scale * l2e) - st.x, 0.f) - st.y;
+                            pr[z] = (t_live && pos >= start && pos < end) ? exp2f(x) : 0.f;
+                        }
+                        if (f16) {
+                            const __half2 hh = __floats2half2_rn(pr[0], pr[1]);
+                            pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&hh);
+                        } else {
+                            const __nv_bfloat162 hh = __floats2bfloat162_rn(pr[0], pr[1]);
+                            pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&hh);
+                        }
+                    }
+                    // Positions 32 q32 .. + 31: chunk q32 / 2 of the row, 16-byte
+                    // pieces 4 (q32 % 2) .. + 3 at their swizzled slots.
+                    const uint32_t chunk = prow + (uint32_t)(q32 >> 1) * kTile;
+#pragma unroll
+                    for (int pc = 0; pc < 4; ++pc) {
+                        const int piece = 4 * (q32 & 1) + pc;
+                        sts128(chunk + (uint32_t)((piece ^ (u & 7)) << 4), pk[4 * pc], pk[4 * pc + 1],
+                               pk[4 * pc + 2], pk[4 * pc + 3]);
+                    }
+                }
+                tc_before();
+                fence_async_proxy();  // GEMM2 (async proxy) reads the P these threads wrote
+                __syncwarp();
+                if (lane == 0) {
+                    bar_arrive(su32(&c.s_empty[sb]));
+                    bar_arrive(su32(&c.p_ready[sb]));
+                }
+                if (++sb == 2) {
+                    sb = 0;
+                    sph ^= 1u;
+                }
+                lb ^= 1;
+            }
+        if (nblk == 0) {  // no query reaches these keys: dV is zero
+            if (t < a.kv)
+                for (int d = 0; d < kTcD; d += 4)
+                    *reinterpret_cast<float4 *>(a.dv + ((int64_t)t * a.nkv + g) * kTcD + d) = make_float4(0.f, 0.f, 0.f, 0.f);
+            continue;
+        }
+        // dV of the unit: TMEM columns 256 .. 319 of lane u.
+        if (!tc_wait_warp(su32(&c.dv_full), dph, a, c, lane)) return;
+        dph ^= 1u;
+        tc_after();
+#pragma unroll 1
+        for (int h32 = 0; h32 < 2; ++h32) {
+            uint32_t v[32];
+            tc_ld_32x32(tmem + ((uint32_t)(32 * w) << 16) + 2u * kTcP + (uint32_t)(32 * h32), v);
+            tc_wait_ld(v);
+            if (t_live) {
+                float4 *out = reinterpret_cast<float4 *>(a.dv + ((int64_t)t * a.nkv + g) * kTcD + 32 * h32);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    out[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                         __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+            }
+        }
+        tc_before();
+        __syncwarp();
+        if (lane == 0) bar_arrive(su32(&c.dv_empty));
+    }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) mha_grad_v_tc_kernel(const __grid_constant__ TcArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t smem = (su32(smem_raw) + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (smem - su32(smem_raw));
+    TcCtl &c = *reinterpret_cast<TcCtl *>(base);
+    float2 *lse_s = reinterpret_cast<float2 *>(base + kOffLse);  // [2][128]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kTcStages; ++s) {
+            bar_init(su32(&c.full[s]), 1);
+            bar_init(su32(&c.empty[s]), 1);
+        }
+        bar_init(su32(&c.k_full), 1);
+        bar_init(su32(&c.k_empty), 1);
+        for (int b = 0; b < 2; ++b) {
+            bar_init(su32(&c.s_full[b]), 1);
+            bar_init(su32(&c.s_empty[b]), kTcSoftWarps);
+            bar_init(su32(&c.p_ready[b]), kTcSoftWarps);
+            bar_init(su32(&c.p_empty[b]), 1);
+        }
+        bar_init(su32(&c.dv_full), 1);
+        bar_init(su32(&c.dv_empty), kTcSoftWarps);
+        bar_init(su32(&c.mma_done), 1);
+        bar_init(su32(&c.lse_full[0]), kTcSoftWarps);
+        bar_init(su32(&c.lse_full[1]), kTcSoftWarps);
+        c.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kTcMmaWarp) tc_alloc(su32(&c.tmem_base), 512);
+    tc_before();
+    __syncthreads();
+    tc_after();
+    const uint32_t tmem = c.tmem_base;
+    if (warp == kTcLoadWarp && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.q_map)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.k_map)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.o_map)) : "memory");
+    }
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (warp == kTcLoadWarp) {
+        if (lane == 0) tc_role_load(a, c, smem);
+        __syncwarp();
+    } else if (warp == kTcMmaWarp) {
+        if (lane == 0) tc_role_mma(a, c, smem, tmem);
+        __syncwarp();
+    } else {
+        tc_role_soft(a, c, smem, lse_s, tmem, warp, lane);
+    }
+    tc_before();
+    __syncthreads();
+    if (warp == kTcMmaWarp) {
+        tc_after();
+        tc_dealloc(tmem, 512);
+    }
+}
+
+bool tc_applies(const void *q, const void *k, const void *go, const float *lse, const float *dv,
+                const mha_grad_v_params *p, int dtype) {
+    return dtype != DGRAD_F32 && p->head_dim == (uint32_t)kTcD && aligned(q, 16) && aligned(k, 16) &&
+           aligned(go, 16) && aligned(lse, 8) && aligned(dv, 16);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            ptr = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }();
+    return fn;
+}
+
+// [len][heads][64] 16-bit tensor, box [128][1][64], 128-byte swizzle.
+bool encode_heads_map(CUtensorMap *m, const void *ptr, int len, int heads) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = tc_encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)kTcD, (cuuint64_t)heads, (cuuint64_t)len};
+    const cuuint64_t strides[2] = {(cuuint64_t)kTcD * 2, (cuuint64_t)heads * kTcD * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)kTcD, 1, 128};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int launch_tc(const void *q, const void *k, const void *go, const float *lse, float *dv, const mha_grad_v_params *p,
+              int dtype, cudaStream_t st) {
+    TcArgs a{};
+    a.q_seq = (int)p->q_seq;
+    a.causal = p->kv_seq == 0;
+    a.kv = a.causal ? a.q_seq : (int)p->kv_seq;
+    a.nh = (int)p->num_heads;
+    a.nkv = (int)p->num_kv_heads;
+    a.hpk = a.nh / a.nkv;
+    a.window = (int)p->window_size;
+    a.t_tiles = (a.kv + kTcT - 1) / kTcT;
+    a.units = (int64_t)a.t_tiles * a.nkv;
+    a.scale = 1.0f / sqrtf((float)kTcD);
+    a.lse = lse;
+    a.dv = dv;
+    a.f16 = dtype == DGRAD_F16 ? 1 : 0;
+    const uint32_t fmt = dtype == DGRAD_BF16 ? 1u : 0u;
+    // D float32, A and B of the input type; GEMM1: both K-major, N = 128;
+    // GEMM2: B (dO) MN-major, N = 64; M = 128.
+    a.idesc1 = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(kTcP >> 3) << 17) | ((uint32_t)(kTcT >> 4) << 24);
+    a.idesc2 = (1u << 4) | (fmt << 7) | (fmt << 10) | (1u << 16) | ((uint32_t)(kTcD >> 3) << 17) |
+               ((uint32_t)(kTcT >> 4) << 24);
+    a.wait_limit_ns = 2000000000ull;
+    if (!encode_heads_map(&a.q_map, q, a.q_seq, a.nh) || !encode_heads_map(&a.k_map, k, a.kv, a.nkv) ||
+        !encode_heads_map(&a.o_map, go, a.q_seq, a.nh))
+        return DGRAD_ERR_UNSUPPORTED;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DGRAD_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return DGRAD_ERR_CUDA;
+    static std::atomic<uint64_t> configured{0};
+    const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
+    if (!bit || !(configured.load() & bit)) {
+        if (cudaFuncSetAttribute(mha_grad_v_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem) !=
+            cudaSuccess)
+            return DGRAD_ERR_CUDA;
+        configured.fetch_or(bit);
+    }
+    const int grid = (int)(a.units < sms ? a.units : sms);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = kTcSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mha_grad_v_tc_kernel, a) == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
 }
 
 }  // namespace

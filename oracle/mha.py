@@ -28,6 +28,8 @@ _I, _P = ctypes.c_int, ctypes.c_void_p
 def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_mha_grad_v_f64.argtypes = [_P, _P, _P, _P, _P] + [_I] * 6
     lib.oracle_mha_grad_v_f64.restype = _I
+    lib.oracle_mha_grad_v_rows_f64.argtypes = [_P, _P, _P, _P, _P] + [_I] * 8
+    lib.oracle_mha_grad_v_rows_f64.restype = _I
     lib.oracle_mha_forward_lse_f64.argtypes = [_P, _P, _P] + [_I] * 6
     lib.oracle_mha_forward_lse_f64.restype = _I
     return lib
@@ -82,4 +84,19 @@ def grad_v(q, k, d_out, lse, kv_seq: int, window: int, lib=None) -> np.ndarray:
                                    q_seq, kv_seq, nh, nkv, hd, window)
     if rc != 0:
         raise ValueError("oracle rejected the shape")
+    return dv
+
+
+def grad_v_rows(q, k, d_out, lse, kv_seq: int, window: int, t_begin: int, t_end: int, lib=None) -> np.ndarray:
+    """Rows t_begin .. t_end - 1 of dV (float64), for checks at sizes where every row costs too much."""
+    lib = lib or load_library()
+    qq, kk, go, ls = _f64(q), _f64(k), _f64(d_out), _f64(lse)
+    q_seq, nh, hd = qq.shape
+    kv, nkv, _ = kk.shape
+    assert go.shape == qq.shape and ls.shape == (q_seq, nh, 2) and kv == kv_len(q_seq, kv_seq)
+    dv = np.empty((t_end - t_begin, nkv, hd), dtype=np.float64)
+    rc = lib.oracle_mha_grad_v_rows_f64(qq.ctypes.data, kk.ctypes.data, go.ctypes.data, ls.ctypes.data,
+                                        dv.ctypes.data, q_seq, kv_seq, nh, nkv, hd, window, t_begin, t_end)
+    if rc != 0:
+        raise ValueError("oracle rejected the shape or range")
     return dv

@@ -30,19 +30,22 @@ static int check(int q_seq, int kv_seq, int nh, int nkv, int hd) {
     return 0;
 }
 
-/* dV as defined above.  Returns 0, or -1 for a bad shape. */
-int oracle_mha_grad_v_f64(const double *q, const double *k, const double *d_out, const double *lse, double *dv,
-                          int q_seq, int kv_seq, int num_heads, int num_kv_heads, int head_dim, int window) {
+/* Rows t in [t_begin, t_end) of dV as defined above (dv holds those rows
+ * only, from row t_begin).  Returns 0, or -1 for a bad shape or range. */
+int oracle_mha_grad_v_rows_f64(const double *q, const double *k, const double *d_out, const double *lse,
+                               double *dv, int q_seq, int kv_seq, int num_heads, int num_kv_heads, int head_dim,
+                               int window, int t_begin, int t_end) {
     if (check(q_seq, kv_seq, num_heads, num_kv_heads, head_dim) != 0 || window < 0) return -1;
     const int causal = kv_seq == 0;
     const int kv = causal ? q_seq : kv_seq;
+    if (t_begin < 0 || t_end > kv || t_begin > t_end) return -1;
     const int hpk = num_heads / num_kv_heads;
     const int64_t q_dim = (int64_t)num_heads * head_dim, kv_dim = (int64_t)num_kv_heads * head_dim;
     const double scale = 1.0 / sqrt((double)head_dim);
-    for (int t = 0; t < kv; ++t)
+    for (int t = t_begin; t < t_end; ++t)
         for (int g = 0; g < num_kv_heads; ++g) {
             const double *kt = k + t * kv_dim + (int64_t)g * head_dim;
-            double *out = dv + t * kv_dim + (int64_t)g * head_dim;
+            double *out = dv + (t - t_begin) * kv_dim + (int64_t)g * head_dim;
             for (int d = 0; d < head_dim; ++d) out[d] = 0.0;
             const int start = causal ? t : 0;
             int end = q_seq;
@@ -63,6 +66,14 @@ int oracle_mha_grad_v_f64(const double *q, const double *k, const double *d_out,
                 }
         }
     return 0;
+}
+
+/* dV as defined above, every row.  Returns 0, or -1 for a bad shape. */
+int oracle_mha_grad_v_f64(const double *q, const double *k, const double *d_out, const double *lse, double *dv,
+                          int q_seq, int kv_seq, int num_heads, int num_kv_heads, int head_dim, int window) {
+    const int kv = kv_seq == 0 ? q_seq : kv_seq;
+    return oracle_mha_grad_v_rows_f64(q, k, d_out, lse, dv, q_seq, kv_seq, num_heads, num_kv_heads, head_dim,
+                                      window, 0, kv < 0 ? 0 : kv);
 }
 
 /* Forward statistics (max score, log of sum of exp(score - max)) of every

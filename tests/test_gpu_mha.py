@@ -95,3 +95,48 @@ def test_dv_off_alignment_and_guard(dg):
     p = dg.MhaParams(*case)
     got = run(dg, q, k, go, lse, p, "f32", dv_offset=1)
     check(got, q, k, go, lse, p, 1e-4)
+
+
+# Tensor-core cases (head_dim 64): one unit; several query blocks under a
+# causal mask (diagonal block masked); full attention with ragged lengths;
+# a window; grouped heads; a single position.
+TC_CASES = [
+    (64, 0, 4, 2, 64, 0), (300, 0, 8, 2, 64, 0), (200, 330, 4, 4, 64, 0), (257, 0, 6, 3, 64, 100),
+    (1, 1, 1, 1, 64, 0), (129, 0, 2, 1, 64, 1), (500, 260, 8, 4, 64, 50),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("case", TC_CASES)
+def test_tensor_core_kernel(dg, dtype, case, parity_log):
+    q, k, go, lse = make_inputs(*case, dtype, seed=3 * sum(case))
+    p = dg.MhaParams(*case)
+    dev = torch.device("cuda")
+    kv = mha.kv_len(case[0], case[1])
+    assert dg.mha_grad_v_select_kernel(q.to(dev), k.to(dev), go.to(dev), lse.to(dev),
+                                       torch.empty(kv, case[3], 64, device=dev), p,
+                                       dg.DTYPE_CODE[dtype]) == dg.DGRAD_KERNEL_TC
+    got = run(dg, q, k, go, lse, p, dtype)
+    err = check(got, q, k, go, lse, p, C_TC[dtype])
+    parity_log(f"mha_grad_v tc {dtype} {case}", err, C_TC[dtype])
+
+
+def test_tensor_core_kernel_more_units_than_sms(dg, parity_log):
+    """160 units (20 key tiles x 8 KV heads) for 152 SMs: the last key tile runs
+    as some CTAs' second unit (K buffer reuse, dV buffer handover, barrier
+    phases carried across units).  The oracle checks three key tiles, the last
+    among them."""
+    case = (2560, 0, 16, 8, 64, 0)
+    q, k, go, lse = make_inputs(*case, "bf16", seed=21)
+    p = dg.MhaParams(*case)
+    got = run(dg, q, k, go, lse, p, "bf16")
+    qd, kd, god, ld = q.double().numpy(), k.double().numpy(), go.double().numpy(), lse.double().numpy()
+    worst = 0.0
+    for t0 in (0, 1280, 2432):
+        ref = mha.grad_v_rows(qd, kd, god, ld, 0, 0, t0, t0 + 128)
+        mag = mha.grad_v_rows(qd, kd, np.abs(god), ld, 0, 0, t0, t0 + 128)
+        bound = C_TC["bf16"] * mag + 1e-6 * np.abs(ref).max()
+        err = np.abs(got[t0:t0 + 128] - ref)
+        assert (err <= bound).all(), f"key tile {t0}: error above the bound"
+        worst = max(worst, float(err.max() / np.abs(ref).max()))
+    parity_log("mha_grad_v tc bf16 (2560, 0, 16, 8, 64, 0), 3 key tiles", worst, C_TC["bf16"])

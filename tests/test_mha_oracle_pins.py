@@ -166,3 +166,11 @@ def test_planted_mutant_is_caught(name, tmp_path):
 
 def test_mutant_sites_are_distinct():
     assert len({m[0] + "->" + m[1] for m in MUTANTS.values()}) == len(MUTANTS)
+
+
+def test_row_range_matches_the_full_result():
+    q, k, go = _rand(20, 0, 4, 2, 8, 11)
+    lse = mha.forward_lse(q, k, 0, 5)
+    full = mha.grad_v(q, k, go, lse, 0, 5)
+    for a, b in ((0, 20), (3, 9), (19, 20), (7, 7)):
+        assert np.array_equal(mha.grad_v_rows(q, k, go, lse, 0, 5, a, b), full[a:b])
