@@ -501,6 +501,61 @@ def rmsnorm_call(dg, dev, stream, calls=40):
     return e0.elapsed_time(e1) / calls, kernel
 
 
+# The attention gradient with respect to V (include/mha_grad_v.h): causal
+# self-attention over 4096 positions, 32 query heads sharing 8 KV heads,
+# head_dim 64, bf16.
+MHA_SHAPE = {"q_seq": 4096, "kv_seq": 0, "num_heads": 32, "num_kv_heads": 8, "head_dim": 64,
+             "window_size": 0, "dtype": "bf16"}
+
+
+def mha_useful_flops(q_seq: int, kv_seq: int, num_heads: int, head_dim: int, window: int) -> float:
+    """4 head_dim FLOPs (the score's dot product and the P dO update) for every
+    (query, key, head) that the mask keeps: keys t < kv with t <= pos when
+    causal (kv_seq == 0) and t > pos - window when window > 0."""
+    import numpy as np
+    kv = q_seq if kv_seq == 0 else kv_seq
+    pos = np.arange(q_seq, dtype=np.int64)
+    hi = np.minimum(pos if kv_seq == 0 else np.full_like(pos, kv - 1), kv - 1)
+    lo = np.maximum(pos - window + 1, 0) if window > 0 else np.zeros_like(pos)
+    pairs = int(np.maximum(hi - lo + 1, 0).sum())
+    return 4.0 * head_dim * num_heads * pairs
+
+
+def mha_call(dg, dev, stream, calls=20):
+    """The attention dV of MHA_SHAPE back to back, timed with events; returns
+    (ms per call, kernel id)."""
+    import torch
+    sh = MHA_SHAPE
+    qs, nh, nkv, hd = sh["q_seq"], sh["num_heads"], sh["num_kv_heads"], sh["head_dim"]
+    kv = qs if sh["kv_seq"] == 0 else sh["kv_seq"]
+    gen = torch.Generator().manual_seed(0)
+    q = torch.randn(qs, nh, hd, generator=gen).to(torch.bfloat16).to(dev)
+    k = torch.randn(kv, nkv, hd, generator=gen).to(torch.bfloat16).to(dev)
+    go = torch.randn(qs, nh, hd, generator=gen).to(torch.bfloat16).to(dev)
+    # Forward statistics of a plausible size (they only set P's scale here; the
+    # parity tests use exact ones): max = |q| |k| / sqrt(d) bound, log_sum = log(pos + 1).
+    lse = torch.empty(qs, nh, 2, device=dev)
+    lse[..., 0] = 4.0
+    lse[..., 1] = torch.log(torch.arange(1, qs + 1, device=dev, dtype=torch.float32))[:, None]
+    dv = torch.empty(kv, nkv, hd, device=dev)
+    p = dg.MhaParams(qs, sh["kv_seq"], nh, nkv, hd, sh["window_size"])
+    code = dg.DTYPE_CODE[sh["dtype"]]
+    kernel = dg.mha_grad_v_select_kernel(q, k, go, lse, dv, p, code)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            dg.mha_grad_v(q, k, go, lse, dv, p, code, stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(calls):
+            dg.mha_grad_v(q, k, go, lse, dv, p, code, stream)
+        e1.record(stream)
+    stream.synchronize()
+    rc = dg.mha_grad_v_check_errors(stream)
+    if rc != 0:
+        raise RuntimeError(f"mha_grad_v: {dg.STATUS.get(rc, rc)}")
+    return e0.elapsed_time(e1) / calls, kernel
+
+
 def run_gpu(args, wl, key):
     import torch
     import torch.distributed as dist
@@ -795,6 +850,18 @@ def run_gpu(args, wl, key):
                 "tensor_frac": r_tf / bf16_peak, "tensor_peak": bf16_peak,
                 "tensor_frac_sustained": r_tf / sustained, "tensor_peak_sustained": sustained,
                 "hbm_frac": r_bytes / (r_ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": r_bytes}
+            # The attention gradient with respect to V (a third operation).
+            m_ms, m_kernel = mha_call(dg, dev, stream)
+            sh = MHA_SHAPE
+            m_tf = mha_useful_flops(sh["q_seq"], sh["kv_seq"], sh["num_heads"], sh["head_dim"],
+                                    sh["window_size"]) / (m_ms * 1e-3) / 1e12
+            out["mha_grad_v"] = {
+                "op": "mha_grad_v: dV of attention, P recomputed from the forward statistics",
+                "workload": ("q_seq={q_seq} causal, heads {num_heads} over {num_kv_heads} KV heads, "
+                             "head_dim {head_dim}, {dtype} in, f32 out").format(**sh),
+                "kernel": {1: "tcgen05", 2: "cuda-core"}.get(m_kernel, str(m_kernel)),
+                "us_per_call": m_ms * 1e3, "tflops": m_tf,
+                "tensor_frac": m_tf / bf16_peak, "tensor_peak": bf16_peak}
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(wl)
         print(json.dumps(out), flush=True)

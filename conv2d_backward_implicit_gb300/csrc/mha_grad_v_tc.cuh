@@ -9,18 +9,20 @@
 //   P^T[t][pos]        = exp(min(S^T / sqrt(64) - max[pos], 0) - log_sum[pos]), masked
 //   GEMM2  dV[t][:]   += P^T (128 x 128) . dO_block (128 x 64)  tcgen05 M128 N64 K16 x8
 // with dV accumulating in TMEM over all the unit's steps.
-//   * warp 5 (one thread): TMA loads -- the unit's K tile, then per step the
+//   * warp 17 (one thread): TMA loads -- the unit's K tile, then per step the
 //     Q and dO blocks of head h through 3-D views [q_seq][H][64] (box
 //     [128][1][64], 128-byte swizzle): Q lands as GEMM1's K-major B operand,
 //     dO as GEMM2's MN-major B operand (atoms of 8 positions x 64 elements);
-//   * warp 4 (one thread): GEMM1 of step i into one of two TMEM score buffers,
+//   * warp 16 (one thread): GEMM1 of step i into one of two TMEM score buffers,
 //     then GEMM2 of step i - 1 (so the softmax of step i overlaps it);
-//   * warps 0-3 (one per TMEM lane quadrant, lane = key t): per step they read
-//     the step's 128 (max, log_sum) pairs into shared memory, read their score
-//     row from TMEM, form P with the page's clamp and the causal / window mask,
-//     round it to the input type and write it as GEMM2's K-major A operand (two
-//     128-byte swizzled chunks of 64 positions); after the unit's last step
-//     they store dV from TMEM to global memory.
+//   * warps 0-15 (warp w: TMEM lane quadrant w % 4, lane = key t, query
+//     columns 32 (w / 4) .. + 31 of the step): each loads the 32 (max,
+//     log_sum) pairs of its columns one per lane (the next step's while this
+//     one computes) and shares them by shuffles, reads its 32 scores from
+//     TMEM, forms P with the page's clamp and the causal / window mask
+//     (hardware ex2), rounds it to the input type and writes it into GEMM2's
+//     K-major A operand (two 128-byte swizzled chunks of 64 positions); after
+//     the unit's last step each warp stores its 16 columns of dV.
 // Every wait is bounded; on timeout the kernel raises its error flag, drains
 // its copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -34,10 +36,10 @@ using namespace tch;
 
 constexpr int kTcT = 128, kTcP = 128, kTcD = 64;  // keys per unit, queries per step, head_dim
 constexpr int kTcStages = 4;
-constexpr int kTcSoftWarps = 4, kTcMmaWarp = 4, kTcLoadWarp = 5;
-constexpr int kTcThreads = 32 * 6;
+constexpr int kTcSoftWarps = 16, kTcMmaWarp = 16, kTcLoadWarp = 17;
+constexpr int kTcThreads = 32 * 18;
 constexpr uint32_t kTile = 128 * 128;  // bytes of a [128][64] 16-bit tile
-constexpr uint32_t kOffLse = 1024, kOffK = 4096, kOffStage = kOffK + kTile;
+constexpr uint32_t kOffK = 4096, kOffStage = kOffK + kTile;
 constexpr uint32_t kOffP = kOffStage + kTcStages * 2 * kTile;
 constexpr uint32_t kTcSmem = 1024 + kOffP + 2 * 2 * kTile;  // + 1 KB alignment slack
 static_assert(kTcSmem <= 232448, "shared memory over the per-block limit");
@@ -59,7 +61,6 @@ struct TcCtl {
     uint64_t k_full, k_empty;
     uint64_t s_full[2], s_empty[2], p_ready[2], p_empty[2];
     uint64_t dv_full, dv_empty, mma_done;
-    uint64_t lse_full[2];  // the softmax warps' shared (max, log_sum) buffer of a step
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -209,15 +210,29 @@ __device__ void tc_role_mma(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t t
     tc_drain(su32(&c.mma_done), 0, a, c);
 }
 
-// Softmax and dV store warps: thread u = 32 w + lane is key row t0 + u.
-__device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, float2 *lse_s, uint32_t tmem, int w,
-                             int lane) {
-    const int u = 32 * w + lane;
+__device__ __forceinline__ float fast_exp2(float x) {  // the SFU's 2^x (x <= 0 here)
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Softmax and dV store warps: warp w holds key rows t0 + 32 (w % 4) + lane and
+// query columns 32 (w / 4) .. + 31 of every step.
+__device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t tmem, int w, int lane) {
+    const int qd = w & 3, cq = w >> 2;
+    const int u = 32 * qd + lane;  // key row within the unit
     const bool f16 = a.f16 != 0;
     const float l2e = 1.4426950408889634f;  // log2(e): exp(x) = 2^(x log2(e))
-    int sb = 0, lb = 0;
+    int sb = 0;
     uint32_t sph = 0, dph = 0;
     int64_t steps = 0;  // this CTA's steps so far (P buffer parity)
+    // (max, log_sum) of query column 32 cq + lane of a step, times log2(e).
+    auto load_stats = [&](int p0, int h) {
+        const int pos = p0 + 32 * cq + lane;
+        float2 st = make_float2(0.f, 0.f);
+        if (pos < a.q_seq) st = __ldg(reinterpret_cast<const float2 *>(a.lse + ((int64_t)pos * a.nh + h) * 2));
+        return make_float2(st.x * l2e, st.y * l2e);
+    };
     for (int64_t un = blockIdx.x; un < a.units; un += gridDim.x) {
         int t0, g, lo, nblk;
         unit_range(a, un, t0, g, lo, nblk);
@@ -226,95 +241,81 @@ __device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, float2 *l
         int end = a.q_seq;
         if (a.window > 0 && t + a.window < end) end = t + a.window;
         const bool t_live = t < a.kv;
-        for (int b = 0; b < nblk; ++b)
-            for (int r = 0; r < a.hpk; ++r, ++steps) {
-                const int h = g * a.hpk + r, p0 = lo + b * kTcP;
-                // The step's forward statistics, one pair per thread, shared
-                // through buffer lb (free again once every warp has reached the
-                // next step's exchange, which it does only after this step).
-                {
-                    const int pos = p0 + u;
-                    float2 st = make_float2(0.f, 0.f);
-                    if (pos < a.q_seq) st = *reinterpret_cast<const float2 *>(a.lse + ((int64_t)pos * a.nh + h) * 2);
-                    lse_s[lb * kTcP + u] = make_float2(st.x * l2e, st.y * l2e);
-                    __syncwarp();
-                    if (lane == 0) bar_arrive(su32(&c.lse_full[lb]));
-                    if (!tc_wait_warp(su32(&c.lse_full[lb]), (uint32_t)((steps >> 1) & 1), a, c, lane)) return;
-                }
-                if (!tc_wait_warp(su32(&c.s_full[sb]), sph, a, c, lane)) return;
-                tc_after();
-                const uint32_t srow = tmem + ((uint32_t)(32 * w) << 16) + (uint32_t)(sb * kTcP);
-                if (!tc_wait_warp(su32(&c.p_empty[sb]), (uint32_t)(((steps >> 1) & 1) ^ 1), a, c, lane)) return;
-                const uint32_t prow = smem + kOffP + (uint32_t)sb * 2u * kTile + (uint32_t)u * 128u;
-#pragma unroll 1
-                for (int q32 = 0; q32 < kTcP / 32; ++q32) {  // 32 query positions at a time
-                    uint32_t v[32];
-                    tc_ld_32x32(srow + (uint32_t)(32 * q32), v);
-                    tc_wait_ld(v);
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float pr[2];
-#pragma unroll
-                        for (int z = 0; z < 2; ++z) {
-                            const int pi = 32 * q32 + e + z, pos = p0 + pi;
-                            const float2 st = lse_s[lb * kTcP + pi];
-                            const float x = fminf(__uint_as_float(v[e + z]) * (a.scale * l2e) - st.x, 0.f) - st.y;
-                            pr[z] = (t_live && pos >= start && pos < end) ? exp2f(x) : 0.f;
-                        }
-                        if (f16) {
-                            const __half2 hh = __floats2half2_rn(pr[0], pr[1]);
-                            pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&hh);
-                        } else {
-                            const __nv_bfloat162 hh = __floats2bfloat162_rn(pr[0], pr[1]);
-                            pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&hh);
-                        }
-                    }
-                    // Positions 32 q32 .. + 31: chunk q32 / 2 of the row, 16-byte
-                    // pieces 4 (q32 % 2) .. + 3 at their swizzled slots.
-                    const uint32_t chunk = prow + (uint32_t)(q32 >> 1) * kTile;
-#pragma unroll
-                    for (int pc = 0; pc < 4; ++pc) {
-                        const int piece = 4 * (q32 & 1) + pc;
-                        sts128(chunk + (uint32_t)((piece ^ (u & 7)) << 4), pk[4 * pc], pk[4 * pc + 1],
-                               pk[4 * pc + 2], pk[4 * pc + 3]);
-                    }
-                }
-                tc_before();
-                fence_async_proxy();  // GEMM2 (async proxy) reads the P these threads wrote
-                __syncwarp();
-                if (lane == 0) {
-                    bar_arrive(su32(&c.s_empty[sb]));
-                    bar_arrive(su32(&c.p_ready[sb]));
-                }
-                if (++sb == 2) {
-                    sb = 0;
-                    sph ^= 1u;
-                }
-                lb ^= 1;
+        const int n = nblk * a.hpk;
+        float2 st_next = n > 0 ? load_stats(lo, g * a.hpk) : make_float2(0.f, 0.f);
+        for (int i = 0; i < n; ++i, ++steps) {
+            const int b = i / a.hpk, r = i - b * a.hpk;
+            const int h = g * a.hpk + r, p0 = lo + b * kTcP;
+            const float2 st_mine = st_next;
+            if (i + 1 < n) {
+                const int b1 = (i + 1) / a.hpk;
+                st_next = load_stats(lo + b1 * kTcP, g * a.hpk + (i + 1 - b1 * a.hpk));
             }
-        if (nblk == 0) {  // no query reaches these keys: dV is zero
-            if (t < a.kv)
-                for (int d = 0; d < kTcD; d += 4)
+            if (!tc_wait_warp(su32(&c.s_full[sb]), sph, a, c, lane)) return;
+            tc_after();
+            uint32_t v[32];
+            tc_ld_32x32(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(sb * kTcP + 32 * cq), v);
+            tc_wait_ld(v);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                float pr[2];
+#pragma unroll
+                for (int z = 0; z < 2; ++z) {
+                    const int pos = p0 + 32 * cq + e + z;
+                    const float mx = __shfl_sync(0xffffffffu, st_mine.x, e + z);
+                    const float ls = __shfl_sync(0xffffffffu, st_mine.y, e + z);
+                    const float x = fminf(__uint_as_float(v[e + z]) * (a.scale * l2e) - mx, 0.f) - ls;
+                    pr[z] = (t_live && pos >= start && pos < end) ? fast_exp2(x) : 0.f;
+                }
+                if (f16) {
+                    const __half2 hh = __floats2half2_rn(pr[0], pr[1]);
+                    pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&hh);
+                } else {
+                    const __nv_bfloat162 hh = __floats2bfloat162_rn(pr[0], pr[1]);
+                    pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&hh);
+                }
+            }
+            tc_before();
+            __syncwarp();
+            if (lane == 0) bar_arrive(su32(&c.s_empty[sb]));  // scores read: the buffer may be refilled
+            if (!tc_wait_warp(su32(&c.p_empty[sb]), (uint32_t)(((steps >> 1) & 1) ^ 1), a, c, lane)) return;
+            // Columns 32 cq .. + 31: chunk cq / 2 of the row, 16-byte pieces
+            // 4 (cq % 2) .. + 3 at their swizzled slots.
+            const uint32_t row = smem + kOffP + (uint32_t)sb * 2u * kTile + (uint32_t)(cq >> 1) * kTile + (uint32_t)u * 128u;
+#pragma unroll
+            for (int pc = 0; pc < 4; ++pc) {
+                const int piece = 4 * (cq & 1) + pc;
+                sts128(row + (uint32_t)((piece ^ (u & 7)) << 4), pk[4 * pc], pk[4 * pc + 1], pk[4 * pc + 2],
+                       pk[4 * pc + 3]);
+            }
+            fence_async_proxy();  // GEMM2 (async proxy) reads the P these threads wrote
+            __syncwarp();
+            if (lane == 0) bar_arrive(su32(&c.p_ready[sb]));
+            if (++sb == 2) {
+                sb = 0;
+                sph ^= 1u;
+            }
+        }
+        if (n == 0) {  // no query reaches these keys: dV is zero
+            if (t_live)
+                for (int d = 16 * cq; d < 16 * cq + 16; d += 4)
                     *reinterpret_cast<float4 *>(a.dv + ((int64_t)t * a.nkv + g) * kTcD + d) = make_float4(0.f, 0.f, 0.f, 0.f);
             continue;
         }
-        // dV of the unit: TMEM columns 256 .. 319 of lane u.
+        // dV of the unit: this warp's 16 columns (TMEM 256 + 16 cq ..) of lane u.
         if (!tc_wait_warp(su32(&c.dv_full), dph, a, c, lane)) return;
         dph ^= 1u;
         tc_after();
-#pragma unroll 1
-        for (int h32 = 0; h32 < 2; ++h32) {
-            uint32_t v[32];
-            tc_ld_32x32(tmem + ((uint32_t)(32 * w) << 16) + 2u * kTcP + (uint32_t)(32 * h32), v);
-            tc_wait_ld(v);
-            if (t_live) {
-                float4 *out = reinterpret_cast<float4 *>(a.dv + ((int64_t)t * a.nkv + g) * kTcD + 32 * h32);
+        uint32_t v[32];
+        tc_ld_32x32(tmem + ((uint32_t)(32 * qd) << 16) + 2u * kTcP + (uint32_t)(16 * cq), v);  // 32 columns read,
+        tc_wait_ld(v);                                                                            // 16 used
+        if (t_live) {
+            float4 *out = reinterpret_cast<float4 *>(a.dv + ((int64_t)t * a.nkv + g) * kTcD + 16 * cq);
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    out[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                         __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
-            }
+            for (int e = 0; e < 4; ++e)
+                out[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                     __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
         }
         tc_before();
         __syncwarp();
@@ -327,7 +328,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) mha_grad_v_tc_kernel(const __gr
     const uint32_t smem = (su32(smem_raw) + 1023u) & ~1023u;
     uint8_t *base = smem_raw + (smem - su32(smem_raw));
     TcCtl &c = *reinterpret_cast<TcCtl *>(base);
-    float2 *lse_s = reinterpret_cast<float2 *>(base + kOffLse);  // [2][128]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcStages; ++s) {
@@ -345,8 +345,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) mha_grad_v_tc_kernel(const __gr
         bar_init(su32(&c.dv_full), 1);
         bar_init(su32(&c.dv_empty), kTcSoftWarps);
         bar_init(su32(&c.mma_done), 1);
-        bar_init(su32(&c.lse_full[0]), kTcSoftWarps);
-        bar_init(su32(&c.lse_full[1]), kTcSoftWarps);
         c.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -369,7 +367,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) mha_grad_v_tc_kernel(const __gr
         if (lane == 0) tc_role_mma(a, c, smem, tmem);
         __syncwarp();
     } else {
-        tc_role_soft(a, c, smem, lse_s, tmem, warp, lane);
+        tc_role_soft(a, c, smem, tmem, warp, lane);
     }
     tc_before();
     __syncthreads();

@@ -113,3 +113,17 @@ def test_rmsnorm_flops_and_bytes():
     # X and W_proj bf16, W_norm bf16, C float32
     assert b == 8192 * 4096 * 2 + 4096 * 2 + 4096 * 4096 * 2 + 8192 * 4096 * 4
     assert bench.RMS_SHAPE["dtype"] == "bf16" and bench.RMS_SHAPE["n"] % 64 == 0 and bench.RMS_SHAPE["k"] % 8 == 0
+
+
+def test_mha_useful_flops_counts_the_kept_pairs():
+    import bench
+    # causal 4 positions: 1 + 2 + 3 + 4 = 10 (query, key) pairs per head
+    assert bench.mha_useful_flops(4, 0, 2, 8, 0) == 4 * 8 * 2 * 10
+    # full attention 3 queries x 5 keys
+    assert bench.mha_useful_flops(3, 5, 1, 4, 0) == 4 * 4 * 15
+    # causal with window 2: 1 + 2 + 2 + 2
+    assert bench.mha_useful_flops(4, 0, 1, 1, 2) == 4 * 7
+    # brute force on a windowed full-attention case
+    q, kv, w = 7, 5, 3
+    pairs = sum(1 for pos in range(q) for t in range(kv) if t > pos - w)
+    assert bench.mha_useful_flops(q, kv, 1, 1, w) == 4 * pairs
