@@ -91,6 +91,16 @@ __device__ __forceinline__ bool tc_wait_warp(uint32_t bar, uint32_t parity, cons
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// This CTA's k-th unit, or -1: units are dealt to the CTAs in rounds, every
+// other round in reverse order, so that under a causal mask (units sorted by
+// decreasing work) a CTA with a heavy unit in one round gets a light one in
+// the next.
+__device__ __forceinline__ int64_t unit_of(const TcArgs &a, int k) {
+    const int64_t G = gridDim.x;
+    const int64_t u = (int64_t)k * G + ((k & 1) ? G - 1 - blockIdx.x : blockIdx.x);
+    return u < a.units ? u : -1;
+}
+
 // The query blocks of a unit: [lo, hi) in steps of 128 (then the heads of the group).
 __device__ __forceinline__ void unit_range(const TcArgs &a, int64_t u, int &t0, int &g, int &lo, int &nblk) {
     t0 = (int)(u / a.nkv) * kTcT;
@@ -107,7 +117,9 @@ __device__ void tc_role_load(const TcArgs &a, TcCtl &c, uint32_t smem) {
     uint32_t ph = 0, kph = 0;
     int64_t issued = 0, k_issued = 0;
     bool aborted = false;
-    for (int64_t u = blockIdx.x; u < a.units && !aborted; u += gridDim.x) {
+    for (int k = 0; !aborted; ++k) {
+        const int64_t u = unit_of(a, k);
+        if (u < 0) break;
         int t0, g, lo, nblk;
         unit_range(a, u, t0, g, lo, nblk);
         if (nblk == 0) continue;  // no query reaches these keys: nothing to load
@@ -146,7 +158,9 @@ __device__ void tc_role_mma(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t t
     uint32_t ph = 0, sph = 0, kph = 0, dph = 0;
     int64_t gstep = 0;  // this CTA's steps so far: score / P buffer gstep % 2, its use gstep / 2
     bool aborted = false;
-    for (int64_t u = blockIdx.x; u < a.units && !aborted; u += gridDim.x) {
+    for (int k = 0; !aborted; ++k) {
+        const int64_t u = unit_of(a, k);
+        if (u < 0) break;
         int t0, g, lo, nblk;
         unit_range(a, u, t0, g, lo, nblk);
         const int n = nblk * a.hpk;
@@ -233,7 +247,9 @@ __device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t 
         if (pos < a.q_seq) st = __ldg(reinterpret_cast<const float2 *>(a.lse + ((int64_t)pos * a.nh + h) * 2));
         return make_float2(st.x * l2e, st.y * l2e);
     };
-    for (int64_t un = blockIdx.x; un < a.units; un += gridDim.x) {
+    for (int k = 0;; ++k) {
+        const int64_t un = unit_of(a, k);
+        if (un < 0) break;
         int t0, g, lo, nblk;
         unit_range(a, un, t0, g, lo, nblk);
         const int t = t0 + u;
