@@ -9,20 +9,22 @@
 //   P^T[t][pos]        = exp(min(S^T / sqrt(64) - max[pos], 0) - log_sum[pos]), masked
 //   GEMM2  dV[t][:]   += P^T (128 x 128) . dO_block (128 x 64)  tcgen05 M128 N64 K16 x8
 // with dV accumulating in TMEM over all the unit's steps.
-//   * warp 17 (one thread): TMA loads -- the unit's K tile, then per step the
-//     Q and dO blocks of head h through 3-D views [q_seq][H][64] (box
-//     [128][1][64], 128-byte swizzle): Q lands as GEMM1's K-major B operand,
-//     dO as GEMM2's MN-major B operand (atoms of 8 positions x 64 elements);
-//   * warp 16 (one thread): GEMM1 of step i into one of two TMEM score buffers,
-//     then GEMM2 of step i - 1 (so the softmax of step i overlaps it);
+//   * warps 17-18 (one thread each): TMA loads of the Q and dO blocks of head
+//     h through 3-D views [q_seq][H][64] (box [128][1][64], 128-byte swizzle):
+//     Q lands as GEMM1's K-major B operand, dO as GEMM2's MN-major B operand
+//     (atoms of 8 positions x 64 elements).  One thread's copies complete one
+//     after another (about 1.1K cycles each) while different warps' overlap, so
+//     warp 17 loads the Q blocks and the unit's K tile, warp 18 the dO blocks
+//     and with each the forward statistics of its positions (for the head pair
+//     of h, through a [q_seq][2 H] float32 view);
+//   * warp 16 (one thread): GEMM1 two steps ahead of GEMM2, into two TMEM score
+//     buffers; GEMM2 takes P^T from TMEM as its A operand;
 //   * warps 0-15 (warp w: TMEM lane quadrant w % 4, lane = key t, query
-//     columns 32 (w / 4) .. + 31 of the step): each loads the 32 (max,
-//     log_sum) pairs of its columns one per lane (the next step's while this
-//     one computes) and shares them by shuffles, reads its 32 scores from
-//     TMEM, forms P with the page's clamp and the causal / window mask
-//     (hardware ex2), rounds it to the input type and writes it into GEMM2's
-//     K-major A operand (two 128-byte swizzled chunks of 64 positions); after
-//     the unit's last step each warp stores its 16 columns of dV.
+//     columns 32 (w / 4) .. + 31 of the step): fold the forward statistics of
+//     their columns, read their 32 scores from TMEM, form P with the page's
+//     clamp and the causal / window mask (hardware ex2), round it to the input
+//     type and store it, two values per column, into a TMEM P buffer; after the
+//     unit's last step each warp stores its 16 columns of dV.
 // Every wait is bounded; on timeout the kernel raises its error flag, drains
 // its copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -36,16 +38,30 @@ using namespace tch;
 
 constexpr int kTcT = 128, kTcP = 128, kTcD = 64;  // keys per unit, queries per step, head_dim
 constexpr int kTcStages = 4;
-constexpr int kTcSoftWarps = 16, kTcMmaWarp = 16, kTcLoadWarp = 17;
-constexpr int kTcThreads = 32 * 18;
+constexpr int kTcSoftWarps = 16, kTcMmaWarp = 16, kTcLoadWarp = 17, kTcLoadWarps = 2;
+constexpr int kTcThreads = 32 * (kTcLoadWarp + kTcLoadWarps);
+constexpr int kTcLoadPar = kTcLoadWarps / 2;  // step parities (one Q and one dO warp each)
+static_assert(kTcLoadWarps % 2 == 0 && kTcStages % kTcLoadPar == 0, "load warps own whole stages");
 constexpr uint32_t kTile = 128 * 128;  // bytes of a [128][64] 16-bit tile
-constexpr uint32_t kOffK = 4096, kOffStage = kOffK + kTile;
-constexpr uint32_t kOffP = kOffStage + kTcStages * 2 * kTile;
-constexpr uint32_t kTcSmem = 1024 + kOffP + 2 * 2 * kTile;  // + 1 KB alignment slack
+// Control block [0, 1 KB); per softmax warp 256 bytes: its 32 folded
+// (b, -l) pairs; then the K tile, the Q and dO rings (1 KB aligned for the
+// 128-byte swizzle) and the statistics ring: beside each dO slot, (max,
+// log_sum) of its 128 positions for an even / odd head pair.
+constexpr uint32_t kOffStats = 1024, kStatsBytes = 256;
+constexpr uint32_t kOffK = 5120;
+static_assert(kOffStats + kTcSoftWarps * kStatsBytes <= kOffK, "statistics overlap the K tile");
+constexpr uint32_t kOffQ = kOffK + kTile, kOffO = kOffQ + kTcStages * kTile;
+constexpr uint32_t kOffL = kOffO + kTcStages * kTile, kLseBox = 128 * 16;  // [128][4] float32 per slot
+// Tensor memory columns: scores S^T (two buffers of 128 float32), dV (64
+// float32), P^T (two buffers of 64 columns, each two 16-bit values).
+constexpr uint32_t kColS = 0, kColDv = 256, kColP = 320;
+constexpr uint32_t kTcSmem = 1024 + kOffL + kTcStages * kLseBox;  // + 1 KB alignment slack
+static_assert(kOffK % 1024 == 0, "operand tiles must be 1 KB aligned");
 static_assert(kTcSmem <= 232448, "shared memory over the per-block limit");
 
 struct TcArgs {
     CUtensorMap q_map, k_map, o_map;  // [len][heads][64] views, box [128][1][64], 128-byte swizzle
+    CUtensorMap l_map;                // LSE as [q_seq][2 H] float32, box [128][4] (two heads' pairs)
     const float *lse;
     float *dv;
     int q_seq, kv, nh, nkv, hpk, window, causal, t_tiles;
@@ -57,7 +73,7 @@ struct TcArgs {
 };
 
 struct TcCtl {
-    uint64_t full[kTcStages], empty[kTcStages];
+    uint64_t full_q[kTcStages], full_o[kTcStages], empty_q[kTcStages], empty_o[kTcStages];
     uint64_t k_full, k_empty;
     uint64_t s_full[2], s_empty[2], p_ready[2], p_empty[2];
     uint64_t dv_full, dv_empty, mma_done;
@@ -85,11 +101,6 @@ __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, const TcA
 __device__ __forceinline__ void tc_drain(uint32_t bar, uint32_t parity, const TcArgs &a, TcCtl &c) {
     if (!bar_try(bar, parity)) tc_wait_long(bar, parity, a, c, false);
 }
-__device__ __forceinline__ bool tc_wait_warp(uint32_t bar, uint32_t parity, const TcArgs &a, TcCtl &c, int lane) {
-    int ok = 0;
-    if (lane == 0) ok = tc_wait(bar, parity, a, c) ? 1 : 0;
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
 
 // This CTA's k-th unit, or -1: units are dealt to the CTAs in rounds, every
 // other round in reverse order, so that under a causal mask (units sorted by
@@ -112,10 +123,17 @@ __device__ __forceinline__ void unit_range(const TcArgs &a, int64_t u, int &t0, 
     nblk = hi > lo ? (hi - lo + kTcP - 1) / kTcP : 0;
 }
 
-__device__ void tc_role_load(const TcArgs &a, TcCtl &c, uint32_t smem) {
-    int s = 0;
-    uint32_t ph = 0, kph = 0;
-    int64_t issued = 0, k_issued = 0;
+// Load warp lw: tensor lw % 2 (0: Q, 1: dO) of the steps whose index in this
+// CTA is lw / 2 modulo kTcLoadPar; warp 0 also loads K.
+__device__ void tc_role_load(const TcArgs &a, TcCtl &c, uint32_t smem, int lw) {
+    const int tensor = lw & 1, par = lw >> 1;
+    const CUtensorMap *map = tensor ? &a.o_map : &a.q_map;
+    uint64_t *full = tensor ? c.full_o : c.full_q;
+    uint64_t *empty = tensor ? c.empty_o : c.empty_q;
+    const uint32_t ring = smem + (tensor ? kOffO : kOffQ);
+    int64_t gi = 0;  // this CTA's steps so far
+    int64_t k_issued = 0, last = -1;
+    uint32_t kph = 0;
     bool aborted = false;
     for (int k = 0; !aborted; ++k) {
         const int64_t u = unit_of(a, k);
@@ -123,42 +141,79 @@ __device__ void tc_role_load(const TcArgs &a, TcCtl &c, uint32_t smem) {
         int t0, g, lo, nblk;
         unit_range(a, u, t0, g, lo, nblk);
         if (nblk == 0) continue;  // no query reaches these keys: nothing to load
-        if (!tc_wait(su32(&c.k_empty), kph ^ 1u, a, c)) break;
-        bar_expect_tx(su32(&c.k_full), kTile);
-        tma_load_3d(smem + kOffK, &a.k_map, 0, g, t0, su32(&c.k_full));
-        ++k_issued;
-        kph ^= 1u;
+        if (lw == 0) {
+            if (!tc_wait(su32(&c.k_empty), kph ^ 1u, a, c)) break;
+            bar_expect_tx(su32(&c.k_full), kTile);
+            tma_load_3d(smem + kOffK, &a.k_map, 0, g, t0, su32(&c.k_full));
+            ++k_issued;
+            kph ^= 1u;
+        }
         for (int b = 0; b < nblk && !aborted; ++b)
-            for (int r = 0; r < a.hpk; ++r) {
-                if (!tc_wait(su32(&c.empty[s]), ph ^ 1u, a, c)) {
+            for (int r = 0; r < a.hpk; ++r, ++gi) {
+                if (gi % kTcLoadPar != par) continue;
+                const int s = (int)(gi % kTcStages);
+                if (!tc_wait(su32(&empty[s]), (uint32_t)(((gi / kTcStages) & 1) ^ 1), a, c)) {
                     aborted = true;
                     break;
                 }
                 const int h = g * a.hpk + r, p0 = lo + b * kTcP;
-                const uint32_t st = smem + kOffStage + (uint32_t)s * 2u * kTile;
-                bar_expect_tx(su32(&c.full[s]), 2 * kTile);
-                tma_load_3d(st, &a.q_map, 0, h, p0, su32(&c.full[s]));
-                tma_load_3d(st + kTile, &a.o_map, 0, h, p0, su32(&c.full[s]));
-                ++issued;
-                if (++s == kTcStages) {
-                    s = 0;
-                    ph ^= 1u;
-                }
+                bar_expect_tx(su32(&full[s]), tensor ? kTile + kLseBox : kTile);
+                tma_load_3d(ring + (uint32_t)s * kTile, map, 0, h, p0, su32(&full[s]));
+                if (tensor) tma_load_2d(smem + kOffL + (uint32_t)s * kLseBox, &a.l_map, 4 * (h >> 1), p0, su32(&full[s]));
+                last = gi;
             }
     }
-    // Copies still landing must finish before the CTA exits.
-    const int64_t k_end = issued < kTcStages ? issued : kTcStages;
-    for (int64_t q = issued - k_end; q < issued; ++q)
-        tc_drain(su32(&c.full[q % kTcStages]), (uint32_t)((q / kTcStages) & 1), a, c);
+    // Copies still landing must finish before the CTA exits: this warp owns
+    // kTcStages / kTcLoadPar stages, so only its last that many can be in flight.
+    for (int j = 0; j < kTcStages / kTcLoadPar; ++j) {
+        const int64_t q = last - (int64_t)j * kTcLoadPar;
+        if (q >= 0) tc_drain(su32(&full[q % kTcStages]), (uint32_t)((q / kTcStages) & 1), a, c);
+    }
     if (k_issued) tc_drain(su32(&c.k_full), (uint32_t)((k_issued - 1) & 1), a, c);
 }
 
+// Issue order per unit of n steps: GEMM1 of steps 0 and 1, then for each step j
+// GEMM1 of step j + 2 (as soon as the softmax has read step j's scores, which
+// frees their TMEM buffer) before GEMM2 of step j (once its P is written), so
+// that the scores of the next step are ready whenever the softmax warps finish
+// one.  Buffers and barrier phases follow this CTA's step count gs: scores / P
+// buffer gs % 2, Q / dO ring slot gs % kTcStages.
 __device__ void tc_role_mma(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t tmem) {
-    int s = 0, sb = 0;
-    uint32_t ph = 0, sph = 0, kph = 0, dph = 0;
-    int64_t gstep = 0;  // this CTA's steps so far: score / P buffer gstep % 2, its use gstep / 2
-    bool aborted = false;
-    for (int k = 0; !aborted; ++k) {
+    uint32_t kph = 0, dph = 0;
+    int64_t base = 0;  // this CTA's steps before the current unit
+    bool ok = true;
+    auto gemm1 = [&](int64_t gs, uint64_t kd, bool last) {
+        const int s = (int)(gs % kTcStages), b = (int)(gs & 1);
+        if (!tc_wait(su32(&c.full_q[s]), (uint32_t)((gs / kTcStages) & 1), a, c) ||
+            !tc_wait(su32(&c.s_empty[b]), (uint32_t)(((gs >> 1) & 1) ^ 1), a, c))
+            return false;
+        tc_after();
+        const uint64_t qd = desc_k(smem + kOffQ + (uint32_t)s * kTile);
+#pragma unroll
+        for (int k16 = 0; k16 < 4; ++k16)
+            tc_mma_f16(tmem + kColS + (uint32_t)(b * kTcP), kd + 2u * k16, qd + 2u * k16, a.idesc1, k16 != 0);
+        tc_commit_to(su32(&c.s_full[b]));
+        tc_commit_to(su32(&c.empty_q[s]));
+        if (last) tc_commit_to(su32(&c.k_empty));  // the unit's last read of its K tile
+        return true;
+    };
+    auto gemm2 = [&](int64_t gs, bool first) {
+        const int s = (int)(gs % kTcStages), b = (int)(gs & 1);
+        if (!tc_wait(su32(&c.full_o[s]), (uint32_t)((gs / kTcStages) & 1), a, c) ||
+            !tc_wait(su32(&c.p_ready[b]), (uint32_t)((gs >> 1) & 1), a, c) ||
+            (first && !tc_wait(su32(&c.dv_empty), dph ^ 1u, a, c)))
+            return false;
+        tc_after();
+        const uint64_t od = desc_mn(smem + kOffO + (uint32_t)s * kTile, 1024u, 1024u);
+#pragma unroll
+        for (int k16 = 0; k16 < 8; ++k16)  // A = P^T from tensor memory, 8 columns (16 positions) per K step
+            tc_mma_f16_ts(tmem + kColDv, tmem + kColP + (uint32_t)b * 64u + 8u * k16, od + 128u * k16, a.idesc2,
+                          !first || k16 != 0);
+        tc_commit_to(su32(&c.p_empty[b]));
+        tc_commit_to(su32(&c.empty_o[s]));
+        return true;
+    };
+    for (int k = 0; ok; ++k) {
         const int64_t u = unit_of(a, k);
         if (u < 0) break;
         int t0, g, lo, nblk;
@@ -169,56 +224,15 @@ __device__ void tc_role_mma(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t t
         kph ^= 1u;
         tc_after();
         const uint64_t kd = desc_k(smem + kOffK);
-        int s_prev = 0, sb_prev = 0;
-        int64_t g_prev = 0;
-        for (int i = 0; i <= n && !aborted; ++i) {
-            if (i < n) {  // GEMM1 of step i
-                if (!tc_wait(su32(&c.full[s]), ph, a, c) || !tc_wait(su32(&c.s_empty[sb]), sph ^ 1u, a, c)) {
-                    aborted = true;
-                    break;
-                }
-                tc_after();
-                const uint64_t qd = desc_k(smem + kOffStage + (uint32_t)s * 2u * kTile);
-#pragma unroll
-                for (int k16 = 0; k16 < 4; ++k16)
-                    tc_mma_f16(tmem + (uint32_t)(sb * kTcP), kd + 2u * k16, qd + 2u * k16, a.idesc1, k16 != 0);
-                tc_commit_to(su32(&c.s_full[sb]));
-                if (i == n - 1) tc_commit_to(su32(&c.k_empty));  // the unit's last read of its K tile
-            }
-            if (i >= 1) {  // GEMM2 of step i - 1
-                const int j = i - 1;
-                if (!tc_wait(su32(&c.p_ready[sb_prev]), (uint32_t)((g_prev >> 1) & 1), a, c) ||
-                    (j == 0 && !tc_wait(su32(&c.dv_empty), dph ^ 1u, a, c))) {
-                    aborted = true;
-                    break;
-                }
-                tc_after();
-                const uint32_t pbuf = smem + kOffP + (uint32_t)sb_prev * 2u * kTile;
-                const uint64_t od = desc_mn(smem + kOffStage + (uint32_t)s_prev * 2u * kTile + kTile, 1024u, 1024u);
-#pragma unroll
-                for (int k16 = 0; k16 < 8; ++k16)
-                    tc_mma_f16(tmem + 2u * kTcP, desc_k(pbuf + (uint32_t)(k16 >> 2) * kTile) + 2u * (k16 & 3),
-                               od + 128u * k16, a.idesc2, (j | k16) != 0);
-                tc_commit_to(su32(&c.p_empty[sb_prev]));
-                tc_commit_to(su32(&c.empty[s_prev]));
-            }
-            if (i < n) {
-                s_prev = s;
-                sb_prev = sb;
-                g_prev = gstep++;
-                if (++s == kTcStages) {
-                    s = 0;
-                    ph ^= 1u;
-                }
-                if (++sb == 2) {
-                    sb = 0;
-                    sph ^= 1u;
-                }
-            }
+        for (int j = 0; j < 2 && j < n && ok; ++j) ok = gemm1(base + j, kd, j == n - 1);
+        for (int j = 0; j < n && ok; ++j) {
+            if (j + 2 < n) ok = gemm1(base + j + 2, kd, j + 2 == n - 1);
+            ok = ok && gemm2(base + j, j == 0);
         }
-        if (aborted) break;
+        if (!ok) break;
         tc_commit_to(su32(&c.dv_full));
         dph ^= 1u;
+        base += n;
     }
     tc_commit_to(su32(&c.mma_done));
     tc_drain(su32(&c.mma_done), 0, a, c);
@@ -231,22 +245,23 @@ __device__ __forceinline__ float fast_exp2(float x) {  // the SFU's 2^x (x <= 0 
 }
 
 // Softmax and dV store warps: warp w holds key rows t0 + 32 (w % 4) + lane and
-// query columns 32 (w / 4) .. + 31 of every step.
+// query columns 32 (w / 4) .. + 31 of every step.  Lane l takes the forward
+// statistics of column l from the step's slot of the statistics ring (landed
+// with dO, so valid until GEMM2 has run), folds them and shares them through
+// the warp's 32 folded pairs.  With c = log2(e) / sqrt(64),
+// m = max log2(e) and l = log_sum log2(e) of a column, the page's
+// P = exp(min(s - max, 0) - log_sum) is 2^x with x = min(S c - (m + l), -l):
+// one FMA, one min and the SFU's 2^x per score.
 __device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t tmem, int w, int lane) {
     const int qd = w & 3, cq = w >> 2;
     const int u = 32 * qd + lane;  // key row within the unit
     const bool f16 = a.f16 != 0;
     const float l2e = 1.4426950408889634f;  // log2(e): exp(x) = 2^(x log2(e))
+    const float cs = a.scale * l2e;
+    const uint32_t stats = smem + kOffStats + (uint32_t)w * kStatsBytes;  // this warp's 32 (b, -l) pairs
     int sb = 0;
     uint32_t sph = 0, dph = 0;
-    int64_t steps = 0;  // this CTA's steps so far (P buffer parity)
-    // (max, log_sum) of query column 32 cq + lane of a step, times log2(e).
-    auto load_stats = [&](int p0, int h) {
-        const int pos = p0 + 32 * cq + lane;
-        float2 st = make_float2(0.f, 0.f);
-        if (pos < a.q_seq) st = __ldg(reinterpret_cast<const float2 *>(a.lse + ((int64_t)pos * a.nh + h) * 2));
-        return make_float2(st.x * l2e, st.y * l2e);
-    };
+    int64_t steps = 0;  // this CTA's steps so far (P buffer parity, ring slot)
     for (int k = 0;; ++k) {
         const int64_t un = unit_of(a, k);
         if (un < 0) break;
@@ -258,31 +273,47 @@ __device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t 
         if (a.window > 0 && t + a.window < end) end = t + a.window;
         const bool t_live = t < a.kv;
         const int n = nblk * a.hpk;
-        float2 st_next = n > 0 ? load_stats(lo, g * a.hpk) : make_float2(0.f, 0.f);
         for (int i = 0; i < n; ++i, ++steps) {
-            const int b = i / a.hpk, r = i - b * a.hpk;
-            const int h = g * a.hpk + r, p0 = lo + b * kTcP;
-            const float2 st_mine = st_next;
-            if (i + 1 < n) {
-                const int b1 = (i + 1) / a.hpk;
-                st_next = load_stats(lo + b1 * kTcP, g * a.hpk + (i + 1 - b1 * a.hpk));
+            const int c0 = lo + (i / a.hpk) * kTcP + 32 * cq;  // this warp's first query column
+            const int slot = (int)(steps % kTcStages);
+            if (!tc_wait(su32(&c.full_o[slot]), (uint32_t)((steps / kTcStages) & 1), a, c)) return;
+            float2 st;  // (max, log_sum) of column c0 + lane, head h of the pair (h & 1)
+            {
+                const int h = g * a.hpk + i % a.hpk;
+                asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
+                             : "=f"(st.x), "=f"(st.y)
+                             : "r"(smem + kOffL + (uint32_t)slot * kLseBox + (uint32_t)(32 * cq + lane) * 16u +
+                                   (uint32_t)(h & 1) * 8u)
+                             : "memory");
             }
-            if (!tc_wait_warp(su32(&c.s_full[sb]), sph, a, c, lane)) return;
+            __syncwarp();  // the previous step's readers of the folded pairs are done
+            {
+                const float l = st.y * l2e;
+                asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(stats + (uint32_t)lane * 8u), "f"(fmaf(st.x, l2e, l)),
+                             "f"(-l)
+                             : "memory");
+            }
+            __syncwarp();
+            if (!tc_wait(su32(&c.s_full[sb]), sph, a, c)) return;
             tc_after();
             uint32_t v[32];
-            tc_ld_32x32(tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(sb * kTcP + 32 * cq), v);
+            tc_ld_32x32(tmem + ((uint32_t)(32 * qd) << 16) + kColS + (uint32_t)(sb * kTcP + 32 * cq), v);
             tc_wait_ld(v);
+            // Every column of this row inside the mask: no per-score test.
+            const bool whole = t_live && start <= c0 && c0 + 31 < end;
             uint32_t pk[16];
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
+                const uint4 bl = lds128(stats + (uint32_t)e * 8u);  // (b, -l) of columns e, e + 1
                 float pr[2];
+                pr[0] = fast_exp2(fminf(fmaf(__uint_as_float(v[e]), cs, -__uint_as_float(bl.x)), __uint_as_float(bl.y)));
+                pr[1] = fast_exp2(fminf(fmaf(__uint_as_float(v[e + 1]), cs, -__uint_as_float(bl.z)), __uint_as_float(bl.w)));
+                if (!whole) {
 #pragma unroll
-                for (int z = 0; z < 2; ++z) {
-                    const int pos = p0 + 32 * cq + e + z;
-                    const float mx = __shfl_sync(0xffffffffu, st_mine.x, e + z);
-                    const float ls = __shfl_sync(0xffffffffu, st_mine.y, e + z);
-                    const float x = fminf(__uint_as_float(v[e + z]) * (a.scale * l2e) - mx, 0.f) - ls;
-                    pr[z] = (t_live && pos >= start && pos < end) ? fast_exp2(x) : 0.f;
+                    for (int z = 0; z < 2; ++z) {
+                        const int pos = c0 + e + z;
+                        if (!(t_live && pos >= start && pos < end)) pr[z] = 0.f;
+                    }
                 }
                 if (f16) {
                     const __half2 hh = __floats2half2_rn(pr[0], pr[1]);
@@ -295,17 +326,13 @@ __device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t 
             tc_before();
             __syncwarp();
             if (lane == 0) bar_arrive(su32(&c.s_empty[sb]));  // scores read: the buffer may be refilled
-            if (!tc_wait_warp(su32(&c.p_empty[sb]), (uint32_t)(((steps >> 1) & 1) ^ 1), a, c, lane)) return;
-            // Columns 32 cq .. + 31: chunk cq / 2 of the row, 16-byte pieces
-            // 4 (cq % 2) .. + 3 at their swizzled slots.
-            const uint32_t row = smem + kOffP + (uint32_t)sb * 2u * kTile + (uint32_t)(cq >> 1) * kTile + (uint32_t)u * 128u;
-#pragma unroll
-            for (int pc = 0; pc < 4; ++pc) {
-                const int piece = 4 * (cq & 1) + pc;
-                sts128(row + (uint32_t)((piece ^ (u & 7)) << 4), pk[4 * pc], pk[4 * pc + 1], pk[4 * pc + 2],
-                       pk[4 * pc + 3]);
-            }
-            fence_async_proxy();  // GEMM2 (async proxy) reads the P these threads wrote
+            if (!tc_wait(su32(&c.p_empty[sb]), (uint32_t)(((steps >> 1) & 1) ^ 1), a, c)) return;
+            tc_after();
+            // P^T of this warp's rows, query columns 32 cq .. + 31: tensor
+            // memory columns 16 cq .. + 15 of P buffer sb (GEMM2's A operand).
+            tc_st_32x16(tmem + ((uint32_t)(32 * qd) << 16) + kColP + (uint32_t)sb * 64u + (uint32_t)(16 * cq), pk);
+            tc_wait_st();
+            tc_before();
             __syncwarp();
             if (lane == 0) bar_arrive(su32(&c.p_ready[sb]));
             if (++sb == 2) {
@@ -320,11 +347,11 @@ __device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t 
             continue;
         }
         // dV of the unit: this warp's 16 columns (TMEM 256 + 16 cq ..) of lane u.
-        if (!tc_wait_warp(su32(&c.dv_full), dph, a, c, lane)) return;
+        if (!tc_wait(su32(&c.dv_full), dph, a, c)) return;
         dph ^= 1u;
         tc_after();
         uint32_t v[32];
-        tc_ld_32x32(tmem + ((uint32_t)(32 * qd) << 16) + 2u * kTcP + (uint32_t)(16 * cq), v);  // 32 columns read,
+        tc_ld_32x32(tmem + ((uint32_t)(32 * qd) << 16) + kColDv + (uint32_t)(16 * cq), v);  // 32 columns read,
         tc_wait_ld(v);                                                                            // 16 used
         if (t_live) {
             float4 *out = reinterpret_cast<float4 *>(a.dv + ((int64_t)t * a.nkv + g) * kTcD + 16 * cq);
@@ -347,8 +374,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) mha_grad_v_tc_kernel(const __gr
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcStages; ++s) {
-            bar_init(su32(&c.full[s]), 1);
-            bar_init(su32(&c.empty[s]), 1);
+            bar_init(su32(&c.full_q[s]), 1);
+            bar_init(su32(&c.full_o[s]), 1);
+            bar_init(su32(&c.empty_q[s]), 1);
+            bar_init(su32(&c.empty_o[s]), 1);
         }
         bar_init(su32(&c.k_full), 1);
         bar_init(su32(&c.k_empty), 1);
@@ -369,15 +398,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) mha_grad_v_tc_kernel(const __gr
     __syncthreads();
     tc_after();
     const uint32_t tmem = c.tmem_base;
-    if (warp == kTcLoadWarp && lane == 0) {
+    if (warp >= kTcLoadWarp && lane == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.q_map)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.k_map)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.o_map)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&a.l_map)) : "memory");
     }
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (warp == kTcLoadWarp) {
-        if (lane == 0) tc_role_load(a, c, smem);
+    if (warp >= kTcLoadWarp) {
+        if (lane == 0) tc_role_load(a, c, smem, warp - kTcLoadWarp);
         __syncwarp();
     } else if (warp == kTcMmaWarp) {
         if (lane == 0) tc_role_mma(a, c, smem, tmem);
@@ -393,10 +423,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) mha_grad_v_tc_kernel(const __gr
     }
 }
 
+// The statistics view needs rows of a multiple of 16 bytes: an even head count.
 bool tc_applies(const void *q, const void *k, const void *go, const float *lse, const float *dv,
                 const mha_grad_v_params *p, int dtype) {
-    return dtype != DGRAD_F32 && p->head_dim == (uint32_t)kTcD && aligned(q, 16) && aligned(k, 16) &&
-           aligned(go, 16) && aligned(lse, 8) && aligned(dv, 16);
+    return dtype != DGRAD_F32 && p->head_dim == (uint32_t)kTcD && p->num_heads % 2 == 0 && aligned(q, 16) &&
+           aligned(k, 16) && aligned(go, 16) && aligned(lse, 16) && aligned(dv, 16);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn() {
@@ -425,6 +456,19 @@ bool encode_heads_map(CUtensorMap *m, const void *ptr, int len, int heads) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// LSE [q_seq][heads][2] float32 as [q_seq][2 heads], box [128][4], no swizzle.
+bool encode_lse_map(CUtensorMap *m, const float *ptr, int len, int heads) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = tc_encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)heads * 2, (cuuint64_t)len};
+    const cuuint64_t strides[1] = {(cuuint64_t)heads * 2 * sizeof(float)};
+    const cuuint32_t box[2] = {4, 128};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int launch_tc(const void *q, const void *k, const void *go, const float *lse, float *dv, const mha_grad_v_params *p,
               int dtype, cudaStream_t st) {
     TcArgs a{};
@@ -449,7 +493,7 @@ int launch_tc(const void *q, const void *k, const void *go, const float *lse, fl
                ((uint32_t)(kTcT >> 4) << 24);
     a.wait_limit_ns = 2000000000ull;
     if (!encode_heads_map(&a.q_map, q, a.q_seq, a.nh) || !encode_heads_map(&a.k_map, k, a.kv, a.nkv) ||
-        !encode_heads_map(&a.o_map, go, a.q_seq, a.nh))
+        !encode_heads_map(&a.o_map, go, a.q_seq, a.nh) || !encode_lse_map(&a.l_map, lse, a.q_seq, a.nh))
         return DGRAD_ERR_UNSUPPORTED;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DGRAD_ERR_CUDA;

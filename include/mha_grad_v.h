@@ -27,7 +27,7 @@
  *
  * Arithmetic: the CUDA-core kernel (every dtype and shape) computes in
  * float32: scores, exponentials and the sums.  The tensor-core kernel
- * (bf16 / fp16, head_dim 64, 16-byte aligned pointers; see
+ * (bf16 / fp16, head_dim 64, an even num_heads, 16-byte aligned pointers; see
  * mha_grad_v_select_kernel) forms the scores with tcgen05 (exact products,
  * float32 sums), P in float32, rounds P to the input type for the second
  * product (with dO) and sums in float32.
@@ -69,8 +69,9 @@ int mha_grad_v(const void *q, const void *k, const void *d_out, const float *lse
 
 /* Which kernel mha_grad_v runs for these arguments: DGRAD_KERNEL_TC or
  * DGRAD_KERNEL_SIMT, or a negative dgrad_status for invalid arguments.  The
- * tensor-core kernel takes DGRAD_BF16 / DGRAD_F16 with head_dim 64 and Q, K
- * and dO 16-byte aligned; host logic only. */
+ * tensor-core kernel takes DGRAD_BF16 / DGRAD_F16 with head_dim 64, an even
+ * num_heads (its statistics view needs rows of a multiple of 16 bytes) and Q,
+ * K, dO, LSE and dV 16-byte aligned; host logic only. */
 int mha_grad_v_select_kernel(const void *q, const void *k, const void *d_out, const float *lse,
                              const float *dv, const mha_grad_v_params *p, int dtype);
 

@@ -362,6 +362,11 @@ def test_mha_grad_v_validation_and_selection(lib):
     assert sel(Q + 1, K, O, L, V, p, dg.DGRAD_BF16) == -3                      # element alignment
     assert sel(Q, K, O, L + 2, V, p, dg.DGRAD_BF16) == -3
     assert sel(Q, K, O, L, V, dg.MhaParams(128, 0, 8, 2, 512, 0), dg.DGRAD_BF16) == -4  # head_dim
+    assert sel(Q, K, O, L, V, p, dg.DGRAD_BF16) == dg.DGRAD_KERNEL_TC
+    assert sel(Q, K, O, L, V, p, dg.DGRAD_F16) == dg.DGRAD_KERNEL_TC
+    assert sel(Q, K, O, L, V, dg.MhaParams(128, 0, 3, 1, 64, 0), dg.DGRAD_BF16) == dg.DGRAD_KERNEL_SIMT  # odd heads
+    assert sel(Q, K, O, L + 8, V, p, dg.DGRAD_BF16) == dg.DGRAD_KERNEL_SIMT    # LSE not 16-byte aligned
+    assert sel(Q, K, O, L, V, dg.MhaParams(128, 0, 8, 2, 32, 0), dg.DGRAD_BF16) == dg.DGRAD_KERNEL_SIMT  # head_dim
     assert dg.mha_grad_v_set_kernel(dg.DGRAD_KERNEL_SIMT) == dg.DGRAD_KERNEL_AUTO
     try:
         assert sel(Q, K, O, L, V, p, dg.DGRAD_BF16) == dg.DGRAD_KERNEL_SIMT

@@ -97,12 +97,12 @@ def test_dv_off_alignment_and_guard(dg):
     check(got, q, k, go, lse, p, 1e-4)
 
 
-# Tensor-core cases (head_dim 64): one unit; several query blocks under a
-# causal mask (diagonal block masked); full attention with ragged lengths;
-# a window; grouped heads; a single position.
+# Tensor-core cases (head_dim 64, an even number of heads): one unit; several
+# query blocks under a causal mask (diagonal block masked); full attention with
+# ragged lengths; a window; grouped heads; a single position.
 TC_CASES = [
     (64, 0, 4, 2, 64, 0), (300, 0, 8, 2, 64, 0), (200, 330, 4, 4, 64, 0), (257, 0, 6, 3, 64, 100),
-    (1, 1, 1, 1, 64, 0), (129, 0, 2, 1, 64, 1), (500, 260, 8, 4, 64, 50),
+    (1, 1, 2, 1, 64, 0), (129, 0, 2, 1, 64, 1), (500, 260, 8, 4, 64, 50),
 ]
 
 
