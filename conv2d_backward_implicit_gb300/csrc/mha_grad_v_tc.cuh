@@ -9,22 +9,24 @@
 //   P^T[t][pos]        = exp(min(S^T / sqrt(64) - max[pos], 0) - log_sum[pos]), masked
 //   GEMM2  dV[t][:]   += P^T (128 x 128) . dO_block (128 x 64)  tcgen05 M128 N64 K16 x8
 // with dV accumulating in TMEM over all the unit's steps.
-//   * warps 17-18 (one thread each): TMA loads of the Q and dO blocks of head
+//   * warps 18-19 (one thread each): TMA loads of the Q and dO blocks of head
 //     h through 3-D views [q_seq][H][64] (box [128][1][64], 128-byte swizzle):
 //     Q lands as GEMM1's K-major B operand, dO as GEMM2's MN-major B operand
 //     (atoms of 8 positions x 64 elements).  One thread's copies complete one
 //     after another (about 1.1K cycles each) while different warps' overlap, so
-//     warp 17 loads the Q blocks and the unit's K tile, warp 18 the dO blocks
+//     warp 18 loads the Q blocks and the unit's K tile, warp 19 the dO blocks
 //     and with each the forward statistics of its positions (for the head pair
 //     of h, through a [q_seq][2 H] float32 view);
-//   * warp 16 (one thread): GEMM1 two steps ahead of GEMM2, into two TMEM score
-//     buffers; GEMM2 takes P^T from TMEM as its A operand;
-//   * warps 0-15 (warp w: TMEM lane quadrant w % 4, lane = key t, query
-//     columns 32 (w / 4) .. + 31 of the step): fold the forward statistics of
-//     their columns, read their 32 scores from TMEM, form P with the page's
-//     clamp and the causal / window mask (hardware ex2), round it to the input
-//     type and store it, two values per column, into a TMEM P buffer; after the
-//     unit's last step each warp stores its 16 columns of dV.
+//   * warps 16 and 17 (converged, lane 0 issuing): GEMM1 (two steps ahead of
+//     GEMM2, into two TMEM score buffers) and GEMM2 (P^T from TMEM as its A
+//     operand), each warp with its own waits and commits;
+//   * warps 0-15, two groups of 8 taking alternate steps (warp w: TMEM lane
+//     quadrant w % 4, lane = key t, query columns 64 ((w / 4) % 2) .. + 63):
+//     fold the forward statistics of their columns, read their scores from
+//     TMEM, form P with the page's clamp and the causal / window mask
+//     (hardware ex2), round it to the input type and store it, two values per
+//     column, into a TMEM P buffer; after the unit's last step each warp
+//     stores 16 columns of dV.
 // Every wait is bounded; on timeout the kernel raises its error flag, drains
 // its copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
@@ -38,23 +40,26 @@ using namespace tch;
 
 constexpr int kTcT = 128, kTcP = 128, kTcD = 64;  // keys per unit, queries per step, head_dim
 constexpr int kTcStages = 4;
-constexpr int kTcSoftWarps = 16, kTcMmaWarp = 16, kTcLoadWarp = 17, kTcLoadWarps = 2;
+constexpr int kTcSoftWarps = 16, kTcMmaWarp = 16, kTcMma2Warp = 17, kTcLoadWarp = 18, kTcLoadWarps = 2;
 constexpr int kTcThreads = 32 * (kTcLoadWarp + kTcLoadWarps);
 constexpr int kTcLoadPar = kTcLoadWarps / 2;  // step parities (one Q and one dO warp each)
 static_assert(kTcLoadWarps % 2 == 0 && kTcStages % kTcLoadPar == 0, "load warps own whole stages");
 constexpr uint32_t kTile = 128 * 128;  // bytes of a [128][64] 16-bit tile
-// Control block [0, 1 KB); per softmax warp 256 bytes: its 32 folded
+// Control block [0, 1 KB); per softmax warp 512 bytes: its 64 folded
 // (b, -l) pairs; then the K tile, the Q and dO rings (1 KB aligned for the
 // 128-byte swizzle) and the statistics ring: beside each dO slot, (max,
 // log_sum) of its 128 positions for an even / odd head pair.
-constexpr uint32_t kOffStats = 1024, kStatsBytes = 256;
-constexpr uint32_t kOffK = 5120;
+constexpr uint32_t kOffStats = 1024, kStatsBytes = 512;
+constexpr uint32_t kOffK = 9216;
 static_assert(kOffStats + kTcSoftWarps * kStatsBytes <= kOffK, "statistics overlap the K tile");
 constexpr uint32_t kOffQ = kOffK + kTile, kOffO = kOffQ + kTcStages * kTile;
 constexpr uint32_t kOffL = kOffO + kTcStages * kTile, kLseBox = 128 * 16;  // [128][4] float32 per slot
 // Tensor memory columns: scores S^T (two buffers of 128 float32), dV (64
-// float32), P^T (two buffers of 64 columns, each two 16-bit values).
+// float32), P^T (three buffers of 64 columns, each two 16-bit values: the
+// softmax of step i + 2 can store its P while GEMM2 of step i - 1 runs).
+constexpr int kPBufs = 3;
 constexpr uint32_t kColS = 0, kColDv = 256, kColP = 320;
+static_assert(kColP + kPBufs * 64 <= 512, "tensor memory columns");
 constexpr uint32_t kTcSmem = 1024 + kOffL + kTcStages * kLseBox;  // + 1 KB alignment slack
 static_assert(kOffK % 1024 == 0, "operand tiles must be 1 KB aligned");
 static_assert(kTcSmem <= 232448, "shared memory over the per-block limit");
@@ -75,8 +80,8 @@ struct TcArgs {
 struct TcCtl {
     uint64_t full_q[kTcStages], full_o[kTcStages], empty_q[kTcStages], empty_o[kTcStages];
     uint64_t k_full, k_empty;
-    uint64_t s_full[2], s_empty[2], p_ready[2], p_empty[2];
-    uint64_t dv_full, dv_empty, mma_done;
+    uint64_t s_full[2], s_empty[2], p_ready[kPBufs], p_empty[kPBufs];
+    uint64_t dv_full, dv_empty, mma_done[2];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -172,47 +177,19 @@ __device__ void tc_role_load(const TcArgs &a, TcCtl &c, uint32_t smem, int lw) {
     if (k_issued) tc_drain(su32(&c.k_full), (uint32_t)((k_issued - 1) & 1), a, c);
 }
 
-// Issue order per unit of n steps: GEMM1 of steps 0 and 1, then for each step j
-// GEMM1 of step j + 2 (as soon as the softmax has read step j's scores, which
-// frees their TMEM buffer) before GEMM2 of step j (once its P is written), so
-// that the scores of the next step are ready whenever the softmax warps finish
-// one.  Buffers and barrier phases follow this CTA's step count gs: scores / P
-// buffer gs % 2, Q / dO ring slot gs % kTcStages.
-__device__ void tc_role_mma(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t tmem) {
-    uint32_t kph = 0, dph = 0;
-    int64_t base = 0;  // this CTA's steps before the current unit
+// The MMA issue: GEMM1 by warp 16, GEMM2 by warp 17 (a thread's tcgen05
+// commit tracks only its own MMAs, and the two products share no operand or
+// accumulator, so each warp waits, issues and commits on its own; issuing the
+// small MMAs is what bounds one thread).  Each whole warp runs its loop (waits
+// and descriptors warp-uniform); lane 0 alone issues the MMAs and commits.
+// GEMM1 runs two steps ahead of GEMM2: it fills scores buffer gs % 2 as soon as
+// the softmax has read that buffer's previous scores.  Buffers and barrier
+// phases follow this CTA's step count gs: scores buffer gs % 2, P buffer
+// gs % kPBufs, Q / dO ring slot gs % kTcStages.
+__device__ void tc_role_gemm1(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t tmem, uint32_t leader) {
+    uint32_t kph = 0;
+    int64_t gs = 0;
     bool ok = true;
-    auto gemm1 = [&](int64_t gs, uint64_t kd, bool last) {
-        const int s = (int)(gs % kTcStages), b = (int)(gs & 1);
-        if (!tc_wait(su32(&c.full_q[s]), (uint32_t)((gs / kTcStages) & 1), a, c) ||
-            !tc_wait(su32(&c.s_empty[b]), (uint32_t)(((gs >> 1) & 1) ^ 1), a, c))
-            return false;
-        tc_after();
-        const uint64_t qd = desc_k(smem + kOffQ + (uint32_t)s * kTile);
-#pragma unroll
-        for (int k16 = 0; k16 < 4; ++k16)
-            tc_mma_f16(tmem + kColS + (uint32_t)(b * kTcP), kd + 2u * k16, qd + 2u * k16, a.idesc1, k16 != 0);
-        tc_commit_to(su32(&c.s_full[b]));
-        tc_commit_to(su32(&c.empty_q[s]));
-        if (last) tc_commit_to(su32(&c.k_empty));  // the unit's last read of its K tile
-        return true;
-    };
-    auto gemm2 = [&](int64_t gs, bool first) {
-        const int s = (int)(gs % kTcStages), b = (int)(gs & 1);
-        if (!tc_wait(su32(&c.full_o[s]), (uint32_t)((gs / kTcStages) & 1), a, c) ||
-            !tc_wait(su32(&c.p_ready[b]), (uint32_t)((gs >> 1) & 1), a, c) ||
-            (first && !tc_wait(su32(&c.dv_empty), dph ^ 1u, a, c)))
-            return false;
-        tc_after();
-        const uint64_t od = desc_mn(smem + kOffO + (uint32_t)s * kTile, 1024u, 1024u);
-#pragma unroll
-        for (int k16 = 0; k16 < 8; ++k16)  // A = P^T from tensor memory, 8 columns (16 positions) per K step
-            tc_mma_f16_ts(tmem + kColDv, tmem + kColP + (uint32_t)b * 64u + 8u * k16, od + 128u * k16, a.idesc2,
-                          !first || k16 != 0);
-        tc_commit_to(su32(&c.p_empty[b]));
-        tc_commit_to(su32(&c.empty_o[s]));
-        return true;
-    };
     for (int k = 0; ok; ++k) {
         const int64_t u = unit_of(a, k);
         if (u < 0) break;
@@ -224,18 +201,62 @@ __device__ void tc_role_mma(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t t
         kph ^= 1u;
         tc_after();
         const uint64_t kd = desc_k(smem + kOffK);
-        for (int j = 0; j < 2 && j < n && ok; ++j) ok = gemm1(base + j, kd, j == n - 1);
-        for (int j = 0; j < n && ok; ++j) {
-            if (j + 2 < n) ok = gemm1(base + j + 2, kd, j + 2 == n - 1);
-            ok = ok && gemm2(base + j, j == 0);
+        for (int j = 0; j < n; ++j, ++gs) {
+            const int s = (int)(gs % kTcStages), b = (int)(gs & 1);
+            if (!tc_wait(su32(&c.full_q[s]), (uint32_t)((gs / kTcStages) & 1), a, c) ||
+                !tc_wait(su32(&c.s_empty[b]), (uint32_t)(((gs >> 1) & 1) ^ 1), a, c)) {
+                ok = false;
+                break;
+            }
+            tc_after();
+            const uint64_t qd = desc_k(smem + kOffQ + (uint32_t)s * kTile);
+#pragma unroll
+            for (int k16 = 0; k16 < 4; ++k16)
+                tc_mma_f16_if(tmem + kColS + (uint32_t)(b * kTcP), kd + 2u * k16, qd + 2u * k16, a.idesc1, k16 != 0,
+                              leader);
+            tc_commit_to_if(su32(&c.s_full[b]), leader);
+            tc_commit_to_if(su32(&c.empty_q[s]), leader);
+            if (j == n - 1) tc_commit_to_if(su32(&c.k_empty), leader);  // the unit's last read of its K tile
+        }
+    }
+    tc_commit_to_if(su32(&c.mma_done[0]), leader);
+    tc_drain(su32(&c.mma_done[0]), 0, a, c);
+}
+
+__device__ void tc_role_gemm2(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t tmem, uint32_t leader) {
+    uint32_t dph = 0;
+    int64_t gs = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+        const int64_t u = unit_of(a, k);
+        if (u < 0) break;
+        int t0, g, lo, nblk;
+        unit_range(a, u, t0, g, lo, nblk);
+        const int n = nblk * a.hpk;
+        if (n == 0) continue;
+        for (int j = 0; j < n; ++j, ++gs) {
+            const int s = (int)(gs % kTcStages), b = (int)(gs % kPBufs);
+            if (!tc_wait(su32(&c.full_o[s]), (uint32_t)((gs / kTcStages) & 1), a, c) ||
+                !tc_wait(su32(&c.p_ready[b]), (uint32_t)((gs / kPBufs) & 1), a, c) ||
+                (j == 0 && !tc_wait(su32(&c.dv_empty), dph ^ 1u, a, c))) {
+                ok = false;
+                break;
+            }
+            tc_after();
+            const uint64_t od = desc_mn(smem + kOffO + (uint32_t)s * kTile, 1024u, 1024u);
+#pragma unroll
+            for (int k16 = 0; k16 < 8; ++k16)  // A = P^T from tensor memory, 8 columns (16 positions) per K step
+                tc_mma_f16_ts_if(tmem + kColDv, tmem + kColP + (uint32_t)b * 64u + 8u * k16, od + 128u * k16,
+                                 a.idesc2, j != 0 || k16 != 0, leader);
+            tc_commit_to_if(su32(&c.p_empty[b]), leader);
+            tc_commit_to_if(su32(&c.empty_o[s]), leader);
         }
         if (!ok) break;
-        tc_commit_to(su32(&c.dv_full));
+        tc_commit_to_if(su32(&c.dv_full), leader);
         dph ^= 1u;
-        base += n;
     }
-    tc_commit_to(su32(&c.mma_done));
-    tc_drain(su32(&c.mma_done), 0, a, c);
+    tc_commit_to_if(su32(&c.mma_done[1]), leader);
+    tc_drain(su32(&c.mma_done[1]), 0, a, c);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {  // the SFU's 2^x (x <= 0 here)
@@ -244,24 +265,27 @@ __device__ __forceinline__ float fast_exp2(float x) {  // the SFU's 2^x (x <= 0 
     return y;
 }
 
-// Softmax and dV store warps: warp w holds key rows t0 + 32 (w % 4) + lane and
-// query columns 32 (w / 4) .. + 31 of every step.  Lane l takes the forward
-// statistics of column l from the step's slot of the statistics ring (landed
-// with dO, so valid until GEMM2 has run), folds them and shares them through
-// the warp's 32 folded pairs.  With c = log2(e) / sqrt(64),
-// m = max log2(e) and l = log_sum log2(e) of a column, the page's
+// Softmax and dV store warps, two groups of 8 taking alternate steps (group
+// gs % 2 takes this CTA's step gs, with scores buffer gs % 2), so that one
+// group's waits and stores overlap the other's exponentials.  Warp w of group
+// w / 8 holds key rows t0 + 32 (w % 4) + lane and query columns 64 ((w / 4) % 2)
+// .. + 63 of its steps, in two chunks of 32.  Lane l takes the forward
+// statistics of columns l and 32 + l of its 64 from the step's slot of the
+// statistics ring (landed with dO, so valid until GEMM2 has run), folds them
+// and shares them through the warp's 64 folded pairs.  With c = log2(e) /
+// sqrt(64), m = max log2(e) and l = log_sum log2(e) of a column, the page's
 // P = exp(min(s - max, 0) - log_sum) is 2^x with x = min(S c - (m + l), -l):
 // one FMA, one min and the SFU's 2^x per score.
 __device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t tmem, int w, int lane) {
-    const int qd = w & 3, cq = w >> 2;
+    const int qd = w & 3, ch = (w >> 2) & 1, gp = w >> 3, cq = w >> 2;
     const int u = 32 * qd + lane;  // key row within the unit
     const bool f16 = a.f16 != 0;
     const float l2e = 1.4426950408889634f;  // log2(e): exp(x) = 2^(x log2(e))
     const float cs = a.scale * l2e;
-    const uint32_t stats = smem + kOffStats + (uint32_t)w * kStatsBytes;  // this warp's 32 (b, -l) pairs
-    int sb = 0;
+    const uint32_t stats = smem + kOffStats + (uint32_t)w * kStatsBytes;  // this warp's 64 (b, -l) pairs
+    const uint32_t lane_tm = (uint32_t)(32 * qd) << 16;
     uint32_t sph = 0, dph = 0;
-    int64_t steps = 0;  // this CTA's steps so far (P buffer parity, ring slot)
+    uint32_t base = 0;  // this CTA's steps before the current unit
     for (int k = 0;; ++k) {
         const int64_t un = unit_of(a, k);
         if (un < 0) break;
@@ -273,86 +297,101 @@ __device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t 
         if (a.window > 0 && t + a.window < end) end = t + a.window;
         const bool t_live = t < a.kv;
         const int n = nblk * a.hpk;
-        for (int i = 0; i < n; ++i, ++steps) {
-            const int c0 = lo + (i / a.hpk) * kTcP + 32 * cq;  // this warp's first query column
-            const int slot = (int)(steps % kTcStages);
-            if (!tc_wait(su32(&c.full_o[slot]), (uint32_t)((steps / kTcStages) & 1), a, c)) return;
-            float2 st;  // (max, log_sum) of column c0 + lane, head h of the pair (h & 1)
+        int i = (int)((base ^ (uint32_t)gp) & 1u);  // this group's first step of the unit
+        int qb = i / a.hpk, r = i - qb * a.hpk;     // its query block and head of the group
+        for (; i < n; i += 2) {
+            const uint32_t gs = base + (uint32_t)i;
+            const int c0 = lo + qb * kTcP + 64 * ch;  // this warp's first query column
+            const uint32_t slot = gs % kTcStages;
+            if (!tc_wait(su32(&c.full_o[slot]), (gs / kTcStages) & 1u, a, c)) return;
             {
-                const int h = g * a.hpk + i % a.hpk;
-                asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];"
-                             : "=f"(st.x), "=f"(st.y)
-                             : "r"(smem + kOffL + (uint32_t)slot * kLseBox + (uint32_t)(32 * cq + lane) * 16u +
-                                   (uint32_t)(h & 1) * 8u)
+                // (max, log_sum) of columns c0 + lane and c0 + 32 + lane, head h of the pair (h & 1)
+                const uint32_t src = smem + kOffL + slot * kLseBox + (uint32_t)(64 * ch + lane) * 16u +
+                                     (uint32_t)((g * a.hpk + r) & 1) * 8u;
+                float2 s0, s1;
+                asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(s0.x), "=f"(s0.y) : "r"(src) : "memory");
+                asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(s1.x), "=f"(s1.y) : "r"(src + 512u) : "memory");
+                __syncwarp();  // the previous step's readers of the folded pairs are done
+                const float l0 = s0.y * l2e, l1 = s1.y * l2e;
+                asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(stats + (uint32_t)lane * 8u), "f"(fmaf(s0.x, l2e, l0)),
+                             "f"(-l0)
                              : "memory");
-            }
-            __syncwarp();  // the previous step's readers of the folded pairs are done
-            {
-                const float l = st.y * l2e;
-                asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(stats + (uint32_t)lane * 8u), "f"(fmaf(st.x, l2e, l)),
-                             "f"(-l)
+                asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(stats + 256u + (uint32_t)lane * 8u),
+                             "f"(fmaf(s1.x, l2e, l1)), "f"(-l1)
                              : "memory");
+                __syncwarp();
             }
-            __syncwarp();
-            if (!tc_wait(su32(&c.s_full[sb]), sph, a, c)) return;
+            if (!tc_wait(su32(&c.s_full[gp]), sph, a, c)) return;
+            sph ^= 1u;
             tc_after();
-            uint32_t v[32];
-            tc_ld_32x32(tmem + ((uint32_t)(32 * qd) << 16) + kColS + (uint32_t)(sb * kTcP + 32 * cq), v);
-            tc_wait_ld(v);
-            // Every column of this row inside the mask: no per-score test.
-            const bool whole = t_live && start <= c0 && c0 + 31 < end;
-            uint32_t pk[16];
+            const uint32_t pb = gs % kPBufs;
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-                const uint4 bl = lds128(stats + (uint32_t)e * 8u);  // (b, -l) of columns e, e + 1
-                float pr[2];
-                pr[0] = fast_exp2(fminf(fmaf(__uint_as_float(v[e]), cs, -__uint_as_float(bl.x)), __uint_as_float(bl.y)));
-                pr[1] = fast_exp2(fminf(fmaf(__uint_as_float(v[e + 1]), cs, -__uint_as_float(bl.z)), __uint_as_float(bl.w)));
-                if (!whole) {
+            for (int kc = 0; kc < 2; ++kc) {
+                uint32_t v[32];
+                tc_ld_32x32(tmem + lane_tm + kColS + (uint32_t)(gp * kTcP + 64 * ch + 32 * kc), v);
+                tc_wait_ld(v);
+                if (kc == 1) {  // both chunks read: the scores buffer may be refilled
+                    tc_before();
+                    __syncwarp();
+                    if (lane == 0) bar_arrive(su32(&c.s_empty[gp]));
+                }
+                const int cc = c0 + 32 * kc;
+                // Every column of this chunk inside the mask: no per-score test.
+                const bool whole = t_live && start <= cc && cc + 31 < end;
+                uint32_t pk[16];
 #pragma unroll
-                    for (int z = 0; z < 2; ++z) {
-                        const int pos = c0 + e + z;
-                        if (!(t_live && pos >= start && pos < end)) pr[z] = 0.f;
+                for (int e = 0; e < 32; e += 2) {
+                    const uint4 bl = lds128(stats + (uint32_t)(32 * kc + e) * 8u);  // (b, -l) of columns e, e + 1
+                    float pr[2];
+                    pr[0] = fast_exp2(fminf(fmaf(__uint_as_float(v[e]), cs, -__uint_as_float(bl.x)), __uint_as_float(bl.y)));
+                    pr[1] = fast_exp2(fminf(fmaf(__uint_as_float(v[e + 1]), cs, -__uint_as_float(bl.z)), __uint_as_float(bl.w)));
+                    if (!whole) {
+#pragma unroll
+                        for (int z = 0; z < 2; ++z) {
+                            const int pos = cc + e + z;
+                            if (!(t_live && pos >= start && pos < end)) pr[z] = 0.f;
+                        }
+                    }
+                    if (f16) {
+                        const __half2 hh = __floats2half2_rn(pr[0], pr[1]);
+                        pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&hh);
+                    } else {
+                        const __nv_bfloat162 hh = __floats2bfloat162_rn(pr[0], pr[1]);
+                        pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&hh);
                     }
                 }
-                if (f16) {
-                    const __half2 hh = __floats2half2_rn(pr[0], pr[1]);
-                    pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&hh);
-                } else {
-                    const __nv_bfloat162 hh = __floats2bfloat162_rn(pr[0], pr[1]);
-                    pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&hh);
+                if (kc == 0) {  // P buffer pb free (GEMM2 of step gs - 3 has run)
+                    if (!tc_wait(su32(&c.p_empty[pb]), ((gs / kPBufs) & 1u) ^ 1u, a, c)) return;
+                    tc_after();
                 }
+                // P^T of this warp's rows, query columns 64 ch + 32 kc .. + 31:
+                // tensor memory columns 32 ch + 16 kc .. + 15 of P buffer pb.
+                tc_st_32x16(tmem + lane_tm + kColP + pb * 64u + (uint32_t)(32 * ch + 16 * kc), pk);
             }
-            tc_before();
-            __syncwarp();
-            if (lane == 0) bar_arrive(su32(&c.s_empty[sb]));  // scores read: the buffer may be refilled
-            if (!tc_wait(su32(&c.p_empty[sb]), (uint32_t)(((steps >> 1) & 1) ^ 1), a, c)) return;
-            tc_after();
-            // P^T of this warp's rows, query columns 32 cq .. + 31: tensor
-            // memory columns 16 cq .. + 15 of P buffer sb (GEMM2's A operand).
-            tc_st_32x16(tmem + ((uint32_t)(32 * qd) << 16) + kColP + (uint32_t)sb * 64u + (uint32_t)(16 * cq), pk);
             tc_wait_st();
             tc_before();
             __syncwarp();
-            if (lane == 0) bar_arrive(su32(&c.p_ready[sb]));
-            if (++sb == 2) {
-                sb = 0;
-                sph ^= 1u;
+            if (lane == 0) bar_arrive(su32(&c.p_ready[pb]));
+            r += 2;
+            while (r >= a.hpk) {
+                r -= a.hpk;
+                ++qb;
             }
         }
+        base += (uint32_t)n;
         if (n == 0) {  // no query reaches these keys: dV is zero
             if (t_live)
                 for (int d = 16 * cq; d < 16 * cq + 16; d += 4)
                     *reinterpret_cast<float4 *>(a.dv + ((int64_t)t * a.nkv + g) * kTcD + d) = make_float4(0.f, 0.f, 0.f, 0.f);
             continue;
         }
-        // dV of the unit: this warp's 16 columns (TMEM 256 + 16 cq ..) of lane u.
+        // dV of the unit: this warp's 16 columns (kColDv + 16 cq ..) of lane u.
         if (!tc_wait(su32(&c.dv_full), dph, a, c)) return;
         dph ^= 1u;
         tc_after();
         uint32_t v[32];
-        tc_ld_32x32(tmem + ((uint32_t)(32 * qd) << 16) + kColDv + (uint32_t)(16 * cq), v);  // 32 columns read,
-        tc_wait_ld(v);                                                                            // 16 used
+        tc_ld_32x32(tmem + lane_tm + kColDv + (uint32_t)(16 * cq), v);  // 32 columns read, 16 used
+        tc_wait_ld(v);
         if (t_live) {
             float4 *out = reinterpret_cast<float4 *>(a.dv + ((int64_t)t * a.nkv + g) * kTcD + 16 * cq);
 #pragma unroll
@@ -383,13 +422,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) mha_grad_v_tc_kernel(const __gr
         bar_init(su32(&c.k_empty), 1);
         for (int b = 0; b < 2; ++b) {
             bar_init(su32(&c.s_full[b]), 1);
-            bar_init(su32(&c.s_empty[b]), kTcSoftWarps);
-            bar_init(su32(&c.p_ready[b]), kTcSoftWarps);
+            bar_init(su32(&c.s_empty[b]), kTcSoftWarps / 2);  // one group
+        }
+        for (int b = 0; b < kPBufs; ++b) {
+            bar_init(su32(&c.p_ready[b]), kTcSoftWarps / 2);
             bar_init(su32(&c.p_empty[b]), 1);
         }
         bar_init(su32(&c.dv_full), 1);
         bar_init(su32(&c.dv_empty), kTcSoftWarps);
-        bar_init(su32(&c.mma_done), 1);
+        bar_init(su32(&c.mma_done[0]), 1);
+        bar_init(su32(&c.mma_done[1]), 1);
         c.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -410,7 +452,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) mha_grad_v_tc_kernel(const __gr
         if (lane == 0) tc_role_load(a, c, smem, warp - kTcLoadWarp);
         __syncwarp();
     } else if (warp == kTcMmaWarp) {
-        if (lane == 0) tc_role_mma(a, c, smem, tmem);
+        tc_role_gemm1(a, c, smem, tmem, lane == 0 ? 1u : 0u);
+        __syncwarp();
+    } else if (warp == kTcMma2Warp) {
+        tc_role_gemm2(a, c, smem, tmem, lane == 0 ? 1u : 0u);
         __syncwarp();
     } else {
         tc_role_soft(a, c, smem, tmem, warp, lane);

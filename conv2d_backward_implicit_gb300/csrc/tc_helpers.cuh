@@ -103,6 +103,31 @@ __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d, uint32_t a_tmem, uint6
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
+// Warp-converged issue: every lane runs the loop (descriptors stay warp
+// uniform) and only the lanes with `issue` set execute the instruction.
+__device__ __forceinline__ void tc_mma_f16_if(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc,
+                                              uint32_t issue) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(issue)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma_f16_ts_if(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                 uint32_t acc, uint32_t issue) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+        "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc), "r"(issue)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit_to_if(uint32_t bar, uint32_t issue) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar),
+        "r"(issue)
+        : "memory");
+}
 // 32 lanes x 16 consecutive 32-bit columns from registers; completes at tc_wait_st.
 __device__ __forceinline__ void tc_st_32x16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
