@@ -54,12 +54,10 @@ constexpr uint32_t kOffK = 9216;
 static_assert(kOffStats + kTcSoftWarps * kStatsBytes <= kOffK, "statistics overlap the K tile");
 constexpr uint32_t kOffQ = kOffK + kTile, kOffO = kOffQ + kTcStages * kTile;
 constexpr uint32_t kOffL = kOffO + kTcStages * kTile, kLseBox = 128 * 16;  // [128][4] float32 per slot
-// Tensor memory columns: scores S^T (two buffers of 128 float32), dV (64
-// float32), P^T (three buffers of 64 columns, each two 16-bit values: the
-// softmax of step i + 2 can store its P while GEMM2 of step i - 1 runs).
-constexpr int kPBufs = 3;
-constexpr uint32_t kColS = 0, kColDv = 256, kColP = 320;
-static_assert(kColP + kPBufs * 64 <= 512, "tensor memory columns");
+// Tensor memory columns, one set per step parity p: scores S^T (128
+// float32) at 128 p, a dV partial sum (64 float32) at 256 + 64 p, P^T (64
+// columns, each two 16-bit values) at 384 + 64 p.
+constexpr uint32_t kColS = 0, kColDv = 256, kColP = 384;
 constexpr uint32_t kTcSmem = 1024 + kOffL + kTcStages * kLseBox;  // + 1 KB alignment slack
 static_assert(kOffK % 1024 == 0, "operand tiles must be 1 KB aligned");
 static_assert(kTcSmem <= 232448, "shared memory over the per-block limit");
@@ -80,8 +78,8 @@ struct TcArgs {
 struct TcCtl {
     uint64_t full_q[kTcStages], full_o[kTcStages], empty_q[kTcStages], empty_o[kTcStages];
     uint64_t k_full, k_empty;
-    uint64_t s_full[2], s_empty[2], p_ready[kPBufs], p_empty[kPBufs];
-    uint64_t dv_full, dv_empty, mma_done[2];
+    uint64_t s_full[2], s_empty[2], p_ready[2], p_empty[2];
+    uint64_t dv_full[2], dv_empty, mma_done[2];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -177,19 +175,50 @@ __device__ void tc_role_load(const TcArgs &a, TcCtl &c, uint32_t smem, int lw) {
     if (k_issued) tc_drain(su32(&c.k_full), (uint32_t)((k_issued - 1) & 1), a, c);
 }
 
-// The MMA issue: GEMM1 by warp 16, GEMM2 by warp 17 (a thread's tcgen05
-// commit tracks only its own MMAs, and the two products share no operand or
-// accumulator, so each warp waits, issues and commits on its own; issuing the
-// small MMAs is what bounds one thread).  Each whole warp runs its loop (waits
-// and descriptors warp-uniform); lane 0 alone issues the MMAs and commits.
-// GEMM1 runs two steps ahead of GEMM2: it fills scores buffer gs % 2 as soon as
-// the softmax has read that buffer's previous scores.  Buffers and barrier
-// phases follow this CTA's step count gs: scores buffer gs % 2, P buffer
-// gs % kPBufs, Q / dO ring slot gs % kTcStages.
-__device__ void tc_role_gemm1(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t tmem, uint32_t leader) {
-    uint32_t kph = 0;
-    int64_t gs = 0;
+// The MMA issue, split by step parity: warp 16 + p issues GEMM1 and GEMM2 of
+// this CTA's steps gs with gs % 2 = p (a thread's tcgen05 commit tracks only
+// its own MMAs, and the two parities share no accumulator; issuing the small
+// MMAs is what bounds one thread).  The whole warp runs the loop (waits and
+// descriptors warp-uniform); lane 0 alone issues the MMAs and commits.  GEMM1
+// of a parity's next step is issued as soon as the softmax has read the
+// current step's scores, before GEMM2 of the current step.  Ring slots and
+// barrier phases follow gs: Q / dO slot gs % kTcStages; the parity's scores,
+// P and dV columns and barriers once per own step.
+__device__ void tc_role_mma(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t tmem, int par, uint32_t leader) {
+    uint32_t kph = 0, dph = 0, ph = 0;  // K tile, dV (per unit), own-step phases
+    uint32_t base = 0;                  // this CTA's steps before the current unit
+    const uint32_t s_col = tmem + kColS + 128u * (uint32_t)par, dv_col = tmem + kColDv + 64u * (uint32_t)par;
+    const uint32_t p_col = tmem + kColP + 64u * (uint32_t)par;
     bool ok = true;
+    auto gemm1 = [&](uint32_t gs, uint64_t kd, uint32_t phase) {
+        const uint32_t s = gs % kTcStages;
+        if (!tc_wait(su32(&c.full_q[s]), (gs / kTcStages) & 1u, a, c) ||
+            !tc_wait(su32(&c.s_empty[par]), phase ^ 1u, a, c))  // scores of the previous own step read
+            return false;
+        tc_after();
+        const uint64_t qd = desc_k(smem + kOffQ + s * kTile);
+#pragma unroll
+        for (int k16 = 0; k16 < 4; ++k16)
+            tc_mma_f16_if(s_col, kd + 2u * k16, qd + 2u * k16, a.idesc1, k16 != 0, leader);
+        tc_commit_to_if(su32(&c.s_full[par]), leader);
+        tc_commit_to_if(su32(&c.empty_q[s]), leader);
+        return true;
+    };
+    auto gemm2 = [&](uint32_t gs, uint32_t phase, bool first) {
+        const uint32_t s = gs % kTcStages;
+        if (!tc_wait(su32(&c.full_o[s]), (gs / kTcStages) & 1u, a, c) ||
+            !tc_wait(su32(&c.p_ready[par]), phase, a, c) ||
+            (first && !tc_wait(su32(&c.dv_empty), dph ^ 1u, a, c)))
+            return false;
+        tc_after();
+        const uint64_t od = desc_mn(smem + kOffO + s * kTile, 1024u, 1024u);
+#pragma unroll
+        for (int k16 = 0; k16 < 8; ++k16)  // A = P^T from tensor memory, 8 columns (16 positions) per K step
+            tc_mma_f16_ts_if(dv_col, p_col + 8u * k16, od + 128u * k16, a.idesc2, !first || k16 != 0, leader);
+        tc_commit_to_if(su32(&c.p_empty[par]), leader);
+        tc_commit_to_if(su32(&c.empty_o[s]), leader);
+        return true;
+    };
     for (int k = 0; ok; ++k) {
         const int64_t u = unit_of(a, k);
         if (u < 0) break;
@@ -201,62 +230,23 @@ __device__ void tc_role_gemm1(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t
         kph ^= 1u;
         tc_after();
         const uint64_t kd = desc_k(smem + kOffK);
-        for (int j = 0; j < n; ++j, ++gs) {
-            const int s = (int)(gs % kTcStages), b = (int)(gs & 1);
-            if (!tc_wait(su32(&c.full_q[s]), (uint32_t)((gs / kTcStages) & 1), a, c) ||
-                !tc_wait(su32(&c.s_empty[b]), (uint32_t)(((gs >> 1) & 1) ^ 1), a, c)) {
-                ok = false;
-                break;
-            }
-            tc_after();
-            const uint64_t qd = desc_k(smem + kOffQ + (uint32_t)s * kTile);
-#pragma unroll
-            for (int k16 = 0; k16 < 4; ++k16)
-                tc_mma_f16_if(tmem + kColS + (uint32_t)(b * kTcP), kd + 2u * k16, qd + 2u * k16, a.idesc1, k16 != 0,
-                              leader);
-            tc_commit_to_if(su32(&c.s_full[b]), leader);
-            tc_commit_to_if(su32(&c.empty_q[s]), leader);
-            if (j == n - 1) tc_commit_to_if(su32(&c.k_empty), leader);  // the unit's last read of its K tile
-        }
-    }
-    tc_commit_to_if(su32(&c.mma_done[0]), leader);
-    tc_drain(su32(&c.mma_done[0]), 0, a, c);
-}
-
-__device__ void tc_role_gemm2(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t tmem, uint32_t leader) {
-    uint32_t dph = 0;
-    int64_t gs = 0;
-    bool ok = true;
-    for (int k = 0; ok; ++k) {
-        const int64_t u = unit_of(a, k);
-        if (u < 0) break;
-        int t0, g, lo, nblk;
-        unit_range(a, u, t0, g, lo, nblk);
-        const int n = nblk * a.hpk;
-        if (n == 0) continue;
-        for (int j = 0; j < n; ++j, ++gs) {
-            const int s = (int)(gs % kTcStages), b = (int)(gs % kPBufs);
-            if (!tc_wait(su32(&c.full_o[s]), (uint32_t)((gs / kTcStages) & 1), a, c) ||
-                !tc_wait(su32(&c.p_ready[b]), (uint32_t)((gs / kPBufs) & 1), a, c) ||
-                (j == 0 && !tc_wait(su32(&c.dv_empty), dph ^ 1u, a, c))) {
-                ok = false;
-                break;
-            }
-            tc_after();
-            const uint64_t od = desc_mn(smem + kOffO + (uint32_t)s * kTile, 1024u, 1024u);
-#pragma unroll
-            for (int k16 = 0; k16 < 8; ++k16)  // A = P^T from tensor memory, 8 columns (16 positions) per K step
-                tc_mma_f16_ts_if(tmem + kColDv, tmem + kColP + (uint32_t)b * 64u + 8u * k16, od + 128u * k16,
-                                 a.idesc2, j != 0 || k16 != 0, leader);
-            tc_commit_to_if(su32(&c.p_empty[b]), leader);
-            tc_commit_to_if(su32(&c.empty_o[s]), leader);
+        const int i0 = (int)((base ^ (uint32_t)par) & 1u);  // this parity's first step of the unit
+        if (i0 < n) ok = gemm1(base + (uint32_t)i0, kd, ph);
+        for (int i = i0; i < n && ok; i += 2) {
+            if (i + 2 < n) ok = gemm1(base + (uint32_t)i + 2, kd, ph ^ 1u);
+            ok = ok && gemm2(base + (uint32_t)i, ph, i == i0);
+            ph ^= 1u;
         }
         if (!ok) break;
-        tc_commit_to_if(su32(&c.dv_full), leader);
+        // Both parities' last reads of the K tile are done once both commit
+        // (with no GEMM1 in this unit, the commit covers earlier MMAs only).
+        tc_commit_to_if(su32(&c.k_empty), leader);
+        if (i0 < n) tc_commit_to_if(su32(&c.dv_full[par]), leader);
         dph ^= 1u;
+        base += (uint32_t)n;
     }
-    tc_commit_to_if(su32(&c.mma_done[1]), leader);
-    tc_drain(su32(&c.mma_done[1]), 0, a, c);
+    tc_commit_to_if(su32(&c.mma_done[par]), leader);
+    tc_drain(su32(&c.mma_done[par]), 0, a, c);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {  // the SFU's 2^x (x <= 0 here)
@@ -284,8 +274,9 @@ __device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t 
     const float cs = a.scale * l2e;
     const uint32_t stats = smem + kOffStats + (uint32_t)w * kStatsBytes;  // this warp's 64 (b, -l) pairs
     const uint32_t lane_tm = (uint32_t)(32 * qd) << 16;
-    uint32_t sph = 0, dph = 0;
-    uint32_t base = 0;  // this CTA's steps before the current unit
+    uint32_t own = 0;             // phase of this group's scores / P barriers (once per own step)
+    uint32_t dph0 = 0, dph1 = 0;  // phases of the two parities' dV barriers
+    uint32_t base = 0;            // this CTA's steps before the current unit
     for (int k = 0;; ++k) {
         const int64_t un = unit_of(a, k);
         if (un < 0) break;
@@ -321,10 +312,8 @@ __device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t 
                              : "memory");
                 __syncwarp();
             }
-            if (!tc_wait(su32(&c.s_full[gp]), sph, a, c)) return;
-            sph ^= 1u;
+            if (!tc_wait(su32(&c.s_full[gp]), own, a, c)) return;
             tc_after();
-            const uint32_t pb = gs % kPBufs;
 #pragma unroll
             for (int kc = 0; kc < 2; ++kc) {
                 uint32_t v[32];
@@ -360,18 +349,19 @@ __device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t 
                         pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&hh);
                     }
                 }
-                if (kc == 0) {  // P buffer pb free (GEMM2 of step gs - 3 has run)
-                    if (!tc_wait(su32(&c.p_empty[pb]), ((gs / kPBufs) & 1u) ^ 1u, a, c)) return;
+                if (kc == 0) {  // the parity's P buffer free (GEMM2 of its previous step has run)
+                    if (!tc_wait(su32(&c.p_empty[gp]), own ^ 1u, a, c)) return;
                     tc_after();
                 }
                 // P^T of this warp's rows, query columns 64 ch + 32 kc .. + 31:
-                // tensor memory columns 32 ch + 16 kc .. + 15 of P buffer pb.
-                tc_st_32x16(tmem + lane_tm + kColP + pb * 64u + (uint32_t)(32 * ch + 16 * kc), pk);
+                // tensor memory columns 32 ch + 16 kc .. + 15 of the parity's P buffer.
+                tc_st_32x16(tmem + lane_tm + kColP + 64u * (uint32_t)gp + (uint32_t)(32 * ch + 16 * kc), pk);
             }
             tc_wait_st();
             tc_before();
             __syncwarp();
-            if (lane == 0) bar_arrive(su32(&c.p_ready[pb]));
+            if (lane == 0) bar_arrive(su32(&c.p_ready[gp]));
+            own ^= 1u;
             r += 2;
             while (r >= a.hpk) {
                 r -= a.hpk;
@@ -385,19 +375,27 @@ __device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t 
                     *reinterpret_cast<float4 *>(a.dv + ((int64_t)t * a.nkv + g) * kTcD + d) = make_float4(0.f, 0.f, 0.f, 0.f);
             continue;
         }
-        // dV of the unit: this warp's 16 columns (kColDv + 16 cq ..) of lane u.
-        if (!tc_wait(su32(&c.dv_full), dph, a, c)) return;
-        dph ^= 1u;
-        tc_after();
-        uint32_t v[32];
-        tc_ld_32x32(tmem + lane_tm + kColDv + (uint32_t)(16 * cq), v);  // 32 columns read, 16 used
-        tc_wait_ld(v);
+        // dV of the unit: the sum of the two parities' partial sums (a parity
+        // without steps in the unit has none), this warp's 16 columns of lane u.
+        float acc[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            if ((int)(((base - (uint32_t)n) ^ (uint32_t)p) & 1u) >= n) continue;
+            if (!tc_wait(su32(&c.dv_full[p]), p ? dph1 : dph0, a, c)) return;
+            if (p) dph1 ^= 1u; else dph0 ^= 1u;
+            tc_after();
+            uint32_t v[32];
+            tc_ld_32x32(tmem + lane_tm + kColDv + 64u * (uint32_t)p + (uint32_t)(16 * cq), v);  // 16 of 32 used
+            tc_wait_ld(v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc[e] += __uint_as_float(v[e]);
+        }
         if (t_live) {
             float4 *out = reinterpret_cast<float4 *>(a.dv + ((int64_t)t * a.nkv + g) * kTcD + 16 * cq);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                out[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                     __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+            for (int e = 0; e < 4; ++e) out[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
         }
         tc_before();
         __syncwarp();
@@ -419,16 +417,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) mha_grad_v_tc_kernel(const __gr
             bar_init(su32(&c.empty_o[s]), 1);
         }
         bar_init(su32(&c.k_full), 1);
-        bar_init(su32(&c.k_empty), 1);
+        bar_init(su32(&c.k_empty), 2);  // both MMA warps
         for (int b = 0; b < 2; ++b) {
             bar_init(su32(&c.s_full[b]), 1);
             bar_init(su32(&c.s_empty[b]), kTcSoftWarps / 2);  // one group
         }
-        for (int b = 0; b < kPBufs; ++b) {
+        for (int b = 0; b < 2; ++b) {
             bar_init(su32(&c.p_ready[b]), kTcSoftWarps / 2);
             bar_init(su32(&c.p_empty[b]), 1);
+            bar_init(su32(&c.dv_full[b]), 1);
         }
-        bar_init(su32(&c.dv_full), 1);
         bar_init(su32(&c.dv_empty), kTcSoftWarps);
         bar_init(su32(&c.mma_done[0]), 1);
         bar_init(su32(&c.mma_done[1]), 1);
@@ -451,11 +449,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) mha_grad_v_tc_kernel(const __gr
     if (warp >= kTcLoadWarp) {
         if (lane == 0) tc_role_load(a, c, smem, warp - kTcLoadWarp);
         __syncwarp();
-    } else if (warp == kTcMmaWarp) {
-        tc_role_gemm1(a, c, smem, tmem, lane == 0 ? 1u : 0u);
-        __syncwarp();
-    } else if (warp == kTcMma2Warp) {
-        tc_role_gemm2(a, c, smem, tmem, lane == 0 ? 1u : 0u);
+    } else if (warp == kTcMmaWarp || warp == kTcMma2Warp) {
+        tc_role_mma(a, c, smem, tmem, warp - kTcMmaWarp, lane == 0 ? 1u : 0u);
         __syncwarp();
     } else {
         tc_role_soft(a, c, smem, tmem, warp, lane);
