@@ -942,6 +942,19 @@ def profile_rmsnorm(args):
     return 0
 
 
+def profile_mha(args):
+    """Only the attention dV of MHA_SHAPE, args.profile_mha times back to back
+    (the inputs of mha_call), for an ncu capture."""
+    import torch
+    import conv2d_backward_implicit_gb300 as dg
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream()
+    ms, kernel = mha_call(dg, dev, stream, calls=args.profile_mha)
+    print(json.dumps({"profile_mha": args.profile_mha, "kernel": kernel, **MHA_SHAPE}), flush=True)
+    return 0
+
+
 def record_traffic_file(args, wl, key):
     """Writes profiles/dgrad_tc_<key>.traffic.json from the CSV of ncu_traffic_command."""
     with open(args.record_traffic) as f:
@@ -997,6 +1010,9 @@ def main(argv=None):
                     help="only launch the fused RMSNorm + matmul L times on an m x 4096 x 4096 bf16 "
                          "problem (for an ncu capture; m from --rmsnorm-m)")
     ap.add_argument("--rmsnorm-m", type=int, default=2048, help="rows of X for --profile-rmsnorm")
+    ap.add_argument("--profile-mha", type=int, default=0, metavar="L",
+                    help="only launch the attention dV of the bench shape L times after 3 warm-up launches "
+                         "(for an ncu capture)")
     ap.add_argument("--probe", choices=sorted(PROBES), default=None,
                     help="build and run a device-rate probe (tcgen05.mma, TMA loads or stores)")
     args = ap.parse_args(argv)
@@ -1010,6 +1026,8 @@ def main(argv=None):
         return profile_run(args, wl, args.config)
     if args.profile_rmsnorm > 0:
         return profile_rmsnorm(args)
+    if args.profile_mha > 0:
+        return profile_mha(args)
     if args.impl == "reference":
         args.steps = 10 if args.steps is None else args.steps
         args.warmup = 1 if args.warmup is None else args.warmup

@@ -71,7 +71,6 @@ struct TcArgs {
     int64_t units;
     float scale;
     uint32_t idesc1, idesc2;
-    int f16;
     uint64_t wait_limit_ns;
 };
 
@@ -255,6 +254,36 @@ __device__ __forceinline__ float fast_exp2(float x) {  // the SFU's 2^x (x <= 0 
     return y;
 }
 
+// P^T of one 32-column chunk of a warp's scores v (this lane's row): 2^x with
+// x = min(S c - b, -l) from the folded pairs at `pairs`, masked per column
+// when kMasked (row t, columns cc ..; kept where start <= pos < end and the
+// row exists), rounded to T and packed two columns per 32-bit value.
+template <bool kF16, bool kMasked>
+__device__ __forceinline__ void softmax_chunk(const uint32_t (&v)[32], uint32_t pairs, float cs, int cc, int start,
+                                              int end, bool t_live, uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+        const uint4 bl = lds128(pairs + (uint32_t)e * 8u);  // (b, -l) of columns e, e + 1
+        float pr[2];
+        pr[0] = fast_exp2(fminf(fmaf(__uint_as_float(v[e]), cs, -__uint_as_float(bl.x)), __uint_as_float(bl.y)));
+        pr[1] = fast_exp2(fminf(fmaf(__uint_as_float(v[e + 1]), cs, -__uint_as_float(bl.z)), __uint_as_float(bl.w)));
+        if (kMasked) {
+#pragma unroll
+            for (int z = 0; z < 2; ++z) {
+                const int pos = cc + e + z;
+                if (!(t_live && pos >= start && pos < end)) pr[z] = 0.f;
+            }
+        }
+        if (kF16) {
+            const __half2 hh = __floats2half2_rn(pr[0], pr[1]);
+            pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&hh);
+        } else {
+            const __nv_bfloat162 hh = __floats2bfloat162_rn(pr[0], pr[1]);
+            pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&hh);
+        }
+    }
+}
+
 // Softmax and dV store warps, two groups of 8 taking alternate steps (group
 // gs % 2 takes this CTA's step gs, with scores buffer gs % 2), so that one
 // group's waits and stores overlap the other's exponentials.  Warp w of group
@@ -266,10 +295,10 @@ __device__ __forceinline__ float fast_exp2(float x) {  // the SFU's 2^x (x <= 0 
 // sqrt(64), m = max log2(e) and l = log_sum log2(e) of a column, the page's
 // P = exp(min(s - max, 0) - log_sum) is 2^x with x = min(S c - (m + l), -l):
 // one FMA, one min and the SFU's 2^x per score.
+template <bool kF16>
 __device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t tmem, int w, int lane) {
     const int qd = w & 3, ch = (w >> 2) & 1, gp = w >> 3, cq = w >> 2;
     const int u = 32 * qd + lane;  // key row within the unit
-    const bool f16 = a.f16 != 0;
     const float l2e = 1.4426950408889634f;  // log2(e): exp(x) = 2^(x log2(e))
     const float cs = a.scale * l2e;
     const uint32_t stats = smem + kOffStats + (uint32_t)w * kStatsBytes;  // this warp's 64 (b, -l) pairs
@@ -328,27 +357,10 @@ __device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t 
                 // Every column of this chunk inside the mask: no per-score test.
                 const bool whole = t_live && start <= cc && cc + 31 < end;
                 uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const uint4 bl = lds128(stats + (uint32_t)(32 * kc + e) * 8u);  // (b, -l) of columns e, e + 1
-                    float pr[2];
-                    pr[0] = fast_exp2(fminf(fmaf(__uint_as_float(v[e]), cs, -__uint_as_float(bl.x)), __uint_as_float(bl.y)));
-                    pr[1] = fast_exp2(fminf(fmaf(__uint_as_float(v[e + 1]), cs, -__uint_as_float(bl.z)), __uint_as_float(bl.w)));
-                    if (!whole) {
-#pragma unroll
-                        for (int z = 0; z < 2; ++z) {
-                            const int pos = cc + e + z;
-                            if (!(t_live && pos >= start && pos < end)) pr[z] = 0.f;
-                        }
-                    }
-                    if (f16) {
-                        const __half2 hh = __floats2half2_rn(pr[0], pr[1]);
-                        pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&hh);
-                    } else {
-                        const __nv_bfloat162 hh = __floats2bfloat162_rn(pr[0], pr[1]);
-                        pk[e >> 1] = *reinterpret_cast<const uint32_t *>(&hh);
-                    }
-                }
+                if (whole)
+                    softmax_chunk<kF16, false>(v, stats + 256u * (uint32_t)kc, cs, cc, start, end, t_live, pk);
+                else
+                    softmax_chunk<kF16, true>(v, stats + 256u * (uint32_t)kc, cs, cc, start, end, t_live, pk);
                 if (kc == 0) {  // the parity's P buffer free (GEMM2 of its previous step has run)
                     if (!tc_wait(su32(&c.p_empty[gp]), own ^ 1u, a, c)) return;
                     tc_after();
@@ -403,6 +415,7 @@ __device__ void tc_role_soft(const TcArgs &a, TcCtl &c, uint32_t smem, uint32_t 
     }
 }
 
+template <bool kF16>
 __global__ void __launch_bounds__(kTcThreads, 1) mha_grad_v_tc_kernel(const __grid_constant__ TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t smem = (su32(smem_raw) + 1023u) & ~1023u;
@@ -453,7 +466,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) mha_grad_v_tc_kernel(const __gr
         tc_role_mma(a, c, smem, tmem, warp - kTcMmaWarp, lane == 0 ? 1u : 0u);
         __syncwarp();
     } else {
-        tc_role_soft(a, c, smem, tmem, warp, lane);
+        tc_role_soft<kF16>(a, c, smem, tmem, warp, lane);
     }
     tc_before();
     __syncthreads();
@@ -524,7 +537,6 @@ int launch_tc(const void *q, const void *k, const void *go, const float *lse, fl
     a.scale = 1.0f / sqrtf((float)kTcD);
     a.lse = lse;
     a.dv = dv;
-    a.f16 = dtype == DGRAD_F16 ? 1 : 0;
     const uint32_t fmt = dtype == DGRAD_BF16 ? 1u : 0u;
     // D float32, A and B of the input type; GEMM1: both K-major, N = 128;
     // GEMM2: B (dO) MN-major, N = 64; M = 128.
@@ -542,8 +554,10 @@ int launch_tc(const void *q, const void *k, const void *go, const float *lse, fl
     static std::atomic<uint64_t> configured{0};
     const uint64_t bit = dev < 64 ? (uint64_t)1 << dev : 0;
     if (!bit || !(configured.load() & bit)) {
-        if (cudaFuncSetAttribute(mha_grad_v_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(mha_grad_v_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kTcSmem) != cudaSuccess ||
+            cudaFuncSetAttribute(mha_grad_v_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kTcSmem) != cudaSuccess)
             return DGRAD_ERR_CUDA;
         configured.fetch_or(bit);
     }
@@ -558,7 +572,9 @@ int launch_tc(const void *q, const void *k, const void *go, const float *lse, fl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mha_grad_v_tc_kernel, a) == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
+    const cudaError_t e = dtype == DGRAD_F16 ? cudaLaunchKernelEx(&cfg, mha_grad_v_tc_kernel<true>, a)
+                                             : cudaLaunchKernelEx(&cfg, mha_grad_v_tc_kernel<false>, a);
+    return e == cudaSuccess ? DGRAD_OK : DGRAD_ERR_CUDA;
 }
 
 }  // namespace
