@@ -301,9 +301,13 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// The MMA roles run on their whole warp (control flow and descriptor
+// arithmetic warp-uniform, which issues the small MMAs faster than a lone
+// divergent lane); the tcgen05 instructions themselves execute in lane 0 only.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        "{\n\t.reg .pred q;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 q, l, 0;\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
         : "memory");
 }
 
@@ -312,16 +316,16 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
                                        uint32_t idesc, uint32_t accumulate) {
     if constexpr (TF32) {
         asm volatile(
-            "{\n\t.reg .pred p;\n\t"
+            "{\n\t.reg .pred p, q;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 q, l, 0;\n\t"
             "setp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "@q tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
             "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
             : "memory");
     } else {
         asm volatile(
-            "{\n\t.reg .pred p;\n\t"
+            "{\n\t.reg .pred p, q;\n\t.reg .u32 l;\n\tmov.u32 l, %%laneid;\n\tsetp.eq.u32 q, l, 0;\n\t"
             "setp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
             "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
             : "memory");
     }
@@ -1307,7 +1311,7 @@ __device__ void role_weights(const TcParams &p, Shared &sh, uint32_t w_base, uin
     }
 }
 
-// Warp 8, lane 0: tcgen05.mma issue.  D[ci, pos] (TMEM, 256 columns per
+// Warp 8 (converged; lane 0 issues): tcgen05.mma.  D[ci, pos] (TMEM, 256 columns per
 // buffer) += W_tap[ci, co] (A: packed weights) x G[co, pos + shift(tap)]
 // (B: the frame window seen from the tap's start row).
 template <bool TF32, int V>
@@ -1420,7 +1424,7 @@ __device__ __forceinline__ int st_cols(const TcParams &p) {
     return p.st_qhalo ? p.st_tw * p.st_n : p.st_n;
 }
 
-// Warp 8, lane 0, stacked-phase mode: D[position, (phase, ci)] (TMEM, st_n
+// Warp 8 (converged; lane 0 issues), stacked-phase mode: D[position, (phase, ci)] (TMEM, st_n
 // columns per buffer) += G[position + shift(tap), co] (A: the frame window
 // seen from the tap's start row) x W_tap[(phase, ci), co] (B: resident packed
 // weights of the chunk and tap).
@@ -2354,7 +2358,7 @@ __device__ void role_epilogue(const TcParams &p, Shared &sh, uint32_t stage, uin
 // a G stage is hbp rows of 128 bytes (64 grad_out channels), row h = 64u + b
 // holding grad_out[n, :, ih0 + ph - (kH-1) + u, b - kPmLeft].
 
-// MMA warp, lane 0: two M = 128 halves per tile, each into its own
+// MMA warp (converged; lane 0 issues): two M = 128 halves per tile, each into its own
 // accumulator buffer (kW x 64 columns): for kernel row kh, A = window rows
 // from 64 (kH-1-kh) + pw + 128 half, B = the kW packed taps (kh, 0..kW-1).
 __device__ void role_mma_pm(const TcParams &p, Shared &sh, uint32_t g_base, uint32_t w_base,
@@ -2693,7 +2697,7 @@ __global__ void __launch_bounds__(Roles<V>::threads, 1)
         if (lane == 0 && p.nw != 0 && p.gather_tma) weight_stream_producer(p, sh, w_base);
         __syncwarp();
     } else if (warp == R::mma_warp) {
-        if (lane == 0) {
+        {  // the whole warp: tc_mma / tc_commit issue from lane 0
             if constexpr (PM)
                 role_mma_pm(p, sh, g_base, w_base, tmem);
             else
