@@ -35,6 +35,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "nvtx_range.h"
+
 namespace dgrad {
 
 constexpr int kMaxPhases = 16;  // stride <= 4

@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(256) dgrad_simt_kernel(const T *__restrict__ g
 
 int launch_simt(const Plan &plan, const void *grad_out, const void *weight, float *grad_in,
                 void *stream) {
+    NvtxRange range("conv2d_grad_input: dgrad (CUDA cores)");
     const SimtParams &p = plan.simt;
     const int64_t total = (int64_t)p.N * p.Ci * p.H * p.W;
     const int threads = 256;

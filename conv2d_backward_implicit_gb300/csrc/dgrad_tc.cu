@@ -2858,6 +2858,7 @@ bool encode_out_map(TcParams &p) {
 
 int launch_tc(const Plan &plan, const void *grad_out, const void *packed, float *grad_in,
               void *stream) {
+    NvtxRange range("conv2d_grad_input: dgrad (tcgen05)");
     TcParams p = plan.tc;
     p.grad_out = grad_out;
     p.packed = packed;

@@ -18,6 +18,7 @@
 #include <cstdint>
 
 #include "mha_grad_v.h"
+#include "nvtx_range.h"
 
 namespace mhadv {
 
@@ -196,6 +197,7 @@ extern "C" {
 int mha_grad_v(const void *q, const void *k, const void *d_out, const float *lse, float *dv,
                const mha_grad_v_params *p, int dtype, struct CUstream_st *stream) {
     using namespace mhadv;
+    dgrad::NvtxRange range("mha_grad_v");
     const int kern = select(q, k, d_out, lse, dv, p, dtype);
     if (kern < 0) return -kern;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

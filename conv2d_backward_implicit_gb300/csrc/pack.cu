@@ -189,6 +189,7 @@ int launch_elementwise(K kern, int64_t total, void *stream, A... args) {
 }  // namespace
 
 int launch_space_to_depth(const FwdSplit &f, const void *x, void *xs, int esize, void *stream) {
+    NvtxRange range("conv2d_forward: space-to-depth of x");
     const int64_t total = (int64_t)f.N * f.nr * f.nc * f.Ci * f.Hx * f.Wx;
     if (esize == 4)
         return launch_elementwise(space_to_depth_kernel<float>, total, stream, static_cast<const float *>(x),
@@ -198,6 +199,7 @@ int launch_space_to_depth(const FwdSplit &f, const void *x, void *xs, int esize,
 }
 
 int launch_split_weights(const FwdSplit &f, const void *w, void *ws, int esize, void *stream) {
+    NvtxRange range("conv2d_forward: split weights");
     const int64_t total = (int64_t)f.Co * f.nr * f.nc * f.Ci * f.KH * f.KW;
     if (esize == 4)
         return launch_elementwise(split_weights_kernel<float>, total, stream, static_cast<const float *>(w),
@@ -208,6 +210,7 @@ int launch_split_weights(const FwdSplit &f, const void *w, void *ws, int esize, 
 
 int launch_flip_transpose(const void *w, void *wt, int Co, int Ci, int kH, int kW, int esize,
                           void *stream) {
+    NvtxRange range("conv2d_forward: flip weights");
     const int64_t total = (int64_t)Co * Ci * kH * kW;
     if (total == 0) return (int)cudaSuccess;
     int64_t blocks = (total + 255) / 256;
@@ -233,6 +236,7 @@ int launch_flip_transpose(const void *w, void *wt, int Co, int Ci, int kH, int k
 }
 
 int launch_pack(const Plan &plan, const void *weight, void *packed, void *stream) {
+    NvtxRange range("conv2d_grad_input: pack weights");
     const PackParams &k = plan.pack;
     if (k.total_elems == 0) return (int)cudaSuccess;
     const int threads = 256;

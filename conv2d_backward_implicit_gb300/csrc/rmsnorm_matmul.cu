@@ -44,6 +44,8 @@
 
 #include <atomic>
 #include <cmath>
+
+#include "nvtx_range.h"
 #include <cstdint>
 
 #include "rmsnorm_matmul.h"
@@ -613,6 +615,7 @@ extern "C" {
 int rmsnorm_matmul(const void *x, const void *w_norm, const void *w_proj, float *c, const rmsnorm_matmul_params *p,
                    int dtype, struct CUstream_st *stream) {
     using namespace rmsmm;
+    dgrad::NvtxRange range("rmsnorm_matmul");
     const int k = select(x, w_norm, w_proj, c, p, dtype);
     if (k < 0) return -k;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
