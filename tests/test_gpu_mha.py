@@ -140,3 +140,19 @@ def test_tensor_core_kernel_more_units_than_sms(dg, parity_log):
         assert (err <= bound).all(), f"key tile {t0}: error above the bound"
         worst = max(worst, float(err.max() / np.abs(ref).max()))
     parity_log("mha_grad_v tc bf16 (2560, 0, 16, 8, 64, 0), 3 key tiles", worst, C_TC["bf16"])
+
+
+def test_odd_head_count_runs_on_cuda_cores(dg, parity_log):
+    """An odd number of query heads (here 3 over one KV head) leaves the
+    tensor-core kernel's statistics view without 16-byte rows: auto selection
+    takes the CUDA-core kernel, which must still meet its bound."""
+    case = (150, 0, 3, 1, 64, 0)
+    q, k, go, lse = make_inputs(*case, "bf16", seed=5)
+    p = dg.MhaParams(*case)
+    dev = torch.device("cuda")
+    assert dg.mha_grad_v_select_kernel(q.to(dev), k.to(dev), go.to(dev), lse.to(dev),
+                                       torch.empty(150, 1, 64, device=dev), p,
+                                       dg.DTYPE_CODE["bf16"]) == dg.DGRAD_KERNEL_SIMT
+    got = run(dg, q, k, go, lse, p, "bf16")
+    err = check(got, q, k, go, lse, p, 1e-4)
+    parity_log("mha_grad_v auto, odd heads bf16 (150, 0, 3, 1, 64, 0)", err, 1e-4)
