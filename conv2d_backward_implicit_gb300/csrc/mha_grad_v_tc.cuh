@@ -2,13 +2,15 @@
 // mha_grad_v.cu): bf16 / fp16 Q, K, dO with head_dim 64, sm_103a.
 //
 // Work unit: 128 key positions t of one KV head g (units ordered by key tile,
-// so under a causal mask the units with the most query blocks start first),
-// one persistent CTA per SM.  For every block of 128 query positions that can
-// reach the unit and every head h of the group (a "step"):
+// so under a causal mask the units with the most query blocks come first,
+// dealt to the persistent CTAs, one per SM, in rounds of alternating
+// direction).  For every block of 128 query positions that can reach the unit
+// and every head h of the group (a "step"):
 //   GEMM1  S^T[t][pos] = K_tile (128 x 64) . Q_block^T        tcgen05 M128 N128 K16 x4
 //   P^T[t][pos]        = exp(min(S^T / sqrt(64) - max[pos], 0) - log_sum[pos]), masked
 //   GEMM2  dV[t][:]   += P^T (128 x 128) . dO_block (128 x 64)  tcgen05 M128 N64 K16 x8
-// with dV accumulating in TMEM over all the unit's steps.
+// with dV accumulating in TMEM over all the unit's steps, one partial sum per
+// step parity.
 //   * warps 18-19 (one thread each): TMA loads of the Q and dO blocks of head
 //     h through 3-D views [q_seq][H][64] (box [128][1][64], 128-byte swizzle):
 //     Q lands as GEMM1's K-major B operand, dO as GEMM2's MN-major B operand
@@ -17,16 +19,18 @@
 //     warp 18 loads the Q blocks and the unit's K tile, warp 19 the dO blocks
 //     and with each the forward statistics of its positions (for the head pair
 //     of h, through a [q_seq][2 H] float32 view);
-//   * warps 16 and 17 (converged, lane 0 issuing): GEMM1 (two steps ahead of
-//     GEMM2, into two TMEM score buffers) and GEMM2 (P^T from TMEM as its A
-//     operand), each warp with its own waits and commits;
+//   * warps 16 and 17 (converged, lane 0 issuing), one per step parity: GEMM1
+//     of the parity's next step (into its TMEM scores) ahead of GEMM2 of its
+//     current one (P^T from TMEM as the A operand, into its dV partial sum),
+//     each warp with its own waits and commits;
 //   * warps 0-15, two groups of 8 taking alternate steps (warp w: TMEM lane
 //     quadrant w % 4, lane = key t, query columns 64 ((w / 4) % 2) .. + 63):
 //     fold the forward statistics of their columns, read their scores from
 //     TMEM, form P with the page's clamp and the causal / window mask
 //     (hardware ex2), round it to the input type and store it, two values per
-//     column, into a TMEM P buffer; after the unit's last step each warp
-//     stores 16 columns of dV.
+//     column, into the parity's TMEM P buffer; after the unit's last step each
+//     warp adds the two parities' partial sums for 16 columns of dV and stores
+//     them.
 // Every wait is bounded; on timeout the kernel raises its error flag, drains
 // its copies and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
