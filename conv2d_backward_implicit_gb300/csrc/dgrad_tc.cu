@@ -530,12 +530,14 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Tc
     return wait_slow(bar, parity, p.wait_limit_ns, sh, true);
 }
 
-// Whole warp: lane 0 waits, the verdict is broadcast.
+// Whole warp: every lane polls the barrier (no divergent branch around a lone
+// polling lane) and one vote gives the warp a single verdict, also when the
+// wait runs out.
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, const TcParams &p,
                                               Shared &sh, int lane) {
-    int ok = 0;
-    if (lane == 0) ok = wait_bar(bar, parity, p, sh) ? 1 : 0;
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    (void)lane;
+    const bool ok = wait_bar(bar, parity, p, sh);
+    return __all_sync(0xffffffffu, ok) != 0;
 }
 
 // Waits that must end even while aborting (copies / MMAs already in flight).
