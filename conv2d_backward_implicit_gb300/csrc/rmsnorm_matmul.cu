@@ -115,10 +115,12 @@ __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, const Params
 __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity, const Params &p, Ctl &c) {
     if (!bar_try(bar, parity)) wait_long(bar, parity, p, c, false);
 }
+// Whole warp: every lane polls (no divergent branch around a lone polling
+// lane) and one vote gives the warp a single verdict, also on a timeout.
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const Params &p, Ctl &c, int lane) {
-    int ok = 0;
-    if (lane == 0) ok = wait(bar, parity, p, c) ? 1 : 0;
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    (void)lane;
+    const bool ok = wait(bar, parity, p, c);
+    return __all_sync(0xffffffffu, ok) != 0;
 }
 
 // ----------------------------------------------------------------- roles
